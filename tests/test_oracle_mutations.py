@@ -1,0 +1,132 @@
+"""Plant plausible mistakes in the CPU oracle and show the pins catch each one.
+
+Every mutation is applied with ``monkeypatch`` to the oracle's own module on the CPU for
+the duration of one test; the pins of ``oracle_pins`` then have to fail.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import attention as oatt
+from oracle import mla as omla
+from tests import oracle_pins as pins
+
+
+def _fails(check, *args):
+    with pytest.raises((AssertionError, ValueError, IndexError)):
+        check(*args)
+
+
+def _decode_pins():
+    return [
+        (pins.check_decode_brute, oracle.decode_gqa),
+        (pins.check_decode_sdpa, oracle.decode_gqa),
+    ]
+
+
+def _any_fails(checks):
+    caught = 0
+    for check, *args in checks:
+        try:
+            check(*args)
+        except (AssertionError, ValueError, IndexError):
+            caught += 1
+    assert caught > 0, "no pin caught the planted mistake"
+
+
+def test_interleaved_head_mapping_is_caught(monkeypatch):
+    # h % Hkv instead of h // G
+    def unit(q, k_cache, v_cache, seq_lens, scale, b, j):
+        n_kv = k_cache.shape[2]
+        s = int(seq_lens[b])
+        heads = np.arange(q.shape[1])[np.arange(q.shape[1]) % n_kv == j]
+        return oatt.attend(q[b, heads, :], k_cache[b, :s, j, :], v_cache[b, :s, j, :], scale)
+    monkeypatch.setattr(oatt, "decode_gqa_unit", unit)
+    _fails(pins.check_decode_brute, oracle.decode_gqa)
+    _fails(pins.check_decode_sdpa, oracle.decode_gqa)
+
+
+def test_dropped_scale_is_caught(monkeypatch):
+    real = oatt.attend
+    monkeypatch.setattr(oatt, "attend", lambda q, k, v, scale, allowed=None: real(q, k, v, 1.0, allowed))
+    _any_fails(_decode_pins())
+    _fails(pins.check_prefill_sdpa, oracle.prefill_gqa_causal)
+
+
+def test_missing_normalisation_is_caught(monkeypatch):
+    def attend(q_rows, keys, values, scale, allowed=None):
+        s = float(scale) * (np.asarray(q_rows, float) @ np.asarray(keys, float).T)
+        if allowed is not None:
+            s = np.where(allowed, s, -np.inf)
+        e = np.exp(s - s.max(axis=1, keepdims=True))
+        return e @ np.asarray(values, float)
+    monkeypatch.setattr(oatt, "attend", attend)
+    _any_fails(_decode_pins())
+
+
+def test_causal_off_by_one_is_caught(monkeypatch):
+    monkeypatch.setattr(oatt, "causal_allowed",
+                        lambda q_len, k_len: np.arange(k_len)[None, :] < np.arange(q_len)[:, None] + (k_len - q_len))
+    _fails(pins.check_prefill_brute, oracle.prefill_gqa_causal)
+    _fails(pins.check_prefill_closed_forms, oracle.prefill_gqa_causal)
+
+
+def test_anticausal_mask_is_caught(monkeypatch):
+    monkeypatch.setattr(oatt, "causal_allowed",
+                        lambda q_len, k_len: np.arange(k_len)[None, :] >= np.arange(q_len)[:, None])
+    _fails(pins.check_prefill_sdpa, oracle.prefill_gqa_causal)
+
+
+def test_last_token_dropped_is_caught(monkeypatch):
+    real = oatt.decode_gqa_unit
+    monkeypatch.setattr(oatt, "decode_gqa_unit",
+                        lambda q, k, v, lens, scale, b, j: real(q, k, v, np.maximum(np.asarray(lens) - 1, 0), scale, b, j))
+    _any_fails(_decode_pins())
+
+
+def test_values_from_key_cache_is_caught(monkeypatch):
+    real = oatt.decode_gqa_unit
+    monkeypatch.setattr(oatt, "decode_gqa_unit",
+                        lambda q, k, v, lens, scale, b, j: real(q, k, k, lens, scale, b, j))
+    _any_fails(_decode_pins())
+
+
+def test_lse_in_log2_is_caught():
+    real = oatt.attend_partial
+
+    def attend_partial(q_rows, keys, values, scale):
+        o, lse = real(q_rows, keys, values, scale)
+        return o, lse / np.log(2.0)
+    _fails(pins.check_split_merge, oatt.attend, attend_partial, oatt.lse_merge)
+
+
+def test_merge_without_max_weighting_is_caught():
+    def bad_merge(o_parts, lse_parts):
+        return np.asarray(o_parts).mean(axis=0)
+    _fails(pins.check_split_merge, oatt.attend, oatt.attend_partial, bad_merge)
+
+
+def test_mla_dropped_rope_term_is_caught(monkeypatch):
+    real = omla.mla_decode_absorbed
+    monkeypatch.setattr(omla, "mla_decode_absorbed",
+                        lambda q_lat, q_rope, c, kr, lens, scale: real(q_lat, 0 * q_rope, c, kr, lens, scale))
+    _fails(pins.check_mla_absorbed_equals_naive, omla.absorb_query, omla.mla_decode_absorbed,
+           omla.apply_uv, omla.mla_decode_naive)
+    _fails(pins.check_mla_is_mqa, omla.mla_decode_absorbed, oracle.decode_gqa)
+
+
+def test_mla_wrong_absorption_operand_is_caught():
+    def absorb_rows(q_nope, w_uk):   # contracts W_UK over r instead of d_nope (W·q, square case)
+        q_nope = np.asarray(q_nope, float)
+        w = np.asarray(w_uk, float)
+        return np.einsum("hrn,bhn->bhr", w[:, :q_nope.shape[2], :q_nope.shape[2]], q_nope)
+    _fails(pins.check_mla_absorbed_equals_naive, absorb_rows, omla.mla_decode_absorbed,
+           omla.apply_uv, omla.mla_decode_naive)
+
+
+def test_mla_naive_shared_rope_sign_error_is_caught(monkeypatch):
+    real = omla.mla_decode_naive
+    monkeypatch.setattr(omla, "mla_decode_naive",
+                        lambda qn, qr, c, kr, wuk, wuv, lens, scale: real(qn, qr, c, -kr, wuk, wuv, lens, scale))
+    _fails(pins.check_mla_naive_brute, omla.mla_decode_naive)
