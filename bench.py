@@ -1,0 +1,645 @@
+#!/usr/bin/env python
+"""Benchmark of the KV-cache attention hot path on B300 (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Headline workload (default): MiniMind-shaped GQA decode — B=32, Hq=8, Hkv=4, D=96, bf16
+cache, one new query token per sequence, cache lengths uniform in [512, 2048] from the
+seed. A step is one ``attn_decode_gqa`` call (split-KV decode kernel + log-sum-exp merge)
+over the whole batch. ``value`` = algorithmic KV bytes read per step (each cached K/V
+element of the live lengths once) ÷ the device time per step, in GB/s, with the inputs
+resident in HBM; the timed steps cycle through enough distinct cache sets that they
+cannot be served from L2 (≥ 4 × the L2 size in total).
+
+The line also carries: ``roofline`` (the decode call's achieved GB/s against the measured
+HBM copy bandwidth), ``e2e`` (same metric through the Python API with pinned host inputs
+copied in and the output copied back inside the timed region), ``cpu_baseline`` (the fp64
+CPU oracle on the host cores, bounded sample), ``clocks`` (NVML samples taken during the
+timed region), ``gpu_launches`` and ``also`` (the other workloads: Llama-3-8B-shaped decode
+with Hkv 32/8/1, MLA absorbed decode, causal prefill, each with its own roofline).
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this path has) on the
+same workload and metric, on the host cores, and prints the same line with
+``"impl": "reference"``. Under torchrun with N > 1 each rank runs an independent replica
+on its own GPU and its own sequences (weak scaling, no collective on the data path);
+rank 0 prints the aggregate.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "decode attn KV-read HBM GB/s (% of ~8 TB/s), tokens/s; prefill TFLOP/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ============================================================================ environment
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK}, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """NVML samples of the SM clock and the clock-event reasons while the timed region runs."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, device_index, period_s=0.01):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.period, self.stop_flag, self.thread, self.h = period_s, threading.Event(), None, None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            bus = torch.cuda.get_device_properties(device_index).pci_bus_id if hasattr(
+                torch.cuda.get_device_properties(device_index), "pci_bus_id") else None
+            self.h = (pynvml.nvmlDeviceGetHandleByPciBusId(bus) if bus else
+                      pynvml.nvmlDeviceGetHandleByIndex(device_index))
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+        except Exception as e:  # pragma: no cover - NVML missing
+            self.error = repr(e)
+
+    def _run(self):
+        while not self.stop_flag.is_set():
+            try:
+                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for bit, name in self.REASONS.items():
+                    if r & bit and bit != 0x1:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.h is not None:
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self.stop_flag.set()
+        if self.thread:
+            self.thread.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+def source_sha(relpath):
+    with open(os.path.join(ROOT, relpath), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel_src, workload_name):
+    """DRAM bytes per launch from a committed ncu summary, if its kernel source is unchanged.
+
+    profiles/*.md lines of the form
+      traffic: <workload> <kernel_src> <source_sha16> <bytes_per_launch>
+    """
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    sha = source_sha(kernel_src)
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith((".md", ".txt")):
+            continue
+        for line in open(os.path.join(pdir, fn), encoding="utf-8"):
+            parts = line.strip().split()
+            if len(parts) == 5 and parts[0] == "traffic:" and parts[1] == workload_name and parts[2] == kernel_src:
+                if parts[3] == sha:
+                    return float(parts[4])
+    return None
+
+
+# ============================================================================ workloads
+
+class DecodeGqa:
+    kind = "decode"
+    kernel_src = "mla_kv_cache_flash_b300/csrc/decode_gqa_bf16.cu"
+
+    def __init__(self, w, device, rank, l2_bytes):
+        import mla_kv_cache_flash_b300 as mk
+        self.mk, self.w, self.device = mk, w, device
+        self.name = w.name
+        self.sets = []
+        first = W.decode_inputs(w, device, seed=w.seed + 1000 * rank)
+        self.lens = first["seq_lens"].cpu().numpy()
+        elt = 2 if w.dtype == "bf16" else 4
+        self.bytes_per_step = int(self.lens.sum()) * 2 * w.n_kv_heads * w.head_dim * elt
+        self.flops_per_step = 4 * w.head_dim * w.n_q_heads * int(self.lens.sum())
+        cache_bytes = first["k_cache"].nbytes * 2
+        n_sets = max(1, math.ceil(4 * l2_bytes / max(cache_bytes, 1)))
+        self.sets.append(first)
+        for i in range(1, n_sets):
+            s = W.decode_inputs(w, device, seed=w.seed + 1000 * rank)
+            self.sets.append(s)
+        self.max_s = int(self.lens.max())
+        self.out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.float32, device=device)
+        code = mk.ATTN_BF16 if w.dtype == "bf16" else mk.ATTN_F32
+        self.n_split = mk.decode_gqa_num_splits(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, self.max_s, code)
+        nb = mk.decode_gqa_workspace_size(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, self.max_s, code)
+        self.ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=device)
+        self.launches_per_step = 1 + (self.n_split > 1)
+        self.l2_note = f"rotating {n_sets} distinct cache sets ({n_sets * cache_bytes / 1e6:.0f} MB, L2 {l2_bytes / 1e6:.0f} MB)"
+
+    def step(self, i):
+        s = self.sets[i % len(self.sets)]
+        self.mk.decode_gqa(s["q"], s["k_cache"], s["v_cache"], s["seq_lens"], out=self.out, scale=self.w.scale,
+                           max_s=self.max_s, workspace=self.ws)
+
+    def host_inputs(self):
+        s = self.sets[0]
+        return {k: s[k].cpu().pin_memory() for k in ("q", "k_cache", "v_cache", "seq_lens")}
+
+    def e2e_step(self, host, dev_bufs, out_host):
+        for k, t in host.items():
+            dev_bufs[k].copy_(t, non_blocking=True)
+        self.mk.decode_gqa(dev_bufs["q"], dev_bufs["k_cache"], dev_bufs["v_cache"], dev_bufs["seq_lens"],
+                           out=self.out, scale=self.w.scale, max_s=self.max_s, workspace=self.ws)
+        out_host.copy_(self.out, non_blocking=True)
+
+    def oracle_units(self):
+        return [(b, j) for b in range(self.w.batch) for j in range(self.w.n_kv_heads)]
+
+    def unit_bytes(self, unit):
+        b, _ = unit
+        elt = 2 if self.w.dtype == "bf16" else 4
+        return int(self.lens[b]) * 2 * self.w.head_dim * elt
+
+    def host_arrays(self):
+        s = self.sets[0]
+        return {"q": s["q"].float().cpu().numpy(), "k": s["k_cache"].float().cpu().numpy(),
+                "v": s["v_cache"].float().cpu().numpy(), "lens": self.lens, "scale": self.w.scale}
+
+    def describe(self):
+        w = self.w
+        return {"workload": w.name, "B": w.batch, "Hq": w.n_q_heads, "Hkv": w.n_kv_heads, "D": w.head_dim,
+                "S_max": w.s_max, "lengths": (f"uniform[{w.length_range[0]},{w.length_range[1]}] seed {w.seed}"
+                                              if w.length_range else f"all {int(self.lens[0])}"),
+                "sum_lengths": int(self.lens.sum()), "n_split": self.n_split, "cache_dtype": w.dtype,
+                "l2": self.l2_note}
+
+
+class DecodeMla(DecodeGqa):
+    kernel_src = "mla_kv_cache_flash_b300/csrc/decode_mla.cu"
+
+    def __init__(self, w, device, rank, l2_bytes):
+        import mla_kv_cache_flash_b300 as mk
+        self.mk, self.w, self.device, self.name = mk, w, device, w.name
+        first = W.mla_inputs(w, device, seed=w.seed + 1000 * rank)
+        self.lens = first["seq_lens"].cpu().numpy()
+        row = (w.kv_lora_rank + w.rope_dim) * 2
+        self.bytes_per_step = int(self.lens.sum()) * row
+        self.flops_per_step = int(self.lens.sum()) * w.n_q_heads * (2 * (w.kv_lora_rank + w.rope_dim)
+                                                                    + 2 * w.kv_lora_rank)
+        cache_bytes = first["c_cache"].nbytes + first["kr_cache"].nbytes
+        n_sets = max(1, math.ceil(4 * l2_bytes / cache_bytes))
+        self.sets = []
+        for i in range(n_sets):
+            s = first if i == 0 else W.mla_inputs(w, device, seed=w.seed + 1000 * rank)
+            s["q_lat"] = torch.einsum("hnr,bhn->bhr", s["w_uk"].float(), s["q_nope"].float()).to(torch.bfloat16).contiguous()
+            self.sets.append(s)
+        self.max_s = int(self.lens.max())
+        self.out = torch.empty((w.batch, w.n_q_heads, w.kv_lora_rank), dtype=torch.float32, device=device)
+        self.n_split = mk.decode_mla_num_splits(w.batch, w.n_q_heads, w.kv_lora_rank, w.rope_dim, self.max_s)
+        nb = mk.decode_mla_workspace_size(w.batch, w.n_q_heads, w.kv_lora_rank, w.rope_dim, self.max_s)
+        self.ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=device)
+        self.launches_per_step = 1 + (self.n_split > 1)
+        self.l2_note = f"rotating {n_sets} distinct latent caches ({n_sets * cache_bytes / 1e6:.0f} MB, L2 {l2_bytes / 1e6:.0f} MB)"
+
+    def step(self, i):
+        s = self.sets[i % len(self.sets)]
+        self.mk.decode_mla_absorbed(s["q_lat"], s["q_rope"], s["c_cache"], s["kr_cache"], s["seq_lens"], self.w.scale,
+                                    out_lat=self.out, max_s=self.max_s, workspace=self.ws)
+
+    def host_inputs(self):
+        s = self.sets[0]
+        return {k: s[k].cpu().pin_memory() for k in ("q_lat", "q_rope", "c_cache", "kr_cache", "seq_lens")}
+
+    def e2e_step(self, host, dev_bufs, out_host):
+        for k, t in host.items():
+            dev_bufs[k].copy_(t, non_blocking=True)
+        d = dev_bufs
+        self.mk.decode_mla_absorbed(d["q_lat"], d["q_rope"], d["c_cache"], d["kr_cache"], d["seq_lens"], self.w.scale,
+                                    out_lat=self.out, max_s=self.max_s, workspace=self.ws)
+        out_host.copy_(self.out, non_blocking=True)
+
+    def oracle_units(self):
+        return [(b, 0) for b in range(self.w.batch)]
+
+    def unit_bytes(self, unit):
+        return int(self.lens[unit[0]]) * (self.w.kv_lora_rank + self.w.rope_dim) * 2
+
+    def host_arrays(self):
+        s = self.sets[0]
+        return {"q_lat": s["q_lat"].float().cpu().numpy(), "q_rope": s["q_rope"].float().cpu().numpy(),
+                "c": s["c_cache"].float().cpu().numpy(), "kr": s["kr_cache"].float().cpu().numpy(),
+                "lens": self.lens, "scale": self.w.scale}
+
+    def describe(self):
+        w = self.w
+        return {"workload": w.name, "B": w.batch, "Hq": w.n_q_heads, "kv_lora_rank": w.kv_lora_rank,
+                "rope_dim": w.rope_dim, "S": int(self.lens[0]), "n_split": self.n_split, "cache_dtype": "bf16",
+                "l2": self.l2_note}
+
+
+class Prefill:
+    kind = "prefill"
+    kernel_src = "mla_kv_cache_flash_b300/csrc/prefill.cu"
+
+    def __init__(self, w, device, rank, l2_bytes):
+        import mla_kv_cache_flash_b300 as mk
+        self.mk, self.w, self.device, self.name = mk, w, device, w.name
+        first = W.prefill_inputs(w, device, seed=w.seed + 1000 * rank)
+        self.lens = first["lengths"]
+        self.flops_per_step = sum(4 * w.head_dim * w.n_q_heads * int(s) * (int(s) + 1) // 2 for s in self.lens)
+        io = first["q"].nbytes + first["k"].nbytes + first["v"].nbytes + first["q"].numel() * 4
+        n_sets = max(1, math.ceil(4 * l2_bytes / io))
+        self.sets = [first] + [W.prefill_inputs(w, device, seed=w.seed + 1000 * rank) for _ in range(n_sets - 1)]
+        self.out = torch.empty((first["q"].shape[0], w.n_q_heads, w.head_dim), dtype=torch.float32, device=device)
+        self.launches_per_step = 1
+        self.bytes_per_step = io
+        self.l2_note = f"rotating {n_sets} input sets ({n_sets * io / 1e6:.0f} MB, L2 {l2_bytes / 1e6:.0f} MB)"
+
+    def step(self, i):
+        s = self.sets[i % len(self.sets)]
+        self.mk.prefill_gqa_causal(s["q"], s["k"], s["v"], s["cu_seqlens"], s["max_seqlen"], out=self.out,
+                                   scale=self.w.scale)
+
+    def describe(self):
+        w = self.w
+        return {"workload": w.name, "B": w.batch, "Hq": w.n_q_heads, "Hkv": w.n_kv_heads, "D": w.head_dim,
+                "lengths": [int(x) for x in self.lens], "causal_flops": self.flops_per_step, "l2": self.l2_note}
+
+
+WORKLOADS = {
+    "minimind_gqa": lambda: (DecodeGqa, W.MINIMIND_GQA),
+    "llama_hkv32": lambda: (DecodeGqa, W.LLAMA3_8B[32]),
+    "llama_hkv8": lambda: (DecodeGqa, W.LLAMA3_8B[8]),
+    "llama_hkv1": lambda: (DecodeGqa, W.LLAMA3_8B[1]),
+    "mla": lambda: (DecodeMla, W.MINIMIND_MLA),
+    "prefill": lambda: (Prefill, W.PREFILL_UNIFORM),
+    "prefill_ragged": lambda: (Prefill, W.PREFILL_RAGGED),
+}
+DEFAULT_STEPS = {"minimind_gqa": 60000, "llama_hkv32": 400, "llama_hkv8": 2000, "llama_hkv1": 10000,
+                 "mla": 40000, "prefill": 2000, "prefill_ragged": 1500}
+
+
+# ============================================================================ timing
+
+def time_device(run, steps, warmup, graph_len, stream):
+    """Device time of `steps` calls of run(i): CUDA graphs of `graph_len` calls replayed back to
+    back (so host launch cost is off the clock), CUDA events on the launching stream."""
+    for i in range(warmup):
+        run(i)
+    torch.cuda.synchronize()
+    graph_len = max(1, min(graph_len, steps))
+    reps, rem = divmod(steps, graph_len)
+    g_full = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_full, stream=stream):
+        for i in range(graph_len):
+            run(i)
+    g_rem = None
+    if rem:
+        g_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_rem, stream=stream):
+            for i in range(rem):
+                run(i)
+    g_full.replay()  # warm the graph itself
+    torch.cuda.synchronize()
+    return reps, g_full, g_rem
+
+
+def timed_region(reps, g_full, g_rem, stream, barrier):
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return start.elapsed_time(end) / 1e3
+
+
+def run_workload(cls, w, device, rank, steps, warmup, l2, stream, barrier, want_e2e):
+    wl = cls(w, device, rank, l2)
+    graph_len = len(getattr(wl, "sets", [0])) * max(1, 256 // max(1, len(getattr(wl, "sets", [0]))))
+    if wl.kind == "prefill":
+        graph_len = min(graph_len, 8)
+    reps, g_full, g_rem = time_device(wl.step, steps, warmup, graph_len, stream)
+    with ClockSampler(device.index) as clk:
+        t = timed_region(reps, g_full, g_rem, stream, barrier)
+    res = {"wl": wl, "seconds": t, "clocks": clk.summary()}
+    del g_full, g_rem
+    if want_e2e and hasattr(wl, "e2e_step"):
+        host = wl.host_inputs()
+        dev_bufs = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+        out_host = torch.empty(wl.out.shape, dtype=wl.out.dtype, pin_memory=True)
+        n_e2e = 20
+        for _ in range(3):
+            wl.e2e_step(host, dev_bufs, out_host)
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        for _ in range(n_e2e):
+            wl.e2e_step(host, dev_bufs, out_host)
+            torch.cuda.current_stream().synchronize()   # the result is read on the host each step
+        end.record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        barrier()
+        res["e2e_seconds"] = wall / n_e2e
+        res["e2e_h2d"] = sum(v.nbytes for v in host.values())
+        res["e2e_d2h"] = out_host.nbytes
+    return res
+
+
+def summarize(res, steps, peaks, peak_src, world):
+    wl = res["wl"]
+    per_step = res["seconds"] / steps
+    if wl.kind == "decode":
+        achieved = wl.bytes_per_step / per_step / 1e9
+        value, unit = achieved * world, "GB/s"
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": profiled_traffic(wl.kernel_src, wl.name),
+                "peak_source": f"{peak_src} HBM copy bandwidth (MEASURED_PEAKS hbm_gbs)",
+                "algorithmic_bytes_per_launch": wl.bytes_per_step,
+                "kernel": "attn_decode_gqa call (split-KV decode kernel + LSE merge when split)"
+                if isinstance(wl, DecodeGqa) and not isinstance(wl, DecodeMla)
+                else "attn_decode_mla_absorbed call (MLA decode kernel + LSE merge when split)",
+                "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)}
+        extra = {"tokens_per_s": round(wl.w.batch * world / per_step, 1),
+                 "pct_of_8tbs": round(100 * achieved / NOMINAL_HBM_GBS, 2)}
+    else:
+        achieved = wl.flops_per_step / per_step / 1e12
+        value, unit = achieved * world, "TFLOP/s"
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": profiled_traffic(wl.kernel_src, wl.name),
+                "peak_source": f"{peak_src} dense bf16 burst (MEASURED_PEAKS bf16_tflops)",
+                "algorithmic_flops_per_launch": wl.flops_per_step, "kernel": "attn_prefill_gqa_causal"}
+        extra = {"tokens_per_s": round(float(np.sum(wl.lens)) * world / per_step, 1)}
+    out = {"value": round(value, 2), "unit": unit, "ms_per_step": round(per_step * 1e3, 5), "roofline": roof,
+           "gpu_launches": steps * wl.launches_per_step, "config": wl.describe(), "clocks": res["clocks"]}
+    out.update(extra)
+    if "e2e_seconds" in res:
+        e = res["e2e_seconds"]
+        ev = (wl.bytes_per_step / e / 1e9) if wl.kind == "decode" else (wl.flops_per_step / e / 1e12)
+        out["e2e"] = {"value": round(ev * world, 3), "unit": unit, "h2d_bytes_per_step": res["e2e_h2d"],
+                      "d2h_bytes_per_step": res["e2e_d2h"], "ms_per_step": round(e * 1e3, 3)}
+    return out
+
+
+# ============================================================================ CPU oracle timing
+
+def _oracle_worker_init(path):
+    global _ARR
+    _ARR = dict(np.load(path, allow_pickle=False))
+
+
+def _oracle_decode_units(units):
+    import oracle
+    a = _ARR
+    done = 0
+    if "q_lat" in a:
+        for b, _ in units:
+            s = int(a["lens"][b])
+            q = np.concatenate([a["q_lat"][b], a["q_rope"][b]], axis=1)
+            k = np.concatenate([a["c"][b, :s], a["kr"][b, :s]], axis=1)
+            oracle.attend(q, k, a["c"][b, :s], float(a["scale"]))
+            done += 1
+        return done
+    g = a["q"].shape[1] // a["k"].shape[2]
+    for b, j in units:
+        s = int(a["lens"][b])
+        oracle.attend(a["q"][b, j * g:(j + 1) * g], a["k"][b, :s, j], a["v"][b, :s, j], float(a["scale"]))
+        done += 1
+    return done
+
+
+def cpu_oracle_rate(wl, budget_s, steps=None, warmup=0):
+    """Time the fp64 oracle on the host cores over a bounded sample of the workload's units.
+    Returns (value in the workload's unit, cores, sample description, seconds per step)."""
+    import multiprocessing as mp
+    import tempfile
+    cores = len(os.sched_getaffinity(0))
+    arrays = wl.host_arrays()
+    tmp = tempfile.NamedTemporaryFile(suffix=".npz", delete=False)
+    np.savez(tmp.name, **{k: np.asarray(v) for k, v in arrays.items()})
+    units = wl.oracle_units()
+    rng = np.random.default_rng(0)
+    order = [units[i] for i in rng.permutation(len(units))]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores, initializer=_oracle_worker_init, initargs=(tmp.name,)) as pool:
+        # calibrate: one unit per worker
+        t0 = time.perf_counter()
+        pool.map(_oracle_decode_units, [[order[i % len(order)]] for i in range(cores)])
+        per_unit = max((time.perf_counter() - t0) / 1.0, 1e-6)  # wall for `cores` units in parallel
+        if steps is None:
+            n_units = max(cores, int(budget_s / per_unit * cores))
+            sample = [order[i % len(order)] for i in range(n_units)]
+            chunks = [sample[i::cores] for i in range(cores)]
+            t0 = time.perf_counter()
+            pool.map(_oracle_decode_units, chunks)
+            wall = time.perf_counter() - t0
+            nbytes = sum(wl.unit_bytes(u) for u in sample)
+            os.unlink(tmp.name)
+            return nbytes / wall / 1e9, cores, f"{n_units} (sequence, kv-head) units of the workload " \
+                f"({n_units / len(units):.2f} passes over its {len(units)} units), fp64 oracle.attend", None
+        # reference arm: `steps` timed steps, each a bounded sample sized to the budget
+        per_step_budget = budget_s / max(1, steps + warmup)
+        n_units = max(1, int(per_step_budget / per_unit * cores))
+        n_units = min(n_units, len(order))
+        workers = min(cores, n_units)
+        cursor = 0
+
+        def one_step():
+            nonlocal cursor
+            sample = [order[(cursor + i) % len(order)] for i in range(n_units)]
+            cursor += n_units
+            if workers == 1:
+                _oracle_worker_init(tmp.name) if "_ARR" not in globals() else None
+                _oracle_decode_units(sample)
+            else:
+                pool.map(_oracle_decode_units, [sample[i::workers] for i in range(workers)])
+            return sum(wl.unit_bytes(u) for u in sample)
+
+        for _ in range(warmup):
+            one_step()
+        t0 = time.perf_counter()
+        nbytes = 0
+        for _ in range(steps):
+            nbytes += one_step()
+        wall = time.perf_counter() - t0
+    os.unlink(tmp.name)
+    return nbytes / wall / 1e9, workers, f"each step {n_units} of the workload's {len(units)} " \
+        f"(sequence, kv-head) units, fp64 oracle.attend", wall / steps
+
+
+# ============================================================================ main
+
+def main():
+    ap = argparse.ArgumentParser(description="KV-cache attention benchmark (one JSON line)")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="minimind_gqa")
+    ap.add_argument("--no-also", action="store_true", help="time only the headline workload")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.gpus != world:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch N>1 with torchrun")
+    steps = args.steps or DEFAULT_STEPS[args.workload]
+    peaks, peak_src = load_peaks()
+    cls, w = WORKLOADS[args.workload]()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        wl = cls(w, torch.device("cpu"), 0, 0) if False else None
+        # the oracle arm runs on the host only; inputs are generated on the CPU
+        wl = _cpu_workload(cls, w)
+        value, cores, sample, per_step = cpu_oracle_rate(wl, budget_s=120.0, steps=steps, warmup=args.warmup)
+        line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+                "steps": steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": wl.describe(),
+                "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        barrier = lambda: dist.barrier(device_ids=[local])  # noqa: E731
+    else:
+        barrier = lambda: None  # noqa: E731
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    import mla_kv_cache_flash_b300 as mk
+    mk.lib()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    stream = torch.cuda.Stream(device)
+
+    with torch.cuda.stream(stream):
+        res = run_workload(cls, w, device, rank, steps, args.warmup, l2, stream, barrier, want_e2e=True)
+    secs = torch.tensor([res["seconds"], res.get("e2e_seconds", 0.0)], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(secs, op=dist.ReduceOp.MAX)
+    res["seconds"], res["e2e_seconds"] = float(secs[0]), float(secs[1])
+    head = summarize(res, steps, peaks, peak_src, world)
+
+    also = []
+    if not args.no_also and world == 1:
+        for name in ("llama_hkv32", "llama_hkv8", "llama_hkv1", "mla", "prefill", "prefill_ragged"):
+            if name == args.workload:
+                continue
+            c2, w2 = WORKLOADS[name]()
+            try:
+                with torch.cuda.stream(stream):
+                    r2 = run_workload(c2, w2, device, rank, max(3, DEFAULT_STEPS[name] // 4), 3, l2, stream,
+                                      barrier, want_e2e=False)
+                s2 = summarize(r2, max(3, DEFAULT_STEPS[name] // 4), peaks, peak_src, 1)
+                also.append({"workload": w2.name, "value": s2["value"], "unit": s2["unit"],
+                             "ms_per_step": s2["ms_per_step"], "roofline": s2["roofline"],
+                             "tokens_per_s": s2.get("tokens_per_s"), "clocks": s2["clocks"],
+                             "config": s2["config"]})
+                del r2
+            except mk.MlakvError as e:
+                also.append({"workload": w2.name, "error": str(e)})
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        value, cores, sample, _ = cpu_oracle_rate(res["wl"], args.cpu_seconds)
+        cpu = {"value": round(value, 4), "unit": head["unit"], "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world, "steps": steps,
+                "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": dict(head["config"], parallelism=f"replicas x{world} (independent sequences per GPU)"),
+                "tokens_per_s": head.get("tokens_per_s"), "pct_of_8tbs": head.get("pct_of_8tbs"),
+                "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": head.get("e2e"),
+                "gpu_launches": head["gpu_launches"], "clocks": head["clocks"], "also": also}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def _cpu_workload(cls, w):
+    """Inputs for the oracle arm, generated on the host with the same recipe."""
+    class HostOnly(cls):
+        def __init__(self, w):
+            self.w, self.name = w, w.name
+            if cls is DecodeMla:
+                s = W.mla_inputs(w, "cpu")
+                s["q_lat"] = torch.einsum("hnr,bhn->bhr", s["w_uk"].float(), s["q_nope"].float()).to(torch.bfloat16).contiguous()
+            else:
+                s = W.decode_inputs(w, "cpu")
+            self.sets = [s]
+            self.lens = s["seq_lens"].numpy()
+            self.n_split = None
+            self.l2_note = "host memory"
+    if cls is Prefill:
+        raise SystemExit("the oracle arm covers the decode workloads")
+    return HostOnly(w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,170 @@
+/*
+ * mlakv.h — C ABI of the KV-cache attention library (libmlakv.so), sm_103a.
+ *
+ * The library computes softmax(q·Kᵀ·scale)·V for new query tokens over a KV cache whose
+ * KV heads are each shared by a group of query heads (GQA; MHA and MQA are its two ends),
+ * causal GQA prefill over packed sequences, and MLA decode over a low-rank latent cache
+ * with a decoupled RoPE key, with W_UK absorbed into the query.
+ *
+ * Sources, by page title and section:
+ *   [MQA&GQA]  "模型架构｜MQA & GQA 调研" (lichtung612 blog): section "Grouped-query attention"
+ *              (GQA-G, GQA-1 = MQA, GQA-H = MHA) and section "代码" (repeat_kv, and
+ *              Attention.forward: cache layout (max_batch, max_seq, n_kv_heads, head_dim),
+ *              cache write before read, scores/√d + mask, fp32 softmax, ·V).
+ *   [EBOOK]    "MHA, MQA và GQA" (coregenaihub ebook): the KV-group count must divide the
+ *              Q-head count; the sim rejects other counts rather than rounding.
+ *   [MLA]      qqstock article on DeepSeek MLA: sections 1-3 (latent c, weight absorption,
+ *              decoupled RoPE key shared by all heads), section 6 (MLA computes like MQA,
+ *              V shares c with the un-RoPE'd K) and its MultiHeadLatentAttention code.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE memory owned by the caller, dense (C-contiguous) in
+ *     the layout stated, 16-byte aligned. The library never allocates, frees or
+ *     synchronises inside a compute call: it validates the host-side arguments, enqueues
+ *     its kernels on `stream` and returns. Results are ready when the stream reaches them.
+ *   - Query head h uses KV head h / (Hq/Hkv) (contiguous groups, the order repeat_kv's
+ *     expand-then-reshape produces) [MQA&GQA, 代码].
+ *   - Outputs and accumulators are fp32. bf16 inputs are widened exactly.
+ *   - Errors found on the host return a negative status before anything is launched;
+ *     the message is available from attn_last_error() on the same thread. Device-side data
+ *     (seq_lens, cu_seqlens) are trusted to lie within the bounds stated.
+ *   - Calls are reentrant. A workspace must not be shared by two calls that can run at
+ *     the same time (different streams); calls on one stream are ordered by the stream.
+ */
+#ifndef MLAKV_H
+#define MLAKV_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st *mlakv_stream_t;
+
+/* Status codes. 0 = success; negative = error, nothing was launched (except ATTN_ERR_CUDA
+ * when the launch itself failed, and ATTN_ERR_TIMEOUT, reported after the fact). */
+enum {
+    ATTN_OK = 0,
+    ATTN_ERR_NULL = -1,        /* a required pointer is NULL */
+    ATTN_ERR_SHAPE = -2,       /* a size < 1 (or < 0 where 0 is allowed), or Hq % Hkv != 0 [EBOOK] */
+    ATTN_ERR_UNSUPPORTED = -3, /* head width / rank / dtype / alignment not built in */
+    ATTN_ERR_WORKSPACE = -4,   /* workspace NULL or smaller than the *_workspace_size query */
+    ATTN_ERR_CUDA = -5,        /* a CUDA call or kernel launch failed (see attn_last_error) */
+    ATTN_ERR_TIMEOUT = -6      /* a kernel's bounded wait gave up (from attn_check_status) */
+};
+
+/* Element type of q and of the cache for attn_decode_gqa. */
+typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
+
+/* ---------------------------------------------------------------------------------------
+ * GQA / MHA / MQA decode: one new query token per sequence over its cache.
+ * [MQA&GQA] Attention.forward with seqlen = 1 and no mask: the new token's K/V are already
+ * in the cache, so sequence b attends cache positions 0 .. seq_lens[b]-1.
+ *
+ *   q        [B, Hq, D]            dtype
+ *   k_cache  [B, S_max, Hkv, D]    dtype  (the page's cache_k layout)
+ *   v_cache  [B, S_max, Hkv, D]    dtype
+ *   seq_lens [B] int32, 0 <= seq_lens[b] <= max_S <= S_max. seq_lens[b] = 0 gives out = 0.
+ *   out      [B, Hq, D] fp32, fully written.
+ *   scale    multiplies q·k before the softmax (1/sqrt(D) for the page's forward).
+ *   S_max    cache capacity (the row stride of the cache, in tokens).
+ *   max_S    host-known upper bound on seq_lens; sizes the split-KV plan. Passing S_max is
+ *            always valid.
+ *   n_split  number of pieces each sequence's cache is cut into (each piece is processed by
+ *            its own thread block and the pieces are merged by log-sum-exp); 0 lets the
+ *            library choose from B, Hkv, max_S and the device's SM count.
+ *   D        64, 96 or 128. Any Hq/Hkv with Hq % Hkv == 0 and Hq/Hkv <= 128.
+ *   workspace, ws_bytes: scratch for the split partials, at least
+ *            attn_decode_gqa_workspace_size(...) bytes with the same arguments; may be
+ *            NULL when that size is 0.
+ * Returns ATTN_OK or an error code.
+ * ------------------------------------------------------------------------------------- */
+size_t attn_decode_gqa_workspace_size(int B, int Hq, int Hkv, int D, int max_S,
+                                      attn_dtype dtype, int n_split);
+
+/* The split count attn_decode_gqa uses for these arguments (n_split = 0 resolved). */
+int attn_decode_gqa_num_splits(int B, int Hq, int Hkv, int D, int max_S, attn_dtype dtype,
+                               int n_split);
+
+int attn_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
+                    const int *seq_lens, float *out,
+                    int B, int Hq, int Hkv, int D, float scale,
+                    int S_max, int max_S, attn_dtype dtype, int n_split,
+                    void *workspace, size_t ws_bytes, mlakv_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * MLA decode with W_UK absorbed [MLA sections 2, 3, 6]: every head attends the same cached
+ * latent row [c_t ‖ kr_t] and averages c_t itself:
+ *   s_t = scale·(q_lat[b,h]·c_t + q_rope[b,h]·kr_t),  out_lat[b,h] = Σ_t softmax(s)_t c_t.
+ * The caller forms q_lat[b,h] = W_UK[h]ᵀ q_nope[b,h] before the call and applies W_UV[h]
+ * to out_lat after it.
+ *
+ *   q_lat       [B, Hq, r]      bf16
+ *   q_rope      [B, Hq, dr]     bf16 (RoPE already applied)
+ *   c_cache     [B, S_max, r]   bf16
+ *   krope_cache [B, S_max, dr]  bf16 (RoPE already applied; one head shared by all)
+ *   seq_lens    [B] int32, 0 <= seq_lens[b] <= max_S <= S_max; 0 gives out_lat = 0.
+ *   out_lat     [B, Hq, r] fp32, fully written.
+ *   scale       1/sqrt(d_nope + dr) for the article's recombined query.
+ *   r = 128, dr = 48 are built in; Hq a multiple of 16 up to 128.
+ *   n_split, max_S, workspace: as for attn_decode_gqa.
+ * ------------------------------------------------------------------------------------- */
+size_t attn_decode_mla_workspace_size(int B, int Hq, int r, int dr, int max_S, int n_split);
+int attn_decode_mla_num_splits(int B, int Hq, int r, int dr, int max_S, int n_split);
+
+int attn_decode_mla_absorbed(const void *q_lat, const void *q_rope, const void *c_cache,
+                             const void *krope_cache, const int *seq_lens, float *out_lat,
+                             int B, int Hq, int r, int dr, float scale,
+                             int S_max, int max_S, int n_split,
+                             void *workspace, size_t ws_bytes, mlakv_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Causal GQA prefill over packed variable-length sequences [MQA&GQA, Attention.forward
+ * with the causal mask; MLA code's is_causal=True]: row i of sequence b attends keys
+ * 0 .. i of the same sequence.
+ *
+ *   q          [T, Hq, D]  bf16, T = cu_seqlens[B]
+ *   k, v       [T, Hkv, D] bf16 (each sequence's own keys/values)
+ *   cu_seqlens [B+1] int32 on the device: 0, then running sums of the lengths.
+ *   out        [T, Hq, D] fp32, every row written.
+ *   max_seqlen   host-known upper bound on the lengths (sizes the grid), >= 0.
+ *   total_tokens T, the row count of q/k/v/out (bounds the tensor maps), >= 0.
+ *   D = 128. Hq % Hkv == 0. max_seqlen = 0 or T = 0 launches nothing.
+ * ------------------------------------------------------------------------------------- */
+int attn_prefill_gqa_causal(const void *q, const void *k, const void *v,
+                            const int *cu_seqlens, float *out,
+                            int B, int Hq, int Hkv, int D, float scale, int max_seqlen,
+                            int total_tokens, mlakv_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Log-sum-exp merge of split partials (the combine step of split-KV decode):
+ *   out[row] = Σ_i e^{lse[row,i] − M} o[row,i,:] / Σ_i e^{lse[row,i] − M},  M = max_i lse[row,i]
+ * where o[row,i,:] is piece i's normalised output and lse[row,i] = ln Σ_t e^{s_t} over the
+ * piece (−inf for an empty piece). A row whose pieces are all empty gives 0.
+ *
+ *   o_part   [rows, n_split, Dv] fp32
+ *   lse_part [rows, n_split] fp32
+ *   out      [rows, Dv] fp32
+ *   1 <= n_split <= 256, Dv a multiple of 4 up to 512.
+ * ------------------------------------------------------------------------------------- */
+int attn_merge_partials(const float *o_part, const float *lse_part, float *out,
+                        int rows, int n_split, int Dv, mlakv_stream_t stream);
+
+/* Message for the last non-zero status returned on this thread ("" if none). */
+const char *attn_last_error(void);
+
+/* Synchronises `stream`, then reads and clears the library's device-side error flags on
+ * the current device. Returns ATTN_OK, ATTN_ERR_TIMEOUT if a kernel gave up a bounded
+ * wait since the last check, or ATTN_ERR_CUDA if the stream reported an error. */
+int attn_check_status(mlakv_stream_t stream);
+
+/* Library version string. */
+const char *attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLAKV_H */

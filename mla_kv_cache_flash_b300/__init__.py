@@ -1,0 +1,258 @@
+"""Python binding of libmlakv.so: KV-cache attention kernels for sm_103a.
+
+Argument marshalling only. Each function checks the tensors' dtype, shape, device and
+contiguity, allocates outputs/workspace with torch (so torch's caching allocator owns all
+memory), and passes raw device pointers plus ``torch.cuda.current_stream()`` to the C ABI
+declared in ``include/mlakv.h``. Every step of the computation runs in the library's CUDA
+kernels; there is no host or PyTorch fallback. If the library is missing, or a call
+returns an error, a ``RuntimeError`` carrying the library's message is raised.
+
+Entry points (same names as the C ABI, without the ``attn_`` prefix):
+  decode_gqa            GQA/MHA/MQA decode over a padded [B, S_max, Hkv, D] cache
+  decode_mla_absorbed   MLA decode over the latent cache [c ‖ kr], W_UK absorbed in q_lat
+  prefill_gqa_causal    causal GQA prefill over packed sequences (cu_seqlens)
+  merge_partials        log-sum-exp merge of split partials
+"""
+
+import ctypes
+import math
+import os
+
+import torch
+
+__all__ = [
+    "ATTN_F32", "ATTN_BF16", "MlakvError", "lib", "lib_path", "decode_gqa", "decode_gqa_workspace_size",
+    "decode_gqa_num_splits", "decode_mla_absorbed", "decode_mla_workspace_size", "decode_mla_num_splits",
+    "prefill_gqa_causal", "merge_partials", "check_status", "last_error", "version",
+]
+
+ATTN_F32 = 0
+ATTN_BF16 = 1
+_STATUS = {0: "ATTN_OK", -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_SHAPE", -3: "ATTN_ERR_UNSUPPORTED",
+           -4: "ATTN_ERR_WORKSPACE", -5: "ATTN_ERR_CUDA", -6: "ATTN_ERR_TIMEOUT"}
+
+lib_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmlakv.so")
+_lib = None
+
+
+class MlakvError(RuntimeError):
+    def __init__(self, code, message):
+        super().__init__(f"{_STATUS.get(code, code)}: {message}")
+        self.code = code
+
+
+_c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
+
+_SIGNATURES = {
+    "attn_decode_gqa_workspace_size": (_c_size, [_c_int] * 6 + [_c_int]),
+    "attn_decode_gqa_num_splits": (_c_int, [_c_int] * 7),
+    "attn_decode_gqa": (_c_int, [_vp] * 5 + [_c_int] * 4 + [_c_float] + [_c_int] * 4 + [_vp, _c_size, _vp]),
+    "attn_decode_mla_workspace_size": (_c_size, [_c_int] * 6),
+    "attn_decode_mla_num_splits": (_c_int, [_c_int] * 6),
+    "attn_decode_mla_absorbed": (_c_int, [_vp] * 6 + [_c_int] * 4 + [_c_float] + [_c_int] * 3 + [_vp, _c_size, _vp]),
+    "attn_prefill_gqa_causal": (_c_int, [_vp] * 5 + [_c_int] * 4 + [_c_float] + [_c_int] * 2 + [_vp]),
+    "attn_merge_partials": (_c_int, [_vp] * 3 + [_c_int] * 3 + [_vp]),
+    "attn_last_error": (ctypes.c_char_p, []),
+    "attn_check_status": (_c_int, [_vp]),
+    "attn_version": (ctypes.c_char_p, []),
+}
+
+
+def lib():
+    """The loaded library (loaded on first use; raises if it was never built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(lib_path):
+            raise RuntimeError(
+                f"{lib_path} is missing: build it with `python -m mla_kv_cache_flash_b300.build` "
+                "(there is no fallback implementation)")
+        handle = ctypes.CDLL(lib_path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def last_error():
+    return lib().attn_last_error().decode()
+
+
+def version():
+    return lib().attn_version().decode()
+
+
+def _check(rc):
+    if rc != 0:
+        raise MlakvError(rc, last_error())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _need(t, name, dtype, ndim, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def check_status():
+    """Synchronise the current stream and raise if a kernel reported a device-side error."""
+    _check(lib().attn_check_status(_stream()))
+
+
+# ----------------------------------------------------------------------------- GQA decode
+
+def decode_gqa_workspace_size(B, Hq, Hkv, D, max_s, dtype, n_split=0):
+    return int(lib().attn_decode_gqa_workspace_size(B, Hq, Hkv, D, max_s, dtype, n_split))
+
+
+def decode_gqa_num_splits(B, Hq, Hkv, D, max_s, dtype, n_split=0):
+    n = lib().attn_decode_gqa_num_splits(B, Hq, Hkv, D, max_s, dtype, n_split)
+    _check(min(n, 0))
+    return n
+
+
+def decode_gqa(q, k_cache, v_cache, seq_lens, out=None, scale=None, max_s=None, n_split=0, workspace=None):
+    """out[b, h] = softmax(scale · q[b, h] · K[b, :S_b, h // G]ᵀ) · V[b, :S_b, h // G].
+
+    q [B, Hq, D]; k_cache, v_cache [B, S_max, Hkv, D] (fp32 or bf16, same dtype as q);
+    seq_lens [B] int32 on the device; returns out [B, Hq, D] fp32. ``max_s`` is a host-known
+    bound on seq_lens (defaults to S_max); ``n_split`` = 0 lets the library choose.
+    """
+    dt = q.dtype
+    if dt not in (torch.float32, torch.bfloat16):
+        raise TypeError("q must be float32 or bfloat16")
+    _need(q, "q", dt, 3)
+    dev = q.device
+    _need(k_cache, "k_cache", dt, 4, dev)
+    _need(v_cache, "v_cache", dt, 4, dev)
+    _need(seq_lens, "seq_lens", torch.int32, 1, dev)
+    B, Hq, D = q.shape
+    _, S_max, Hkv, Dk = k_cache.shape
+    if k_cache.shape[0] != B or Dk != D or v_cache.shape != k_cache.shape or seq_lens.shape[0] != B:
+        raise ValueError("inconsistent shapes for q, k_cache, v_cache, seq_lens")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    max_s = S_max if max_s is None else int(max_s)
+    code = ATTN_F32 if dt == torch.float32 else ATTN_BF16
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    else:
+        _need(out, "out", torch.float32, 3, dev)
+    need = decode_gqa_workspace_size(B, Hq, Hkv, D, max_s, code, n_split)
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _check(lib().attn_decode_gqa(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(out),
+                                 B, Hq, Hkv, D, scale, S_max, max_s, code, n_split,
+                                 _ptr(workspace), ws_bytes, _stream()))
+    return out
+
+
+# ----------------------------------------------------------------------------- MLA decode
+
+def decode_mla_workspace_size(B, Hq, r, dr, max_s, n_split=0):
+    return int(lib().attn_decode_mla_workspace_size(B, Hq, r, dr, max_s, n_split))
+
+
+def decode_mla_num_splits(B, Hq, r, dr, max_s, n_split=0):
+    n = lib().attn_decode_mla_num_splits(B, Hq, r, dr, max_s, n_split)
+    _check(min(n, 0))
+    return n
+
+
+def decode_mla_absorbed(q_lat, q_rope, c_cache, krope_cache, seq_lens, scale, out_lat=None, max_s=None,
+                        n_split=0, workspace=None):
+    """out_lat[b, h] = Σ_t softmax_t(scale·(q_lat·c_t + q_rope·kr_t)) · c_t (bf16 in, fp32 out).
+
+    q_lat [B, Hq, r], q_rope [B, Hq, dr], c_cache [B, S_max, r], krope_cache [B, S_max, dr],
+    seq_lens [B] int32. The caller absorbs W_UK into q_lat and applies W_UV to out_lat.
+    """
+    bf = torch.bfloat16
+    _need(q_lat, "q_lat", bf, 3)
+    dev = q_lat.device
+    _need(q_rope, "q_rope", bf, 3, dev)
+    _need(c_cache, "c_cache", bf, 3, dev)
+    _need(krope_cache, "krope_cache", bf, 3, dev)
+    _need(seq_lens, "seq_lens", torch.int32, 1, dev)
+    B, Hq, r = q_lat.shape
+    dr = q_rope.shape[2]
+    S_max = c_cache.shape[1]
+    if (q_rope.shape[:2] != (B, Hq) or c_cache.shape != (B, S_max, r) or krope_cache.shape != (B, S_max, dr)
+            or seq_lens.shape[0] != B):
+        raise ValueError("inconsistent shapes for q_lat, q_rope, c_cache, krope_cache, seq_lens")
+    max_s = S_max if max_s is None else int(max_s)
+    if out_lat is None:
+        out_lat = torch.empty((B, Hq, r), dtype=torch.float32, device=dev)
+    else:
+        _need(out_lat, "out_lat", torch.float32, 3, dev)
+    need = decode_mla_workspace_size(B, Hq, r, dr, max_s, n_split)
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _check(lib().attn_decode_mla_absorbed(_ptr(q_lat), _ptr(q_rope), _ptr(c_cache), _ptr(krope_cache),
+                                          _ptr(seq_lens), _ptr(out_lat), B, Hq, r, dr, float(scale), S_max,
+                                          max_s, n_split, _ptr(workspace), ws_bytes, _stream()))
+    return out_lat
+
+
+# ----------------------------------------------------------------------------- prefill
+
+def prefill_gqa_causal(q, k, v, cu_seqlens, max_seqlen, out=None, scale=None):
+    """Causal GQA attention of packed sequences over themselves (bf16 in, fp32 out).
+
+    q [T, Hq, D], k/v [T, Hkv, D], cu_seqlens [B+1] int32 on the device, ``max_seqlen`` a
+    host-known bound on the lengths. Returns out [T, Hq, D] fp32.
+    """
+    bf = torch.bfloat16
+    _need(q, "q", bf, 3)
+    dev = q.device
+    _need(k, "k", bf, 3, dev)
+    _need(v, "v", bf, 3, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1, dev)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (T, Hkv, D) or v.shape != k.shape:
+        raise ValueError("inconsistent shapes for q, k, v")
+    B = cu_seqlens.shape[0] - 1
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=torch.float32, device=dev)
+    else:
+        _need(out, "out", torch.float32, 3, dev)
+    _check(lib().attn_prefill_gqa_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(out),
+                                         B, Hq, Hkv, D, scale, int(max_seqlen), T, _stream()))
+    return out
+
+
+# ----------------------------------------------------------------------------- merge
+
+def merge_partials(o_part, lse_part, out=None):
+    """out[row] = Σ_i e^{lse_i − M} o_i / Σ_i e^{lse_i − M}; o_part [rows, n, Dv], lse_part [rows, n]."""
+    _need(o_part, "o_part", torch.float32, 3)
+    dev = o_part.device
+    _need(lse_part, "lse_part", torch.float32, 2, dev)
+    rows, n, dv = o_part.shape
+    if lse_part.shape != (rows, n):
+        raise ValueError("lse_part must be [rows, n_split]")
+    if out is None:
+        out = torch.empty((rows, dv), dtype=torch.float32, device=dev)
+    else:
+        _need(out, "out", torch.float32, 2, dev)
+    _check(lib().attn_merge_partials(_ptr(o_part), _ptr(lse_part), _ptr(out), rows, n, dv, _stream()))
+    return out

@@ -1,0 +1,318 @@
+// The library's C ABI (declared in include/mlakv.h): host-side validation, the split-KV
+// plan, workspace carving and kernel dispatch. Nothing here allocates device memory or
+// synchronises, except attn_check_status, whose job is to synchronise.
+#include "../../include/mlakv.h"
+#include "common.cuh"
+
+#include <math.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#define MLAKV_API extern "C" __attribute__((visibility("default")))
+
+namespace mlakv {
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int ok() {
+    g_err[0] = '\0';
+    return ATTN_OK;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(ATTN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// SM count of the current device. The split plan must be the same for the workspace query
+// and the launch; both run on the caller's current device. Without a device (a host with
+// no GPU) the plan is made for a 148-SM part.
+int device_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 148;
+    }
+    return n;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct SplitPlan {
+    int n_split;
+    int split_len;
+};
+
+// Cut [0, max_S) into n_split pieces of split_len tokens (a multiple of `tile`). With
+// n_split = 0 the count is chosen so that blocks_per_split · n_split covers about
+// `waves` blocks per SM, without making a piece shorter than `min_tiles` tiles.
+SplitPlan plan_splits(int max_S, int tile, long blocks_per_split, int n_split_req, int min_tiles) {
+    SplitPlan p{1, tile};
+    const int max_tiles = max_S > 0 ? (max_S + tile - 1) / tile : 1;
+    int n;
+    if (n_split_req > 0) {
+        n = n_split_req;
+    } else {
+        const long target = 2L * device_sms();
+        n = (int)((target + blocks_per_split - 1) / blocks_per_split);
+        const int cap = max_tiles / (min_tiles > 0 ? min_tiles : 1);
+        if (n > cap) n = cap;
+        if (n > 64) n = 64;
+        if (n < 1) n = 1;
+    }
+    if (n > max_tiles) n = max_tiles;
+    const int tiles_per = (max_tiles + n - 1) / n;
+    p.split_len = tiles_per * tile;
+    p.n_split = max_S > 0 ? (max_S + p.split_len - 1) / p.split_len : 1;
+    if (n_split_req > 0 && p.n_split < n_split_req) {
+        // an explicit request is honoured exactly; trailing pieces are then empty
+        p.n_split = n_split_req;
+    }
+    return p;
+}
+
+// ---------------------------------------------------------------- GQA decode plan
+
+constexpr int kFmaTile = 128;
+
+bool gqa_use_fma(attn_dtype dtype) { return dtype == ATTN_F32; }
+
+SplitPlan gqa_plan(int B, int Hq, int Hkv, int D, int max_S, attn_dtype dtype, int n_split) {
+    const int G = Hq / Hkv;
+    if (gqa_use_fma(dtype)) {
+        const int hb = (G % 8 == 0) ? 8 : (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
+        return plan_splits(max_S, kFmaTile, (long)B * Hkv * (G / hb), n_split, 2);
+    }
+    const int tile = decode_gqa_bf16_tile_tokens(D, G);
+    const int heads_per_block = G < 16 ? G : 16;
+    const long blocks = (long)B * Hkv * ((G + heads_per_block - 1) / heads_per_block);
+    return plan_splits(max_S, tile, blocks, n_split, 4);
+}
+
+size_t partials_bytes(int B, int Hq, int Dv, int n_split) {
+    if (n_split <= 1) return 0;
+    const size_t rows = (size_t)B * Hq;
+    return align_up(rows * n_split * Dv * sizeof(float), 256) + align_up(rows * n_split * sizeof(float), 256);
+}
+
+int check_gqa_shapes(int B, int Hq, int Hkv, int D, int S_max, int max_S, attn_dtype dtype, int n_split) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || S_max < 1)
+        return fail(ATTN_ERR_SHAPE, "B, Hq, Hkv and S_max must be >= 1 (got B=%d Hq=%d Hkv=%d S_max=%d)",
+                    B, Hq, Hkv, S_max);
+    if (Hq % Hkv != 0)
+        return fail(ATTN_ERR_SHAPE, "Hkv=%d does not divide Hq=%d: every KV group needs the same whole "
+                    "number of query heads", Hkv, Hq);
+    if (max_S < 0 || max_S > S_max)
+        return fail(ATTN_ERR_SHAPE, "max_S=%d must lie in [0, S_max=%d]", max_S, S_max);
+    if (n_split < 0 || n_split > 256)
+        return fail(ATTN_ERR_SHAPE, "n_split=%d must lie in [0, 256]", n_split);
+    if (D != 64 && D != 96 && D != 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "head width D=%d not built (64, 96, 128)", D);
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16)
+        return fail(ATTN_ERR_UNSUPPORTED, "dtype %d not built (ATTN_F32, ATTN_BF16)", (int)dtype);
+    if (Hq / Hkv > 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "group size Hq/Hkv=%d above 128", Hq / Hkv);
+    return ATTN_OK;
+}
+
+// ---------------------------------------------------------------- MLA decode plan
+
+constexpr int kMlaRank = 128;
+constexpr int kMlaRope = 48;
+constexpr int kMlaHeadsPerBlock = 16;
+
+int check_mla_shapes(int B, int Hq, int r, int dr, int S_max, int max_S, int n_split) {
+    if (B < 1 || Hq < 1 || S_max < 1)
+        return fail(ATTN_ERR_SHAPE, "B, Hq and S_max must be >= 1 (got B=%d Hq=%d S_max=%d)", B, Hq, S_max);
+    if (max_S < 0 || max_S > S_max)
+        return fail(ATTN_ERR_SHAPE, "max_S=%d must lie in [0, S_max=%d]", max_S, S_max);
+    if (n_split < 0 || n_split > 256)
+        return fail(ATTN_ERR_SHAPE, "n_split=%d must lie in [0, 256]", n_split);
+    if (r != kMlaRank || dr != kMlaRope)
+        return fail(ATTN_ERR_UNSUPPORTED, "MLA rank r=%d, rope width dr=%d not built (r=128, dr=48)", r, dr);
+    if (Hq % kMlaHeadsPerBlock != 0 || Hq > 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "MLA head count Hq=%d must be a multiple of 16 up to 128", Hq);
+    return ATTN_OK;
+}
+
+SplitPlan mla_plan(int B, int Hq, int max_S, int n_split) {
+    return plan_splits(max_S, decode_mla_tile_tokens(), (long)B * (Hq / kMlaHeadsPerBlock), n_split, 4);
+}
+
+}  // namespace
+}  // namespace mlakv
+
+using namespace mlakv;
+
+MLAKV_API const char *attn_last_error(void) { return g_err; }
+
+MLAKV_API const char *attn_version(void) { return "mlakv 0.1.0 (sm_103a)"; }
+
+// ======================================================================== GQA decode
+
+MLAKV_API int attn_decode_gqa_num_splits(int B, int Hq, int Hkv, int D, int max_S, attn_dtype dtype,
+                                         int n_split) {
+    const int rc = check_gqa_shapes(B, Hq, Hkv, D, max_S > 0 ? max_S : 1, max_S, dtype, n_split);
+    if (rc != ATTN_OK) return rc;
+    return gqa_plan(B, Hq, Hkv, D, max_S, dtype, n_split).n_split;
+}
+
+MLAKV_API size_t attn_decode_gqa_workspace_size(int B, int Hq, int Hkv, int D, int max_S, attn_dtype dtype,
+                                                int n_split) {
+    if (check_gqa_shapes(B, Hq, Hkv, D, max_S > 0 ? max_S : 1, max_S, dtype, n_split) != ATTN_OK) return 0;
+    const SplitPlan p = gqa_plan(B, Hq, Hkv, D, max_S, dtype, n_split);
+    return partials_bytes(B, Hq, D, p.n_split);
+}
+
+MLAKV_API int attn_decode_gqa(const void *q, const void *k_cache, const void *v_cache, const int *seq_lens,
+                              float *out, int B, int Hq, int Hkv, int D, float scale, int S_max, int max_S,
+                              attn_dtype dtype, int n_split, void *workspace, size_t ws_bytes,
+                              mlakv_stream_t stream) {
+    if (!q || !k_cache || !v_cache || !seq_lens || !out)
+        return fail(ATTN_ERR_NULL, "attn_decode_gqa: q, k_cache, v_cache, seq_lens and out must be non-NULL");
+    int rc = check_gqa_shapes(B, Hq, Hkv, D, S_max, max_S, dtype, n_split);
+    if (rc != ATTN_OK) return rc;
+    if (!isfinite(scale)) return fail(ATTN_ERR_SHAPE, "scale must be finite");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(seq_lens))
+        return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_gqa: every pointer must be 16-byte aligned");
+    const SplitPlan p = gqa_plan(B, Hq, Hkv, D, max_S, dtype, n_split);
+    const size_t need = partials_bytes(B, Hq, D, p.n_split);
+    if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
+        return fail(ATTN_ERR_WORKSPACE, "attn_decode_gqa: workspace of %zu bytes (16-byte aligned) needed, "
+                    "got %zu at %p", need, workspace ? ws_bytes : (size_t)0, workspace);
+
+    DecodeGqaArgs a{};
+    a.q = q; a.k = k_cache; a.v = v_cache; a.seq_lens = seq_lens; a.out = out;
+    a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.D = D;
+    a.scale_log2 = scale * kLog2e;
+    a.S_max = S_max;
+    a.n_split = p.n_split;
+    a.split_len = p.split_len;
+    if (p.n_split > 1) {
+        const size_t rows = (size_t)B * Hq;
+        a.o_part = static_cast<float *>(workspace);
+        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                               align_up(rows * p.n_split * D * sizeof(float), 256));
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = gqa_use_fma(dtype) ? launch_decode_gqa_f32(a, s) : launch_decode_gqa_bf16(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_decode_gqa: decode kernel launch");
+    if (p.n_split > 1) {
+        e = launch_merge(a.o_part, a.lse_part, out, B * Hq, p.n_split, D, s);
+        if (e != cudaSuccess) return cuda_fail(e, "attn_decode_gqa: merge kernel launch");
+    }
+    return ok();
+}
+
+// ======================================================================== MLA decode
+
+MLAKV_API int attn_decode_mla_num_splits(int B, int Hq, int r, int dr, int max_S, int n_split) {
+    const int rc = check_mla_shapes(B, Hq, r, dr, max_S > 0 ? max_S : 1, max_S, n_split);
+    if (rc != ATTN_OK) return rc;
+    return mla_plan(B, Hq, max_S, n_split).n_split;
+}
+
+MLAKV_API size_t attn_decode_mla_workspace_size(int B, int Hq, int r, int dr, int max_S, int n_split) {
+    if (check_mla_shapes(B, Hq, r, dr, max_S > 0 ? max_S : 1, max_S, n_split) != ATTN_OK) return 0;
+    return partials_bytes(B, Hq, r, mla_plan(B, Hq, max_S, n_split).n_split);
+}
+
+MLAKV_API int attn_decode_mla_absorbed(const void *q_lat, const void *q_rope, const void *c_cache,
+                                       const void *krope_cache, const int *seq_lens, float *out_lat, int B,
+                                       int Hq, int r, int dr, float scale, int S_max, int max_S, int n_split,
+                                       void *workspace, size_t ws_bytes, mlakv_stream_t stream) {
+    if (!q_lat || !q_rope || !c_cache || !krope_cache || !seq_lens || !out_lat)
+        return fail(ATTN_ERR_NULL, "attn_decode_mla_absorbed: every tensor pointer must be non-NULL");
+    int rc = check_mla_shapes(B, Hq, r, dr, S_max, max_S, n_split);
+    if (rc != ATTN_OK) return rc;
+    if (!isfinite(scale)) return fail(ATTN_ERR_SHAPE, "scale must be finite");
+    if (!aligned16(q_lat) || !aligned16(q_rope) || !aligned16(c_cache) || !aligned16(krope_cache) ||
+        !aligned16(out_lat) || !aligned16(seq_lens))
+        return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_mla_absorbed: every pointer must be 16-byte aligned");
+    const SplitPlan p = mla_plan(B, Hq, max_S, n_split);
+    const size_t need = partials_bytes(B, Hq, r, p.n_split);
+    if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
+        return fail(ATTN_ERR_WORKSPACE, "attn_decode_mla_absorbed: workspace of %zu bytes needed, got %zu",
+                    need, workspace ? ws_bytes : (size_t)0);
+    DecodeMlaArgs a{};
+    a.q_lat = q_lat; a.q_rope = q_rope; a.c = c_cache; a.kr = krope_cache; a.seq_lens = seq_lens;
+    a.out = out_lat; a.B = B; a.Hq = Hq; a.scale_log2 = scale * kLog2e; a.S_max = S_max;
+    a.n_split = p.n_split; a.split_len = p.split_len;
+    if (p.n_split > 1) {
+        const size_t rows = (size_t)B * Hq;
+        a.o_part = static_cast<float *>(workspace);
+        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                               align_up(rows * p.n_split * r * sizeof(float), 256));
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_decode_mla(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_decode_mla_absorbed: decode kernel launch");
+    if (p.n_split > 1) {
+        e = launch_merge(a.o_part, a.lse_part, out_lat, B * Hq, p.n_split, r, s);
+        if (e != cudaSuccess) return cuda_fail(e, "attn_decode_mla_absorbed: merge kernel launch");
+    }
+    return ok();
+}
+
+// ======================================================================== prefill
+
+MLAKV_API int attn_prefill_gqa_causal(const void *q, const void *k, const void *v, const int *cu_seqlens,
+                                      float *out, int B, int Hq, int Hkv, int D, float scale, int max_seqlen,
+                                      int total_tokens, mlakv_stream_t stream) {
+    if (!q || !k || !v || !cu_seqlens || !out)
+        return fail(ATTN_ERR_NULL, "attn_prefill_gqa_causal: q, k, v, cu_seqlens and out must be non-NULL");
+    if (B < 1 || Hq < 1 || Hkv < 1 || max_seqlen < 0 || total_tokens < 0)
+        return fail(ATTN_ERR_SHAPE, "B, Hq, Hkv must be >= 1 and max_seqlen, total_tokens >= 0");
+    if (Hq % Hkv != 0)
+        return fail(ATTN_ERR_SHAPE, "Hkv=%d does not divide Hq=%d", Hkv, Hq);
+    if (D != 128) return fail(ATTN_ERR_UNSUPPORTED, "prefill head width D=%d not built (128)", D);
+    if (!isfinite(scale)) return fail(ATTN_ERR_SHAPE, "scale must be finite");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(cu_seqlens))
+        return fail(ATTN_ERR_UNSUPPORTED, "attn_prefill_gqa_causal: every pointer must be 16-byte aligned");
+    if (total_tokens == 0 || max_seqlen == 0) return ok();
+    PrefillArgs a{};
+    a.q = q; a.k = k; a.v = v; a.cu_seqlens = cu_seqlens; a.out = out;
+    a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.T = total_tokens;
+    a.scale_log2 = scale * kLog2e; a.max_seqlen = max_seqlen;
+    cudaError_t e = launch_prefill(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "attn_prefill_gqa_causal: kernel launch");
+    return ok();
+}
+
+// ======================================================================== merge, status
+
+MLAKV_API int attn_merge_partials(const float *o_part, const float *lse_part, float *out, int rows, int n_split,
+                                  int Dv, mlakv_stream_t stream) {
+    if (!o_part || !lse_part || !out) return fail(ATTN_ERR_NULL, "attn_merge_partials: NULL pointer");
+    if (rows < 0 || n_split < 1 || n_split > 256 || Dv < 4)
+        return fail(ATTN_ERR_SHAPE, "attn_merge_partials: rows >= 0, 1 <= n_split <= 256, Dv >= 4");
+    if (Dv % 4 != 0 || Dv > 512) return fail(ATTN_ERR_UNSUPPORTED, "Dv=%d must be a multiple of 4 up to 512", Dv);
+    if (!aligned16(o_part) || !aligned16(out))
+        return fail(ATTN_ERR_UNSUPPORTED, "attn_merge_partials: o_part and out must be 16-byte aligned");
+    cudaError_t e = launch_merge(o_part, lse_part, out, rows, n_split, Dv, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "attn_merge_partials: kernel launch");
+    return ok();
+}
+
+MLAKV_API int attn_check_status(mlakv_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_check_status: stream");
+    int flag = 0;
+    const int rc = prefill_read_and_clear_status(s, &flag);
+    if (rc != 0) return cuda_fail((cudaError_t)rc, "attn_check_status: reading the device flags");
+    if (flag != 0) return fail(ATTN_ERR_TIMEOUT, "a prefill kernel gave up a bounded wait (code 0x%x)", flag);
+    return ok();
+}

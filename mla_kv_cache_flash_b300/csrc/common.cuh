@@ -1,0 +1,101 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#define MLAKV_HIDDEN __attribute__((visibility("hidden")))
+
+namespace mlakv {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ------------------------------------------------------------------ argument bundles
+
+struct DecodeGqaArgs {
+    const void *q;          // [B, Hq, D]
+    const void *k;          // [B, S_max, Hkv, D]
+    const void *v;          // [B, S_max, Hkv, D]
+    const int *seq_lens;    // [B]
+    float *out;             // [B, Hq, D]
+    float *o_part;          // [B, Hq, n_split, D]   (n_split > 1)
+    float *lse_part;        // [B, Hq, n_split]      (n_split > 1)
+    int B, Hq, Hkv, D;
+    float scale_log2;       // scale · log2(e)
+    int S_max;
+    int n_split;
+    int split_len;          // tokens per split (multiple of the kernel's tile)
+};
+
+struct DecodeMlaArgs {
+    const void *q_lat;      // [B, Hq, r]
+    const void *q_rope;     // [B, Hq, dr]
+    const void *c;          // [B, S_max, r]
+    const void *kr;         // [B, S_max, dr]
+    const int *seq_lens;    // [B]
+    float *out;             // [B, Hq, r]
+    float *o_part;          // [B, Hq, n_split, r]
+    float *lse_part;        // [B, Hq, n_split]
+    int B, Hq;
+    float scale_log2;
+    int S_max;
+    int n_split;
+    int split_len;
+};
+
+struct PrefillArgs {
+    const void *q;          // [T, Hq, D]
+    const void *k;          // [T, Hkv, D]
+    const void *v;          // [T, Hkv, D]
+    const int *cu_seqlens;  // [B+1]
+    float *out;             // [T, Hq, D]
+    int B, Hq, Hkv, D, T;
+    float scale_log2;
+    int max_seqlen;
+};
+
+// ------------------------------------------------------------------ launchers (one per TU)
+
+// K1: split-KV GQA decode. Writes out directly when n_split == 1, else the partials.
+MLAKV_HIDDEN cudaError_t launch_decode_gqa_f32(const DecodeGqaArgs &a, cudaStream_t s);
+MLAKV_HIDDEN cudaError_t launch_decode_gqa_bf16(const DecodeGqaArgs &a, cudaStream_t s);
+MLAKV_HIDDEN int decode_gqa_bf16_tile_tokens(int D, int G);
+// K2: log-sum-exp merge of the split partials.
+MLAKV_HIDDEN cudaError_t launch_merge(const float *o_part, const float *lse_part, float *out,
+                                      int rows, int n_split, int Dv, cudaStream_t s);
+// K3: MLA absorbed decode (r = 128, dr = 48).
+MLAKV_HIDDEN cudaError_t launch_decode_mla(const DecodeMlaArgs &a, cudaStream_t s);
+MLAKV_HIDDEN int decode_mla_tile_tokens();
+// K4: causal GQA prefill (D = 128).
+MLAKV_HIDDEN cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s);
+// Device error flags of the TUs that have bounded waits: read-and-clear (synchronous).
+MLAKV_HIDDEN int prefill_read_and_clear_status(cudaStream_t s, int *flag);
+
+// ------------------------------------------------------------------ device helpers
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// bf16 → fp32 is exact: the bf16 bits are the top half of the fp32 bits.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+}  // namespace mlakv

@@ -1,0 +1,196 @@
+// K1 (CUDA-core form): split-KV decode for GQA/MHA/MQA, fp32 accumulate on the FMA pipe.
+//
+// Used for the fp32 cache, where tensor cores would lose precision (TF32 keeps 10 mantissa
+// bits). One thread block handles one (sequence b, KV head j, split, block of HB query
+// heads of j's group). The HB heads are stacked so each K/V element is loaded once per
+// block and feeds all HB heads ("模型架构｜MQA & GQA 调研", section "代码": repeat_kv
+// would instead re-read each K/V byte once per query head).
+//
+// Per 128-token tile each of the 4 warps takes 32 tokens, one token per lane:
+//   scores   lane t computes s[h] = (scale·log2 e)·q_h·k_t for its token (q in shared memory,
+//            read as broadcasts), so the softmax works in the base-2 domain;
+//   softmax  running max m_h and sum l_h per warp (warp-shuffle max/sum), rescale by
+//            2^(m_old − m_new) — the online form of the page's fp32 softmax;
+//   P·V      lanes own D/32 output columns; p_t is broadcast by shuffle and V rows are read
+//            coalesced.
+// The four warps' states are merged in shared memory at the end. With one split the block
+// writes out = O / l; otherwise it writes the normalised partial and lse = ln Σ e^s for K2.
+#include "common.cuh"
+
+#include <math.h>
+
+namespace mlakv {
+namespace {
+
+__device__ __forceinline__ void load8(const float *p, float (&x)[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&x)[8]) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4 *>(p));
+    x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x);
+    x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+    x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z);
+    x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
+}
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T, int D, int HB>
+__global__ void __launch_bounds__(128) decode_gqa_fma_kernel(const DecodeGqaArgs a) {
+    constexpr int DPL = D / 32;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = a.Hq / a.Hkv;
+    const int n_hblk = G / HB;
+    const int j = blockIdx.y / n_hblk;
+    const int h0 = j * G + (blockIdx.y % n_hblk) * HB;
+    const int b = blockIdx.z;
+    const int split = blockIdx.x;
+    const int S = a.seq_lens[b];
+    const int t_begin = split * a.split_len;
+    const int t_end = min(S, t_begin + a.split_len);
+
+    __shared__ __align__(16) float q_s[HB][D];
+    __shared__ float m_s[4][HB];
+    __shared__ float l_s[4][HB];
+    __shared__ __align__(16) float o_s[4][HB][D];
+
+    const T *qg = static_cast<const T *>(a.q) + ((size_t)b * a.Hq + h0) * D;
+    for (int i = threadIdx.x; i < HB * D; i += 128) q_s[i / D][i % D] = to_f(qg[i]) * a.scale_log2;
+    __syncthreads();
+
+    float m[HB], l[HB], o[HB][DPL];
+#pragma unroll
+    for (int h = 0; h < HB; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) o[h][i] = 0.f;
+    }
+
+    const size_t row_stride = (size_t)a.Hkv * D;
+    const T *kb = static_cast<const T *>(a.k) + ((size_t)b * a.S_max * a.Hkv + j) * D;
+    const T *vb = static_cast<const T *>(a.v) + ((size_t)b * a.S_max * a.Hkv + j) * D;
+
+    for (int t0 = t_begin + warp * 32; t0 < t_end; t0 += 128) {
+        const int t = t0 + lane;
+        const bool valid = t < t_end;
+        float s[HB];
+#pragma unroll
+        for (int h = 0; h < HB; ++h) s[h] = 0.f;
+        if (valid) {
+            const T *kr = kb + (size_t)t * row_stride;
+#pragma unroll 2
+            for (int c = 0; c < D; c += 8) {
+                float x[8];
+                load8(kr + c, x);
+#pragma unroll
+                for (int h = 0; h < HB; ++h)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) s[h] = fmaf(q_s[h][c + e], x[e], s[h]);
+            }
+        }
+        float p[HB];
+#pragma unroll
+        for (int h = 0; h < HB; ++h) {
+            // lane 0 is always valid here (t0 < t_end), so the tile max is finite
+            const float mn = fmaxf(m[h], warp_max(valid ? s[h] : -INFINITY));
+            const float alpha = exp2f(m[h] - mn);
+            p[h] = valid ? exp2f(s[h] - mn) : 0.f;
+            l[h] = l[h] * alpha + warp_sum(p[h]);
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) o[h][i] *= alpha;
+            m[h] = mn;
+        }
+        const int n = min(32, t_end - t0);
+        for (int tt = 0; tt < n; ++tt) {
+            const T *vr = vb + (size_t)(t0 + tt) * row_stride;
+            float vv[DPL];
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) vv[i] = to_f(vr[lane + 32 * i]);
+#pragma unroll
+            for (int h = 0; h < HB; ++h) {
+                const float pt = __shfl_sync(0xffffffffu, p[h], tt);
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) o[h][i] = fmaf(pt, vv[i], o[h][i]);
+            }
+        }
+    }
+
+    if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < HB; ++h) {
+            m_s[warp][h] = m[h];
+            l_s[warp][h] = l[h];
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < HB; ++h)
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) o_s[warp][h][lane + 32 * i] = o[h][i];
+    __syncthreads();
+
+    for (int idx = threadIdx.x; idx < HB * D; idx += 128) {
+        const int h = idx / D;
+        const int d = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, m_s[w][h]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const float f = exp2f(m_s[w][h] - M);
+                L = fmaf(l_s[w][h], f, L);
+                O = fmaf(o_s[w][h][d], f, O);
+            }
+        }
+        const size_t row = (size_t)b * a.Hq + h0 + h;
+        const float val = L > 0.f ? O / L : 0.f;
+        if (a.n_split == 1) {
+            a.out[row * D + d] = val;
+        } else {
+            a.o_part[(row * a.n_split + split) * D + d] = val;
+            if (d == 0) a.lse_part[row * a.n_split + split] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+        }
+    }
+}
+
+template <typename T, int D>
+cudaError_t launch_d(const DecodeGqaArgs &a, cudaStream_t s) {
+    const int G = a.Hq / a.Hkv;
+    const int hb = (G % 8 == 0) ? 8 : (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
+    const dim3 grid(a.n_split, a.Hkv * (G / hb), a.B);
+    switch (hb) {
+        case 8: decode_gqa_fma_kernel<T, D, 8><<<grid, 128, 0, s>>>(a); break;
+        case 4: decode_gqa_fma_kernel<T, D, 4><<<grid, 128, 0, s>>>(a); break;
+        case 2: decode_gqa_fma_kernel<T, D, 2><<<grid, 128, 0, s>>>(a); break;
+        default: decode_gqa_fma_kernel<T, D, 1><<<grid, 128, 0, s>>>(a); break;
+    }
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_t(const DecodeGqaArgs &a, cudaStream_t s) {
+    switch (a.D) {
+        case 64: return launch_d<T, 64>(a, s);
+        case 96: return launch_d<T, 96>(a, s);
+        case 128: return launch_d<T, 128>(a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_gqa_f32(const DecodeGqaArgs &a, cudaStream_t s) { return launch_t<float>(a, s); }
+
+cudaError_t launch_decode_gqa_fma_bf16(const DecodeGqaArgs &a, cudaStream_t s) {
+    return launch_t<__nv_bfloat16>(a, s);
+}
+
+}  // namespace mlakv

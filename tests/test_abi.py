@@ -1,0 +1,170 @@
+"""The C-ABI library loads, exports every entry point the header declares, and rejects bad
+host-side arguments with the documented status before launching anything.
+
+Runs without a GPU: every call here fails validation first, so no kernel is launched and
+no device memory is touched (the pointers below are never dereferenced).
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_kv_cache_flash_b300 as mk
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mlakv.h")
+
+OK, NULL, SHAPE, UNSUP, WS = 0, -1, -2, -3, -4
+P = ctypes.c_void_p(1 << 20)   # aligned, non-NULL, never dereferenced
+PU = ctypes.c_void_p((1 << 20) + 2)   # misaligned
+N0 = ctypes.c_void_p(0)
+S0 = ctypes.c_void_p(0)
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(mk.lib_path):
+        from mla_kv_cache_flash_b300 import build
+        build.build()
+    return mk.lib()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("attn_decode_gqa", "attn_decode_mla_absorbed", "attn_prefill_gqa_causal",
+                 "attn_merge_partials", "attn_last_error", "attn_check_status"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_only_the_abi_is_exported():
+    out = os.popen(f"nm -D --defined-only {mk.lib_path}").read()
+    ours = [ln.split()[-1] for ln in out.splitlines() if " T " in ln]
+    assert set(declared_functions()) <= set(ours)
+    assert not [n for n in ours if "mlakv" in n], "internal symbols leaked into the dynamic table"
+
+
+def test_version(L):
+    assert "sm_103a" in mk.version()
+
+
+def gqa(L, q=P, k=P, v=P, lens=P, out=P, B=2, Hq=8, Hkv=2, D=64, scale=0.125, S_max=128, max_S=128,
+        dtype=0, n_split=0, ws=N0, ws_bytes=0):
+    return L.attn_decode_gqa(q, k, v, lens, out, B, Hq, Hkv, D, scale, S_max, max_S, dtype, n_split,
+                             ws, ws_bytes, S0)
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v", "lens", "out"])
+def test_gqa_null_pointers(L, which):
+    assert gqa(L, **{which: N0}) == NULL
+    assert "non-NULL" in mk.last_error()
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(Hq=0), dict(Hkv=0), dict(S_max=0), dict(max_S=-1),
+                                dict(max_S=129), dict(Hq=32, Hkv=3), dict(Hq=32, Hkv=6), dict(n_split=-1),
+                                dict(n_split=257), dict(scale=float("nan")), dict(scale=float("inf"))])
+def test_gqa_bad_shapes(L, kw):
+    assert gqa(L, **kw) == SHAPE
+
+
+def test_gqa_divisibility_message(L):
+    assert gqa(L, Hq=32, Hkv=3) == SHAPE
+    assert "does not divide" in mk.last_error()
+
+
+@pytest.mark.parametrize("kw", [dict(D=80), dict(D=256), dict(dtype=2), dict(Hq=256, Hkv=1), dict(q=PU),
+                                dict(k=PU), dict(out=PU)])
+def test_gqa_unsupported(L, kw):
+    assert gqa(L, **kw) == UNSUP
+
+
+def test_gqa_workspace_checks(L):
+    need = L.attn_decode_gqa_workspace_size(2, 8, 2, 64, 128, 0, 2)
+    assert need > 0
+    assert L.attn_decode_gqa_num_splits(2, 8, 2, 64, 128, 0, 2) == 2
+    assert gqa(L, n_split=2) == WS
+    assert gqa(L, n_split=2, ws=P, ws_bytes=need - 1) == WS
+    assert gqa(L, n_split=2, ws=PU, ws_bytes=need) == WS
+    # one split needs no workspace
+    assert L.attn_decode_gqa_workspace_size(2, 8, 2, 64, 128, 0, 1) == 0
+
+
+def test_gqa_split_plan_bounds(L):
+    # never more splits than tiles of the longest sequence; an explicit count is honoured
+    assert L.attn_decode_gqa_num_splits(1, 1, 1, 64, 1, 0, 0) == 1
+    assert L.attn_decode_gqa_num_splits(1, 1, 1, 64, 0, 0, 0) == 1
+    assert L.attn_decode_gqa_num_splits(2, 8, 2, 64, 128, 0, 7) == 7
+    n = L.attn_decode_gqa_num_splits(1, 32, 1, 128, 8192, 1, 0)
+    assert 1 <= n <= 64
+    assert L.attn_decode_gqa_num_splits(64, 32, 32, 128, 8192, 1, 0) >= 1
+    assert L.attn_decode_gqa_num_splits(2, 8, 3, 64, 128, 0, 0) == SHAPE
+
+
+def mla(L, ql=P, qr=P, c=P, kr=P, lens=P, out=P, B=2, Hq=16, r=128, dr=48, scale=1 / 12, S_max=64, max_S=64,
+        n_split=0, ws=N0, ws_bytes=0):
+    return L.attn_decode_mla_absorbed(ql, qr, c, kr, lens, out, B, Hq, r, dr, scale, S_max, max_S, n_split,
+                                      ws, ws_bytes, S0)
+
+
+@pytest.mark.parametrize("which", ["ql", "qr", "c", "kr", "lens", "out"])
+def test_mla_null_pointers(L, which):
+    assert mla(L, **{which: N0}) == NULL
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(Hq=0), dict(S_max=0), dict(max_S=65), dict(n_split=-2)])
+def test_mla_bad_shapes(L, kw):
+    assert mla(L, **kw) == SHAPE
+
+
+@pytest.mark.parametrize("kw", [dict(r=64), dict(dr=64), dict(Hq=8), dict(Hq=144), dict(c=PU)])
+def test_mla_unsupported(L, kw):
+    assert mla(L, **kw) == UNSUP
+
+
+def test_mla_workspace(L):
+    need = L.attn_decode_mla_workspace_size(2, 16, 128, 48, 4096, 4)
+    assert need >= 2 * 16 * 4 * 128 * 4
+    assert mla(L, S_max=4096, max_S=4096, n_split=4) == WS
+
+
+def prefill(L, q=P, k=P, v=P, cu=P, out=P, B=2, Hq=8, Hkv=2, D=128, scale=0.088, max_seqlen=64, T=100):
+    return L.attn_prefill_gqa_causal(q, k, v, cu, out, B, Hq, Hkv, D, scale, max_seqlen, T, S0)
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v", "cu", "out"])
+def test_prefill_null_pointers(L, which):
+    assert prefill(L, **{which: N0}) == NULL
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(Hq=0), dict(Hkv=0), dict(Hq=8, Hkv=3), dict(max_seqlen=-1),
+                                dict(T=-1), dict(scale=float("nan"))])
+def test_prefill_bad_shapes(L, kw):
+    assert prefill(L, **kw) == SHAPE
+
+
+@pytest.mark.parametrize("kw", [dict(D=64), dict(D=96), dict(q=PU)])
+def test_prefill_unsupported(L, kw):
+    assert prefill(L, **kw) == UNSUP
+
+
+def test_prefill_empty_is_a_no_op(L):
+    assert prefill(L, T=0) == OK
+    assert prefill(L, max_seqlen=0) == OK
+
+
+def test_merge_checks(L):
+    assert L.attn_merge_partials(N0, P, P, 4, 2, 64, S0) == NULL
+    assert L.attn_merge_partials(P, P, P, 4, 0, 64, S0) == SHAPE
+    assert L.attn_merge_partials(P, P, P, 4, 2, 66, S0) == UNSUP
+    assert L.attn_merge_partials(P, P, P, -1, 2, 64, S0) == SHAPE

@@ -1,0 +1,157 @@
+"""GQA/MHA/MQA decode and the LSE merge on the GPU against the fp64 CPU oracle.
+
+Tolerances (max |Δ| over every output element): 1e-5 for the fp32 cache, 3e-3 for the
+bf16 caches (fp32 accumulation and fp32 output in both cases).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import mla_kv_cache_flash_b300 as mk
+import oracle
+import workloads as W
+from workloads import to_f64
+
+pytestmark = pytest.mark.gpu
+
+TOL_F32 = 1e-5
+TOL_BF16 = 3e-3
+DEV = "cuda"
+
+
+def _oracle_decode(inp, scale, batches=None):
+    q = to_f64(inp["q"])
+    lens = inp["seq_lens"].cpu().numpy()
+    k, v = inp["k_cache"], inp["v_cache"]
+    B, Hq, D = q.shape
+    Hkv = k.shape[2]
+    g = Hq // Hkv
+    out = np.zeros((B, Hq, D))
+    for b in (range(B) if batches is None else batches):
+        s = int(lens[b])
+        kb = to_f64(k[b, :s])
+        vb = to_f64(v[b, :s])
+        for j in range(Hkv):
+            out[b, j * g:(j + 1) * g] = oracle.attend(q[b, j * g:(j + 1) * g], kb[:, j], vb[:, j], scale)
+    return out
+
+
+def _max_err(got, ref, batches=None):
+    g = got.detach().cpu().double().numpy()
+    if batches is not None:
+        g, ref = g[list(batches)], ref[list(batches)]
+    return float(np.abs(g - ref).max())
+
+
+@pytest.mark.parametrize("hkv", [2, 8, 1])
+@pytest.mark.parametrize("n_split", [0, 1, 2, 3, 7])
+def test_tiny_fp32(hkv, n_split):
+    w = W.TINY_FP32[hkv]
+    inp = W.decode_inputs(w, DEV)
+    out = mk.decode_gqa(inp["q"], inp["k_cache"], inp["v_cache"], inp["seq_lens"], scale=w.scale,
+                        n_split=n_split)
+    torch.cuda.synchronize()
+    ref = oracle.decode_gqa(to_f64(inp["q"]), to_f64(inp["k_cache"]), to_f64(inp["v_cache"]),
+                            inp["seq_lens"].cpu().numpy(), w.scale)
+    assert _max_err(out, ref) <= TOL_F32
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("D", [64, 96, 128])
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (8, 8), (8, 1), (32, 1), (12, 4), (6, 2), (64, 2)])
+def test_shapes_and_ragged_lengths(dtype, D, hq, hkv):
+    # lengths cover: empty, one token, one short of a tile, a ragged tail, and S_max
+    lens = (0, 1, 127, 129, 300, 517)
+    w = W.DecodeWorkload("ragged", 0, len(lens), hq, hkv, D, 517, dtype, lengths=lens, sub=7)
+    inp = W.decode_inputs(w, DEV)
+    tol = TOL_F32 if dtype == "fp32" else TOL_BF16
+    ref = _oracle_decode(inp, w.scale)
+    for n_split in (0, 1, 5):
+        out = mk.decode_gqa(inp["q"], inp["k_cache"], inp["v_cache"], inp["seq_lens"], scale=w.scale,
+                            n_split=n_split)
+        torch.cuda.synchronize()
+        assert _max_err(out, ref) <= tol, n_split
+        assert torch.all(out[0] == 0)
+
+
+def test_single_token_is_v0():
+    w = W.DecodeWorkload("one", 0, 3, 8, 2, 128, 64, "bf16", lengths=(1, 1, 1))
+    inp = W.decode_inputs(w, DEV)
+    out = mk.decode_gqa(inp["q"], inp["k_cache"], inp["v_cache"], inp["seq_lens"])
+    v0 = inp["v_cache"][:, 0].float().repeat_interleave(4, dim=1)
+    assert torch.equal(out, v0)
+
+
+def test_more_splits_than_tiles():
+    w = W.DecodeWorkload("few", 0, 2, 8, 2, 64, 200, "fp32", lengths=(3, 200))
+    inp = W.decode_inputs(w, DEV)
+    ref = _oracle_decode(inp, w.scale)
+    out = mk.decode_gqa(inp["q"], inp["k_cache"], inp["v_cache"], inp["seq_lens"], n_split=64)
+    torch.cuda.synchronize()
+    assert _max_err(out, ref) <= TOL_F32
+
+
+def test_max_s_bound_smaller_than_capacity():
+    w = W.DecodeWorkload("bound", 0, 4, 16, 4, 128, 4096, "bf16", lengths=(700, 5, 1000, 999))
+    inp = W.decode_inputs(w, DEV)
+    ref = _oracle_decode(inp, w.scale)
+    out = mk.decode_gqa(inp["q"], inp["k_cache"], inp["v_cache"], inp["seq_lens"], max_s=1000)
+    torch.cuda.synchronize()
+    assert _max_err(out, ref) <= TOL_BF16
+
+
+def test_deterministic_and_stream_ordered_workspace():
+    w = W.MINIMIND_GQA
+    inp = W.decode_inputs(w, DEV)
+    n = mk.decode_gqa_num_splits(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.s_max, mk.ATTN_BF16)
+    ws = torch.empty(mk.decode_gqa_workspace_size(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.s_max,
+                                                  mk.ATTN_BF16, max(n, 2)), dtype=torch.uint8, device=DEV)
+    inp2 = W.decode_inputs(w, DEV, seed=w.seed + 5)
+    a = mk.decode_gqa(inp["q"], inp["k_cache"], inp["v_cache"], inp["seq_lens"], n_split=max(n, 2), workspace=ws)
+    b = mk.decode_gqa(inp2["q"], inp2["k_cache"], inp2["v_cache"], inp2["seq_lens"], n_split=max(n, 2),
+                      workspace=ws)
+    a2 = mk.decode_gqa(inp["q"], inp["k_cache"], inp["v_cache"], inp["seq_lens"], n_split=max(n, 2), workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(a, a2)
+    assert _max_err(b, _oracle_decode(inp2, w.scale)) <= TOL_BF16
+
+
+def test_minimind_gqa_full():
+    w = W.MINIMIND_GQA
+    inp = W.decode_inputs(w, DEV)
+    out = mk.decode_gqa(inp["q"], inp["k_cache"], inp["v_cache"], inp["seq_lens"], scale=w.scale,
+                        max_s=int(inp["seq_lens"].max()))
+    torch.cuda.synchronize()
+    assert _max_err(out, _oracle_decode(inp, w.scale)) <= TOL_BF16
+
+
+@pytest.mark.parametrize("hkv", [8, 1, 32])
+def test_llama3_8b_full(hkv):
+    w = W.LLAMA3_8B[hkv]
+    inp = W.decode_inputs(w, DEV)
+    out = mk.decode_gqa(inp["q"], inp["k_cache"], inp["v_cache"], inp["seq_lens"], scale=w.scale)
+    torch.cuda.synchronize()
+    # MHA holds 8 GiB of cache: the oracle checks a fixed sample of 8 sequences there
+    batches = None if hkv != 32 else [0, 9, 18, 27, 36, 45, 54, 63]
+    ref = _oracle_decode(inp, w.scale, batches)
+    assert _max_err(out, ref, batches) <= TOL_BF16
+    del inp
+    torch.cuda.empty_cache()
+
+
+def test_merge_partials_against_oracle():
+    g = torch.Generator(device=DEV)
+    g.manual_seed(77)
+    rows, n, dv = 37, 9, 128
+    o = torch.randn((rows, n, dv), generator=g, device=DEV)
+    lse = torch.randn((rows, n), generator=g, device=DEV) * 5
+    lse[3, :] = float("-inf")            # a row with only empty pieces
+    lse[5, ::2] = float("-inf")          # some empty pieces
+    out = mk.merge_partials(o, lse)
+    torch.cuda.synchronize()
+    on, ln = to_f64(o), to_f64(lse)
+    for r in range(rows):
+        ref = oracle.lse_merge(on[r][:, None, :], ln[r][:, None])[0]
+        assert np.abs(out[r].cpu().double().numpy() - ref).max() <= 1e-5
+    assert torch.all(out[3] == 0)
