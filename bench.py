@@ -76,19 +76,22 @@ class ClockSampler:
                0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
 
     def __init__(self, device_index, period_s=0.01):
-        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.samples, self.reasons, self.max_mhz, self.error = [], set(), None, None
         self.period, self.stop_flag, self.thread, self.h = period_s, threading.Event(), None, None
         try:
             import pynvml
             pynvml.nvmlInit()
             self.nv = pynvml
-            bus = torch.cuda.get_device_properties(device_index).pci_bus_id if hasattr(
-                torch.cuda.get_device_properties(device_index), "pci_bus_id") else None
-            self.h = (pynvml.nvmlDeviceGetHandleByPciBusId(bus) if bus else
-                      pynvml.nvmlDeviceGetHandleByIndex(device_index))
+            props = torch.cuda.get_device_properties(device_index)
+            try:
+                bus = "%08X:%02X:%02X.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+                self.h = pynvml.nvmlDeviceGetHandleByPciBusId(bus.encode())
+            except Exception:
+                self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
         except Exception as e:  # pragma: no cover - NVML missing
             self.error = repr(e)
+            self.h = None
 
     def _run(self):
         while not self.stop_flag.is_set():
@@ -115,7 +118,8 @@ class ClockSampler:
 
     def summary(self):
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": 0,
+                    "error": getattr(self, "error", "no sample taken")}
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
                 "reasons": sorted(self.reasons), "samples": len(self.samples)}
 
@@ -462,62 +466,63 @@ def _oracle_decode_units(units):
 
 
 def cpu_oracle_rate(wl, budget_s, steps=None, warmup=0):
-    """Time the fp64 oracle on the host cores over a bounded sample of the workload's units.
-    Returns (value in the workload's unit, cores, sample description, seconds per step)."""
+    """Time the fp64 oracle on the host cores over a bounded sample of the workload's units
+    (one unit = one sequence and KV head). Returns (value in GB/s of KV read, cores used,
+    sample description, seconds per step or None)."""
     import multiprocessing as mp
     import tempfile
+    global _ARR
     cores = len(os.sched_getaffinity(0))
-    arrays = wl.host_arrays()
-    tmp = tempfile.NamedTemporaryFile(suffix=".npz", delete=False)
-    np.savez(tmp.name, **{k: np.asarray(v) for k, v in arrays.items()})
+    arrays = {k: np.asarray(v) for k, v in wl.host_arrays().items()}
     units = wl.oracle_units()
-    rng = np.random.default_rng(0)
-    order = [units[i] for i in rng.permutation(len(units))]
+    order = [units[i] for i in np.random.default_rng(0).permutation(len(units))]
+    _ARR = arrays
+    t0 = time.perf_counter()
+    _oracle_decode_units(order[:min(8, len(order))])
+    per_unit = (time.perf_counter() - t0) / min(8, len(order))
+    tmp = tempfile.NamedTemporaryFile(suffix=".npz", delete=False)
+    tmp.close()
+    np.savez(tmp.name, **arrays)
     ctx = mp.get_context("spawn")
-    with ctx.Pool(cores, initializer=_oracle_worker_init, initargs=(tmp.name,)) as pool:
-        # calibrate: one unit per worker
-        t0 = time.perf_counter()
-        pool.map(_oracle_decode_units, [[order[i % len(order)]] for i in range(cores)])
-        per_unit = max((time.perf_counter() - t0) / 1.0, 1e-6)  # wall for `cores` units in parallel
-        if steps is None:
-            n_units = max(cores, int(budget_s / per_unit * cores))
-            sample = [order[i % len(order)] for i in range(n_units)]
-            chunks = [sample[i::cores] for i in range(cores)]
+    try:
+        with ctx.Pool(cores, initializer=_oracle_worker_init, initargs=(tmp.name,)) as pool:
+            pool.map(_oracle_decode_units, [[order[0]]] * cores)   # workers up and loaded
+            if steps is None:
+                passes = max(1, int(budget_s / max(per_unit * len(units) / cores, 1e-9)))
+                sample = order * passes
+                t0 = time.perf_counter()
+                pool.map(_oracle_decode_units, [sample[i::cores] for i in range(cores)])
+                wall = time.perf_counter() - t0
+                nbytes = passes * sum(wl.unit_bytes(u) for u in units)
+                return (nbytes / wall / 1e9, cores,
+                        f"{passes} full pass(es) over all {len(units)} (sequence, kv-head) units, fp64 oracle.attend, "
+                        f"{cores} worker processes", None)
+            per_step_budget = budget_s / max(1, steps + warmup)
+            n_units = int(min(len(order), max(1, per_step_budget / per_unit * cores)))
+            workers = min(cores, n_units)
+            cursor = 0
+
+            def one_step():
+                nonlocal cursor
+                sample = [order[(cursor + i) % len(order)] for i in range(n_units)]
+                cursor += n_units
+                if workers == 1:
+                    _oracle_decode_units(sample)
+                else:
+                    pool.map(_oracle_decode_units, [sample[i::workers] for i in range(workers)])
+                return sum(wl.unit_bytes(u) for u in sample)
+
+            for _ in range(warmup):
+                one_step()
             t0 = time.perf_counter()
-            pool.map(_oracle_decode_units, chunks)
+            nbytes = sum(one_step() for _ in range(steps))
             wall = time.perf_counter() - t0
-            nbytes = sum(wl.unit_bytes(u) for u in sample)
-            os.unlink(tmp.name)
-            return nbytes / wall / 1e9, cores, f"{n_units} (sequence, kv-head) units of the workload " \
-                f"({n_units / len(units):.2f} passes over its {len(units)} units), fp64 oracle.attend", None
-        # reference arm: `steps` timed steps, each a bounded sample sized to the budget
-        per_step_budget = budget_s / max(1, steps + warmup)
-        n_units = max(1, int(per_step_budget / per_unit * cores))
-        n_units = min(n_units, len(order))
-        workers = min(cores, n_units)
-        cursor = 0
-
-        def one_step():
-            nonlocal cursor
-            sample = [order[(cursor + i) % len(order)] for i in range(n_units)]
-            cursor += n_units
-            if workers == 1:
-                _oracle_worker_init(tmp.name) if "_ARR" not in globals() else None
-                _oracle_decode_units(sample)
-            else:
-                pool.map(_oracle_decode_units, [sample[i::workers] for i in range(workers)])
-            return sum(wl.unit_bytes(u) for u in sample)
-
-        for _ in range(warmup):
-            one_step()
-        t0 = time.perf_counter()
-        nbytes = 0
-        for _ in range(steps):
-            nbytes += one_step()
-        wall = time.perf_counter() - t0
-    os.unlink(tmp.name)
-    return nbytes / wall / 1e9, workers, f"each step {n_units} of the workload's {len(units)} " \
-        f"(sequence, kv-head) units, fp64 oracle.attend", wall / steps
+    finally:
+        os.unlink(tmp.name)
+    what = "all" if n_units == len(units) else f"{n_units} of the"
+    return (nbytes / wall / 1e9, workers,
+            f"each step {what} {len(units)} (sequence, kv-head) units of the workload, fp64 oracle.attend, "
+            f"{workers} worker processes", wall / steps)
 
 
 # ============================================================================ main

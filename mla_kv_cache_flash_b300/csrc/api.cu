@@ -96,7 +96,7 @@ SplitPlan gqa_plan(int B, int Hq, int Hkv, int D, int max_S, attn_dtype dtype, i
         return plan_splits(max_S, kFmaTile, (long)B * Hkv * (G / hb), n_split, 2);
     }
     const int tile = decode_gqa_bf16_tile_tokens(D, G);
-    const int heads_per_block = G < 16 ? G : 16;
+    const int heads_per_block = decode_gqa_bf16_heads_per_block(G);
     const long blocks = (long)B * Hkv * ((G + heads_per_block - 1) / heads_per_block);
     return plan_splits(max_S, tile, blocks, n_split, 4);
 }
@@ -310,9 +310,12 @@ MLAKV_API int attn_check_status(mlakv_stream_t stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "attn_check_status: stream");
-    int flag = 0;
-    const int rc = prefill_read_and_clear_status(s, &flag);
+    unsigned flag = 0, f = 0;
+    int rc = decode_gqa_read_and_clear_status(s, &f);
+    flag |= f;
+    if (rc == 0) rc = decode_mla_read_and_clear_status(s, &f), flag |= f;
+    if (rc == 0) rc = prefill_read_and_clear_status(s, &f), flag |= f;
     if (rc != 0) return cuda_fail((cudaError_t)rc, "attn_check_status: reading the device flags");
-    if (flag != 0) return fail(ATTN_ERR_TIMEOUT, "a prefill kernel gave up a bounded wait (code 0x%x)", flag);
+    if (flag != 0) return fail(ATTN_ERR_TIMEOUT, "a kernel gave up a bounded wait (flags 0x%x)", flag);
     return ok();
 }

@@ -62,6 +62,7 @@ struct PrefillArgs {
 MLAKV_HIDDEN cudaError_t launch_decode_gqa_f32(const DecodeGqaArgs &a, cudaStream_t s);
 MLAKV_HIDDEN cudaError_t launch_decode_gqa_bf16(const DecodeGqaArgs &a, cudaStream_t s);
 MLAKV_HIDDEN int decode_gqa_bf16_tile_tokens(int D, int G);
+MLAKV_HIDDEN int decode_gqa_bf16_heads_per_block(int G);
 // K2: log-sum-exp merge of the split partials.
 MLAKV_HIDDEN cudaError_t launch_merge(const float *o_part, const float *lse_part, float *out,
                                       int rows, int n_split, int Dv, cudaStream_t s);
@@ -71,7 +72,9 @@ MLAKV_HIDDEN int decode_mla_tile_tokens();
 // K4: causal GQA prefill (D = 128).
 MLAKV_HIDDEN cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s);
 // Device error flags of the TUs that have bounded waits: read-and-clear (synchronous).
-MLAKV_HIDDEN int prefill_read_and_clear_status(cudaStream_t s, int *flag);
+MLAKV_HIDDEN int decode_gqa_read_and_clear_status(cudaStream_t s, unsigned *flag);
+MLAKV_HIDDEN int decode_mla_read_and_clear_status(cudaStream_t s, unsigned *flag);
+MLAKV_HIDDEN int prefill_read_and_clear_status(cudaStream_t s, unsigned *flag);
 
 // ------------------------------------------------------------------ device helpers
 

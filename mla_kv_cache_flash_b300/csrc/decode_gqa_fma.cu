@@ -1,7 +1,7 @@
-// K1 (CUDA-core form): split-KV decode for GQA/MHA/MQA, fp32 accumulate on the FMA pipe.
+// K1 (CUDA-core form): split-KV decode for GQA/MHA/MQA over an fp32 cache, fp32 FMA.
 //
-// Used for the fp32 cache, where tensor cores would lose precision (TF32 keeps 10 mantissa
-// bits). One thread block handles one (sequence b, KV head j, split, block of HB query
+// The fp32 cache stays off the tensor cores, which would round it (TF32 keeps 10 mantissa
+// bits) and break the fp32 tolerance; the bf16 cache has its own tensor-core kernel. One thread block handles one (sequence b, KV head j, split, block of HB query
 // heads of j's group). The HB heads are stacked so each K/V element is loaded once per
 // block and feeds all HB heads ("模型架构｜MQA & GQA 调研", section "代码": repeat_kv
 // would instead re-read each K/V byte once per query head).
@@ -188,9 +188,5 @@ cudaError_t launch_t(const DecodeGqaArgs &a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_decode_gqa_f32(const DecodeGqaArgs &a, cudaStream_t s) { return launch_t<float>(a, s); }
-
-cudaError_t launch_decode_gqa_fma_bf16(const DecodeGqaArgs &a, cudaStream_t s) {
-    return launch_t<__nv_bfloat16>(a, s);
-}
 
 }  // namespace mlakv

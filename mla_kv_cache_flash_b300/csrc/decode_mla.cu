@@ -139,6 +139,11 @@ __global__ void __launch_bounds__(128) decode_mla_fma_kernel(const DecodeMlaArgs
 
 int decode_mla_tile_tokens() { return TILE; }
 
+int decode_mla_read_and_clear_status(cudaStream_t, unsigned *flag) {
+    *flag = 0;
+    return 0;
+}
+
 cudaError_t launch_decode_mla(const DecodeMlaArgs &a, cudaStream_t s) {
     const dim3 grid(a.n_split, a.Hq / HB, a.B);
     decode_mla_fma_kernel<<<grid, 128, 0, s>>>(a);
