@@ -95,6 +95,34 @@ int attn_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
                     void *workspace, size_t ws_bytes, mlakv_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * attn_decode_gqa for callers that may not allocate device memory. No source page has a
+ * counterpart to this entry point; it exists for the library's users.
+ *
+ * attn_decode_gqa takes its split scratch from the caller. A caller that cannot allocate —
+ * a plugin inside a host program that owns all device memory, a serving loop that must not
+ * call cudaMalloc because it can synchronise the device and stall other streams, code that
+ * runs where the allocator cannot be entered — calls this instead. It takes the same
+ * arguments minus the workspace, and keeps the split partials in a fixed array built into
+ * the library (attn_decode_gqa_noalloc_max_scratch() bytes, 16 MiB, held by every GPU that
+ * loads the library until the process exits). It allocates and frees nothing.
+ *   - Sizes whose partials need more than that return ATTN_ERR_WORKSPACE (ask for fewer
+ *     splits, or use attn_decode_gqa).
+ *   - The first call on a device looks up the array's device address on that device (the
+ *     device must be current); make that first call before any stream capture.
+ *   - Every call uses the same array, which keeps the last call's contents (nothing in it
+ *     needs to start at zero). Calls whose kernels can overlap on the GPU — other streams,
+ *     other host threads — race on it; order them.
+ * Results are identical to attn_decode_gqa with the same arguments.
+ * ------------------------------------------------------------------------------------- */
+size_t attn_decode_gqa_noalloc_max_scratch(void);
+
+int attn_decode_gqa_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                            const int *seq_lens, float *out,
+                            int B, int Hq, int Hkv, int D, float scale,
+                            int S_max, int max_S, attn_dtype dtype, int n_split,
+                            mlakv_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * MLA decode with W_UK absorbed [MLA sections 2, 3, 6]: every head attends the same cached
  * latent row [c_t ‖ kr_t] and averages c_t itself:
  *   s_t = scale·(q_lat[b,h]·c_t + q_rope[b,h]·kr_t),  out_lat[b,h] = Σ_t softmax(s)_t c_t.

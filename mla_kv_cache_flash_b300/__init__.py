@@ -22,7 +22,7 @@ import torch
 
 __all__ = [
     "ATTN_F32", "ATTN_BF16", "MlakvError", "lib", "lib_path", "decode_gqa", "decode_gqa_workspace_size",
-    "decode_gqa_num_splits", "decode_mla_absorbed", "decode_mla_workspace_size", "decode_mla_num_splits",
+    "decode_gqa_num_splits", "decode_gqa_noalloc", "decode_mla_absorbed", "decode_mla_workspace_size", "decode_mla_num_splits",
     "prefill_gqa_causal", "merge_partials", "check_status", "last_error", "version",
 ]
 
@@ -47,6 +47,8 @@ _SIGNATURES = {
     "attn_decode_gqa_workspace_size": (_c_size, [_c_int] * 6 + [_c_int]),
     "attn_decode_gqa_num_splits": (_c_int, [_c_int] * 7),
     "attn_decode_gqa": (_c_int, [_vp] * 5 + [_c_int] * 4 + [_c_float] + [_c_int] * 4 + [_vp, _c_size, _vp]),
+    "attn_decode_gqa_noalloc_max_scratch": (_c_size, []),
+    "attn_decode_gqa_noalloc": (_c_int, [_vp] * 5 + [_c_int] * 4 + [_c_float] + [_c_int] * 4 + [_vp]),
     "attn_decode_mla_workspace_size": (_c_size, [_c_int] * 6),
     "attn_decode_mla_num_splits": (_c_int, [_c_int] * 6),
     "attn_decode_mla_absorbed": (_c_int, [_vp] * 6 + [_c_int] * 4 + [_c_float] + [_c_int] * 3 + [_vp, _c_size, _vp]),
@@ -161,6 +163,32 @@ def decode_gqa(q, k_cache, v_cache, seq_lens, out=None, scale=None, max_s=None, 
     _check(lib().attn_decode_gqa(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(out),
                                  B, Hq, Hkv, D, scale, S_max, max_s, code, n_split,
                                  _ptr(workspace), ws_bytes, _stream()))
+    return out
+
+
+def decode_gqa_noalloc(q, k_cache, v_cache, seq_lens, out, scale=None, max_s=None, n_split=0):
+    """decode_gqa for callers that must not allocate device memory.
+
+    The split scratch lives in a fixed array inside the library instead of a caller
+    workspace, and ``out`` must be passed in, so the call allocates nothing. Calls whose
+    kernels can overlap on the GPU share that array and must be ordered by the caller.
+    """
+    dt = q.dtype
+    if dt not in (torch.float32, torch.bfloat16):
+        raise TypeError("q must be float32 or bfloat16")
+    _need(q, "q", dt, 3)
+    dev = q.device
+    _need(k_cache, "k_cache", dt, 4, dev)
+    _need(v_cache, "v_cache", dt, 4, dev)
+    _need(seq_lens, "seq_lens", torch.int32, 1, dev)
+    _need(out, "out", torch.float32, 3, dev)
+    B, Hq, D = q.shape
+    _, S_max, Hkv, _ = k_cache.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    max_s = S_max if max_s is None else int(max_s)
+    code = ATTN_F32 if dt == torch.float32 else ATTN_BF16
+    _check(lib().attn_decode_gqa_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(out),
+                                         B, Hq, Hkv, D, scale, S_max, max_s, code, n_split, _stream()))
     return out
 
 

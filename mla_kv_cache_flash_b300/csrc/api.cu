@@ -152,6 +152,10 @@ SplitPlan mla_plan(int B, int Hq, int max_S, int n_split) {
 }
 
 }  // namespace
+
+// Lets other translation units report through attn_last_error().
+int report_error(int code, const char *message) { return fail(code, "%s", message); }
+
 }  // namespace mlakv
 
 using namespace mlakv;

@@ -76,6 +76,9 @@ MLAKV_HIDDEN int decode_gqa_read_and_clear_status(cudaStream_t s, unsigned *flag
 MLAKV_HIDDEN int decode_mla_read_and_clear_status(cudaStream_t s, unsigned *flag);
 MLAKV_HIDDEN int prefill_read_and_clear_status(cudaStream_t s, unsigned *flag);
 
+// Sets the thread's attn_last_error() message and returns `code`.
+MLAKV_HIDDEN int report_error(int code, const char *message);
+
 // ------------------------------------------------------------------ device helpers
 
 __device__ __forceinline__ float warp_max(float x) {
