@@ -69,59 +69,98 @@ def dist_env():
 
 
 class ClockSampler:
-    """NVML samples of the SM clock and the clock-event reasons while the timed region runs."""
+    """Samples of the SM clock and the clock-event reasons taken while the timed region runs:
+    NVML through pynvml when it is importable, else ``nvidia-smi --query-gpu ... -lms``."""
 
     REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
                0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
 
-    def __init__(self, device_index, period_s=0.01):
+    def __init__(self, device_index, period_s=0.02):
         self.samples, self.reasons, self.max_mhz, self.error = [], set(), None, None
-        self.period, self.stop_flag, self.thread, self.h = period_s, threading.Event(), None, None
+        self.period, self.stop_flag, self.thread, self.h, self.proc = period_s, threading.Event(), None, None, None
+        props = torch.cuda.get_device_properties(device_index)
+        try:
+            self.bus = "%08X:%02X:%02X.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+        except Exception:
+            self.bus = None
         try:
             import pynvml
             pynvml.nvmlInit()
             self.nv = pynvml
-            props = torch.cuda.get_device_properties(device_index)
             try:
-                bus = "%08X:%02X:%02X.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
-                self.h = pynvml.nvmlDeviceGetHandleByPciBusId(bus.encode())
+                self.h = pynvml.nvmlDeviceGetHandleByPciBusId(self.bus.encode())
             except Exception:
                 self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception as e:  # pragma: no cover - NVML missing
-            self.error = repr(e)
+        except Exception as e:
+            self.error = f"pynvml: {e!r}; using nvidia-smi"
             self.h = None
 
-    def _run(self):
+    def _add_reasons(self, mask):
+        for bit, name in self.REASONS.items():
+            if mask & bit and bit != 0x1:
+                self.reasons.add(name)
+
+    def _run_nvml(self):
         while not self.stop_flag.is_set():
             try:
                 self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-                r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                for bit, name in self.REASONS.items():
-                    if r & bit and bit != 0x1:
-                        self.reasons.add(name)
+                self._add_reasons(self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h))
             except Exception:
                 pass
             time.sleep(self.period)
 
+    def _run_smi(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 3:
+                continue
+            try:
+                self.samples.append(float(parts[0]))
+                self.max_mhz = float(parts[1])
+                self._add_reasons(int(parts[2], 16))
+            except ValueError:
+                pass
+
     def __enter__(self):
         if self.h is not None:
-            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread = threading.Thread(target=self._run_nvml, daemon=True)
             self.thread.start()
+            return self
+        import subprocess
+        cmd = ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+               "--format=csv,noheader,nounits", "-lms", str(int(self.period * 1000))]
+        if self.bus:
+            cmd += ["-i", self.bus]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._run_smi, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)    # let the first sample land before the timed work starts
+        except Exception as e:
+            self.error = f"{self.error}; nvidia-smi: {e!r}"
         return self
 
     def __exit__(self, *exc):
         self.stop_flag.set()
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
         if self.thread:
-            self.thread.join()
+            self.thread.join(timeout=5)
 
     def summary(self):
+        out = {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
+               "reasons": sorted(self.reasons), "samples": len(self.samples),
+               "source": "nvml" if self.h is not None else "nvidia-smi"}
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": 0,
-                    "error": getattr(self, "error", "no sample taken")}
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+            out["error"] = self.error or "no sample taken"
+        return out
 
 
 def source_sha(relpath):
