@@ -344,6 +344,17 @@ class Prefill:
         self.mk.prefill_gqa_causal(s["q"], s["k"], s["v"], s["cu_seqlens"], s["max_seqlen"], out=self.out,
                                    scale=self.w.scale)
 
+    def host_inputs(self):
+        s = self.sets[0]
+        return {k: s[k].cpu().pin_memory() for k in ("q", "k", "v", "cu_seqlens")}
+
+    def e2e_step(self, host, dev_bufs, out_host):
+        for k, t in host.items():
+            dev_bufs[k].copy_(t, non_blocking=True)
+        self.mk.prefill_gqa_causal(dev_bufs["q"], dev_bufs["k"], dev_bufs["v"], dev_bufs["cu_seqlens"],
+                                   self.sets[0]["max_seqlen"], out=self.out, scale=self.w.scale)
+        out_host.copy_(self.out, non_blocking=True)
+
     def describe(self):
         w = self.w
         return {"workload": w.name, "B": w.batch, "Hq": w.n_q_heads, "Hkv": w.n_kv_heads, "D": w.head_dim,
@@ -469,7 +480,7 @@ def summarize(res, steps, peaks, peak_src, world):
     out = {"value": round(value, 2), "unit": unit, "ms_per_step": round(per_step * 1e3, 5), "roofline": roof,
            "gpu_launches": steps * wl.launches_per_step, "config": wl.describe(), "clocks": res["clocks"]}
     out.update(extra)
-    if "e2e_seconds" in res:
+    if res.get("e2e_seconds"):
         e = res["e2e_seconds"]
         ev = (wl.bytes_per_step / e / 1e9) if wl.kind == "decode" else (wl.flops_per_step / e / 1e12)
         out["e2e"] = {"value": round(ev * world, 3), "unit": unit, "h2d_bytes_per_step": res["e2e_h2d"],

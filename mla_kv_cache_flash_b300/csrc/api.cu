@@ -56,17 +56,20 @@ struct SplitPlan {
 };
 
 // Cut [0, max_S) into n_split pieces of split_len tokens (a multiple of `tile`). With
-// n_split = 0 the count is chosen so that blocks_per_split · n_split covers about
-// `waves` blocks per SM, without making a piece shorter than `min_tiles` tiles.
-SplitPlan plan_splits(int max_S, int tile, long blocks_per_split, int n_split_req, int min_tiles) {
+// n_split = 0 the count is the largest that keeps the whole grid (blocks_per_split ·
+// n_split blocks) within one wave of `resident` blocks per SM, without making a piece
+// shorter than `min_tiles` tiles. A second, partial wave of equally long blocks would nearly
+// double the time (measured on B300: MQA decode 62.8 µs with 256 blocks, 95.4 µs with 320).
+SplitPlan plan_splits(int max_S, int tile, long blocks_per_split, int n_split_req, int min_tiles,
+                      int resident = 2) {
     SplitPlan p{1, tile};
     const int max_tiles = max_S > 0 ? (max_S + tile - 1) / tile : 1;
     int n;
     if (n_split_req > 0) {
         n = n_split_req;
     } else {
-        const long target = 2L * device_sms();
-        n = (int)((target + blocks_per_split - 1) / blocks_per_split);
+        const long slots = (long)resident * device_sms();
+        n = (int)(slots / blocks_per_split);
         const int cap = max_tiles / (min_tiles > 0 ? min_tiles : 1);
         if (n > cap) n = cap;
         if (n > 64) n = 64;
@@ -275,17 +278,17 @@ MLAKV_API int attn_decode_mla_absorbed(const void *q_lat, const void *q_rope, co
 MLAKV_API int attn_prefill_gqa_causal(const void *q, const void *k, const void *v, const int *cu_seqlens,
                                       float *out, int B, int Hq, int Hkv, int D, float scale, int max_seqlen,
                                       int total_tokens, mlakv_stream_t stream) {
-    if (!q || !k || !v || !cu_seqlens || !out)
-        return fail(ATTN_ERR_NULL, "attn_prefill_gqa_causal: q, k, v, cu_seqlens and out must be non-NULL");
     if (B < 1 || Hq < 1 || Hkv < 1 || max_seqlen < 0 || total_tokens < 0)
         return fail(ATTN_ERR_SHAPE, "B, Hq, Hkv must be >= 1 and max_seqlen, total_tokens >= 0");
+    if (!cu_seqlens || (total_tokens > 0 && (!q || !k || !v || !out)))
+        return fail(ATTN_ERR_NULL, "attn_prefill_gqa_causal: q, k, v, cu_seqlens and out must be non-NULL");
     if (Hq % Hkv != 0)
         return fail(ATTN_ERR_SHAPE, "Hkv=%d does not divide Hq=%d", Hkv, Hq);
     if (D != 128) return fail(ATTN_ERR_UNSUPPORTED, "prefill head width D=%d not built (128)", D);
     if (!isfinite(scale)) return fail(ATTN_ERR_SHAPE, "scale must be finite");
+    if (total_tokens == 0 || max_seqlen == 0) return ok();
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(cu_seqlens))
         return fail(ATTN_ERR_UNSUPPORTED, "attn_prefill_gqa_causal: every pointer must be 16-byte aligned");
-    if (total_tokens == 0 || max_seqlen == 0) return ok();
     PrefillArgs a{};
     a.q = q; a.k = k; a.v = v; a.cu_seqlens = cu_seqlens; a.out = out;
     a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.T = total_tokens;

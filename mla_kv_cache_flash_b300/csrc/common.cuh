@@ -76,6 +76,24 @@ MLAKV_HIDDEN int decode_gqa_read_and_clear_status(cudaStream_t s, unsigned *flag
 MLAKV_HIDDEN int decode_mla_read_and_clear_status(cudaStream_t s, unsigned *flag);
 MLAKV_HIDDEN int prefill_read_and_clear_status(cudaStream_t s, unsigned *flag);
 
+// Launch `kern` on `s` with programmatic stream serialisation allowed: the kernel may start
+// before the previous kernel in the stream has finished, and must call griddep_wait() before
+// it touches memory that kernel may write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Sets the thread's attn_last_error() message and returns `code`.
 MLAKV_HIDDEN int report_error(int code, const char *message);
 
@@ -96,6 +114,13 @@ __device__ __forceinline__ float warp_sum(float x) {
 // bf16 → fp32 is exact: the bf16 bits are the top half of the fp32 bits.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Programmatic dependent launch. griddep_wait() returns once every grid this one depends on
+// has completed and its memory is visible (at once for a kernel launched without the
+// attribute); griddep_launch_dependents() lets the next kernel in the stream launch now, so
+// its blocks can be resident and set up while this grid finishes.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
     uint4 r;

@@ -83,6 +83,16 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
     const int h0 = j * G + hb * C::HEADS;
     const int b = blockIdx.z;
     const int split = blockIdx.x;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kConsumers);
+        }
+        fence_mbar_init();
+    }
+    // everything above overlaps the previous kernel in the stream; the inputs are read below
+    griddep_wait();
+    griddep_launch_dependents();
     const int S = a.seq_lens[b];
     const int t_begin = split * a.split_len;
     const int t_end = min(S, t_begin + a.split_len);
@@ -97,13 +107,6 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
             const uint4 v = r < heads ? __ldg(qg + (size_t)r * (D / 8) + c) : make_uint4(0, 0, 0, 0);
             *reinterpret_cast<uint4 *>(smem + C::Q_OFF + r * C::QPITCH + c * 16) = v;
         }
-    }
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, kConsumers);
-        }
-        fence_mbar_init();
     }
     __syncthreads();
 
@@ -331,8 +334,8 @@ cudaError_t launch_cfg(const DecodeGqaArgs &a, cudaStream_t st) {
     }
     const int G = a.Hq / a.Hkv;
     const dim3 grid(a.n_split, a.Hkv * ((G + C::HEADS - 1) / C::HEADS), a.B);
-    kern<<<grid, kThreads, C::SMEM, st>>>(km, vm, a);
-    return cudaGetLastError();
+    e = launch_pdl(kern, grid, dim3(kThreads), C::SMEM, st, km, vm, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int D>

@@ -76,6 +76,16 @@ decode_mla_kernel(const __grid_constant__ CUtensorMap cmap, const __grid_constan
     const int h0 = blockIdx.y * kHeads;
     const int b = blockIdx.z;
     const int split = blockIdx.x;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kConsumers);
+        }
+        fence_mbar_init();
+    }
+    // everything above overlaps the previous kernel in the stream; the inputs are read below
+    griddep_wait();
+    griddep_launch_dependents();
     const int S = a.seq_lens[b];
     const int t_begin = split * a.split_len;
     const int t_end = min(S, t_begin + a.split_len);
@@ -92,13 +102,6 @@ decode_mla_kernel(const __grid_constant__ CUtensorMap cmap, const __grid_constan
             const uint4 v = c < R / 8 ? __ldg(ql + r * (R / 8) + c) : __ldg(qr + r * (DR / 8) + (c - R / 8));
             *reinterpret_cast<uint4 *>(smem + Q_OFF + r * QPITCH + c * 16) = v;
         }
-    }
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, kConsumers);
-        }
-        fence_mbar_init();
     }
     __syncthreads();
 
@@ -287,8 +290,8 @@ cudaError_t launch_decode_mla(const DecodeMlaArgs &a, cudaStream_t st) {
         attr_set = true;
     }
     const dim3 grid(a.n_split, a.Hq / kHeads, a.B);
-    decode_mla_kernel<<<grid, kThreads, SMEM, st>>>(cm, km, a);
-    return cudaGetLastError();
+    const cudaError_t e = launch_pdl(decode_mla_kernel, grid, dim3(kThreads), SMEM, st, cm, km, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 int decode_mla_read_and_clear_status(cudaStream_t s, unsigned *flag) {

@@ -7,7 +7,9 @@
 // have lse = −inf and weigh nothing; a row with only empty splits is 0.
 //
 // One warp per output row: the lanes find M and the weight sum over the splits, then each
-// lane accumulates 4 consecutive output columns at a time with 16-byte loads.
+// lane accumulates 4 consecutive output columns at a time with 16-byte loads. The kernel is
+// launched as a programmatic dependent of the decode kernel, so its blocks are resident and
+// waiting when the partials are complete instead of paying a full launch after them.
 #include "common.cuh"
 
 #include <math.h>
@@ -22,6 +24,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const float *__restrict__ o_
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * 4 + warp;
+    griddep_wait();                 // the partials come from the previous kernel in the stream
+    griddep_launch_dependents();
     if (row >= rows) return;
     const float *lse = lse_part + (size_t)row * n_split;
     float M = -INFINITY;
@@ -57,8 +61,9 @@ __global__ void __launch_bounds__(128) merge_kernel(const float *__restrict__ o_
 cudaError_t launch_merge(const float *o_part, const float *lse_part, float *out, int rows,
                          int n_split, int Dv, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
-    merge_kernel<<<(rows + 3) / 4, 128, 0, s>>>(o_part, lse_part, out, rows, n_split, Dv);
-    return cudaGetLastError();
+    const cudaError_t e = launch_pdl(merge_kernel, dim3((rows + 3) / 4), dim3(128), 0, s, o_part, lse_part, out,
+                                     rows, n_split, Dv);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace mlakv

@@ -1,0 +1,98 @@
+"""Causal GQA prefill on the GPU (tcgen05 kernel) against the fp64 CPU oracle.
+
+Tolerance: max |Δ| ≤ 3e-3 over every output element compared (bf16 inputs, fp32
+accumulation, fp32 output). Small cases compare every row and head; the full-size
+workloads (8 × 2048 tokens, and 8 ragged sequences of 256 to 4096 tokens, Hq=32, Hkv=8,
+D=128) compare every row of a fixed sample of query heads, one from each KV group.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import mla_kv_cache_flash_b300 as mk
+import oracle
+import workloads as W
+from workloads import to_f64
+
+pytestmark = pytest.mark.gpu
+
+TOL = 3e-3
+DEV = "cuda"
+
+
+def _run(inp, scale):
+    out = mk.prefill_gqa_causal(inp["q"], inp["k"], inp["v"], inp["cu_seqlens"], inp["max_seqlen"], scale=scale)
+    mk.check_status()
+    return out
+
+
+def _ref(inp, scale, heads=None):
+    return oracle.prefill_gqa_causal(to_f64(inp["q"]), to_f64(inp["k"]), to_f64(inp["v"]),
+                                     inp["cu_seqlens"].cpu().numpy(), scale, heads=heads)
+
+
+def _err(out, ref, heads=None):
+    got = out.detach().cpu().double().numpy()
+    if heads is not None:
+        got, ref = got[:, heads], ref[:, heads]
+    return float(np.abs(got - ref).max())
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (8, 8), (8, 1), (6, 2), (4, 4), (16, 8)])
+def test_small_ragged_every_row(hq, hkv):
+    # lengths: one token, a few, a tile plus a ragged tail, several tiles and a tail
+    w = W.PrefillWorkload("prefill_small", 4, 4, hq, hkv, 128, lengths=(1, 5, 130, 300), sub=5)
+    inp = W.prefill_inputs(w, DEV)
+    out = _run(inp, w.scale)
+    err = _err(out, _ref(inp, w.scale))
+    print(f"hq={hq} hkv={hkv} max|err|={err:.3e}")
+    assert err <= TOL
+
+
+def test_empty_sequences_and_exact_tiles():
+    w = W.PrefillWorkload("prefill_edges", 4, 5, 8, 2, 128, lengths=(0, 128, 0, 256, 129), sub=6)
+    inp = W.prefill_inputs(w, DEV)
+    out = _run(inp, w.scale)
+    err = _err(out, _ref(inp, w.scale))
+    print(f"edges max|err|={err:.3e}")
+    assert err <= TOL
+
+
+def test_first_row_is_v0_and_scale_argument():
+    w = W.PrefillWorkload("prefill_row0", 4, 2, 8, 2, 128, lengths=(200, 77), sub=7)
+    inp = W.prefill_inputs(w, DEV)
+    out = _run(inp, 0.05)
+    cu = inp["cu_seqlens"].cpu().numpy()
+    for b in range(2):
+        v0 = inp["v"][int(cu[b])].float().repeat_interleave(4, dim=0)
+        assert torch.equal(out[int(cu[b])], v0)
+    assert _err(out, _ref(inp, 0.05)) <= TOL
+
+
+def test_zero_length_launches_nothing():
+    q = torch.zeros((0, 8, 128), dtype=torch.bfloat16, device=DEV)
+    kv = torch.zeros((0, 2, 128), dtype=torch.bfloat16, device=DEV)
+    cu = torch.zeros(3, dtype=torch.int32, device=DEV)
+    out = mk.prefill_gqa_causal(q, kv, kv, cu, 0)
+    assert out.shape == (0, 8, 128)
+
+
+def test_deterministic():
+    w = W.PrefillWorkload("prefill_det", 4, 3, 8, 2, 128, lengths=(500, 33, 700), sub=8)
+    inp = W.prefill_inputs(w, DEV)
+    a = _run(inp, w.scale)
+    b = _run(inp, w.scale)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("wl", [W.PREFILL_UNIFORM, W.PREFILL_RAGGED], ids=["uniform", "ragged"])
+def test_full_size_sampled_heads(wl):
+    inp = W.prefill_inputs(wl, DEV)
+    out = _run(inp, wl.scale)
+    g = wl.n_q_heads // wl.n_kv_heads
+    heads = [j * g + (j % g) for j in range(wl.n_kv_heads)]     # one head of every KV group
+    err = _err(out, _ref(inp, wl.scale, heads=heads), heads)
+    print(f"{wl.name} heads={heads} max|err|={err:.3e}")
+    assert err <= TOL
+    assert torch.isfinite(out).all()
