@@ -20,7 +20,7 @@
 // are merged in shared memory; the block writes out = O/l (one split) or the normalised
 // partial and lse = ln Σ e^s for the log-sum-exp merge kernel.
 //
-// Every mbarrier wait is bounded (MLAKV_WAIT_TIMEOUT_NS); a wait that runs out sets a bit in
+// Every mbarrier wait is bounded (MLAKV_WAIT_TIMEOUT_CYCLES); a wait that runs out sets a bit in
 // g_decode_gqa_status and the block returns, so a broken pipeline cannot hang the GPU.
 #include "ptx.cuh"
 #include "tensor_map.cuh"

@@ -4,25 +4,30 @@
 // the qqstock MLA code's scaled_dot_product_attention with is_causal=True): row i of a
 // sequence attends keys 0 .. i of the same sequence through KV head h / G,
 //   out[i, h] = Σ_{t ≤ i} softmax_t(scale · q[i,h]·k[t,j]) · v[t,j].
-// It is the one dense contraction of the path, so both products run on tcgen05:
+// It is the one dense contraction of the path, so both products run on tcgen05.
 //
-// One thread block = (sequence b, 128-row query tile qt, two query heads of one KV group).
-// The two heads share the KV head, so every K/V tile that lands in shared memory feeds two
-// 128×128 score tiles (GQA: each K/V byte is fetched once per pair of query heads, not per
-// head). Query tiles with the most KV tiles are scheduled first. Warp roles:
-//   warp 0     TMA producer: the two Q tiles once, then K and V tiles (128 keys × 128 columns,
-//              128-byte swizzle) through a 2-stage ring.
-//   warp 1     allocates 512 TMEM columns; lane 0 issues every MMA:
+// Work item = (sequence b, 128-row query tile qt, two query heads of one KV group; one head
+// when the group size is odd). The two heads share the KV head, so every K/V tile that lands
+// in shared memory feeds two 128×128 score tiles. The kernel is persistent: one block per
+// SM walks a fixed list of items, longest (most KV tiles) first, dealt to the blocks in
+// alternating order so their totals stay even. One item's output stores and the next item's
+// Q load overlap the MMAs. Warp roles:
+//   warp 0     TMA producer: each item's two Q tiles, then its K and V tiles (128 keys × 128
+//              columns, 128-byte swizzle) through a 2-stage ring that runs across items.
+//   warp 1     allocates 512 TMEM columns once; the warp runs the MMA loop and lane 0
+//              issues every MMA:
 //                S_t = Q_t · K_nᵀ   (M=128, N=128, K=16 × 8; A, B K-major in shared memory)
 //                O_t += P_t · V_n   (A = P from TMEM, B = V MN-major in shared memory)
 //              and commits each group to an mbarrier.
 //   warps 2-9  softmax, one warpgroup per query tile; thread = one query row (one TMEM
-//              lane). It reads its 128 scores from TMEM, applies the causal mask on the
-//              diagonal tile, keeps a running max m and sum l in the base-2 domain and writes
-//              P = 2^(s·scale·log2 e − m) as bf16 back over its scores. The output is
-//              rescaled only when the row max grows by more than 2^8 (the result is exact for
-//              any reference value; this only bounds the range of P and l).
-// At the end each softmax thread reads its O row from TMEM and writes O / l (fp32).
+//              lane). It reads its 128 scores from TMEM, masks the diagonal tile, keeps a
+//              running max m and sum l in the base-2 domain and writes
+//              P = 2^(s·scale·log2 e − m) as bf16 over its scores. The output is rescaled
+//              only when the row max grows by more than 2^8 (the result is exact for any
+//              reference value; this only bounds the range of P and l). At the end of an
+//              item it reads its O row from TMEM and writes O / l (fp32).
+// The softmax uses Blackwell's paired fp32 FMA/add (two lanes of work per instruction) and
+// the three-input max, which halve its instruction count.
 //
 // TMEM: per query tile t, columns [256t, 256t+128) hold S (P aliases its first 64 columns,
 // two bf16 per column) and [256t+128, 256t+256) hold O. An S tile is written only after the
@@ -31,10 +36,10 @@
 // Precision: P is rounded to bf16 for the tensor cores, a relative error of up to 2^-8 per
 // weight. Rows with many keys average it away, but rows near the start of a sequence see
 // few keys (row 1 sees 2); in the first kSplitTiles query tiles P is therefore split into a
-// bf16 head and a bf16 residual and both are multiplied with V, which leaves an error near
-// 2^-16 there.
+// bf16 head and a bf16 residual (columns [64, 128) of the S region) and both are multiplied
+// with V, which leaves an error near 2^-16 there.
 //
-// Every wait is bounded (MLAKV_WAIT_TIMEOUT_NS): a wait that runs out sets a bit in
+// Every wait is bounded (MLAKV_WAIT_TIMEOUT_CYCLES): a wait that runs out sets a bit in
 // g_prefill_status and the thread abandons its loop; every thread still reaches the final
 // barrier, so tensor memory is always released.
 #include "ptx.cuh"
@@ -50,12 +55,12 @@ __device__ unsigned g_prefill_status;
 namespace {
 
 constexpr int HD = 128;                      // head width
-constexpr int BM = 128;                      // query rows per tile
+constexpr int BM = 128;                      // query rows per tile (TMEM lanes)
 constexpr int BN = 128;                      // keys per KV tile
 constexpr int NSTAGE = 2;                    // K/V ring depth
 constexpr int TILE_BYTES = BM * HD * 2;      // one 128 × 128 bf16 tile: 32 KB
 constexpr int BOX_BYTES = TILE_BYTES / 2;    // one TMA box: 128 rows × 64 columns (128 B)
-constexpr int Q_OFF = 0;
+constexpr int Q_OFF = 0;                     // two Q tiles
 constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
 constexpr int V_OFF = K_OFF + NSTAGE * TILE_BYTES;
 constexpr int BAR_OFF = V_OFF + NSTAGE * TILE_BYTES;
@@ -79,72 +84,119 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, HD, false, true);   // P from T
 // mbarrier slots (8 bytes each) inside the barrier block
 enum : int {
     kQFull = 0,
-    kKFull = 1,          // + stage
-    kVFull = 3,          // + stage
-    kKvEmpty = 5,        // + stage
-    kSFull = 7,          // + query tile
-    kPReady = 9,         // + query tile
-    kODone = 11          // + query tile
+    kQEmpty = 1,         // the item's last S MMAs are done: its Q tiles may be replaced
+    kKFull = 2,          // + stage
+    kVFull = 4,          // + stage
+    kKvEmpty = 6,        // + stage
+    kSFull = 8,          // + query tile
+    kPReady = 10,        // + query tile
+    kODone = 12          // + query tile
 };
 
-// Row max of x = s·c (c = scale·log2 e) over one row of a score tile in TMEM (128 columns at
-// s_addr). DIAG: the diagonal tile of a causal sequence, where key i is visible to `row` only
-// if i <= row (key 0 always is, so the result is finite).
-template <bool DIAG>
-__device__ __forceinline__ float row_max(uint32_t s_addr, float c, int row) {
-    float mx = -INFINITY;
-#pragma unroll
-    for (int ch = 0; ch < BN / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(s_addr + ch * 32, r);
-        tmem_ld_wait(r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float x = __uint_as_float(r[i]) * c;
-            mx = (!DIAG || ch * 32 + i <= row) ? fmaxf(mx, x) : mx;
-        }
-    }
-    return mx;
+// ------------------------------------------------------------------ paired fp32 arithmetic
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
-// P = 2^(s·c − m) for the same row (0 for hidden keys), as bf16 pairs over TMEM columns
-// [0, 64) of the row's S region; P columns of chunk k lie below the S columns still to be
-// read, so each chunk is read before anything overwrites it. With SPLIT the bf16 residuals
-// p − bf16(p) go to columns [64, 128) after the whole row has been read. Adds the unrounded
-// weights to l.
+// The largest (NEG: smallest) visible raw score of one row held in registers, so that the row
+// max of x = s·c is c times it (c = scale·log2 e; NEG when c < 0). DIAG: the diagonal tile,
+// where key i is visible only to rows `row` >= i (key 0 always is, so the result is finite).
+// Eight independent partial extrema keep the dependency chains short.
+template <bool DIAG, bool NEG>
+__device__ __forceinline__ float row_extreme(const uint32_t (&r)[BN], int row) {
+    constexpr float kNone = NEG ? INFINITY : -INFINITY;
+    float e[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) e[i] = kNone;
+#pragma unroll
+    for (int i = 0; i < BN; i += 2) {
+        float v0 = __uint_as_float(r[i]), v1 = __uint_as_float(r[i + 1]);
+        if (DIAG) {
+            v0 = i <= row ? v0 : kNone;
+            v1 = i + 1 <= row ? v1 : kNone;
+        }
+        const int k = (i >> 1) & 7;
+        e[k] = NEG ? fmin3(e[k], v0, v1) : fmax3(e[k], v0, v1);
+    }
+    return NEG ? fminf(fmin3(e[0], e[1], e[2]), fmin3(fmin3(e[3], e[4], e[5]), e[6], e[7]))
+               : fmaxf(fmax3(e[0], e[1], e[2]), fmax3(fmax3(e[3], e[4], e[5]), e[6], e[7]));
+}
+
+// P = 2^(s·c − m) for the row held in registers (0 for hidden keys), written as bf16 pairs to
+// TMEM columns [0, 64) of the row's S region; with SPLIT also the bf16 residual p − bf16(p)
+// to columns [64, 128). The whole row is already in registers, so nothing is overwritten
+// before it is read. Adds the unrounded weights to l.
 template <bool DIAG, bool SPLIT>
-__device__ __forceinline__ void write_p(uint32_t s_addr, float c, float m, int row, float &l) {
-    uint32_t lo[SPLIT ? BN / 2 : 1];
+__device__ __forceinline__ void write_p(const uint32_t (&r)[BN], float c, float m, int row, float &l,
+                                        uint32_t s_addr) {
+    const uint64_t c2 = f2pack(c, c), nm2 = f2pack(-m, -m);
+    uint64_t acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = 0;
 #pragma unroll
     for (int ch = 0; ch < BN / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(s_addr + ch * 32, r);
-        tmem_ld_wait(r);
-        uint32_t hi[16];
+        uint32_t hi[16], lo[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int k0 = ch * 32 + 2 * i;
-            float p0 = fast_exp2(fmaf(__uint_as_float(r[2 * i]), c, -m));
-            float p1 = fast_exp2(fmaf(__uint_as_float(r[2 * i + 1]), c, -m));
+            float x0, x1;
+            f2unpack(ffma2(f2pack(__uint_as_float(r[k0]), __uint_as_float(r[k0 + 1])), c2, nm2), x0, x1);
+            float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
             if (DIAG) {
                 p0 = k0 <= row ? p0 : 0.f;
                 p1 = k0 + 1 <= row ? p1 : 0.f;
             }
-            l += p0 + p1;
+            acc[i & 3] = fadd2(acc[i & 3], f2pack(p0, p1));
             hi[i] = pack_bf16x2(p0, p1);
-            if constexpr (SPLIT) lo[ch * 16 + i] = pack_bf16x2(p0 - bf16_lo(hi[i]), p1 - bf16_hi(hi[i]));
+            if constexpr (SPLIT) lo[i] = pack_bf16x2(p0 - bf16_lo(hi[i]), p1 - bf16_hi(hi[i]));
         }
         tmem_st16(s_addr + ch * 16, hi);
+        if constexpr (SPLIT) tmem_st16(s_addr + BN / 2 + ch * 16, lo);
     }
-    if constexpr (SPLIT) {
-#pragma unroll
-        for (int ch = 0; ch < BN / 32; ++ch) {
-            uint32_t part[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) part[i] = lo[ch * 16 + i];
-            tmem_st16(s_addr + 64 + ch * 16, part);
-        }
-    }
+    float a0, a1;
+    f2unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), a0, a1);
+    l += a0 + a1;
+}
+
+// The k-th item of block `blk` (of `nblk`) in the dealt order: item positions are taken in
+// rounds of nblk, alternating direction, over the list sorted longest first.
+struct Item {
+    int qt, b, h0;
+};
+__device__ __forceinline__ bool item_at(int k, int blk, int nblk, int n_items, int per_qt, int n_hgrp,
+                                        int heads_per_cta, int n_qt, Item &it) {
+    const int pos = k * nblk + ((k & 1) ? (nblk - 1 - blk) : blk);
+    if (pos >= n_items) return false;
+    it.qt = n_qt - 1 - pos / per_qt;
+    const int rem = pos % per_qt;
+    it.b = rem / n_hgrp;
+    it.h0 = (rem % n_hgrp) * heads_per_cta;
+    return true;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -158,26 +210,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // work item; the longest query tiles (most KV tiles) come first
     const int n_hgrp = a.Hq / heads_per_cta;
     const int per_qt = a.B * n_hgrp;
-    const int qt = n_qt - 1 - (int)(blockIdx.x / per_qt);
-    const int rem = (int)(blockIdx.x % per_qt);
-    const int b = rem / n_hgrp;
-    const int h0 = (rem % n_hgrp) * heads_per_cta;
-    const int n_mt = heads_per_cta;                 // query tiles in this block (heads h0, h0+1)
-    const int j = h0 / (a.Hq / a.Hkv);              // their KV head
-
-    griddep_wait();
-    const int seq0 = a.cu_seqlens[b];
-    const int S = a.cu_seqlens[b + 1] - seq0;
-    if (qt * BM >= S) return;                       // the whole block leaves before any setup
-    const int n_kv = qt + 1;                        // KV tiles 0 .. qt (causal, equal lengths)
-    const bool split_p = qt < kSplitTiles;          // short rows: P as bf16 head + residual
+    const int n_items = n_qt * per_qt;
+    const int n_mt = heads_per_cta;                 // query tiles per item (heads h0, h0+1)
+    const int G = a.Hq / a.Hkv;
+    const int blk = blockIdx.x, nblk = gridDim.x;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(kQFull), 1);
+        mbar_init(bar(kQEmpty), 1);
         for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(bar(kKFull + s), 1);
             mbar_init(bar(kVFull + s), 1);
@@ -198,6 +240,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    griddep_wait();                                 // cu_seqlens and the inputs are read below
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -205,117 +248,175 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             prefetch_tensormap(&qmap);
             prefetch_tensormap(&kmap);
             prefetch_tensormap(&vmap);
-            const int q_tok = seq0 + qt * BM;
-            mbar_arrive_expect_tx(bar(kQFull), n_mt * TILE_BYTES);
-            for (int t = 0; t < n_mt; ++t)
-                for (int bx = 0; bx < 2; ++bx)
-                    tma_load_3d(sb + Q_OFF + t * TILE_BYTES + bx * BOX_BYTES, &qmap, bx * 64, h0 + t, q_tok,
-                                bar(kQFull), l2_evict_first_policy());
-            int issued = 0;
-            for (int n = 0; n < n_kv; ++n) {
-                const int s = n % NSTAGE;
-                if (!mbar_wait_bounded(bar(kKvEmpty + s), ((n / NSTAGE) & 1) ^ 1, &g_prefill_status, kStatusEmptyWait))
+            const uint64_t pol_q = l2_evict_first_policy();
+            int g_kv = 0, n_done = 0;
+            bool ok = true;
+            Item it;
+            for (int k = 0; ok && item_at(k, blk, nblk, n_items, per_qt, n_hgrp, heads_per_cta, n_qt, it); ++k) {
+                const int seq0 = a.cu_seqlens[it.b];
+                const int S = a.cu_seqlens[it.b + 1] - seq0;
+                if (it.qt * BM >= S) continue;
+                const int j = it.h0 / G;
+                if (n_done > 0 && !mbar_wait_bounded(bar(kQEmpty), (n_done - 1) & 1, &g_prefill_status, kStatusEmptyWait)) {
+                    ok = false;
                     break;
-                const int k_tok = seq0 + n * BN;
-                mbar_arrive_expect_tx(bar(kKFull + s), TILE_BYTES);
-                for (int bx = 0; bx < 2; ++bx)
-                    tma_load_3d_nohint(sb + K_OFF + s * TILE_BYTES + bx * BOX_BYTES, &kmap, bx * 64, j, k_tok,
-                                       bar(kKFull + s));
-                mbar_arrive_expect_tx(bar(kVFull + s), TILE_BYTES);
-                for (int bx = 0; bx < 2; ++bx)
-                    tma_load_3d_nohint(sb + V_OFF + s * TILE_BYTES + bx * BOX_BYTES, &vmap, bx * 64, j, k_tok,
-                                       bar(kVFull + s));
-                issued = n + 1;
+                }
+                mbar_arrive_expect_tx(bar(kQFull), n_mt * TILE_BYTES);
+                for (int t = 0; t < n_mt; ++t)
+                    for (int bx = 0; bx < 2; ++bx)
+                        tma_load_3d(sb + Q_OFF + t * TILE_BYTES + bx * BOX_BYTES, &qmap, bx * 64, it.h0 + t,
+                                    seq0 + it.qt * BM, bar(kQFull), pol_q);
+                for (int n = 0; n <= it.qt; ++n, ++g_kv) {
+                    const int s = g_kv % NSTAGE;
+                    if (!mbar_wait_bounded(bar(kKvEmpty + s), ((g_kv / NSTAGE) & 1) ^ 1, &g_prefill_status,
+                                           kStatusEmptyWait)) {
+                        ok = false;
+                        break;
+                    }
+                    const int k_tok = seq0 + n * BN;
+                    mbar_arrive_expect_tx(bar(kKFull + s), TILE_BYTES);
+                    for (int bx = 0; bx < 2; ++bx)
+                        tma_load_3d_nohint(sb + K_OFF + s * TILE_BYTES + bx * BOX_BYTES, &kmap, bx * 64, j, k_tok,
+                                           bar(kKFull + s));
+                    mbar_arrive_expect_tx(bar(kVFull + s), TILE_BYTES);
+                    for (int bx = 0; bx < 2; ++bx)
+                        tma_load_3d_nohint(sb + V_OFF + s * TILE_BYTES + bx * BOX_BYTES, &vmap, bx * 64, j, k_tok,
+                                           bar(kVFull + s));
+                }
+                ++n_done;
             }
             // no copy may still be in flight when the block exits
-            mbar_wait_bounded(bar(kQFull), 0, &g_prefill_status, kStatusDrainWait);
-            for (int n = issued > NSTAGE ? issued - NSTAGE : 0; n < issued; ++n) {
-                mbar_wait_bounded(bar(kKFull + n % NSTAGE), (n / NSTAGE) & 1, &g_prefill_status, kStatusDrainWait);
-                mbar_wait_bounded(bar(kVFull + n % NSTAGE), (n / NSTAGE) & 1, &g_prefill_status, kStatusDrainWait);
+            if (n_done > 0) mbar_wait_bounded(bar(kQFull), (n_done - 1) & 1, &g_prefill_status, kStatusDrainWait);
+            for (int g = g_kv > NSTAGE ? g_kv - NSTAGE : 0; g < g_kv; ++g) {
+                mbar_wait_bounded(bar(kKFull + g % NSTAGE), (g / NSTAGE) & 1, &g_prefill_status, kStatusDrainWait);
+                mbar_wait_bounded(bar(kVFull + g % NSTAGE), (g / NSTAGE) & 1, &g_prefill_status, kStatusDrainWait);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            bool ok = mbar_wait_bounded(bar(kQFull), 0, &g_prefill_status, kStatusFullWait);
-            for (int n = 0; n < n_kv && ok; ++n) {
-                const int s = n % NSTAGE;
-                const uint32_t ph = (n / NSTAGE) & 1;
-                if (!mbar_wait_bounded(bar(kKFull + s), ph, &g_prefill_status, kStatusFullWait)) {
+        // The whole warp runs the loop, so the descriptors stay warp-uniform; lane 0 alone
+        // issues the MMAs and the commits that track them. Descriptors are built once: a
+        // byte offset inside shared memory (< 256 KB) adds to the 14-bit start-address field
+        // in 16-byte units without carrying out of it.
+        const uint64_t q_desc = sdesc_sw128(sb + Q_OFF, 16, 1024);
+        const uint64_t k_desc = sdesc_sw128(sb + K_OFF, 16, 1024);
+        const uint64_t v_desc = sdesc_sw128(sb + V_OFF, BOX_BYTES, 1024);
+        auto wait_all = [&](int idx, uint32_t parity, unsigned code) {
+            const bool got = mbar_wait_bounded(bar(idx), parity, &g_prefill_status, code);
+            return __all_sync(0xffffffffu, got);
+        };
+        int g = 0, n_done = 0;                      // iterations and items of this block so far
+        bool ok = true;
+        Item it;
+        for (int k = 0; ok && item_at(k, blk, nblk, n_items, per_qt, n_hgrp, heads_per_cta, n_qt, it); ++k) {
+            const int S = a.cu_seqlens[it.b + 1] - a.cu_seqlens[it.b];
+            if (it.qt * BM >= S) continue;
+            const bool split_p = it.qt < kSplitTiles;
+            if (!wait_all(kQFull, n_done & 1, kStatusFullWait)) {
+                ok = false;
+                break;
+            }
+            for (int n = 0; n <= it.qt; ++n, ++g) {
+                const int s = g % NSTAGE;
+                const uint32_t ph = (g / NSTAGE) & 1;
+                if (!wait_all(kKFull + s, ph, kStatusFullWait)) {
                     ok = false;
                     break;
                 }
-                for (int t = 0; t < n_mt && ok; ++t) {
-                    // the previous P·V of this tile must be done before S overwrites P
-                    if (n > 0 && !mbar_wait_bounded(bar(kODone + t), (n - 1) & 1, &g_prefill_status, kStatusMmaWait)) {
+                for (int t = 0; t < n_mt; ++t) {
+                    // the previous P·V of this tile (maybe of the previous item) must be done
+                    // before S overwrites P
+                    if (g > 0 && !wait_all(kODone + t, (g - 1) & 1, kStatusMmaWait)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t qa = sb + Q_OFF + t * TILE_BYTES;
-                    const uint32_t ka = sb + K_OFF + s * TILE_BYTES;
+                    if (lane == 0) {
+                        const uint64_t kd = k_desc + (uint64_t)((s * TILE_BYTES) >> 4);
+                        const uint64_t qd = q_desc + (uint64_t)((t * TILE_BYTES) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < HD / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-                        umma_ss(tmem + 256 * t, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                                kIdescS, kk > 0);
+                        for (int kk = 0; kk < HD / 16; ++kk) {
+                            const uint32_t off = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
+                            umma_ss(tmem + 256 * t, qd + off, kd + off, kIdescS, kk > 0);
+                        }
+                        umma_commit(bar(kSFull + t));
+                        if (n == it.qt && t == n_mt - 1) umma_commit(bar(kQEmpty));
                     }
-                    umma_commit(bar(kSFull + t));
+                    __syncwarp();
                 }
                 if (!ok) break;
-                if (!mbar_wait_bounded(bar(kVFull + s), ph, &g_prefill_status, kStatusFullWait)) {
+                if (!wait_all(kVFull + s, ph, kStatusFullWait)) {
                     ok = false;
                     break;
                 }
-                const uint32_t va = sb + V_OFF + s * TILE_BYTES;
-                for (int t = 0; t < n_mt && ok; ++t) {
-                    if (!mbar_wait_bounded(bar(kPReady + t), n & 1, &g_prefill_status, kStatusMmaWait)) {
+                for (int t = 0; t < n_mt; ++t) {
+                    if (!wait_all(kPReady + t, g & 1, kStatusMmaWait)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t o = tmem + 256 * t + 128;
-                    const uint32_t p = tmem + 256 * t;
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
-                        umma_ts(o, p + kk * 8, sdesc_sw128(va + kk * 2048, BOX_BYTES, 1024), kIdescPV,
-                                (n > 0 || kk > 0) ? 1u : 0u);
-                    if (split_p) {
+                    if (lane == 0) {
+                        const uint32_t p = tmem + 256 * t;
+                        const uint64_t vd = v_desc + (uint64_t)((s * TILE_BYTES) >> 4);
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk)
-                            umma_ts(o, p + 64 + kk * 8, sdesc_sw128(va + kk * 2048, BOX_BYTES, 1024), kIdescPV, 1u);
+                            umma_ts(p + 128, p + kk * 8, vd + ((kk * 2048) >> 4), kIdescPV, (n > 0 || kk > 0) ? 1u : 0u);
+                        if (split_p) {
+#pragma unroll
+                            for (int kk = 0; kk < BN / 16; ++kk)
+                                umma_ts(p + 128, p + BN / 2 + kk * 8, vd + ((kk * 2048) >> 4), kIdescPV, 1u);
+                        }
+                        umma_commit(bar(kODone + t));
                     }
-                    umma_commit(bar(kODone + t));
+                    __syncwarp();
                 }
-                // release the stage; the last one is never reused, so nothing arrives after exit
-                if (ok && n + 1 < n_kv) umma_commit(bar(kKvEmpty + s));
+                if (!ok) break;
+                if (lane == 0) umma_commit(bar(kKvEmpty + s));
+                __syncwarp();
             }
+            ++n_done;
+        }
+        // the last commits must have arrived before the block exits
+        if (g > 0) {
+            mbar_wait_bounded(bar(kKvEmpty + (g - 1) % NSTAGE), ((g - 1) / NSTAGE) & 1, &g_prefill_status,
+                              kStatusDrainWait);
+            mbar_wait_bounded(bar(kQEmpty), (n_done - 1) & 1, &g_prefill_status, kStatusDrainWait);
         }
     } else {
         // ------------------------------------------------------------ softmax warpgroups
         const int t = (warp - 2) >> 2;               // query tile of this warpgroup
         const int quarter = warp & 3;                // the TMEM lanes this warp may touch
         const int row = quarter * 32 + lane;         // query row within the tile
-        if (t < n_mt) {
-            const uint32_t s_addr = tmem + 256 * t + ((uint32_t)(quarter * 32) << 16);
-            const uint32_t o_addr = s_addr + 128;
+        const uint32_t s_addr = tmem + 256 * t + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t o_addr = s_addr + 128;
+        const bool neg = a.scale_log2 < 0.f;         // the row max of s·c is then c·min(s)
+        int g = 0;
+        bool ok = t < n_mt;
+        Item it;
+        for (int k = 0; ok && item_at(k, blk, nblk, n_items, per_qt, n_hgrp, heads_per_cta, n_qt, it); ++k) {
+            const int seq0 = a.cu_seqlens[it.b];
+            const int S = a.cu_seqlens[it.b + 1] - seq0;
+            if (it.qt * BM >= S) continue;
+            const bool split_p = it.qt < kSplitTiles;
             float m_ref = -INFINITY, l = 0.f;
-            bool ok = true;
-            for (int n = 0; n < n_kv; ++n) {
+            for (int n = 0; n <= it.qt; ++n, ++g) {
                 // the warp decides together: the TMEM accesses below are warp-collective
-                const bool got = mbar_wait_bounded(bar(kSFull + t), n & 1, &g_prefill_status, kStatusFullWait);
+                const bool got = mbar_wait_bounded(bar(kSFull + t), g & 1, &g_prefill_status, kStatusFullWait);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const bool diag = n == qt;
-                const float mt = diag ? row_max<true>(s_addr, a.scale_log2, row)
-                                      : row_max<false>(s_addr, a.scale_log2, row);
+                uint32_t r[BN];
+                tmem_ld128_sync(s_addr, r);
+                const bool diag = n == it.qt;
+                const float ext = neg ? (diag ? row_extreme<true, true>(r, row) : row_extreme<false, true>(r, row))
+                                      : (diag ? row_extreme<true, false>(r, row) : row_extreme<false, false>(r, row));
+                const float mt = ext * a.scale_log2;
                 float alpha = 1.f;
                 bool grow = false;
                 if (n == 0) {
-                    m_ref = mt;
+                    m_ref = mt;                      // key 0 of a tile is always visible
                 } else if (mt > m_ref + kRescaleLog2) {
                     alpha = fast_exp2(m_ref - mt);
                     m_ref = mt;
@@ -326,45 +427,51 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     // O (complete up to tile n-1: S_n was issued after that P·V finished) *= alpha
 #pragma unroll
                     for (int c = 0; c < HD / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(o_addr + c * 32, r);
-                        tmem_ld_wait(r);
+                        uint32_t o[32];
+                        tmem_ld32(o_addr + c * 32, o);
+                        tmem_ld_wait(o);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(o_addr + c * 32, r);
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(o_addr + c * 32, o);
                     }
                 }
                 if (split_p)
-                    diag ? write_p<true, true>(s_addr, a.scale_log2, m_ref, row, l)
-                         : write_p<false, true>(s_addr, a.scale_log2, m_ref, row, l);
+                    diag ? write_p<true, true>(r, a.scale_log2, m_ref, row, l, s_addr)
+                         : write_p<false, true>(r, a.scale_log2, m_ref, row, l, s_addr);
                 else if (diag)
-                    write_p<true, false>(s_addr, a.scale_log2, m_ref, row, l);
+                    write_p<true, false>(r, a.scale_log2, m_ref, row, l, s_addr);
                 else
-                    write_p<false, false>(s_addr, a.scale_log2, m_ref, row, l);
+                    write_p<false, false>(r, a.scale_log2, m_ref, row, l, s_addr);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(bar(kPReady + t));
             }
-            const bool done = ok && mbar_wait_bounded(bar(kODone + t), (n_kv - 1) & 1, &g_prefill_status, kStatusMmaWait);
-            if (__all_sync(0xffffffffu, done)) {
-                tc_fence_after();
-                const int q_row = qt * BM + row;
-                const float inv = 1.f / l;
-                float4 *dst = reinterpret_cast<float4 *>(a.out + ((size_t)(seq0 + q_row) * a.Hq + h0 + t) * HD);
+            if (!ok) break;
+            // epilogue: the item's last P·V of this tile is iteration g-1
+            const bool done = mbar_wait_bounded(bar(kODone + t), (g - 1) & 1, &g_prefill_status, kStatusMmaWait);
+            if (!__all_sync(0xffffffffu, done)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int q_row = it.qt * BM + row;
+            const float inv = 1.f / l;
+            float4 *dst = reinterpret_cast<float4 *>(a.out + ((size_t)(seq0 + q_row) * a.Hq + it.h0 + t) * HD);
 #pragma unroll
-                for (int c = 0; c < HD / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(o_addr + c * 32, r);
-                    tmem_ld_wait(r);
-                    if (q_row < S) {
+            for (int c = 0; c < HD / 64; ++c) {
+                uint32_t o[64];
+                tmem_ld64_sync(o_addr + c * 64, o);
+                if (q_row < S) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            dst[c * 8 + i] = make_float4(
-                                __uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                                __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
-                    }
+                    for (int i = 0; i < 16; ++i)
+                        dst[c * 16 + i] = make_float4(
+                            __uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                            __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
                 }
             }
+            // the next item's first P·V overwrites O; it waits for this warpgroup's next
+            // "P ready", which comes after these loads
+            tc_fence_before();
         }
     }
 
@@ -382,21 +489,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t st) {
     if (a.D != HD) return cudaErrorInvalidValue;
     CUtensorMap qm, km, vm;
-    const uint32_t box[3] = {64, 1, BM};
+    const uint32_t qbox[3] = {64, 1, BM};
+    const uint32_t kvbox[3] = {64, 1, BN};
     {
         const uint64_t dims[3] = {(uint64_t)HD, (uint64_t)a.Hq, (uint64_t)a.T};
         const uint64_t strides[2] = {(uint64_t)HD * 2, (uint64_t)a.Hq * HD * 2};
-        cudaError_t e = encode_tensor_map(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, dims, strides, box,
+        cudaError_t e = encode_tensor_map(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, dims, strides, qbox,
                                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         if (e != cudaSuccess) return e;
     }
     {
         const uint64_t dims[3] = {(uint64_t)HD, (uint64_t)a.Hkv, (uint64_t)a.T};
         const uint64_t strides[2] = {(uint64_t)HD * 2, (uint64_t)a.Hkv * HD * 2};
-        cudaError_t e = encode_tensor_map(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.k, dims, strides, box,
+        cudaError_t e = encode_tensor_map(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.k, dims, strides, kvbox,
                                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         if (e == cudaSuccess)
-            e = encode_tensor_map(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.v, dims, strides, box,
+            e = encode_tensor_map(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.v, dims, strides, kvbox,
                                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         if (e != cudaSuccess) return e;
     }
@@ -409,11 +517,15 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t st) {
     const int G = a.Hq / a.Hkv;
     const int heads_per_cta = (G % 2 == 0) ? 2 : 1;
     const int n_qt = (a.max_seqlen + BM - 1) / BM;
-    const long blocks = (long)n_qt * a.B * (a.Hq / heads_per_cta);
-    if (blocks <= 0) return cudaSuccess;
-    if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
-    const cudaError_t e = launch_pdl(prefill_kernel, dim3((unsigned)blocks), dim3(kThreads), SMEM, st, qm, km, vm, a,
-                                     n_qt, heads_per_cta);
+    const long n_items = (long)n_qt * a.B * (a.Hq / heads_per_cta);
+    if (n_items <= 0) return cudaSuccess;
+    if (n_items > 0x7fffffffL) return cudaErrorInvalidValue;
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorInvalidDevice;
+    const int grid = (int)(n_items < sms ? n_items : sms);
+    const cudaError_t e = launch_pdl(prefill_kernel, dim3(grid), dim3(kThreads), SMEM, st, qm, km, vm, a, n_qt,
+                                     heads_per_cta);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

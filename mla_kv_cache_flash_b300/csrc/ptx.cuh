@@ -9,10 +9,12 @@
 
 namespace mlakv {
 
-// A bounded wait gives up after this many nanoseconds of %globaltimer, sets a status bit
-// and lets the kernel return instead of hanging.
-#ifndef MLAKV_WAIT_TIMEOUT_NS
-#define MLAKV_WAIT_TIMEOUT_NS 2000000000ull
+// A bounded wait gives up after this many SM clock cycles (about 2 s at the B300's 2.03 GHz
+// boost clock, longer at lower clocks), sets a status bit and lets the kernel return instead
+// of hanging. The SM cycle counter is read because it costs a few cycles, where the global
+// nanosecond timer is far slower to read and would sit on every wake-up path.
+#ifndef MLAKV_WAIT_TIMEOUT_CYCLES
+#define MLAKV_WAIT_TIMEOUT_CYCLES 4000000000ll
 #endif
 
 enum : unsigned {
@@ -66,14 +68,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with parity `parity` to complete. Returns false (after setting
-// `code` in *status) if it has not completed within MLAKV_WAIT_TIMEOUT_NS.
+// `code` in *status) if it has not completed within MLAKV_WAIT_TIMEOUT_CYCLES.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, unsigned *status, unsigned code,
-                                                  uint64_t timeout_ns = MLAKV_WAIT_TIMEOUT_NS) {
+                                                  long long timeout_cycles = MLAKV_WAIT_TIMEOUT_CYCLES) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > timeout_ns) {
+        if (clock64() - t0 > timeout_cycles) {
             atomicOr(status, code);
             return false;
         }

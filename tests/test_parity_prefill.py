@@ -78,12 +78,16 @@ def test_zero_length_launches_nothing():
     assert out.shape == (0, 8, 128)
 
 
-def test_deterministic():
-    w = W.PrefillWorkload("prefill_det", 4, 3, 8, 2, 128, lengths=(500, 33, 700), sub=8)
+def test_deterministic_under_full_occupancy():
+    # enough blocks that two share every SM and warps run ahead of each other: any missing
+    # synchronisation between the softmax warps and the MMA issuer shows up as run-to-run
+    # differences (the kernel's arithmetic order is fixed, so correct runs are bit-identical)
+    w = W.PrefillWorkload("prefill_det", 4, 8, 32, 8, 128, lengths=(1024, 1000, 777, 1024, 64, 900, 1024, 513), sub=8)
     inp = W.prefill_inputs(w, DEV)
-    a = _run(inp, w.scale)
-    b = _run(inp, w.scale)
-    assert torch.equal(a, b)
+    first = _run(inp, w.scale)
+    for _ in range(6):
+        assert torch.equal(_run(inp, w.scale), first)
+    assert _err(first, _ref(inp, w.scale, heads=[0, 13, 31]), [0, 13, 31]) <= TOL
 
 
 @pytest.mark.parametrize("wl", [W.PREFILL_UNIFORM, W.PREFILL_RAGGED], ids=["uniform", "ragged"])
