@@ -29,15 +29,16 @@
 // The softmax uses Blackwell's paired fp32 FMA/add (two lanes of work per instruction) and
 // the three-input max, which halve its instruction count.
 //
-// TMEM: per query tile t, columns [256t, 256t+128) hold S (P aliases its first 64 columns,
-// two bf16 per column) and [256t+128, 256t+256) hold O. An S tile is written only after the
+// TMEM: per query tile t, columns [256t, 256t+128) hold S and [256t+128, 256t+256) hold O.
+// P (two bf16 per column) overwrites S in place: keys 32q .. 32q+31 use the first 16 of
+// columns [32q, 32q+32), and the residual of the first kSplitTiles tiles the other 16. An S tile is written only after the
 // previous P·V of the same tile has completed, so P is never overwritten while in use.
 //
 // Precision: P is rounded to bf16 for the tensor cores, a relative error of up to 2^-8 per
 // weight. Rows with many keys average it away, but rows near the start of a sequence see
 // few keys (row 1 sees 2); in the first kSplitTiles query tiles P is therefore split into a
-// bf16 head and a bf16 residual (columns [64, 128) of the S region) and both are multiplied
-// with V, which leaves an error near 2^-16 there.
+// bf16 head and a bf16 residual and both are multiplied with V, which leaves an error near
+// 2^-16 there.
 //
 // Every wait is bounded (MLAKV_WAIT_TIMEOUT_CYCLES): a wait that runs out sets a bit in
 // g_prefill_status and the thread abandons its loop; every thread still reaches the final
@@ -60,11 +61,12 @@ constexpr int BN = 128;                      // keys per KV tile
 constexpr int NSTAGE = 2;                    // K/V ring depth
 constexpr int TILE_BYTES = BM * HD * 2;      // one 128 × 128 bf16 tile: 32 KB
 constexpr int BOX_BYTES = TILE_BYTES / 2;    // one TMA box: 128 rows × 64 columns (128 B)
-constexpr int Q_OFF = 0;                     // two Q tiles
-constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
+constexpr int Q_SLOTS = 3;                   // Q tiles rotate through three slots
+constexpr int Q_OFF = 0;
+constexpr int K_OFF = Q_OFF + Q_SLOTS * TILE_BYTES;
 constexpr int V_OFF = K_OFF + NSTAGE * TILE_BYTES;
 constexpr int BAR_OFF = V_OFF + NSTAGE * TILE_BYTES;
-constexpr int N_BARS = 16;
+constexpr int N_BARS = 24;
 constexpr int SLOT_OFF = BAR_OFF + N_BARS * 8;
 constexpr int SMEM = SLOT_OFF + 16 + 1024;   // + alignment slack
 static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -83,14 +85,15 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, HD, false, true);   // P from T
 
 // mbarrier slots (8 bytes each) inside the barrier block
 enum : int {
-    kQFull = 0,
-    kQEmpty = 1,         // the item's last S MMAs are done: its Q tiles may be replaced
-    kKFull = 2,          // + stage
-    kVFull = 4,          // + stage
-    kKvEmpty = 6,        // + stage
-    kSFull = 8,          // + query tile
-    kPReady = 10,        // + query tile
-    kODone = 12          // + query tile
+    kQFull = 0,          // + Q slot
+    kQEmpty = 3,         // + Q slot: the last S MMA reading the slot is done
+    kKFull = 6,          // + stage
+    kVFull = 8,          // + stage
+    kKEmpty = 10,        // + stage: both S MMAs reading the K tile are done
+    kVEmpty = 12,        // + stage: both P·V MMAs reading the V tile are done
+    kSFull = 14,         // + query tile
+    kPReady = 16,        // + query tile
+    kODone = 18          // + query tile
 };
 
 // ------------------------------------------------------------------ paired fp32 arithmetic
@@ -123,60 +126,72 @@ __device__ __forceinline__ float fmin3(float a, float b, float c) {
     return d;
 }
 
-// The largest (NEG: smallest) visible raw score of one row held in registers, so that the row
-// max of x = s·c is c times it (c = scale·log2 e; NEG when c < 0). DIAG: the diagonal tile,
+// The largest (NEG: smallest) visible raw score of one row of the S tile in TMEM, so that the
+// row max of x = s·c is c times it (c = scale·log2 e; NEG when c < 0). DIAG: the diagonal tile,
 // where key i is visible only to rows `row` >= i (key 0 always is, so the result is finite).
-// Eight independent partial extrema keep the dependency chains short.
+// The row is read in two 64-column halves to keep register use low; eight independent partial
+// extrema keep the dependency chains short.
 template <bool DIAG, bool NEG>
-__device__ __forceinline__ float row_extreme(const uint32_t (&r)[BN], int row) {
+__device__ __forceinline__ float row_extreme(uint32_t s_addr, int row) {
     constexpr float kNone = NEG ? INFINITY : -INFINITY;
     float e[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) e[i] = kNone;
 #pragma unroll
-    for (int i = 0; i < BN; i += 2) {
-        float v0 = __uint_as_float(r[i]), v1 = __uint_as_float(r[i + 1]);
-        if (DIAG) {
-            v0 = i <= row ? v0 : kNone;
-            v1 = i + 1 <= row ? v1 : kNone;
+    for (int h = 0; h < 2; ++h) {
+        uint32_t r[64];
+        tmem_ld64_sync(s_addr + 64 * h, r);
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+            float v0 = __uint_as_float(r[i]), v1 = __uint_as_float(r[i + 1]);
+            if (DIAG) {
+                v0 = 64 * h + i <= row ? v0 : kNone;
+                v1 = 64 * h + i + 1 <= row ? v1 : kNone;
+            }
+            const int k = (i >> 1) & 7;
+            e[k] = NEG ? fmin3(e[k], v0, v1) : fmax3(e[k], v0, v1);
         }
-        const int k = (i >> 1) & 7;
-        e[k] = NEG ? fmin3(e[k], v0, v1) : fmax3(e[k], v0, v1);
     }
     return NEG ? fminf(fmin3(e[0], e[1], e[2]), fmin3(fmin3(e[3], e[4], e[5]), e[6], e[7]))
                : fmaxf(fmax3(e[0], e[1], e[2]), fmax3(fmax3(e[3], e[4], e[5]), e[6], e[7]));
 }
 
-// P = 2^(s·c − m) for the row held in registers (0 for hidden keys), written as bf16 pairs to
-// TMEM columns [0, 64) of the row's S region; with SPLIT also the bf16 residual p − bf16(p)
-// to columns [64, 128). The whole row is already in registers, so nothing is overwritten
-// before it is read. Adds the unrounded weights to l.
+// P = 2^(s·c − m) for the same row (0 for hidden keys), as bf16 pairs. Keys 32q .. 32q+31
+// (chunk q) own TMEM columns [32q, 32q+32) of the row's S region: P goes to the first 16 of
+// them and, with SPLIT, the bf16 residual p − bf16(p) to the last 16. A chunk's columns are
+// written only after that chunk of S has been read. Adds the unrounded weights to l.
 template <bool DIAG, bool SPLIT>
-__device__ __forceinline__ void write_p(const uint32_t (&r)[BN], float c, float m, int row, float &l,
-                                        uint32_t s_addr) {
+__device__ __forceinline__ void write_p(uint32_t s_addr, float c, float m, int row, float &l) {
     const uint64_t c2 = f2pack(c, c), nm2 = f2pack(-m, -m);
     uint64_t acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = 0;
 #pragma unroll
-    for (int ch = 0; ch < BN / 32; ++ch) {
-        uint32_t hi[16], lo[16];
+    for (int h = 0; h < 2; ++h) {
+        uint32_t r[64];
+        tmem_ld64_sync(s_addr + 64 * h, r);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int k0 = ch * 32 + 2 * i;
-            float x0, x1;
-            f2unpack(ffma2(f2pack(__uint_as_float(r[k0]), __uint_as_float(r[k0 + 1])), c2, nm2), x0, x1);
-            float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-            if (DIAG) {
-                p0 = k0 <= row ? p0 : 0.f;
-                p1 = k0 + 1 <= row ? p1 : 0.f;
+        for (int ch = 0; ch < 2; ++ch) {
+            const int q = 2 * h + ch;
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int kr = ch * 32 + 2 * i;      // index within the half
+                const int k0 = 64 * h + kr;          // key index within the tile
+                float x0, x1;
+                f2unpack(ffma2(f2pack(__uint_as_float(r[kr]), __uint_as_float(r[kr + 1])), c2, nm2), x0, x1);
+                float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                if (DIAG) {
+                    p0 = k0 <= row ? p0 : 0.f;
+                    p1 = k0 + 1 <= row ? p1 : 0.f;
+                }
+                acc[i & 3] = fadd2(acc[i & 3], f2pack(p0, p1));
+                hi[i] = pack_bf16x2(p0, p1);
+                if constexpr (SPLIT) lo[i] = pack_bf16x2(p0 - bf16_lo(hi[i]), p1 - bf16_hi(hi[i]));
             }
-            acc[i & 3] = fadd2(acc[i & 3], f2pack(p0, p1));
-            hi[i] = pack_bf16x2(p0, p1);
-            if constexpr (SPLIT) lo[i] = pack_bf16x2(p0 - bf16_lo(hi[i]), p1 - bf16_hi(hi[i]));
+            tmem_st16(s_addr + 32 * q, hi);
+            if constexpr (SPLIT) tmem_st16(s_addr + 32 * q + 16, lo);
         }
-        tmem_st16(s_addr + ch * 16, hi);
-        if constexpr (SPLIT) tmem_st16(s_addr + BN / 2 + ch * 16, lo);
     }
     float a0, a1;
     f2unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), a0, a1);
@@ -218,12 +233,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int blk = blockIdx.x, nblk = gridDim.x;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(kQFull), 1);
-        mbar_init(bar(kQEmpty), 1);
+        for (int q = 0; q < Q_SLOTS; ++q) {
+            mbar_init(bar(kQFull + q), 1);
+            mbar_init(bar(kQEmpty + q), 1);
+        }
         for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(bar(kKFull + s), 1);
             mbar_init(bar(kVFull + s), 1);
-            mbar_init(bar(kKvEmpty + s), 1);
+            mbar_init(bar(kKEmpty + s), 1);
+            mbar_init(bar(kVEmpty + s), 1);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(kSFull + t), 1);
@@ -249,7 +267,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             prefetch_tensormap(&kmap);
             prefetch_tensormap(&vmap);
             const uint64_t pol_q = l2_evict_first_policy();
-            int g_kv = 0, n_done = 0;
+            int g_kv = 0, qc = 0;                    // K/V tiles and Q tiles loaded so far
             bool ok = true;
             Item it;
             for (int k = 0; ok && item_at(k, blk, nblk, n_items, per_qt, n_hgrp, heads_per_cta, n_qt, it); ++k) {
@@ -257,19 +275,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 const int S = a.cu_seqlens[it.b + 1] - seq0;
                 if (it.qt * BM >= S) continue;
                 const int j = it.h0 / G;
-                if (n_done > 0 && !mbar_wait_bounded(bar(kQEmpty), (n_done - 1) & 1, &g_prefill_status, kStatusEmptyWait)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(bar(kQFull), n_mt * TILE_BYTES);
-                for (int t = 0; t < n_mt; ++t)
+                // Q tile t of this item goes to slot qc % 3; the slot's previous tile must be
+                // done with (its last S MMA complete)
+                for (int t = 0; t < n_mt && ok; ++t, ++qc) {
+                    const int q = qc % Q_SLOTS, u = qc / Q_SLOTS;
+                    if (u > 0 && !mbar_wait_bounded(bar(kQEmpty + q), (u - 1) & 1, &g_prefill_status, kStatusEmptyWait)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(kQFull + q), TILE_BYTES);
                     for (int bx = 0; bx < 2; ++bx)
-                        tma_load_3d(sb + Q_OFF + t * TILE_BYTES + bx * BOX_BYTES, &qmap, bx * 64, it.h0 + t,
-                                    seq0 + it.qt * BM, bar(kQFull), pol_q);
-                for (int n = 0; n <= it.qt; ++n, ++g_kv) {
+                        tma_load_3d(sb + Q_OFF + q * TILE_BYTES + bx * BOX_BYTES, &qmap, bx * 64, it.h0 + t,
+                                    seq0 + it.qt * BM, bar(kQFull + q), pol_q);
+                }
+                for (int n = 0; ok && n <= it.qt; ++n, ++g_kv) {
                     const int s = g_kv % NSTAGE;
-                    if (!mbar_wait_bounded(bar(kKvEmpty + s), ((g_kv / NSTAGE) & 1) ^ 1, &g_prefill_status,
-                                           kStatusEmptyWait)) {
+                    const uint32_t free_ph = ((g_kv / NSTAGE) & 1) ^ 1;
+                    if (!mbar_wait_bounded(bar(kKEmpty + s), free_ph, &g_prefill_status, kStatusEmptyWait)) {
                         ok = false;
                         break;
                     }
@@ -278,15 +300,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     for (int bx = 0; bx < 2; ++bx)
                         tma_load_3d_nohint(sb + K_OFF + s * TILE_BYTES + bx * BOX_BYTES, &kmap, bx * 64, j, k_tok,
                                            bar(kKFull + s));
+                    if (!mbar_wait_bounded(bar(kVEmpty + s), free_ph, &g_prefill_status, kStatusEmptyWait)) {
+                        ok = false;
+                        break;
+                    }
                     mbar_arrive_expect_tx(bar(kVFull + s), TILE_BYTES);
                     for (int bx = 0; bx < 2; ++bx)
                         tma_load_3d_nohint(sb + V_OFF + s * TILE_BYTES + bx * BOX_BYTES, &vmap, bx * 64, j, k_tok,
                                            bar(kVFull + s));
                 }
-                ++n_done;
             }
             // no copy may still be in flight when the block exits
-            if (n_done > 0) mbar_wait_bounded(bar(kQFull), (n_done - 1) & 1, &g_prefill_status, kStatusDrainWait);
+            for (int i = qc > Q_SLOTS ? qc - Q_SLOTS : 0; i < qc; ++i)
+                mbar_wait_bounded(bar(kQFull + i % Q_SLOTS), (i / Q_SLOTS) & 1, &g_prefill_status, kStatusDrainWait);
             for (int g = g_kv > NSTAGE ? g_kv - NSTAGE : 0; g < g_kv; ++g) {
                 mbar_wait_bounded(bar(kKFull + g % NSTAGE), (g / NSTAGE) & 1, &g_prefill_status, kStatusDrainWait);
                 mbar_wait_bounded(bar(kVFull + g % NSTAGE), (g / NSTAGE) & 1, &g_prefill_status, kStatusDrainWait);
@@ -298,6 +324,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // issues the MMAs and the commits that track them. Descriptors are built once: a
         // byte offset inside shared memory (< 256 KB) adds to the 14-bit start-address field
         // in 16-byte units without carrying out of it.
+        //
+        // Issue order for iteration g (KV tile g of this block): S_0(g), P·V_1(g−1), S_1(g),
+        // P·V_0(g). Each tile's chain S → softmax → P·V → next S is offset by half a period
+        // from the other's, so one tile's softmax runs while the tensor core works for the
+        // other. S_t(g) waits for P·V_t(g−1) to finish, since it overwrites P_t.
         const uint64_t q_desc = sdesc_sw128(sb + Q_OFF, 16, 1024);
         const uint64_t k_desc = sdesc_sw128(sb + K_OFF, 16, 1024);
         const uint64_t v_desc = sdesc_sw128(sb + V_OFF, BOX_BYTES, 1024);
@@ -305,83 +336,108 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             const bool got = mbar_wait_bounded(bar(idx), parity, &g_prefill_status, code);
             return __all_sync(0xffffffffu, got);
         };
-        int g = 0, n_done = 0;                      // iterations and items of this block so far
+        auto issue_s = [&](int t, int qslot, int s) {     // S_t = Q(slot) · K(stage s)ᵀ
+            if (lane == 0) {
+                const uint64_t kd = k_desc + (uint64_t)((s * TILE_BYTES) >> 4);
+                const uint64_t qd = q_desc + (uint64_t)((qslot * TILE_BYTES) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
+                    umma_ss(tmem + 256 * t, qd + off, kd + off, kIdescS, kk > 0);
+                }
+                umma_commit(bar(kSFull + t));
+            }
+            __syncwarp();
+        };
+        auto issue_pv = [&](int t, int s, bool first, bool split) {   // O_t (+)= P_t · V(stage s)
+            if (lane == 0) {
+                const uint32_t p = tmem + 256 * t;
+                const uint64_t vd = v_desc + (uint64_t)((s * TILE_BYTES) >> 4);
+                // keys 16kk .. 16kk+15: P in columns 32·(kk/2) + 8·(kk%2) .. +8, residual 16 further
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    umma_ts(p + 128, p + 32 * (kk >> 1) + 8 * (kk & 1), vd + ((kk * 2048) >> 4), kIdescPV,
+                            (!first || kk > 0) ? 1u : 0u);
+                if (split) {
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        umma_ts(p + 128, p + 32 * (kk >> 1) + 16 + 8 * (kk & 1), vd + ((kk * 2048) >> 4), kIdescPV,
+                                1u);
+                }
+                umma_commit(bar(kODone + t));
+            }
+            __syncwarp();
+        };
+        auto commit = [&](int idx) {
+            if (lane == 0) umma_commit(bar(idx));
+            __syncwarp();
+        };
+        int g = 0, qc = 0;                           // iterations and Q tiles of this block so far
         bool ok = true;
+        // the deferred P·V_1 of the previous iteration
+        bool pend = false, pend_first = false, pend_split = false;
+        int pend_s = 0;
+        auto flush_pv1 = [&]() {
+            if (!pend) return true;
+            if (!wait_all(kPReady + 1, (g - 1) & 1, kStatusMmaWait)) return false;
+            tc_fence_after();
+            issue_pv(1, pend_s, pend_first, pend_split);
+            commit(kVEmpty + pend_s);                // both P·V of that stage are issued
+            pend = false;
+            return true;
+        };
         Item it;
         for (int k = 0; ok && item_at(k, blk, nblk, n_items, per_qt, n_hgrp, heads_per_cta, n_qt, it); ++k) {
             const int S = a.cu_seqlens[it.b + 1] - a.cu_seqlens[it.b];
             if (it.qt * BM >= S) continue;
             const bool split_p = it.qt < kSplitTiles;
-            if (!wait_all(kQFull, n_done & 1, kStatusFullWait)) {
-                ok = false;
-                break;
-            }
+            const int q0 = qc % Q_SLOTS, u0 = qc / Q_SLOTS;
+            const int q1 = (qc + 1) % Q_SLOTS, u1 = (qc + 1) / Q_SLOTS;
+            qc += n_mt;
             for (int n = 0; n <= it.qt; ++n, ++g) {
                 const int s = g % NSTAGE;
                 const uint32_t ph = (g / NSTAGE) & 1;
-                if (!wait_all(kKFull + s, ph, kStatusFullWait)) {
-                    ok = false;
-                    break;
-                }
-                for (int t = 0; t < n_mt; ++t) {
-                    // the previous P·V of this tile (maybe of the previous item) must be done
-                    // before S overwrites P
-                    if (g > 0 && !wait_all(kODone + t, (g - 1) & 1, kStatusMmaWait)) {
-                        ok = false;
-                        break;
-                    }
+                // at an item boundary the previous item's last P·V_1 goes first: S_0 may wait
+                // for the new Q tiles
+                if (n == 0 && !(ok = flush_pv1())) break;
+                if (!(ok = wait_all(kKFull + s, ph, kStatusFullWait))) break;
+                if (n == 0 && !(ok = wait_all(kQFull + q0, u0 & 1, kStatusFullWait))) break;
+                if (g > 0 && !(ok = wait_all(kODone + 0, (g - 1) & 1, kStatusMmaWait))) break;
+                tc_fence_after();
+                issue_s(0, q0, s);
+                if (n == it.qt) commit(kQEmpty + q0);
+                if (n_mt == 1) commit(kKEmpty + s);
+                if (n_mt == 2) {
+                    if (!(ok = flush_pv1())) break;
+                    if (n == 0 && !(ok = wait_all(kQFull + q1, u1 & 1, kStatusFullWait))) break;
+                    if (g > 0 && !(ok = wait_all(kODone + 1, (g - 1) & 1, kStatusMmaWait))) break;
                     tc_fence_after();
-                    if (lane == 0) {
-                        const uint64_t kd = k_desc + (uint64_t)((s * TILE_BYTES) >> 4);
-                        const uint64_t qd = q_desc + (uint64_t)((t * TILE_BYTES) >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < HD / 16; ++kk) {
-                            const uint32_t off = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
-                            umma_ss(tmem + 256 * t, qd + off, kd + off, kIdescS, kk > 0);
-                        }
-                        umma_commit(bar(kSFull + t));
-                        if (n == it.qt && t == n_mt - 1) umma_commit(bar(kQEmpty));
-                    }
-                    __syncwarp();
+                    issue_s(1, q1, s);
+                    if (n == it.qt) commit(kQEmpty + q1);
+                    commit(kKEmpty + s);                 // both S MMAs of this K tile are issued
                 }
-                if (!ok) break;
-                if (!wait_all(kVFull + s, ph, kStatusFullWait)) {
-                    ok = false;
+                if (!(ok = wait_all(kVFull + s, ph, kStatusFullWait) && wait_all(kPReady + 0, g & 1, kStatusMmaWait)))
                     break;
+                tc_fence_after();
+                issue_pv(0, s, n == 0, split_p);
+                if (n_mt == 2) {
+                    pend = true;
+                    pend_s = s;
+                    pend_first = n == 0;
+                    pend_split = split_p;
+                } else {
+                    commit(kVEmpty + s);
                 }
-                for (int t = 0; t < n_mt; ++t) {
-                    if (!wait_all(kPReady + t, g & 1, kStatusMmaWait)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t p = tmem + 256 * t;
-                        const uint64_t vd = v_desc + (uint64_t)((s * TILE_BYTES) >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk)
-                            umma_ts(p + 128, p + kk * 8, vd + ((kk * 2048) >> 4), kIdescPV, (n > 0 || kk > 0) ? 1u : 0u);
-                        if (split_p) {
-#pragma unroll
-                            for (int kk = 0; kk < BN / 16; ++kk)
-                                umma_ts(p + 128, p + BN / 2 + kk * 8, vd + ((kk * 2048) >> 4), kIdescPV, 1u);
-                        }
-                        umma_commit(bar(kODone + t));
-                    }
-                    __syncwarp();
-                }
-                if (!ok) break;
-                if (lane == 0) umma_commit(bar(kKvEmpty + s));
-                __syncwarp();
             }
-            ++n_done;
         }
+        if (ok) ok = flush_pv1();                   // the last iteration's P·V_1 (iteration g-1)
         // the last commits must have arrived before the block exits
-        if (g > 0) {
-            mbar_wait_bounded(bar(kKvEmpty + (g - 1) % NSTAGE), ((g - 1) / NSTAGE) & 1, &g_prefill_status,
-                              kStatusDrainWait);
-            mbar_wait_bounded(bar(kQEmpty), (n_done - 1) & 1, &g_prefill_status, kStatusDrainWait);
+        for (int i = g > NSTAGE ? g - NSTAGE : 0; i < g; ++i) {
+            mbar_wait_bounded(bar(kKEmpty + i % NSTAGE), (i / NSTAGE) & 1, &g_prefill_status, kStatusDrainWait);
+            mbar_wait_bounded(bar(kVEmpty + i % NSTAGE), (i / NSTAGE) & 1, &g_prefill_status, kStatusDrainWait);
         }
+        for (int i = qc > Q_SLOTS ? qc - Q_SLOTS : 0; i < qc; ++i)
+            mbar_wait_bounded(bar(kQEmpty + i % Q_SLOTS), (i / Q_SLOTS) & 1, &g_prefill_status, kStatusDrainWait);
     } else {
         // ------------------------------------------------------------ softmax warpgroups
         const int t = (warp - 2) >> 2;               // query tile of this warpgroup
@@ -407,11 +463,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     break;
                 }
                 tc_fence_after();
-                uint32_t r[BN];
-                tmem_ld128_sync(s_addr, r);
                 const bool diag = n == it.qt;
-                const float ext = neg ? (diag ? row_extreme<true, true>(r, row) : row_extreme<false, true>(r, row))
-                                      : (diag ? row_extreme<true, false>(r, row) : row_extreme<false, false>(r, row));
+                const float ext = neg ? (diag ? row_extreme<true, true>(s_addr, row) : row_extreme<false, true>(s_addr, row))
+                                      : (diag ? row_extreme<true, false>(s_addr, row) : row_extreme<false, false>(s_addr, row));
                 const float mt = ext * a.scale_log2;
                 float alpha = 1.f;
                 bool grow = false;
@@ -436,12 +490,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     }
                 }
                 if (split_p)
-                    diag ? write_p<true, true>(r, a.scale_log2, m_ref, row, l, s_addr)
-                         : write_p<false, true>(r, a.scale_log2, m_ref, row, l, s_addr);
+                    diag ? write_p<true, true>(s_addr, a.scale_log2, m_ref, row, l)
+                         : write_p<false, true>(s_addr, a.scale_log2, m_ref, row, l);
                 else if (diag)
-                    write_p<true, false>(r, a.scale_log2, m_ref, row, l, s_addr);
+                    write_p<true, false>(s_addr, a.scale_log2, m_ref, row, l);
                 else
-                    write_p<false, false>(r, a.scale_log2, m_ref, row, l, s_addr);
+                    write_p<false, false>(s_addr, a.scale_log2, m_ref, row, l);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(bar(kPReady + t));
@@ -457,14 +511,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             const int q_row = it.qt * BM + row;
             const float inv = 1.f / l;
             float4 *dst = reinterpret_cast<float4 *>(a.out + ((size_t)(seq0 + q_row) * a.Hq + it.h0 + t) * HD);
-#pragma unroll
-            for (int c = 0; c < HD / 64; ++c) {
-                uint32_t o[64];
-                tmem_ld64_sync(o_addr + c * 64, o);
+#pragma unroll 1
+            for (int c = 0; c < HD / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(o_addr + c * 32, o);
+                tmem_ld_wait(o);
                 if (q_row < S) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        dst[c * 16 + i] = make_float4(
+                    for (int i = 0; i < 8; ++i)
+                        dst[c * 8 + i] = make_float4(
                             __uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
                             __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
                 }
