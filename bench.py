@@ -216,7 +216,7 @@ class DecodeGqa:
         code = mk.ATTN_BF16 if w.dtype == "bf16" else mk.ATTN_F32
         self.n_split = mk.decode_gqa_num_splits(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, self.max_s, code)
         nb = mk.decode_gqa_workspace_size(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, self.max_s, code)
-        self.ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=device)
+        self.ws = torch.zeros(max(nb, 1), dtype=torch.uint8, device=device)
         self.launches_per_step = 1 + (self.n_split > 1)
         self.l2_note = f"rotating {n_sets} distinct cache sets ({n_sets * cache_bytes / 1e6:.0f} MB, L2 {l2_bytes / 1e6:.0f} MB)"
 

@@ -72,13 +72,19 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
  *   S_max    cache capacity (the row stride of the cache, in tokens).
  *   max_S    host-known upper bound on seq_lens; sizes the split-KV plan. Passing S_max is
  *            always valid.
- *   n_split  number of pieces each sequence's cache is cut into (each piece is processed by
- *            its own thread block and the pieces are merged by log-sum-exp); 0 lets the
- *            library choose from B, Hkv, max_S and the device's SM count.
+ *   n_split  fp32 cache: number of pieces each sequence's cache is cut into (each piece is
+ *            processed by its own thread block and the pieces are merged by log-sum-exp);
+ *            0 lets the library choose from B, Hkv, max_S and the device's SM count.
+ *            bf16 cache: the work is always balanced over one persistent thread block per SM
+ *            (all sequences' cached tokens are cut into equal shares, whatever their
+ *            lengths); n_split > 0 caps the number of blocks at n_split per (sequence, group
+ *            of up to 4 KV heads).
  *   D        64, 96 or 128. Any Hq/Hkv with Hq % Hkv == 0 and Hq/Hkv <= 128.
  *   workspace, ws_bytes: scratch for the split partials, at least
  *            attn_decode_gqa_workspace_size(...) bytes with the same arguments; may be
- *            NULL when that size is 0.
+ *            NULL when that size is 0. For a bf16 cache the workspace also holds one arrival
+ *            counter per segment: it must be zero-filled before its first use, and every
+ *            call that completes leaves it zero-filled again.
  * Returns ATTN_OK or an error code.
  * ------------------------------------------------------------------------------------- */
 size_t attn_decode_gqa_workspace_size(int B, int Hq, int Hkv, int D, int max_S,
@@ -109,8 +115,9 @@ int attn_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
  *     splits, or use attn_decode_gqa).
  *   - The first call on a device looks up the array's device address on that device (the
  *     device must be current); make that first call before any stream capture.
- *   - Every call uses the same array, which keeps the last call's contents (nothing in it
- *     needs to start at zero). Calls whose kernels can overlap on the GPU — other streams,
+ *   - Every call uses the same array. It starts zero-filled when the library loads, and a
+ *     call that completes leaves its counters at zero again (the partials it also holds
+ *     need no initial value). Calls whose kernels can overlap on the GPU — other streams,
  *     other host threads — race on it; order them.
  * Results are identical to attn_decode_gqa with the same arguments.
  * ------------------------------------------------------------------------------------- */

@@ -135,7 +135,8 @@ def decode_gqa(q, k_cache, v_cache, seq_lens, out=None, scale=None, max_s=None, 
 
     q [B, Hq, D]; k_cache, v_cache [B, S_max, Hkv, D] (fp32 or bf16, same dtype as q);
     seq_lens [B] int32 on the device; returns out [B, Hq, D] fp32. ``max_s`` is a host-known
-    bound on seq_lens (defaults to S_max); ``n_split`` = 0 lets the library choose.
+    bound on seq_lens (defaults to S_max); ``n_split`` = 0 lets the library choose. A
+    ``workspace`` passed in must have been zero-filled before its first use (calls leave it so).
     """
     dt = q.dtype
     if dt not in (torch.float32, torch.bfloat16):
@@ -158,7 +159,8 @@ def decode_gqa(q, k_cache, v_cache, seq_lens, out=None, scale=None, max_s=None, 
         _need(out, "out", torch.float32, 3, dev)
     need = decode_gqa_workspace_size(B, Hq, Hkv, D, max_s, code, n_split)
     if need and (workspace is None or workspace.numel() < need):
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        # zero-filled: the library's per-segment counters start at zero and are left at zero
+        workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() if workspace is not None else 0
     _check(lib().attn_decode_gqa(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(out),
                                  B, Hq, Hkv, D, scale, S_max, max_s, code, n_split,

@@ -98,10 +98,8 @@ SplitPlan gqa_plan(int B, int Hq, int Hkv, int D, int max_S, attn_dtype dtype, i
         const int hb = (G % 8 == 0) ? 8 : (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
         return plan_splits(max_S, kFmaTile, (long)B * Hkv * (G / hb), n_split, 2);
     }
-    const int tile = decode_gqa_bf16_tile_tokens(D, G);
-    const int heads_per_block = decode_gqa_bf16_heads_per_block(G);
-    const long blocks = (long)B * Hkv * ((G + heads_per_block - 1) / heads_per_block);
-    return plan_splits(max_S, tile, blocks, n_split, 4);
+    // bf16: the balanced split; n_split reports the persistent grid size
+    return SplitPlan{decode_gqa_stream_blocks(B, Hq, Hkv, D, n_split), 0};
 }
 
 size_t partials_bytes(int B, int Hq, int Dv, int n_split) {
@@ -179,6 +177,7 @@ MLAKV_API int attn_decode_gqa_num_splits(int B, int Hq, int Hkv, int D, int max_
 MLAKV_API size_t attn_decode_gqa_workspace_size(int B, int Hq, int Hkv, int D, int max_S, attn_dtype dtype,
                                                 int n_split) {
     if (check_gqa_shapes(B, Hq, Hkv, D, max_S > 0 ? max_S : 1, max_S, dtype, n_split) != ATTN_OK) return 0;
+    if (!gqa_use_fma(dtype)) return decode_gqa_stream_workspace(B, Hq, Hkv, D, n_split);
     const SplitPlan p = gqa_plan(B, Hq, Hkv, D, max_S, dtype, n_split);
     return partials_bytes(B, Hq, D, p.n_split);
 }
@@ -194,6 +193,30 @@ MLAKV_API int attn_decode_gqa(const void *q, const void *k_cache, const void *v_
     if (!isfinite(scale)) return fail(ATTN_ERR_SHAPE, "scale must be finite");
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(seq_lens))
         return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_gqa: every pointer must be 16-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!gqa_use_fma(dtype)) {
+        // bf16: persistent blocks over an even share of all cached tokens, then the merge
+        const size_t need = decode_gqa_stream_workspace(B, Hq, Hkv, D, n_split);
+        if (!workspace || ws_bytes < need || !aligned16(workspace))
+            return fail(ATTN_ERR_WORKSPACE, "attn_decode_gqa: workspace of %zu bytes (16-byte aligned) needed, "
+                        "got %zu at %p", need, workspace ? ws_bytes : (size_t)0, workspace);
+        DecodeStreamArgs a{};
+        a.q = q; a.k = k_cache; a.v = v_cache; a.seq_lens = seq_lens; a.out = out;
+        a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.D = D;
+        a.scale_log2 = scale * kLog2e;
+        a.S_max = S_max;
+        a.n_blocks = decode_gqa_stream_blocks(B, Hq, Hkv, D, n_split);
+        a.aligned = decode_gqa_stream_aligned(B, Hq, Hkv, n_split) ? 1 : 0;
+        // the partial outputs come first in the workspace, their log-sum-exps after them
+        a.o_part = static_cast<float *>(workspace);
+        const size_t o_bytes = decode_gqa_stream_o_bytes(B, Hq, Hkv, D, n_split);
+        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_bytes);
+        a.counters = reinterpret_cast<int *>(static_cast<char *>(workspace) + o_bytes +
+                                             decode_gqa_stream_lse_bytes(B, Hq, Hkv, D, n_split));
+        const cudaError_t e = launch_decode_gqa_stream(a, s);
+        if (e != cudaSuccess) return cuda_fail(e, "attn_decode_gqa: kernel launch");
+        return ok();
+    }
     const SplitPlan p = gqa_plan(B, Hq, Hkv, D, max_S, dtype, n_split);
     const size_t need = partials_bytes(B, Hq, D, p.n_split);
     if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
@@ -213,8 +236,7 @@ MLAKV_API int attn_decode_gqa(const void *q, const void *k_cache, const void *v_
         a.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                                align_up(rows * p.n_split * D * sizeof(float), 256));
     }
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = gqa_use_fma(dtype) ? launch_decode_gqa_f32(a, s) : launch_decode_gqa_bf16(a, s);
+    cudaError_t e = launch_decode_gqa_f32(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "attn_decode_gqa: decode kernel launch");
     if (p.n_split > 1) {
         e = launch_merge(a.o_part, a.lse_part, out, B * Hq, p.n_split, D, s);

@@ -29,6 +29,27 @@ struct DecodeGqaArgs {
     int split_len;          // tokens per split (multiple of the kernel's tile)
 };
 
+// GQA decode over a bf16 cache with the balanced ("stream-K") split of streamk.cuh.
+struct DecodeStreamArgs {
+    const void *q;          // [B, Hq, D]
+    const void *k;          // [B, S_max, Hkv, D]
+    const void *v;          // [B, S_max, Hkv, D]
+    const int *seq_lens;    // [B]
+    float *out;             // [B, Hq, D]
+    float *o_part;          // [2·n_blocks, hg·heads, D]   partial outputs, two slots per block
+    float *lse_part;        // [2·n_blocks, hg·heads]
+    int B, Hq, Hkv, D;
+    float scale_log2;       // scale · log2(e)
+    int S_max;
+    int n_blocks;           // persistent blocks (grid size)
+    int heads;              // query-head rows per KV head and head block: min(G, 16·MT)
+    int n_hblk;             // head blocks per KV head: ceil(G / (16·MT))
+    int hg;                 // KV heads streamed together in one tile (1, 2 or 4)
+    int tile_tokens;        // tokens per tile
+    int *counters;          // [B · Hkv · n_hblk], zero between calls
+    int aligned;            // 1: block c streams exactly segment c (no segment is shared)
+};
+
 struct DecodeMlaArgs {
     const void *q_lat;      // [B, Hq, r]
     const void *q_rope;     // [B, Hq, dr]
@@ -60,9 +81,14 @@ struct PrefillArgs {
 
 // K1: split-KV GQA decode. Writes out directly when n_split == 1, else the partials.
 MLAKV_HIDDEN cudaError_t launch_decode_gqa_f32(const DecodeGqaArgs &a, cudaStream_t s);
-MLAKV_HIDDEN cudaError_t launch_decode_gqa_bf16(const DecodeGqaArgs &a, cudaStream_t s);
-MLAKV_HIDDEN int decode_gqa_bf16_tile_tokens(int D, int G);
-MLAKV_HIDDEN int decode_gqa_bf16_heads_per_block(int G);
+// K1 (bf16, balanced): the persistent grid size and the workspace it needs; the decode kernel
+// also combines the segments it splits between blocks.
+MLAKV_HIDDEN int decode_gqa_stream_blocks(int B, int Hq, int Hkv, int D, int n_split);
+MLAKV_HIDDEN bool decode_gqa_stream_aligned(int B, int Hq, int Hkv, int n_split);
+MLAKV_HIDDEN size_t decode_gqa_stream_workspace(int B, int Hq, int Hkv, int D, int n_split);
+MLAKV_HIDDEN size_t decode_gqa_stream_o_bytes(int B, int Hq, int Hkv, int D, int n_split);
+MLAKV_HIDDEN size_t decode_gqa_stream_lse_bytes(int B, int Hq, int Hkv, int D, int n_split);
+MLAKV_HIDDEN cudaError_t launch_decode_gqa_stream(const DecodeStreamArgs &a, cudaStream_t s);
 // K2: log-sum-exp merge of the split partials.
 MLAKV_HIDDEN cudaError_t launch_merge(const float *o_part, const float *lse_part, float *out,
                                       int rows, int n_split, int Dv, cudaStream_t s);

@@ -1,4 +1,4 @@
-// K1 (tensor-core form): split-KV decode for GQA/MHA/MQA over a bf16 cache.
+// K1 (tensor-core form): decode for GQA/MHA/MQA over a bf16 cache, split evenly over the GPU.
 //
 // The method ("模型架构｜MQA & GQA 调研", section "代码", Attention.forward with one new token):
 // out[b,h] = softmax(scale · q[b,h]·K[b,:S_b,j]ᵀ) · V[b,:S_b,j] with j = h / G. The page
@@ -6,23 +6,35 @@
 // query heads of KV head j are stacked as the M rows of one MMA tile, so each K/V byte
 // leaves HBM once and feeds all G heads.
 //
-// One thread block = (sequence b, KV head j, block of up to 16·MT heads of j's group, split).
-// Warp 4 is the producer: it streams the split's K and V rows through an NS-stage ring of
-// shared-memory buffers with TMA tensor loads (64-token stages, 64-byte swizzled boxes of 32
-// columns, L2 evict-first hint). Warps 0-3 are consumers; each owns 16 tokens of every stage:
-//   S = Q·Kᵀ      mma.sync m16n8k16 (bf16 → fp32), heads on M, tokens on N, Q from smem;
+// Work split (streamk.cuh): the cache is walked in tiles of TT tokens × HG KV heads (the
+// heads of one token range are read together: in the [B, S_max, Hkv, D] cache their rows
+// are neighbours, which HBM serves far faster than the same rows fetched at different
+// times), and each persistent block takes an equal share of all tiles, whatever the sequence
+// lengths. A block streams its share without pausing at segment boundaries: a segment it
+// covers whole is written to `out`, one it shares with a neighbour becomes a partial
+// (normalised output and ln Σ e^s) that the stream-K merge kernel combines.
+//
+// Block = 4 consumer warps + 1 producer warp, one block per SM. The producer streams each
+// tile's K and V rows through an NS-stage shared-memory ring with TMA tensor loads (one
+// 64-byte swizzled box of 32 columns × TT tokens per head, L2 evict-first hint) and, one
+// segment ahead, the segment's query rows into one of two query buffers. Consumer warp w
+// owns KV head w / WPH of the group and TS = TT / WPH tokens of each tile (WPH = 4 / HG warps
+// per head), in slices of 16:
+//   S = Q·Kᵀ      mma.sync m16n8k16 (bf16 → fp32), query heads on M, tokens on N;
 //   softmax       per-head running max/sum in the base-2 domain (scores · scale·log2 e),
 //                 quad shuffles for the row max, rescale factor 2^(m_old − m_new);
 //   O += P·V      P rounded to bf16 in registers (the S accumulator layout is the A-operand
 //                 layout), V fragments by ldmatrix.trans.
 // Tokens past the sequence end are masked to −inf, and their V rows are zeroed in shared
-// memory so stale cache contents never reach the output. At the end the four warps' states
-// are merged in shared memory; the block writes out = O/l (one split) or the normalised
-// partial and lse = ln Σ e^s for the log-sum-exp merge kernel.
+// memory so stale cache contents never reach the output. At a segment's end a warp that
+// owns its head alone (HG = 4) writes its rows directly; otherwise the warps sharing a head
+// combine their states in shared memory.
 //
-// Every mbarrier wait is bounded (MLAKV_WAIT_TIMEOUT_CYCLES); a wait that runs out sets a bit in
-// g_decode_gqa_status and the block returns, so a broken pipeline cannot hang the GPU.
+// Every mbarrier wait is bounded (MLAKV_WAIT_TIMEOUT_CYCLES); a wait that runs out sets a bit
+// in g_decode_gqa_status, after which the warp skips all further work but still meets its
+// partners at every barrier, so a broken pipeline cannot hang the GPU.
 #include "ptx.cuh"
+#include "streamk.cuh"
 #include "tensor_map.cuh"
 
 #include <math.h>
@@ -33,332 +45,723 @@ __device__ unsigned g_decode_gqa_status;
 
 namespace {
 
-constexpr int kT = 64;             // tokens per pipeline stage
-constexpr int kConsumers = 4;      // consumer warps, 16 tokens of each stage apiece
-constexpr int kThreads = (kConsumers + 1) * 32;
+constexpr int kLseCache = 512;     // per warp: cached partial log-sum-exps of a merge
 
-template <int D, int MT, int NS>
+// NC consumer warps (4 or 8) + 1 producer warp.
+template <int D, int MT, int HG, int NS, int NC>
 struct Cfg {
-    static constexpr int NB = D / 32;               // 64-byte boxes per token row
-    static constexpr int BOX = kT * 64;             // one box: kT rows of 64 bytes
-    static constexpr int KV = NB * BOX;             // K (or V) bytes per stage
+    static constexpr int kConsumers = NC;
+    static constexpr int kThreads = (NC + 1) * 32;
+    static constexpr int TT = HG == 4 ? 32 : 16 * NC;   // tokens per tile
+    static constexpr int WPH = NC / HG;             // warps per KV head
+    static constexpr int TS = TT / WPH;             // tokens per warp per tile
+    static constexpr int SLICES = TS / 16;
+    static constexpr int NB = D / 32;               // 64-byte column boxes per token row
+    static constexpr int BOX = TT * 64;             // one box: TT rows of 64 bytes (one head)
+    static constexpr int KV = NB * HG * BOX;        // K (or V) bytes per stage
     static constexpr int STAGE = 2 * KV;
-    static constexpr int HEADS = 16 * MT;
-    static constexpr int QPITCH = D * 2 + 16;       // padded Q row: conflict-free ldmatrix
+    static constexpr int HEADS = 16 * MT;           // MMA rows per KV head
     static constexpr int Q_OFF = NS * STAGE;
-    static constexpr int BAR_OFF = Q_OFF + HEADS * QPITCH;
-    static constexpr int SMEM = BAR_OFF + 2 * NS * 8 + 1024;   // + alignment slack
-    static constexpr int MERGE_BYTES = kConsumers * HEADS * (D + 2) * 4;
-    static_assert(MERGE_BYTES <= NS * STAGE, "merge scratch must fit in the stage buffers");
-    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static_assert(BOX % 512 == 0 && STAGE % 1024 == 0, "swizzle alignment");
+    static_assert(TT % WPH == 0 && TS % 16 == 0, "whole 16-token slices per warp");
+    static_assert(SLICES >= 1, "at least one 16-token slice per warp");
 };
 
-// Byte offset of 16-byte chunk `cidx` (along D) of token row `row` inside one K/V stage
-// buffer laid out as NB boxes of [kT rows × 64 B] with the 64-byte TMA swizzle
-// (address bits [4,5] ^= bits [7,8], i.e. chunk c of row r sits at c ^ ((r >> 1) & 3)).
-__device__ __forceinline__ uint32_t kv_off(int row, int cidx) {
-    const int box = cidx >> 2;
-    const int c = (cidx & 3) ^ ((row >> 1) & 3);
-    return box * (kT * 64) + row * 64 + c * 16;
+// Shared-memory layout after the ring: two query buffers of NB boxes of q_rows rows, the
+// barriers, the combine scratch (warps sharing a head) and the tile prefix.
+struct Layout {
+    int q_box, q_buf, bar, scr, fac, stats, plist, prefix, total;
+};
+
+template <int D, int MT, int HG, int NS, int NC>
+Layout layout(int q_rows, int heads, int B, int n_blocks) {
+    using C = Cfg<D, MT, HG, NS, NC>;
+    constexpr int kConsumers = NC;
+    Layout L;
+    L.q_box = q_rows * 64;
+    L.q_buf = C::NB * L.q_box;
+    L.bar = C::Q_OFF + 2 * L.q_buf;
+    L.scr = L.bar + 256;
+    const int scr_floats = C::WPH > 1 ? kConsumers * heads * (D + 2) : 0;
+    L.fac = L.scr + scr_floats * 4;
+    L.stats = L.fac + (C::WPH > 1 ? HG * heads * (C::WPH + 1) * 4 : 0);
+    L.plist = L.stats + 2 * HG * heads * 4 + 16;
+    L.prefix = L.plist + kConsumers * (n_blocks + kLseCache) * 4;
+    L.total = L.prefix + (B + 1) * 4 + 1024;
+    return L;
 }
 
-template <int D, int MT, int NS>
-__global__ void __launch_bounds__(kThreads, 2)
+// Byte offset of 16-byte chunk `cidx` (along D) of row `row` in a buffer of 64-byte-wide
+// boxes whose `row` 0 sits at a 512-byte boundary, written by TMA with the 64-byte swizzle
+// (address bits [4,5] ^= bits [7,8]: chunk c of row r sits at c ^ ((r >> 1) & 3)).
+__device__ __forceinline__ uint32_t sw64(int row, int cidx) {
+    return row * 64 + ((((cidx & 3) ^ ((row >> 1) & 3))) << 4);
+}
+
+// One piece of a block's range: tiles [i0, i0 + n_t) of segment (b, gi, hb).
+struct Piece {
+    int b, gi, hb, S, i0, n_t;
+    bool whole;                 // the piece is the whole segment
+};
+
+// Walks the pieces of a block's tile range [t, t_end) using the tile prefix over sequences.
+struct PieceWalker {
+    const int *prefix;          // prefix[b] = Σ_{b' < b} tiles(S_b'), b = 0 .. B
+    const int *seq_lens;
+    int B, seg_per_seq, n_hblk, tile;
+    long long t, t_end;
+    __device__ bool next(Piece &p) {
+        if (t >= t_end) return false;
+        // the last b with seg_per_seq · prefix[b] <= t (sequences with no tiles are skipped)
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((long long)seg_per_seq * prefix[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        p.b = lo;
+        p.S = seq_lens[lo];
+        const int nb = stream_tiles(p.S, tile);
+        const long long fb = (long long)seg_per_seq * prefix[lo];
+        const int q = (int)((t - fb) / nb);
+        p.gi = q / n_hblk;
+        p.hb = q % n_hblk;
+        p.i0 = (int)((t - fb) % nb);
+        const long long seg_end = fb + (long long)(q + 1) * nb;
+        const long long end = seg_end < t_end ? seg_end : t_end;
+        p.n_t = (int)(end - t);
+        p.whole = p.i0 == 0 && end == seg_end;
+        t = end;
+        return true;
+    }
+};
+
+template <int D, int MT, int HG, int NS, int NC>
+__global__ void __launch_bounds__((NC + 1) * 32, 1)
 decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                       const DecodeGqaArgs a) {
-    using C = Cfg<D, MT, NS>;
+                       const __grid_constant__ CUtensorMap qmap, const DecodeStreamArgs a, const Layout L,
+                       int q_rows_loaded) {
+    using C = Cfg<D, MT, HG, NS, NC>;
+    constexpr int TT = C::TT, WPH = C::WPH, TS = C::TS;
+    constexpr int kConsumers = NC, kThreads = C::kThreads;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t full0 = sbase + C::BAR_OFF;
-    const uint32_t empty0 = full0 + NS * 8;
+    const uint32_t full0 = sbase + L.bar;             // NS barriers
+    const uint32_t empty0 = full0 + NS * 8;           // NS barriers
+    const uint32_t qfull0 = empty0 + NS * 8;          // 2 barriers
+    const uint32_t qempty0 = qfull0 + 16;             // 2 barriers
+    const int heads = a.heads;
+    float *scr = reinterpret_cast<float *>(smem + L.scr);     // [warp][head][D+2]   (WPH > 1)
+    float *fac = reinterpret_cast<float *>(smem + L.fac);     // [hg·head][WPH + 1]  (WPH > 1)
+    float *stats = reinterpret_cast<float *>(smem + L.stats); // [2][hg·head] merge max, 1/sum
+    int *flag = reinterpret_cast<int *>(stats + 2 * HG * a.heads);   // "this block merges"
+    int *plist = reinterpret_cast<int *>(smem + L.plist);     // per warp: partial rows of a merge,
+                                                              // then kLseCache cached lse values
+    int *prefix = reinterpret_cast<int *>(smem + L.prefix);   // [B+1]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = a.Hq / a.Hkv;
-    const int n_hblk = (G + C::HEADS - 1) / C::HEADS;
-    const int j = blockIdx.y / n_hblk;
-    const int hb = blockIdx.y % n_hblk;
-    const int heads = min(C::HEADS, G - hb * C::HEADS);
-    const int h0 = j * G + hb * C::HEADS;
-    const int b = blockIdx.z;
-    const int split = blockIdx.x;
+
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, kConsumers);
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(qfull0 + 8 * i, 1);
+            mbar_init(qempty0 + 8 * i, kConsumers);
+        }
         fence_mbar_init();
     }
+    // query rows past those loaded are only ever read as padding rows: keep them zero
+    for (int i = threadIdx.x; i < 2 * L.q_buf / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(smem + C::Q_OFF)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+
     // everything above overlaps the previous kernel in the stream; the inputs are read below
     griddep_wait();
     griddep_launch_dependents();
-    const int S = a.seq_lens[b];
-    const int t_begin = split * a.split_len;
-    const int t_end = min(S, t_begin + a.split_len);
-    const int n_tiles = t_end > t_begin ? (t_end - t_begin + kT - 1) / kT : 0;
-
-    // q rows of this head block → padded shared rows (zero rows beyond `heads`)
-    {
-        const uint4 *qg = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.q) +
-                                                          ((size_t)b * a.Hq + h0) * D);
-        for (int i = threadIdx.x; i < C::HEADS * (D / 8); i += kThreads) {
-            const int r = i / (D / 8), c = i % (D / 8);
-            const uint4 v = r < heads ? __ldg(qg + (size_t)r * (D / 8) + c) : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4 *>(smem + C::Q_OFF + r * C::QPITCH + c * 16) = v;
+    if (warp == 0) {
+        // tile prefix over the sequences (warp scan, 32 sequences at a time)
+        int carry = 0;
+        for (int base = 0; base < a.B; base += 32) {
+            const int b = base + lane;
+            const int v = b < a.B ? stream_tiles(a.seq_lens[b], TT) : 0;
+            int x = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (b < a.B) prefix[b] = carry + x - v;
+            carry += __shfl_sync(0xffffffffu, x, 31);
         }
+        if (lane == 0) prefix[a.B] = carry;
     }
     __syncthreads();
 
+    const int seg_per_seq = (a.Hkv / HG) * a.n_hblk;
+    const long long T = (long long)seg_per_seq * prefix[a.B];
+    const int c = blockIdx.x;
+    if (c == 0 && warp < kConsumers) {
+        // sequences with an empty cache own no tile: their output is zero
+        for (int b = 0; b < a.B; ++b)
+            if (prefix[b + 1] == prefix[b])
+                for (int i = threadIdx.x; i < a.Hq * D / 4; i += kConsumers * 32)
+                    reinterpret_cast<float4 *>(a.out + (size_t)b * a.Hq * D)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    PieceWalker walk{prefix, a.seq_lens, a.B, seg_per_seq, a.n_hblk, TT, 0, 0};
+    if (a.aligned) {
+        // block c streams segment c whole
+        const int b = c / seg_per_seq, q = c % seg_per_seq;
+        const int nb = stream_tiles(a.seq_lens[b], TT);
+        walk.t = (long long)seg_per_seq * prefix[b] + (long long)q * nb;
+        walk.t_end = walk.t + nb;
+    } else if (T > 0) {
+        walk.t = stream_start(c, T, a.n_blocks);
+        walk.t_end = stream_start(c + 1, T, a.n_blocks);
+    }
+
     if (warp == kConsumers) {
         // ------------------------------------------------------------ producer
-        if (lane == 0 && n_tiles > 0) {
+        if (lane == 0 && walk.t < walk.t_end) {
             prefetch_tensormap(&kmap);
             prefetch_tensormap(&vmap);
+            prefetch_tensormap(&qmap);
             const uint64_t pol = l2_evict_first_policy();
-            int issued = 0;
-            for (int i = 0; i < n_tiles; ++i) {
-                const int s = i % NS;
-                if (!mbar_wait_bounded(empty0 + 8 * s, ((i / NS) & 1) ^ 1, &g_decode_gqa_status, kStatusEmptyWait))
+            int g = 0, k = 0;
+            bool ok = true;
+            Piece p;
+            while (ok && walk.next(p)) {
+                const int qb = k & 1;
+                if (k >= 2 && !mbar_wait_bounded(qempty0 + 8 * qb, ((k >> 1) - 1) & 1, &g_decode_gqa_status,
+                                                 kStatusEmptyWait)) {
+                    ok = false;
                     break;
-                const uint32_t dst = sbase + s * C::STAGE;
-                mbar_arrive_expect_tx(full0 + 8 * s, C::STAGE);
-                const int t = t_begin + i * kT;
-#pragma unroll
-                for (int bx = 0; bx < C::NB; ++bx) {
-                    tma_load_4d(dst + bx * C::BOX, &kmap, bx * 32, j, t, b, full0 + 8 * s, pol);
-                    tma_load_4d(dst + C::KV + bx * C::BOX, &vmap, bx * 32, j, t, b, full0 + 8 * s, pol);
                 }
-                issued = i + 1;
+                const int j0 = p.gi * HG;
+                const int h0 = j0 * G + p.hb * C::HEADS;
+                mbar_arrive_expect_tx(qfull0 + 8 * qb, C::NB * q_rows_loaded * 64);
+#pragma unroll
+                for (int bx = 0; bx < C::NB; ++bx)
+                    tma_load_3d(sbase + C::Q_OFF + qb * L.q_buf + bx * L.q_box, &qmap, bx * 32, h0, p.b,
+                                qfull0 + 8 * qb, pol);
+                for (int i = 0; i < p.n_t; ++i, ++g) {
+                    const int s = g % NS;
+                    if (!mbar_wait_bounded(empty0 + 8 * s, ((g / NS) & 1) ^ 1, &g_decode_gqa_status, kStatusEmptyWait)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = sbase + s * C::STAGE;
+                    mbar_arrive_expect_tx(full0 + 8 * s, C::STAGE);
+                    const int t = (p.i0 + i) * TT;
+                    // the HG heads of each column box back to back: neighbouring rows in HBM
+#pragma unroll
+                    for (int bx = 0; bx < C::NB; ++bx)
+#pragma unroll
+                        for (int hh = 0; hh < HG; ++hh)
+                            tma_load_4d(dst + (bx * HG + hh) * C::BOX, &kmap, bx * 32, j0 + hh, t, p.b, full0 + 8 * s, pol);
+#pragma unroll
+                    for (int bx = 0; bx < C::NB; ++bx)
+#pragma unroll
+                        for (int hh = 0; hh < HG; ++hh)
+                            tma_load_4d(dst + C::KV + (bx * HG + hh) * C::BOX, &vmap, bx * 32, j0 + hh, t, p.b,
+                                        full0 + 8 * s, pol);
+                }
+                ++k;
             }
             // no copy may still be in flight when the block exits
-            for (int i = issued > NS ? issued - NS : 0; i < issued; ++i)
+            for (int i = g > NS ? g - NS : 0; i < g; ++i)
                 mbar_wait_bounded(full0 + 8 * (i % NS), (i / NS) & 1, &g_decode_gqa_status, kStatusDrainWait);
+            for (int i = k > 2 ? k - 2 : 0; i < k; ++i)
+                mbar_wait_bounded(qfull0 + 8 * (i & 1), (i >> 1) & 1, &g_decode_gqa_status, kStatusDrainWait);
         }
         return;
     }
 
     // ---------------------------------------------------------------- consumers
-    const int g = lane >> 2;      // row group inside an MMA fragment
+    const int hw = warp / WPH;    // KV head of the group this warp serves
+    const int sub = warp % WPH;   // its share of each tile's tokens
+    const int g8 = lane >> 2;     // row group inside an MMA fragment
     const int cq = lane & 3;      // column pair inside an MMA fragment
     const int mi = lane >> 3;     // ldmatrix: which 8x8 matrix this lane addresses
     const int ri = lane & 7;      // ldmatrix: which row of it
-    float o[MT][D / 8][4];
-    float m[MT][2], l[MT][2];
+    const int qrow0 = a.n_hblk == 1 ? hw * G : 0;     // this head's first query row in the buffer
+    bool ok = true;               // false once a wait has given up: the warp then only keeps
+                                  // step with its partners at the named barriers
+    int g = 0, k = 0;
+    Piece p;
+    while (walk.next(p)) {
+        const int qb = k & 1;
+        const uint32_t qbase = sbase + C::Q_OFF + qb * L.q_buf;
+        if (ok && !mbar_wait_bounded(qfull0 + 8 * qb, (k >> 1) & 1, &g_decode_gqa_status, kStatusFullWait)) ok = false;
+        float o[MT][D / 8][4];
+        float m[MT][2], l[MT][2];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
+        for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            m[mt][r] = -INFINITY;
-            l[mt][r] = 0.f;
+            for (int r = 0; r < 2; ++r) {
+                m[mt][r] = -INFINITY;
+                l[mt][r] = 0.f;
+            }
+#pragma unroll
+            for (int nd = 0; nd < D / 8; ++nd)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[mt][nd][e] = 0.f;
         }
+        const int t_end = min(p.S, (p.i0 + p.n_t) * TT);
+        for (int i = 0; i < p.n_t; ++i, ++g) {
+            const int s = g % NS;
+            if (ok && !mbar_wait_bounded(full0 + 8 * s, (g / NS) & 1, &g_decode_gqa_status, kStatusFullWait))
+                ok = false;
+            if (ok) {
+                const uint32_t kb = sbase + s * C::STAGE + hw * C::BOX;    // this head's K rows
+                const uint32_t vb = kb + C::KV;
 #pragma unroll
-        for (int nd = 0; nd < D / 8; ++nd)
+                for (int sl = 0; sl < C::SLICES; ++sl) {
+                    const int r0 = sub * TS + sl * 16;                      // first row of the slice
+                    const int n_valid = min(16, t_end - ((p.i0 + i) * TT + r0));
+                    if (n_valid <= 0) continue;
+                    if (n_valid < 16) {
+                        // zero the V rows past the sequence end so 0·(stale value) cannot make NaN
+                        uint8_t *vrow = smem + s * C::STAGE + C::KV + hw * C::BOX;
+                        for (int idx = lane; idx < 16 * C::NB * 4; idx += 32) {
+                            const int r = idx / (C::NB * 4), cidx = idx % (C::NB * 4);
+                            if (r >= n_valid)
+                                *reinterpret_cast<uint4 *>(vrow + (cidx >> 2) * HG * C::BOX + sw64(r0 + r, cidx)) =
+                                    make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                    // S = Q·Kᵀ for the slice's 16 tokens
+                    float sc[MT][2][4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o[mt][nd][e] = 0.f;
-    }
-    const uint32_t qbase = sbase + C::Q_OFF;
-    bool ok = true;
-
-    for (int i = 0; i < n_tiles && ok; ++i) {
-        const int s = i % NS;
-        if (!mbar_wait_bounded(full0 + 8 * s, (i / NS) & 1, &g_decode_gqa_status, kStatusFullWait)) {
-            ok = false;
-            break;
-        }
-        const uint32_t kb = sbase + s * C::STAGE;
-        const uint32_t vb = kb + C::KV;
-        const int t0 = t_begin + i * kT + warp * 16;       // first token of this warp's slice
-        const int n_valid = min(16, t_end - t0);
-        if (n_valid > 0) {
-            if (n_valid < 16) {
-                // zero the V rows past the sequence end so 0·(stale value) cannot make NaN
-                uint8_t *vrow = smem + s * C::STAGE + C::KV;
-                for (int idx = lane; idx < 16 * C::NB * 4; idx += 32) {
-                    const int r = idx / (C::NB * 4);
-                    if (r >= n_valid) {
-                        const int row = warp * 16 + r, cidx = idx % (C::NB * 4);
-                        *reinterpret_cast<uint4 *>(vrow + kv_off(row, cidx)) = make_uint4(0, 0, 0, 0);
+                    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        uint32_t b0, b1, b2, b3;
+                        const int cb = 2 * kk + (mi & 1);
+                        ldsm_x4(kb + (cb >> 2) * HG * C::BOX + sw64(r0 + (mi >> 1) * 8 + ri, cb), b0, b1, b2, b3);
+#pragma unroll
+                        for (int mt = 0; mt < MT; ++mt) {
+                            uint32_t a0, a1, a2, a3;
+                            const int ca = 2 * kk + (mi >> 1);
+                            ldsm_x4(qbase + (ca >> 2) * L.q_box + sw64(qrow0 + mt * 16 + (mi & 1) * 8 + ri, ca), a0, a1,
+                                    a2, a3);
+                            mma_bf16_16816(sc[mt][0], a0, a1, a2, a3, b0, b1);
+                            mma_bf16_16816(sc[mt][1], a0, a1, a2, a3, b2, b3);
+                        }
+                    }
+                    // online softmax (base 2) and P in bf16 as the A operand of P·V
+                    uint32_t pa[MT][4];
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            float x[4];
+#pragma unroll
+                            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                                for (int e = 0; e < 2; ++e) {
+                                    const int tok = nt * 8 + 2 * cq + e;
+                                    x[nt * 2 + e] = tok < n_valid ? sc[mt][nt][2 * r + e] * a.scale_log2 : -INFINITY;
+                                }
+                            float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                            const float mn = fmaxf(m[mt][r], mx);    // finite: token 0 of the slice is valid
+                            const float alpha = fast_exp2(m[mt][r] - mn);
+                            m[mt][r] = mn;
+                            float pr[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) pr[e] = fast_exp2(x[e] - mn);
+                            const uint32_t lo = pack_bf16x2(pr[0], pr[1]);   // tokens 2cq, 2cq+1
+                            const uint32_t hi = pack_bf16x2(pr[2], pr[3]);   // tokens 8+2cq, 9+2cq
+                            pa[mt][r] = lo;
+                            pa[mt][2 + r] = hi;
+                            // the row sum uses the rounded weights, so Σ weights = 1 after normalising
+                            const float ps = bf16_lo(lo) + bf16_hi(lo) + bf16_lo(hi) + bf16_hi(hi);
+                            l[mt][r] = l[mt][r] * alpha + ps;
+#pragma unroll
+                            for (int nd = 0; nd < D / 8; ++nd) {
+                                o[mt][nd][2 * r] *= alpha;
+                                o[mt][nd][2 * r + 1] *= alpha;
+                            }
+                        }
+                    }
+                    // O += P·V
+#pragma unroll
+                    for (int pq = 0; pq < D / 16; ++pq) {
+                        uint32_t b0, b1, b2, b3;
+                        const int cv = 2 * pq + (mi >> 1);
+                        ldsm_x4_t(vb + (cv >> 2) * HG * C::BOX + sw64(r0 + (mi & 1) * 8 + ri, cv), b0, b1, b2, b3);
+#pragma unroll
+                        for (int mt = 0; mt < MT; ++mt) {
+                            mma_bf16_16816(o[mt][2 * pq], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], b0, b1);
+                            mma_bf16_16816(o[mt][2 * pq + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], b2, b3);
+                        }
                     }
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
             }
-            // S = Q·Kᵀ for the warp's 16 tokens
-            float sc[MT][2][4];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        }
+        // the query rows of this piece are no longer read
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qempty0 + 8 * qb);
+
+        const int j = p.gi * HG + hw;                          // this warp's KV head
+        const int n_rows = min(heads, G - p.hb * C::HEADS);    // its query heads in this block
+        const size_t out_row0 = (size_t)p.b * a.Hq + j * G + p.hb * C::HEADS;
+        const int slot = 2 * c + (k == 0 ? 0 : 1);
+        const size_t part_row0 = (size_t)slot * HG * heads + hw * heads;
+        if constexpr (WPH == 1) {
+            // ---------------------------------------------------------- direct write
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                for (int r = 0; r < 2; ++r) {
+                    float lr = l[mt][r];
+                    lr += __shfl_xor_sync(0xffffffffu, lr, 1);
+                    lr += __shfl_xor_sync(0xffffffffu, lr, 2);
+                    const int h = mt * 16 + r * 8 + g8;
+                    if (h >= n_rows) continue;
+                    const float inv = ok && lr > 0.f ? 1.f / lr : 0.f;
+                    float *dst = p.whole ? a.out + (out_row0 + h) * D : a.o_part + (part_row0 + h) * D;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                uint32_t b0, b1, b2, b3;
-                {
-                    const int row = warp * 16 + (mi >> 1) * 8 + ri;
-                    ldsm_x4(kb + kv_off(row, 2 * kk + (mi & 1)), b0, b1, b2, b3);
+                    for (int nd = 0; nd < D / 8; ++nd)
+                        *reinterpret_cast<float2 *>(dst + nd * 8 + 2 * cq) =
+                            make_float2(o[mt][nd][2 * r] * inv, o[mt][nd][2 * r + 1] * inv);
+                    if (!p.whole && cq == 0)
+                        a.lse_part[part_row0 + h] = ok && lr > 0.f ? (m[mt][r] + log2f(lr)) * kLn2 : -INFINITY;
                 }
+        } else {
+            // ---------------------------------------------------------- combine the WPH warps of each head
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");   // scratch free
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    uint32_t a0, a1, a2, a3;
-                    const int hrow = mt * 16 + (mi & 1) * 8 + ri;
-                    ldsm_x4(qbase + hrow * C::QPITCH + (2 * kk + (mi >> 1)) * 16, a0, a1, a2, a3);
-                    mma_bf16_16816(sc[mt][0], a0, a1, a2, a3, b0, b1);
-                    mma_bf16_16816(sc[mt][1], a0, a1, a2, a3, b2, b3);
-                }
-            }
-            // online softmax (base 2) and P in bf16 as the A operand of P·V
-            uint32_t pa[MT][4];
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
+            for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    float x[4];
+                    float lr = l[mt][r];
+                    lr += __shfl_xor_sync(0xffffffffu, lr, 1);
+                    lr += __shfl_xor_sync(0xffffffffu, lr, 2);
+                    const int h = mt * 16 + r * 8 + g8;
+                    if (h < heads) {
+                        float *row = scr + (warp * heads + h) * (D + 2);
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int tok = nt * 8 + 2 * cq + e;
-                            x[nt * 2 + e] = tok < n_valid ? sc[mt][nt][2 * r + e] * a.scale_log2 : -INFINITY;
+                        for (int nd = 0; nd < D / 8; ++nd) {
+                            row[nd * 8 + 2 * cq] = o[mt][nd][2 * r];
+                            row[nd * 8 + 2 * cq + 1] = o[mt][nd][2 * r + 1];
                         }
-                    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                    const float mn = fmaxf(m[mt][r], mx);            // finite: token 0 of the slice is valid
-                    const float alpha = fast_exp2(m[mt][r] - mn);
-                    m[mt][r] = mn;
-                    float p[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) p[e] = fast_exp2(x[e] - mn);
-                    const uint32_t lo = pack_bf16x2(p[0], p[1]);     // tokens 2cq, 2cq+1
-                    const uint32_t hi = pack_bf16x2(p[2], p[3]);     // tokens 8+2cq, 9+2cq
-                    pa[mt][r] = lo;
-                    pa[mt][2 + r] = hi;
-                    // the row sum uses the rounded weights, so Σ weights = 1 after normalising
-                    const float ps = bf16_lo(lo) + bf16_hi(lo) + bf16_lo(hi) + bf16_hi(hi);
-                    l[mt][r] = l[mt][r] * alpha + ps;
-#pragma unroll
-                    for (int nd = 0; nd < D / 8; ++nd) {
-                        o[mt][nd][2 * r] *= alpha;
-                        o[mt][nd][2 * r + 1] *= alpha;
+                        if (cq == 0) {
+                            row[D] = ok ? m[mt][r] : -INFINITY;
+                            row[D + 1] = lr;
+                        }
                     }
                 }
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+            // per (head of the group, query row): the warps' weights 2^(m_w − M) / L and ln Σ e^s
+            for (int idx = threadIdx.x; idx < HG * heads; idx += kConsumers * 32) {
+                const int hh = idx / heads, h = idx % heads;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < WPH; ++w) M = fmaxf(M, scr[((hh * WPH + w) * heads + h) * (D + 2) + D]);
+                float f[WPH], Lsum = 0.f;
+#pragma unroll
+                for (int w = 0; w < WPH; ++w) {
+                    const float *row = scr + ((hh * WPH + w) * heads + h) * (D + 2);
+                    f[w] = M == -INFINITY ? 0.f : fast_exp2(row[D] - M);
+                    Lsum = fmaf(row[D + 1], f[w], Lsum);
+                }
+                const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+#pragma unroll
+                for (int w = 0; w < WPH; ++w) fac[idx * (WPH + 1) + w] = f[w] * inv;
+                fac[idx * (WPH + 1) + WPH] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
             }
-            // O += P·V
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+            for (int idx = threadIdx.x; idx < HG * n_rows * D; idx += kConsumers * 32) {
+                const int hh = idx / (n_rows * D), h = (idx / D) % n_rows, d = idx % D;
+                const int fi = hh * heads + h;
+                float val = 0.f;
 #pragma unroll
-            for (int pq = 0; pq < D / 16; ++pq) {
-                uint32_t b0, b1, b2, b3;
-                const int row = warp * 16 + (mi & 1) * 8 + ri;
-                ldsm_x4_t(vb + kv_off(row, 2 * pq + (mi >> 1)), b0, b1, b2, b3);
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    mma_bf16_16816(o[mt][2 * pq], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], b0, b1);
-                    mma_bf16_16816(o[mt][2 * pq + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], b2, b3);
+                for (int w = 0; w < WPH; ++w)
+                    val = fmaf(scr[((hh * WPH + w) * heads + h) * (D + 2) + d], fac[fi * (WPH + 1) + w], val);
+                const int jj = p.gi * HG + hh;
+                if (p.whole) {
+                    a.out[((size_t)p.b * a.Hq + jj * G + p.hb * C::HEADS + h) * D + d] = val;
+                } else {
+                    const size_t pr = (size_t)slot * HG * heads + hh * heads + h;
+                    a.o_part[pr * D + d] = val;
+                    if (d == 0) a.lse_part[pr] = fac[fi * (WPH + 1) + WPH];
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        // ---------------------------------------------------------- finish a shared segment
+        // Publish this block's partial; the last of the segment's blocks to arrive combines all
+        // of them and resets the arrival counter for the next call. A block's first piece is
+        // finished while its stream goes on with the next one. With one warp per KV head
+        // (WPH = 1) each warp does this for its own head alone, with no block-wide barrier;
+        // otherwise the consumer warps do it together.
+        if (!p.whole) {
+            const Piece &q = p;
+            const int nb = stream_tiles(q.S, TT);
+            const long long fs = (long long)seg_per_seq * prefix[q.b] + (long long)(q.gi * a.n_hblk + q.hb) * nb;
+            // the partial slots of all blocks holding tiles of this segment: blocks c0 .. c1, or,
+            // with fewer tiles than blocks (each block then owns at most one tile), the owners of
+            // the segment's nb tiles
+            const bool sparse = T < a.n_blocks;
+            const int c0 = stream_block_of(fs, T, a.n_blocks);
+            const int n_pieces = sparse ? nb : stream_block_of(fs + nb - 1, T, a.n_blocks) - c0 + 1;
+            auto slot_of = [&](int i) {
+                if (sparse) return 2 * stream_block_of(fs + i, T, a.n_blocks);
+                if (i == 0) return stream_start(c0, T, a.n_blocks) < fs ? 2 * c0 + 1 : 2 * c0;
+                return 2 * (c0 + i);
+            };
+            const int seg = q.b * seg_per_seq + q.gi * a.n_hblk + q.hb;
+            // rows of heads hh0 .. hh0+n_hh-1 of the group, merged by n_thr threads from t0:
+            // partial row bases cached in wl, their lse values in wc
+            auto merge_rows = [&](int hh0, int n_hh, int t0, int n_thr, int *wl, float *wc) {
+                for (int i = t0; i < n_pieces; i += n_thr) wl[i] = slot_of(i) * HG * heads;
+                if (WPH == 1) __syncwarp(); else asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+                const int rows = n_hh * n_rows;
+                const bool cached = rows * n_pieces <= kLseCache;
+                if (cached)
+                    for (int e = t0; e < rows * n_pieces; e += n_thr) {
+                        const int r = e / n_pieces, i = e % n_pieces;
+                        wc[e] = __ldcg(a.lse_part + wl[i] + (hh0 + r / n_rows) * heads + r % n_rows);
+                    }
+                if (WPH == 1) __syncwarp(); else asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+                for (int idx = t0; idx < rows * (D / 4); idx += n_thr) {
+                    const int r = idx / (D / 4), col = idx % (D / 4);
+                    const int off = (hh0 + r / n_rows) * heads + r % n_rows;
+                    auto lse_at = [&](int i) { return cached ? wc[r * n_pieces + i] : __ldcg(a.lse_part + wl[i] + off); };
+                    float M = -INFINITY;
+                    for (int i = 0; i < n_pieces; ++i) M = fmaxf(M, lse_at(i));
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    float W = 0.f;
+                    // eight partial rows in flight at a time
+                    for (int i0 = 0; i0 < n_pieces; i0 += 8) {
+                        float4 x[8];
+    #pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            if (i0 + u < n_pieces)
+                                x[u] = __ldcg(reinterpret_cast<const float4 *>(a.o_part + ((size_t)wl[i0 + u] + off) * D) + col);
+    #pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            if (i0 + u < n_pieces) {
+                                const float w = M == -INFINITY ? 0.f : fast_exp2((lse_at(i0 + u) - M) * kLog2e);
+                                W += w;
+                                acc.x = fmaf(w, x[u].x, acc.x);
+                                acc.y = fmaf(w, x[u].y, acc.y);
+                                acc.z = fmaf(w, x[u].z, acc.z);
+                                acc.w = fmaf(w, x[u].w, acc.w);
+                            }
+                    }
+                    const float inv = W > 0.f ? 1.f / W : 0.f;
+                    const int jj = q.gi * HG + hh0 + r / n_rows;
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        a.out + ((size_t)q.b * a.Hq + jj * G + q.hb * C::HEADS + r % n_rows) * D);
+                    dst[col] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                }
+            };
+            if constexpr (WPH == 1) {
+                __syncwarp();
+                int last = 0;
+                if (lane == 0) {
+                    int *cnt = a.counters + (size_t)seg * HG + hw;
+                    const int prev = atomic_add_acq_rel_gpu(cnt, 1);
+                    last = prev == n_pieces - 1;
+                    if (last) *cnt = 0;
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+                    int *wl = plist + warp * (a.n_blocks + kLseCache);
+                    merge_rows(hw, 1, lane, 32, wl, reinterpret_cast<float *>(wl + a.n_blocks));
+                }
+            } else {
+                __threadfence();
+                asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+                if (threadIdx.x == 0) {
+                    int *cnt = a.counters + (size_t)seg * HG;
+                    const int prev = atomic_add_acq_rel_gpu(cnt, 1);
+                    *flag = prev == n_pieces - 1;
+                    if (prev == n_pieces - 1) *cnt = 0;
+                }
+                asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+                if (*flag) {
+                    __threadfence();
+                    merge_rows(0, HG, threadIdx.x, kConsumers * 32, plist, reinterpret_cast<float *>(plist + a.n_blocks));
+                }
+                asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");   // flag, lists reused
+            }
+        }
+        ++k;
     }
-    if (!ok) return;
 
-    // ---------------------------------------------------------------- merge the 4 warps
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");   // all stages consumed
-    float *mrg = reinterpret_cast<float *>(smem);                          // [warp][head][D+2]
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            float lr = l[mt][r];
-            lr += __shfl_xor_sync(0xffffffffu, lr, 1);
-            lr += __shfl_xor_sync(0xffffffffu, lr, 2);
-            const int h = mt * 16 + r * 8 + g;
-            float *row = mrg + (warp * C::HEADS + h) * (D + 2);
-#pragma unroll
-            for (int nd = 0; nd < D / 8; ++nd) {
-                row[nd * 8 + 2 * cq] = o[mt][nd][2 * r];
-                row[nd * 8 + 2 * cq + 1] = o[mt][nd][2 * r + 1];
-            }
-            if (cq == 0) {
-                row[D] = m[mt][r];
-                row[D + 1] = lr;
-            }
-        }
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
-    for (int idx = threadIdx.x; idx < heads * D; idx += kConsumers * 32) {
-        const int h = idx / D, d = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, mrg[(w * C::HEADS + h) * (D + 2) + D]);
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kConsumers; ++w) {
-                const float *row = mrg + (w * C::HEADS + h) * (D + 2);
-                const float f = fast_exp2(row[D] - M);
-                L = fmaf(row[D + 1], f, L);
-                O = fmaf(row[d], f, O);
-            }
-        }
-        const size_t orow = (size_t)b * a.Hq + h0 + h;
-        const float val = L > 0.f ? O / L : 0.f;
-        if (a.n_split == 1) {
-            a.out[orow * D + d] = val;
-        } else {
-            a.o_part[(orow * a.n_split + split) * D + d] = val;
-            if (d == 0) a.lse_part[orow * a.n_split + split] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
-        }
-    }
 }
 
-template <int D, int MT, int NS>
-cudaError_t launch_cfg(const DecodeGqaArgs &a, cudaStream_t st) {
-    using C = Cfg<D, MT, NS>;
-    CUtensorMap km, vm;
+// Ring depth per configuration: about 192 KB of K/V in flight per SM, less where the
+// combine scratch of warps sharing a head needs room.
+template <int D, int MT, int HG, int NC>
+constexpr int ring_depth() {
+    constexpr int stage = 2 * (D / 32) * HG * (HG == 4 ? 32 : 16 * NC) * 64;
+    constexpr int budget = HG == 4 ? 192 * 1024 : MT == 2 ? 128 * 1024 : 176 * 1024;
+    constexpr int n = budget / stage;
+    return n < 2 ? 2 : n;
+}
+
+int mt_for(int G) { return G <= 16 ? 1 : 2; }
+
+// KV heads per tile: 4 when they divide Hkv and a head's query rows fit one MMA tile,
+// else 2, else 1.
+int hg_for(int Hkv, int G) {
+    if (G > 16) return 1;
+    if (Hkv % 4 == 0) return 4;
+    if (Hkv % 2 == 0) return 2;
+    return 1;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        n <= 0) {
+        cudaGetLastError();
+        return 148;
+    }
+    return n;
+}
+
+template <int D, int MT, int HG, int NC>
+cudaError_t launch_cfg(const DecodeStreamArgs &a, cudaStream_t st) {
+    constexpr int NS = ring_depth<D, MT, HG, NC>();
+    using C = Cfg<D, MT, HG, NS, NC>;
+    const int G = a.Hq / a.Hkv;
+    // query rows: the group's HG·G rows (one head block when n_hblk > 1), plus the padding
+    // the last head's 16·MT-row MMA tile reaches past them
+    const int q_loaded = a.n_hblk == 1 ? HG * G : a.heads;
+    const int q_rows = ((a.n_hblk == 1 ? (HG - 1) * G : 0) + 16 * MT + 7) / 8 * 8;
+    const Layout L = layout<D, MT, HG, NS, NC>(q_rows, a.heads, a.B, a.n_blocks);
+    if (L.total > 227 * 1024) return cudaErrorInvalidValue;
+    CUtensorMap km, vm, qm;
     const uint64_t dims[4] = {(uint64_t)D, (uint64_t)a.Hkv, (uint64_t)a.S_max, (uint64_t)a.B};
     const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)a.Hkv * D * 2, (uint64_t)a.S_max * a.Hkv * D * 2};
-    const uint32_t box[4] = {32, 1, kT, 1};
+    const uint32_t box[4] = {32, 1, (uint32_t)C::TT, 1};
     cudaError_t e = encode_tensor_map(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.k, dims, strides, box,
                                       CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (e == cudaSuccess)
         e = encode_tensor_map(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.v, dims, strides, box,
                               CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-    if (e != cudaSuccess) return e;
-    auto kern = decode_gqa_bf16_kernel<D, MT, NS>;
-    static bool attr_set = false;   // per process; the attribute is per function
-    if (!attr_set) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
+    if (e == cudaSuccess) {
+        const uint64_t qdims[3] = {(uint64_t)D, (uint64_t)a.Hq, (uint64_t)a.B};
+        const uint64_t qstrides[2] = {(uint64_t)D * 2, (uint64_t)a.Hq * D * 2};
+        const uint32_t qbox[3] = {32, (uint32_t)q_loaded, 1};
+        e = encode_tensor_map(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, qdims, qstrides, qbox,
+                              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     }
-    const int G = a.Hq / a.Hkv;
-    const dim3 grid(a.n_split, a.Hkv * ((G + C::HEADS - 1) / C::HEADS), a.B);
-    e = launch_pdl(kern, grid, dim3(kThreads), C::SMEM, st, km, vm, a);
+    if (e != cudaSuccess) return e;
+    auto kern = decode_gqa_bf16_kernel<D, MT, HG, NS, NC>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(kern, dim3(a.n_blocks), dim3(C::kThreads), L.total, st, km, vm, qm, a, L, q_loaded);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// One KV head per tile with a single MMA row tile per head: 7 consumer warps over 112-token
+// tiles, for nearly twice the latency hiding per SM (8 warps in all keep 255 registers per
+// thread available; the combine scratch of 32-row heads would not fit beside them).
+template <int D, int MT>
+cudaError_t launch_mt(const DecodeStreamArgs &a, cudaStream_t st) {
+    switch (a.hg) {
+        case 4: return launch_cfg<D, MT, 4, 4>(a, st);
+        case 2: return launch_cfg<D, MT, 2, 4>(a, st);
+        default: return MT == 1 ? launch_cfg<D, MT, 1, 7>(a, st) : launch_cfg<D, MT, 1, 4>(a, st);
+    }
+}
+
 template <int D>
-cudaError_t launch_d(const DecodeGqaArgs &a, cudaStream_t st) {
-    constexpr int NS = D == 128 ? 3 : (D == 96 ? 4 : 6);
-    const int G = a.Hq / a.Hkv;
-    if (G <= 16) return launch_cfg<D, 1, NS>(a, st);
-    return launch_cfg<D, 2, NS>(a, st);
+cudaError_t launch_d(const DecodeStreamArgs &a, cudaStream_t st) {
+    return mt_for(a.Hq / a.Hkv) == 1 ? launch_mt<D, 1>(a, st) : launch_mt<D, 2>(a, st);
 }
 
 }  // namespace
 
-int decode_gqa_bf16_tile_tokens(int, int) { return kT; }
+// Aligned mode: when the (sequence, KV head, head block) segments number between half the
+// SMs and all of them, each gets a block of its own and nothing is shared or merged (the
+// merge of a segment split between blocks can only start after its last piece, which
+// lengthens the tail of a short call more than the uneven segment lengths do).
+bool decode_gqa_stream_aligned(int B, int Hq, int Hkv, int n_split) {
+    const int G = Hq / Hkv;
+    const int MT = mt_for(G);
+    const long long segs = (long long)B * Hkv * ((G + 16 * MT - 1) / (16 * MT));
+    const int sms = sm_count();
+    return n_split == 0 && segs <= sms && 2 * segs >= sms;
+}
 
-int decode_gqa_bf16_heads_per_block(int G) { return G <= 16 ? 16 : 32; }
+int decode_gqa_stream_blocks(int B, int Hq, int Hkv, int D, int n_split) {
+    (void)D;
+    const int G = Hq / Hkv;
+    const int MT = mt_for(G);
+    const int n_hblk = (G + 16 * MT - 1) / (16 * MT);
+    if (decode_gqa_stream_aligned(B, Hq, Hkv, n_split)) return B * Hkv * n_hblk;
+    long long n = sm_count();
+    if (n_split > 0) {
+        const long long cap = (long long)n_split * B * (Hkv / hg_for(Hkv, G)) * n_hblk;
+        if (cap < n) n = cap;
+    }
+    return (int)(n < 1 ? 1 : n);
+}
 
-cudaError_t launch_decode_gqa_bf16(const DecodeGqaArgs &a, cudaStream_t st) {
+// Partial rows: two slots per block, hg·heads query rows per slot.
+static size_t stream_part_rows(int B, int Hq, int Hkv, int D, int n_split) {
+    const int G = Hq / Hkv;
+    const int heads = G < 16 * mt_for(G) ? G : 16 * mt_for(G);
+    return 2 * (size_t)decode_gqa_stream_blocks(B, Hq, Hkv, D, n_split) * hg_for(Hkv, G) * heads;
+}
+
+size_t decode_gqa_stream_o_bytes(int B, int Hq, int Hkv, int D, int n_split) {
+    return (stream_part_rows(B, Hq, Hkv, D, n_split) * D * sizeof(float) + 255) / 256 * 256;
+}
+
+size_t decode_gqa_stream_lse_bytes(int B, int Hq, int Hkv, int D, int n_split) {
+    return (stream_part_rows(B, Hq, Hkv, D, n_split) * sizeof(float) + 255) / 256 * 256;
+}
+
+// Per-segment arrival counters after the partials.
+static size_t stream_counter_bytes(int B, int Hq, int Hkv) {
+    const int G = Hq / Hkv;
+    const int MT = mt_for(G);
+    const size_t segs = (size_t)B * Hkv * ((G + 16 * MT - 1) / (16 * MT));   // one per KV head
+    return (segs * sizeof(int) + 255) / 256 * 256;
+}
+
+size_t decode_gqa_stream_workspace(int B, int Hq, int Hkv, int D, int n_split) {
+    return decode_gqa_stream_o_bytes(B, Hq, Hkv, D, n_split) + decode_gqa_stream_lse_bytes(B, Hq, Hkv, D, n_split) +
+           stream_counter_bytes(B, Hq, Hkv);
+}
+
+cudaError_t launch_decode_gqa_stream(const DecodeStreamArgs &a0, cudaStream_t st) {
+    DecodeStreamArgs a = a0;
+    const int G = a.Hq / a.Hkv;
+    const int MT = mt_for(G);
+    a.heads = G < 16 * MT ? G : 16 * MT;
+    a.n_hblk = (G + 16 * MT - 1) / (16 * MT);
+    a.hg = a.aligned ? 1 : hg_for(a.Hkv, G);
+    a.tile_tokens = a.hg == 4 ? 32 : (a.hg == 1 && MT == 1) ? 112 : 64;
+    cudaError_t e;
     switch (a.D) {
-        case 64: return launch_d<64>(a, st);
-        case 96: return launch_d<96>(a, st);
-        case 128: return launch_d<128>(a, st);
+        case 64: e = launch_d<64>(a, st); break;
+        case 96: e = launch_d<96>(a, st); break;
+        case 128: e = launch_d<128>(a, st); break;
         default: return cudaErrorInvalidValue;
     }
+    return e;
 }
 
 int decode_gqa_read_and_clear_status(cudaStream_t s, unsigned *flag) {

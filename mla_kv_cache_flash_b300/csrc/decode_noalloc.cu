@@ -12,10 +12,12 @@
 // loads the library holds it until the process exits. In host code its name only stands in
 // for the symbol; its device address is looked up with cudaGetSymbolAddress once per device,
 // with that device current, on the first call made on that device. That first call should
-// therefore come before any stream capture. All calls share the one array and it keeps the
-// last call's contents; nothing in it has to start at zero, because every call writes each
-// partial before reading it. Two calls whose kernels can overlap on the GPU (different
-// streams, or different host threads) race on the array and must be ordered by the caller.
+// therefore come before any stream capture. All calls share the one array. It is zero when
+// the library loads; the bf16 kernels keep per-segment arrival counters in it that must
+// start at zero, and every call that completes leaves them at zero again (the partials need
+// no initial value: each is written before it is read). Two calls whose kernels can overlap
+// on the GPU (different streams, or different host threads) race on the array and must be
+// ordered by the caller.
 #include "../../include/mlakv.h"
 #include "common.cuh"
 

@@ -82,6 +82,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Atomic add at GPU scope with acquire-release ordering: the writes the calling thread (and,
+// through a preceding warp or block barrier, its partners) made before it are visible to a
+// thread that later reads the incremented value with acquire ordering, and vice versa.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // 4-D tiled TMA load into shared memory, completing `bytes` on `bar`.
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
                                             uint32_t bar, uint64_t policy) {

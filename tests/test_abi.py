@@ -105,8 +105,12 @@ def test_gqa_split_plan_bounds(L):
     assert L.attn_decode_gqa_num_splits(1, 1, 1, 64, 1, 0, 0) == 1
     assert L.attn_decode_gqa_num_splits(1, 1, 1, 64, 0, 0, 0) == 1
     assert L.attn_decode_gqa_num_splits(2, 8, 2, 64, 128, 0, 7) == 7
+    # bf16 caches: the persistent grid (one block per SM), capped at n_split x segments
+    # (a segment: one sequence's tokens for a group of up to 4 KV heads)
     n = L.attn_decode_gqa_num_splits(1, 32, 1, 128, 8192, 1, 0)
-    assert 1 <= n <= 64
+    assert n >= 1
+    assert L.attn_decode_gqa_num_splits(1, 32, 1, 128, 8192, 1, 3) == min(3, n)
+    assert L.attn_decode_gqa_num_splits(2, 32, 32, 128, 8192, 1, 1) == min(2 * 8, n)
     assert L.attn_decode_gqa_num_splits(64, 32, 32, 128, 8192, 1, 0) >= 1
     assert L.attn_decode_gqa_num_splits(2, 8, 3, 64, 128, 0, 0) == SHAPE
 

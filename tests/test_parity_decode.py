@@ -104,14 +104,13 @@ def test_max_s_bound_smaller_than_capacity():
 def test_deterministic_and_stream_ordered_workspace():
     w = W.MINIMIND_GQA
     inp = W.decode_inputs(w, DEV)
-    n = mk.decode_gqa_num_splits(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.s_max, mk.ATTN_BF16)
-    ws = torch.empty(mk.decode_gqa_workspace_size(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.s_max,
-                                                  mk.ATTN_BF16, max(n, 2)), dtype=torch.uint8, device=DEV)
+    n = 2
+    ws = torch.zeros(mk.decode_gqa_workspace_size(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.s_max,
+                                                  mk.ATTN_BF16, n), dtype=torch.uint8, device=DEV)
     inp2 = W.decode_inputs(w, DEV, seed=w.seed + 5)
-    a = mk.decode_gqa(inp["q"], inp["k_cache"], inp["v_cache"], inp["seq_lens"], n_split=max(n, 2), workspace=ws)
-    b = mk.decode_gqa(inp2["q"], inp2["k_cache"], inp2["v_cache"], inp2["seq_lens"], n_split=max(n, 2),
-                      workspace=ws)
-    a2 = mk.decode_gqa(inp["q"], inp["k_cache"], inp["v_cache"], inp["seq_lens"], n_split=max(n, 2), workspace=ws)
+    a = mk.decode_gqa(inp["q"], inp["k_cache"], inp["v_cache"], inp["seq_lens"], n_split=n, workspace=ws)
+    b = mk.decode_gqa(inp2["q"], inp2["k_cache"], inp2["v_cache"], inp2["seq_lens"], n_split=n, workspace=ws)
+    a2 = mk.decode_gqa(inp["q"], inp["k_cache"], inp["v_cache"], inp["seq_lens"], n_split=n, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(a, a2)
     assert _max_err(b, _oracle_decode(inp2, w.scale)) <= TOL_BF16

@@ -66,11 +66,12 @@ def test_noalloc_matches_workspace_entry_point_twice(shape, n_split):
 def test_noalloc_rejects_sizes_above_its_array():
     cap = mk.lib().attn_decode_gqa_noalloc_max_scratch()
     assert cap == 16 << 20
-    # 64 sequences x 32 heads x 64 splits x 128 floats = 64 MiB of partials: refused before launch
+    # fp32 cache, 64 sequences x 32 heads x 64 splits x 128 floats = 64 MiB of partials:
+    # refused before launch
     B, Hq, Hkv, D, S, n = 64, 32, 1, 128, 8192, 64
-    assert mk.decode_gqa_workspace_size(B, Hq, Hkv, D, S, mk.ATTN_BF16, n) > cap
+    assert mk.decode_gqa_workspace_size(B, Hq, Hkv, D, S, mk.ATTN_F32, n) > cap
     p = ctypes.c_void_p(1 << 20)
-    rc = mk.lib().attn_decode_gqa_noalloc(p, p, p, p, p, B, Hq, Hkv, D, 0.088, S, S, mk.ATTN_BF16, n,
+    rc = mk.lib().attn_decode_gqa_noalloc(p, p, p, p, p, B, Hq, Hkv, D, 0.088, S, S, mk.ATTN_F32, n,
                                           ctypes.c_void_p(0))
     assert rc == -4
     assert "above the built-in" in mk.last_error()
