@@ -77,8 +77,11 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
  *            0 lets the library choose from B, Hkv, max_S and the device's SM count.
  *            bf16 cache: the work is always balanced over one persistent thread block per SM
  *            (all sequences' cached tokens are cut into equal shares, whatever their
- *            lengths); n_split > 0 caps the number of blocks at n_split per (sequence, group
- *            of up to 4 KV heads).
+ *            lengths); n_split > 0 caps the number of blocks at n_split per segment. A
+ *            segment is one sequence's tokens for a group of up to 4 KV heads, or, when
+ *            D = 128 and 16 or more query heads share each KV head (Hq/Hkv a multiple of
+ *            16: those shapes run on the tcgen05 tensor cores), for one KV head and a block
+ *            of 16 or 32 of its query heads.
  *   D        64, 96 or 128. Any Hq/Hkv with Hq % Hkv == 0 and Hq/Hkv <= 128.
  *   workspace, ws_bytes: scratch for the split partials, at least
  *            attn_decode_gqa_workspace_size(...) bytes with the same arguments; may be
@@ -144,7 +147,9 @@ int attn_decode_gqa_noalloc(const void *q, const void *k_cache, const void *v_ca
  *   out_lat     [B, Hq, r] fp32, fully written.
  *   scale       1/sqrt(d_nope + dr) for the article's recombined query.
  *   r = 128, dr = 48 are built in; Hq a multiple of 16 up to 128.
- *   n_split, max_S, workspace: as for attn_decode_gqa.
+ *   n_split, max_S, workspace: as for attn_decode_gqa with a bf16 cache (one persistent
+ *            block per SM; a segment is one sequence and a block of 16 or 32 heads; the
+ *            workspace holds arrival counters and must be zero-filled before its first use).
  * ------------------------------------------------------------------------------------- */
 size_t attn_decode_mla_workspace_size(int B, int Hq, int r, int dr, int max_S, int n_split);
 int attn_decode_mla_num_splits(int B, int Hq, int r, int dr, int max_S, int n_split);

@@ -233,7 +233,7 @@ def decode_mla_absorbed(q_lat, q_rope, c_cache, krope_cache, seq_lens, scale, ou
         _need(out_lat, "out_lat", torch.float32, 3, dev)
     need = decode_mla_workspace_size(B, Hq, r, dr, max_s, n_split)
     if need and (workspace is None or workspace.numel() < need):
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() if workspace is not None else 0
     _check(lib().attn_decode_mla_absorbed(_ptr(q_lat), _ptr(q_rope), _ptr(c_cache), _ptr(krope_cache),
                                           _ptr(seq_lens), _ptr(out_lat), B, Hq, r, dr, float(scale), S_max,

@@ -99,6 +99,7 @@ SplitPlan gqa_plan(int B, int Hq, int Hkv, int D, int max_S, attn_dtype dtype, i
         return plan_splits(max_S, kFmaTile, (long)B * Hkv * (G / hb), n_split, 2);
     }
     // bf16: the balanced split; n_split reports the persistent grid size
+    if (decode_tc_gqa_eligible(B, Hq, Hkv, D)) return SplitPlan{decode_tc_gqa_blocks(B, Hq, Hkv, n_split), 0};
     return SplitPlan{decode_gqa_stream_blocks(B, Hq, Hkv, D, n_split), 0};
 }
 
@@ -145,12 +146,12 @@ int check_mla_shapes(int B, int Hq, int r, int dr, int S_max, int max_S, int n_s
         return fail(ATTN_ERR_UNSUPPORTED, "MLA rank r=%d, rope width dr=%d not built (r=128, dr=48)", r, dr);
     if (Hq % kMlaHeadsPerBlock != 0 || Hq > 128)
         return fail(ATTN_ERR_UNSUPPORTED, "MLA head count Hq=%d must be a multiple of 16 up to 128", Hq);
+    if (!decode_tc_mla_fits(B, Hq))
+        return fail(ATTN_ERR_UNSUPPORTED, "MLA batch B=%d too large for the kernel's shared-memory plan", B);
     return ATTN_OK;
 }
 
-SplitPlan mla_plan(int B, int Hq, int max_S, int n_split) {
-    return plan_splits(max_S, decode_mla_tile_tokens(), (long)B * (Hq / kMlaHeadsPerBlock), n_split, 4);
-}
+
 
 }  // namespace
 
@@ -177,7 +178,9 @@ MLAKV_API int attn_decode_gqa_num_splits(int B, int Hq, int Hkv, int D, int max_
 MLAKV_API size_t attn_decode_gqa_workspace_size(int B, int Hq, int Hkv, int D, int max_S, attn_dtype dtype,
                                                 int n_split) {
     if (check_gqa_shapes(B, Hq, Hkv, D, max_S > 0 ? max_S : 1, max_S, dtype, n_split) != ATTN_OK) return 0;
-    if (!gqa_use_fma(dtype)) return decode_gqa_stream_workspace(B, Hq, Hkv, D, n_split);
+    if (!gqa_use_fma(dtype))
+        return decode_tc_gqa_eligible(B, Hq, Hkv, D) ? decode_tc_gqa_workspace(B, Hq, Hkv, n_split)
+                                                     : decode_gqa_stream_workspace(B, Hq, Hkv, D, n_split);
     const SplitPlan p = gqa_plan(B, Hq, Hkv, D, max_S, dtype, n_split);
     return partials_bytes(B, Hq, D, p.n_split);
 }
@@ -195,11 +198,19 @@ MLAKV_API int attn_decode_gqa(const void *q, const void *k_cache, const void *v_
         return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_gqa: every pointer must be 16-byte aligned");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (!gqa_use_fma(dtype)) {
-        // bf16: persistent blocks over an even share of all cached tokens, then the merge
-        const size_t need = decode_gqa_stream_workspace(B, Hq, Hkv, D, n_split);
+        // bf16: persistent blocks over an even share of all cached tokens, merged in-kernel
+        const bool tc = decode_tc_gqa_eligible(B, Hq, Hkv, D);
+        const size_t need = tc ? decode_tc_gqa_workspace(B, Hq, Hkv, n_split)
+                               : decode_gqa_stream_workspace(B, Hq, Hkv, D, n_split);
         if (!workspace || ws_bytes < need || !aligned16(workspace))
             return fail(ATTN_ERR_WORKSPACE, "attn_decode_gqa: workspace of %zu bytes (16-byte aligned) needed, "
                         "got %zu at %p", need, workspace ? ws_bytes : (size_t)0, workspace);
+        if (tc) {
+            const cudaError_t e = launch_decode_tc_gqa(q, k_cache, v_cache, seq_lens, out, B, Hq, Hkv, scale * kLog2e,
+                                                       S_max, n_split, workspace, s);
+            if (e != cudaSuccess) return cuda_fail(e, "attn_decode_gqa: kernel launch");
+            return ok();
+        }
         DecodeStreamArgs a{};
         a.q = q; a.k = k_cache; a.v = v_cache; a.seq_lens = seq_lens; a.out = out;
         a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.D = D;
@@ -250,12 +261,12 @@ MLAKV_API int attn_decode_gqa(const void *q, const void *k_cache, const void *v_
 MLAKV_API int attn_decode_mla_num_splits(int B, int Hq, int r, int dr, int max_S, int n_split) {
     const int rc = check_mla_shapes(B, Hq, r, dr, max_S > 0 ? max_S : 1, max_S, n_split);
     if (rc != ATTN_OK) return rc;
-    return mla_plan(B, Hq, max_S, n_split).n_split;
+    return decode_tc_mla_blocks(B, Hq, n_split);
 }
 
 MLAKV_API size_t attn_decode_mla_workspace_size(int B, int Hq, int r, int dr, int max_S, int n_split) {
     if (check_mla_shapes(B, Hq, r, dr, max_S > 0 ? max_S : 1, max_S, n_split) != ATTN_OK) return 0;
-    return partials_bytes(B, Hq, r, mla_plan(B, Hq, max_S, n_split).n_split);
+    return decode_tc_mla_workspace(B, Hq, n_split);
 }
 
 MLAKV_API int attn_decode_mla_absorbed(const void *q_lat, const void *q_rope, const void *c_cache,
@@ -270,28 +281,14 @@ MLAKV_API int attn_decode_mla_absorbed(const void *q_lat, const void *q_rope, co
     if (!aligned16(q_lat) || !aligned16(q_rope) || !aligned16(c_cache) || !aligned16(krope_cache) ||
         !aligned16(out_lat) || !aligned16(seq_lens))
         return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_mla_absorbed: every pointer must be 16-byte aligned");
-    const SplitPlan p = mla_plan(B, Hq, max_S, n_split);
-    const size_t need = partials_bytes(B, Hq, r, p.n_split);
-    if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
-        return fail(ATTN_ERR_WORKSPACE, "attn_decode_mla_absorbed: workspace of %zu bytes needed, got %zu",
-                    need, workspace ? ws_bytes : (size_t)0);
-    DecodeMlaArgs a{};
-    a.q_lat = q_lat; a.q_rope = q_rope; a.c = c_cache; a.kr = krope_cache; a.seq_lens = seq_lens;
-    a.out = out_lat; a.B = B; a.Hq = Hq; a.scale_log2 = scale * kLog2e; a.S_max = S_max;
-    a.n_split = p.n_split; a.split_len = p.split_len;
-    if (p.n_split > 1) {
-        const size_t rows = (size_t)B * Hq;
-        a.o_part = static_cast<float *>(workspace);
-        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                               align_up(rows * p.n_split * r * sizeof(float), 256));
-    }
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_decode_mla(a, s);
-    if (e != cudaSuccess) return cuda_fail(e, "attn_decode_mla_absorbed: decode kernel launch");
-    if (p.n_split > 1) {
-        e = launch_merge(a.o_part, a.lse_part, out_lat, B * Hq, p.n_split, r, s);
-        if (e != cudaSuccess) return cuda_fail(e, "attn_decode_mla_absorbed: merge kernel launch");
-    }
+    const size_t need = decode_tc_mla_workspace(B, Hq, n_split);
+    if (!workspace || ws_bytes < need || !aligned16(workspace))
+        return fail(ATTN_ERR_WORKSPACE, "attn_decode_mla_absorbed: workspace of %zu bytes (16-byte aligned) "
+                    "needed, got %zu", need, workspace ? ws_bytes : (size_t)0);
+    const cudaError_t e = launch_decode_tc_mla(q_lat, q_rope, c_cache, krope_cache, seq_lens, out_lat, B, Hq,
+                                               scale * kLog2e, S_max, n_split, workspace,
+                                               reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "attn_decode_mla_absorbed: kernel launch");
     return ok();
 }
 
@@ -342,7 +339,7 @@ MLAKV_API int attn_check_status(mlakv_stream_t stream) {
     unsigned flag = 0, f = 0;
     int rc = decode_gqa_read_and_clear_status(s, &f);
     flag |= f;
-    if (rc == 0) rc = decode_mla_read_and_clear_status(s, &f), flag |= f;
+    if (rc == 0) rc = decode_tc_read_and_clear_status(s, &f), flag |= f;
     if (rc == 0) rc = prefill_read_and_clear_status(s, &f), flag |= f;
     if (rc != 0) return cuda_fail((cudaError_t)rc, "attn_check_status: reading the device flags");
     if (flag != 0) return fail(ATTN_ERR_TIMEOUT, "a kernel gave up a bounded wait (flags 0x%x)", flag);

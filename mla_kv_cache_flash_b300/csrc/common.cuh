@@ -50,22 +50,6 @@ struct DecodeStreamArgs {
     int aligned;            // 1: block c streams exactly segment c (no segment is shared)
 };
 
-struct DecodeMlaArgs {
-    const void *q_lat;      // [B, Hq, r]
-    const void *q_rope;     // [B, Hq, dr]
-    const void *c;          // [B, S_max, r]
-    const void *kr;         // [B, S_max, dr]
-    const int *seq_lens;    // [B]
-    float *out;             // [B, Hq, r]
-    float *o_part;          // [B, Hq, n_split, r]
-    float *lse_part;        // [B, Hq, n_split]
-    int B, Hq;
-    float scale_log2;
-    int S_max;
-    int n_split;
-    int split_len;
-};
-
 struct PrefillArgs {
     const void *q;          // [T, Hq, D]
     const void *k;          // [T, Hkv, D]
@@ -92,14 +76,26 @@ MLAKV_HIDDEN cudaError_t launch_decode_gqa_stream(const DecodeStreamArgs &a, cud
 // K2: log-sum-exp merge of the split partials.
 MLAKV_HIDDEN cudaError_t launch_merge(const float *o_part, const float *lse_part, float *out,
                                       int rows, int n_split, int Dv, cudaStream_t s);
-// K3: MLA absorbed decode (r = 128, dr = 48).
-MLAKV_HIDDEN cudaError_t launch_decode_mla(const DecodeMlaArgs &a, cudaStream_t s);
-MLAKV_HIDDEN int decode_mla_tile_tokens();
+// K1 for Hq/Hkv a multiple of 16 at D = 128, and K3 (MLA absorbed decode, r = 128, dr = 48),
+// on the tcgen05 tensor cores with the same balanced split; the workspace holds two partial
+// slots per block and one zero-initialised arrival counter per segment.
+MLAKV_HIDDEN bool decode_tc_gqa_eligible(int B, int Hq, int Hkv, int D);
+MLAKV_HIDDEN int decode_tc_gqa_blocks(int B, int Hq, int Hkv, int n_split);
+MLAKV_HIDDEN size_t decode_tc_gqa_workspace(int B, int Hq, int Hkv, int n_split);
+MLAKV_HIDDEN cudaError_t launch_decode_tc_gqa(const void *q, const void *k, const void *v, const int *seq_lens,
+                                              float *out, int B, int Hq, int Hkv, float scale_log2, int S_max,
+                                              int n_split, void *ws, cudaStream_t st);
+MLAKV_HIDDEN bool decode_tc_mla_fits(int B, int Hq);
+MLAKV_HIDDEN int decode_tc_mla_blocks(int B, int Hq, int n_split);
+MLAKV_HIDDEN size_t decode_tc_mla_workspace(int B, int Hq, int n_split);
+MLAKV_HIDDEN cudaError_t launch_decode_tc_mla(const void *q_lat, const void *q_rope, const void *c_cache,
+                                              const void *kr_cache, const int *seq_lens, float *out, int B, int Hq,
+                                              float scale_log2, int S_max, int n_split, void *ws, cudaStream_t st);
 // K4: causal GQA prefill (D = 128).
 MLAKV_HIDDEN cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s);
 // Device error flags of the TUs that have bounded waits: read-and-clear (synchronous).
 MLAKV_HIDDEN int decode_gqa_read_and_clear_status(cudaStream_t s, unsigned *flag);
-MLAKV_HIDDEN int decode_mla_read_and_clear_status(cudaStream_t s, unsigned *flag);
+MLAKV_HIDDEN int decode_tc_read_and_clear_status(cudaStream_t s, unsigned *flag);
 MLAKV_HIDDEN int prefill_read_and_clear_status(cudaStream_t s, unsigned *flag);
 
 // Launch `kern` on `s` with programmatic stream serialisation allowed: the kernel may start

@@ -98,43 +98,6 @@ __device__ __forceinline__ uint32_t sw64(int row, int cidx) {
     return row * 64 + ((((cidx & 3) ^ ((row >> 1) & 3))) << 4);
 }
 
-// One piece of a block's range: tiles [i0, i0 + n_t) of segment (b, gi, hb).
-struct Piece {
-    int b, gi, hb, S, i0, n_t;
-    bool whole;                 // the piece is the whole segment
-};
-
-// Walks the pieces of a block's tile range [t, t_end) using the tile prefix over sequences.
-struct PieceWalker {
-    const int *prefix;          // prefix[b] = Σ_{b' < b} tiles(S_b'), b = 0 .. B
-    const int *seq_lens;
-    int B, seg_per_seq, n_hblk, tile;
-    long long t, t_end;
-    __device__ bool next(Piece &p) {
-        if (t >= t_end) return false;
-        // the last b with seg_per_seq · prefix[b] <= t (sequences with no tiles are skipped)
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if ((long long)seg_per_seq * prefix[mid] <= t) lo = mid; else hi = mid - 1;
-        }
-        p.b = lo;
-        p.S = seq_lens[lo];
-        const int nb = stream_tiles(p.S, tile);
-        const long long fb = (long long)seg_per_seq * prefix[lo];
-        const int q = (int)((t - fb) / nb);
-        p.gi = q / n_hblk;
-        p.hb = q % n_hblk;
-        p.i0 = (int)((t - fb) % nb);
-        const long long seg_end = fb + (long long)(q + 1) * nb;
-        const long long end = seg_end < t_end ? seg_end : t_end;
-        p.n_t = (int)(end - t);
-        p.whole = p.i0 == 0 && end == seg_end;
-        t = end;
-        return true;
-    }
-};
-
 template <int D, int MT, int HG, int NS, int NC>
 __global__ void __launch_bounds__((NC + 1) * 32, 1)
 decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,

@@ -1,0 +1,881 @@
+// K1 for wide query groups and K3 (MLA) on the 5th-generation tensor cores: decode over a
+// bf16 cache when 16 or more query heads share each cached row.
+//
+// The method: out[b,h] = softmax(scale · q[b,h]·K[b,:S_b,j]ᵀ) · V[b,:S_b,j], j = h / G
+// ("模型架构｜MQA & GQA 调研", section "代码", Attention.forward with one new token). MLA's
+// absorbed form is the same with K = [c ‖ kr] (176 columns) and V = c (qqstock article on
+// DeepSeek MLA, sections 2, 3 and 6): every head reads the one latent row.
+// With G heads per row the work is about 2·G flops per cached byte (16 at G = 16 over the
+// 176-wide MLA key and 128-wide value, 32 for MQA with 32 heads), which is past what
+// register-fragment tensor cores sustain at HBM speed on one SM. So here both products run as
+// tcgen05 MMAs with the accumulators in tensor memory, and the cached tokens - not the
+// heads - form the 128-row M side:
+//   Sᵀ = K·Qᵀ        M = 128 tokens of a tile, N = the block's N query heads (16 or 32),
+//                    K = key width; A (the cache tile) and B (the query rows) K-major in
+//                    shared memory, 128-byte swizzle (32-byte for MLA's 48-wide rope part).
+//   softmax          one thread per token row reads its N scores from TMEM: base-2 scores,
+//                    a per-head reference maximum m, weights p = 2^(s − m) as a bf16 head
+//                    plus a bf16 residual (p − head), per-thread partial sums l. The reference is raised (and O and l scaled
+//                    down) only when a score exceeds it by more than 2^8, which a block-wide
+//                    vote detects; the result does not depend on the reference, it only
+//                    bounds the range of p.
+//   Oᵀ += Vᵀ·Pᵀ     M = 128 value columns, N heads, K = 128 tokens: Vᵀ is the cache tile read
+//                    MN-major from the same shared memory that TMA filled, Pᵀ is the
+//                    softmax threads' bf16 rows (one token's N weights each) in shared memory,
+//                    multiplied once for the heads and once for the residuals.
+// Precision: a bf16 weight alone is off by up to 2^-9 of itself, which a sequence of a few
+// tokens does not average away (measured: 3.1e-3 on 5-token rows); with the residual the
+// weights carry about 16 significant bits, and the sums l use the same two-part values.
+//
+// The work is split like the register-MMA decode kernel (streamk.cuh): segments = (sequence,
+// KV head, block of N query heads), cut into 128-token tiles laid end to end; each persistent
+// block (one per SM) takes an equal run of tiles. A segment a block covers whole is written
+// to `out`; a shared one leaves a normalised partial and ln Σ e^s in the block's slot, and the
+// last block to finish the segment (acquire-release arrival counter) combines them.
+//
+// Warp roles (192 threads, one block per SM):
+//   warp 0     TMA producer: per piece the query rows into a slot (two slots where shared
+//              memory allows), per tile the cache rows into an NS-stage ring (L2 evict-first).
+//   warp 1     allocates 128 TMEM columns (S double buffer at 0 and 32; O at 64: N columns
+//              for the weights' heads, N for their residuals, summed at the end); lane 0
+//              issues the MMAs: S(g) as soon as tile g lands, P·V(g−1) after it.
+//   warps 2-5  softmax, one thread per token row / TMEM lane; at a piece end the same
+//              threads read Oᵀ (lane = value column) and write the output or the partial.
+// Tokens past a sequence's end get weight 0 and their value rows are zeroed in shared memory
+// before P·V, so stale cache contents never reach the output.
+//
+// Every mbarrier wait is bounded (MLAKV_WAIT_TIMEOUT_CYCLES); a wait that runs out sets a bit
+// in g_decode_tc_status and the thread skips later waits, while still meeting its partners at
+// every named barrier, so the block always reaches its end and frees its tensor memory.
+#include "ptx.cuh"
+#include "streamk.cuh"
+#include "tcgen05.cuh"
+#include "tensor_map.cuh"
+
+#include <math.h>
+
+namespace mlakv {
+
+__device__ unsigned g_decode_tc_status;
+
+namespace {
+
+constexpr int kGqa = 0, kMla = 1;
+constexpr int TILE = 128;                 // tokens per tile (TMEM lanes)
+constexpr int DV = 128;                   // value width: D of GQA, r of MLA
+constexpr int BOX = TILE * 128;           // one 128-byte-swizzled box: 128 rows × 64 columns
+constexpr int ROPE_BOX = TILE * 32;       // one 32-byte-swizzled box: 128 rows × 16 columns
+constexpr int kThreads = 192;
+constexpr int kSoftmax = 128;             // threads of warps 2-5
+constexpr int kPlist = 256;               // partial slots a merge can list in shared memory
+constexpr uint32_t kTmemCols = 128;
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int KIND, int N>
+struct Cfg {
+    static_assert(N == 16 || N == 32, "16 or 32 query heads per block");
+    // ring stage: the key tile (2 boxes of K or c), then V (2 boxes) or kr (3 boxes)
+    static constexpr int STAGE = 2 * BOX + (KIND == kGqa ? 2 * BOX : 3 * ROPE_BOX);
+    static constexpr int NS = KIND == kGqa ? 3 : 4;
+    static constexpr int V_OFF = KIND == kGqa ? 2 * BOX : 0;     // value tile inside a stage
+    static constexpr int Q_BOX = N * 128;                       // N query rows × 64 columns
+    static constexpr int QR_BOX = N * 32;                       // N rows × 16 rope columns
+    static constexpr int Q_BYTES = 2 * Q_BOX + (KIND == kMla ? 3 * QR_BOX : 0);
+    static constexpr int Q_SLOT = (Q_BYTES + 1023) / 1024 * 1024;
+    // query slots: two (the next piece's rows load early) where shared memory allows
+    static constexpr int QS = KIND == kGqa && N == 32 ? 1 : 2;
+    // one token's weights as a row of 2N bf16: the N heads, then the N residuals; the P·V
+    // product takes both as one N = 2N operand (one MMA chain instead of two)
+    static constexpr int P_ROW = 2 * N * 2;
+    static constexpr int P_BYTES = TILE * P_ROW;
+    static constexpr uint32_t P_LAYOUT = N == 32 ? kSw128 : kSw64;
+    static constexpr int Q_OFF = NS * STAGE;
+    static constexpr int P_OFF = Q_OFF + QS * Q_SLOT;           // weights, then their residuals
+    static constexpr int BAR_OFF = P_OFF + P_BYTES;
+    static constexpr int N_BARS = 2 * NS + 10;
+    static constexpr int SCR_OFF = BAR_OFF + 256;
+    static constexpr int MAXRED_OFF = SCR_OFF;                  // [4][N] per-warp tile maxima
+    static constexpr int LRED_OFF = MAXRED_OFF + 4 * N * 4;     // [4][N] per-warp sums
+    static constexpr int STAT_OFF = LRED_OFF + 4 * N * 4;       // [N] 1/L, [N] lse
+    static constexpr int MISC_OFF = STAT_OFF + 2 * N * 4;       // TMEM base, merge flag
+    static constexpr int SHREC_OFF = MISC_OFF + 16;             // [2] shared-segment records
+    static constexpr int PLIST_OFF = SHREC_OFF + 2 * 48;
+    static constexpr int PREFIX_OFF = PLIST_OFF + kPlist * 4;
+    static_assert(STAGE % 1024 == 0 && Q_SLOT % 1024 == 0 && P_BYTES % 1024 == 0, "swizzle alignment");
+    static_assert(N_BARS * 8 <= 256, "barrier area");
+    static size_t smem_bytes(int B) { return PREFIX_OFF + (size_t)(B + 1) * 4 + 1024; }
+};
+
+// Barrier indices.
+template <int NS>
+struct Bars {
+    static constexpr int FULL = 0, EMPTY = NS, QFULL = 2 * NS, QEMPTY = 2 * NS + 2, SFULL = 2 * NS + 4,
+                         SFREE = 2 * NS + 6, PREADY = 2 * NS + 8, PVDONE = 2 * NS + 9;
+};
+
+struct TcArgs {
+    const int *seq_lens;    // [B]
+    float *out;             // [B, Hq, 128]
+    float *o_part;          // [2·n_blocks, N, 128]
+    float *lse_part;        // [2·n_blocks, N]
+    int *counters;          // [segments], zero between calls
+    int B, Hq, G;           // G: query heads per KV head (MLA: all Hq)
+    int seg_per_seq;        // segments per sequence: KV heads × head blocks
+    int n_hblk;             // head blocks of N per KV head
+    float scale_log2;
+    int n_blocks;
+    int aligned;
+};
+
+// Reduce N per-thread values over the 32 lanes of a warp, one head per lane group: after the
+// call, lane L holds the reduction for head L >> (5 − log2 N). Halving exchange: at each step
+// a lane keeps half of its heads and receives its partner's values for them.
+template <int N, bool MAX>
+__device__ __forceinline__ float xpose_reduce(float (&v)[N], int lane) {
+#pragma unroll
+    for (int n = N, o = 16; n > 1; n >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < n / 2; ++j) {
+            const float send = up ? v[j] : v[j + n / 2];
+            const float keep = up ? v[j + n / 2] : v[j];
+            const float r = __shfl_xor_sync(0xffffffffu, send, o);
+            v[j] = MAX ? fmaxf(keep, r) : keep + r;
+        }
+    }
+    float x = v[0];
+#pragma unroll
+    for (int o = N == 32 ? 0 : 1; o > 0; o >>= 1) {
+        const float r = __shfl_xor_sync(0xffffffffu, x, o);
+        x = MAX ? fmaxf(x, r) : x + r;
+    }
+    return x;
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, uint32_t (&r)[N]) {
+    if constexpr (N == 32) tmem_ld32_sync(taddr, r); else tmem_ld16_sync(taddr, r);
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint32_t (&r)[N]) {
+    if constexpr (N == 32) tmem_st32(taddr, r); else tmem_st16(taddr, r);
+}
+
+template <int KIND, int N>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (MLA)
+                 const __grid_constant__ CUtensorMap vmap,    // V (GQA) or kr (MLA)
+                 const __grid_constant__ CUtensorMap qmap,    // q (GQA) or q_lat (MLA)
+                 const __grid_constant__ CUtensorMap qrmap,   // q_rope (MLA)
+                 const TcArgs a) {
+    using C = Cfg<KIND, N>;
+    using BI = Bars<C::NS>;
+    constexpr int NS = C::NS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    auto bar = [&](int i) { return sb + C::BAR_OFF + 8 * i; };
+    float *maxred = reinterpret_cast<float *>(smem + C::MAXRED_OFF);
+    float *lred = reinterpret_cast<float *>(smem + C::LRED_OFF);
+    float *stat = reinterpret_cast<float *>(smem + C::STAT_OFF);
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+    int *plist = reinterpret_cast<int *>(smem + C::PLIST_OFF);
+    int *prefix = reinterpret_cast<int *>(smem + C::PREFIX_OFF);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar(BI::FULL + s), 1);
+            mbar_init(bar(BI::EMPTY + s), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(BI::QFULL + i), 1);
+            mbar_init(bar(BI::QEMPTY + i), 1);
+            mbar_init(bar(BI::SFULL + i), 1);
+            mbar_init(bar(BI::SFREE + i), 4);
+        }
+        mbar_init(bar(BI::PREADY), 4);
+        mbar_init(bar(BI::PVDONE), 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(sb + C::MISC_OFF, kTmemCols);
+        tmem_relinquish();
+    }
+    // everything above overlaps the previous kernel in the stream; the inputs are read below
+    griddep_wait();
+    griddep_launch_dependents();
+    if (warp == 0) {
+        // tile prefix over the sequences (warp scan, 32 sequences at a time)
+        int carry = 0;
+        for (int base = 0; base < a.B; base += 32) {
+            const int b = base + lane;
+            const int v = b < a.B ? stream_tiles(a.seq_lens[b], TILE) : 0;
+            int x = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (b < a.B) prefix[b] = carry + x - v;
+            carry += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (lane == 0) prefix[a.B] = carry;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    const long long T = (long long)a.seg_per_seq * prefix[a.B];
+    const int c = blockIdx.x;
+    PieceWalker walk{prefix, a.seq_lens, a.B, a.seg_per_seq, a.n_hblk, TILE, 0, 0};
+    if (a.aligned) {
+        // block c streams segment c whole
+        const int b = c / a.seg_per_seq, q = c % a.seg_per_seq;
+        const int nb = stream_tiles(a.seq_lens[b], TILE);
+        walk.t = (long long)a.seg_per_seq * prefix[b] + (long long)q * nb;
+        walk.t_end = walk.t + nb;
+    } else if (T > 0) {
+        walk.t = stream_start(c, T, a.n_blocks);
+        walk.t_end = stream_start(c + 1, T, a.n_blocks);
+    }
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && walk.t < walk.t_end) {
+            prefetch_tensormap(&kmap);
+            prefetch_tensormap(&vmap);
+            prefetch_tensormap(&qmap);
+            if (KIND == kMla) prefetch_tensormap(&qrmap);
+            const uint64_t pol = l2_evict_first_policy();
+            int g = 0, k = 0;
+            bool ok = true;
+            Piece p;
+            // A piece's query rows go to slot k % QS once the piece that used the slot before
+            // has issued its last score MMA. With one slot, the piece's first tile is requested
+            // before that wait, so the cache stream does not pause at the piece boundary.
+            auto load_q = [&](const Piece &pc, int kq) {
+                const int qs = kq % C::QS;
+                if (kq >= C::QS && !mbar_wait_bounded(bar(BI::QEMPTY + qs), ((kq / C::QS) - 1) & 1,
+                                                      &g_decode_tc_status, kStatusEmptyWait))
+                    return false;
+                const int h0 = pc.gi * a.G + pc.hb * N;
+                const uint32_t qd = sb + C::Q_OFF + qs * C::Q_SLOT;
+                const uint32_t qb = bar(BI::QFULL + qs);
+                mbar_arrive_expect_tx(qb, C::Q_BYTES);
+                tma_load_3d(qd, &qmap, 0, h0, pc.b, qb, pol);
+                tma_load_3d(qd + C::Q_BOX, &qmap, 64, h0, pc.b, qb, pol);
+                if constexpr (KIND == kMla) {
+#pragma unroll
+                    for (int i = 0; i < 3; ++i) tma_load_3d(qd + 2 * C::Q_BOX + i * C::QR_BOX, &qrmap, 16 * i, h0, pc.b, qb, pol);
+                }
+                return true;
+            };
+            while (ok && walk.next(p)) {
+                const bool q_late = C::QS == 1 && k > 0;
+                if (!q_late && !load_q(p, k)) {
+                    ok = false;
+                    break;
+                }
+                for (int i = 0; i < p.n_t; ++i, ++g) {
+                    const int s = g % NS;
+                    if (!mbar_wait_bounded(bar(BI::EMPTY + s), ((g / NS) & 1) ^ 1, &g_decode_tc_status,
+                                           kStatusEmptyWait)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = sb + s * C::STAGE;
+                    const uint32_t fb = bar(BI::FULL + s);
+                    mbar_arrive_expect_tx(fb, C::STAGE);
+                    const int t = (p.i0 + i) * TILE;
+                    if constexpr (KIND == kGqa) {
+                        tma_load_4d(dst, &kmap, 0, p.gi, t, p.b, fb, pol);
+                        tma_load_4d(dst + BOX, &kmap, 64, p.gi, t, p.b, fb, pol);
+                        tma_load_4d(dst + 2 * BOX, &vmap, 0, p.gi, t, p.b, fb, pol);
+                        tma_load_4d(dst + 3 * BOX, &vmap, 64, p.gi, t, p.b, fb, pol);
+                    } else {
+                        tma_load_3d(dst, &kmap, 0, t, p.b, fb, pol);
+                        tma_load_3d(dst + BOX, &kmap, 64, t, p.b, fb, pol);
+#pragma unroll
+                        for (int r = 0; r < 3; ++r) tma_load_3d(dst + 2 * BOX + r * ROPE_BOX, &vmap, 16 * r, t, p.b, fb, pol);
+                    }
+                    if (q_late && i == 0 && !load_q(p, k)) {
+                        ok = false;
+                        ++g;
+                        break;
+                    }
+                }
+                ++k;
+            }
+            // no copy may still be in flight when the block exits
+            for (int i = g > NS ? g - NS : 0; i < g; ++i)
+                mbar_wait_bounded(bar(BI::FULL + i % NS), (i / NS) & 1, &g_decode_tc_status, kStatusDrainWait);
+            for (int i = k > C::QS ? k - C::QS : 0; i < k; ++i)
+                mbar_wait_bounded(bar(BI::QFULL + i % C::QS), (i / C::QS) & 1, &g_decode_tc_status, kStatusDrainWait);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        // Lane 0 issues every MMA. Two products are due at any time: S(g), into S buffer
+        // g & 1, once tile g has landed (and the softmax has read S(g − 2)); and P·V(g − 1),
+        // once the softmax has written that tile's weights. Lane 0 polls both and issues
+        // whichever is ready first: P·V(g − 1) releases tile g − 1's ring stage, so it must
+        // not wait for tile g to land, and S(g) must not wait for the softmax of tile g − 1.
+        // A piece's last P·V is issued before the next piece's first S, so the piece's
+        // epilogue never waits for the next piece's data.
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(TILE, N, false, false);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(DV, 2 * N, true, true);
+            const uint32_t t_o = tmem + 64;
+            bool ok = true;
+            auto issue_s = [&](int gg, int s, uint32_t qd) {
+                const uint32_t kt = sb + s * C::STAGE;
+                const uint32_t d = tmem + 32 * (gg & 1);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * BOX + (kk & 3) * 32;
+                    const uint32_t qoff = (kk >> 2) * C::Q_BOX + (kk & 3) * 32;
+                    umma_ss(d, sdesc(kt + off, 16, 1024, kSw128), sdesc(qd + qoff, 16, 1024, kSw128), idesc_s,
+                            kk > 0 ? 1u : 0u);
+                }
+                if constexpr (KIND == kMla) {
+#pragma unroll
+                    for (int kk = 0; kk < 3; ++kk)
+                        umma_ss(d, sdesc(kt + 2 * BOX + kk * ROPE_BOX, 16, 256, kSw32),
+                                sdesc(qd + 2 * C::Q_BOX + kk * C::QR_BOX, 16, 256, kSw32), idesc_s, 1u);
+                }
+                umma_commit(bar(BI::SFULL + (gg & 1)));
+            };
+            auto issue_pv = [&](int s, bool first) {
+                const uint32_t v = sb + s * C::STAGE + C::V_OFF;
+                const uint32_t pb = sb + C::P_OFF;
+                // 16 tokens per MMA; columns [0, N) of O take the weights' heads, [N, 2N) their residuals
+#pragma unroll
+                for (int kk = 0; kk < TILE / 16; ++kk)
+                    umma_ss(t_o, sdesc(v + kk * 2048, BOX, 1024, kSw128),
+                            sdesc(pb + kk * 16 * C::P_ROW, C::P_BYTES, 8 * C::P_ROW, C::P_LAYOUT), idesc_o,
+                            (!first || kk > 0) ? 1u : 0u);
+                umma_commit(bar(BI::PVDONE));
+                umma_commit(bar(BI::EMPTY + s));
+            };
+            auto ready_pv = [&](int gg) { return mbar_test_wait(bar(BI::PREADY), gg & 1); };
+            int g = 0, k = 0;
+            bool pend = false, pend_first = false;   // P·V of tile pend_g not yet issued
+            int pend_g = 0, pend_s = 0;
+            Piece p;
+            while (ok && walk.next(p)) {
+                const int qs = k % C::QS;
+                const uint32_t qd = sb + C::Q_OFF + qs * C::Q_SLOT;
+                for (int i = 0; ok && i < p.n_t; ++i, ++g) {
+                    const int s = g % NS;
+                    bool s_done = false;
+                    const long long t0 = clock64();
+                    while (!s_done || pend) {
+                        if (pend && ready_pv(pend_g)) {
+                            tc_fence_after();
+                            issue_pv(pend_s, pend_first);
+                            pend = false;
+                            continue;
+                        }
+                        if (!s_done && mbar_test_wait(bar(BI::FULL + s), (g / NS) & 1) &&
+                            (g < 2 || mbar_test_wait(bar(BI::SFREE + (g & 1)), ((g >> 1) - 1) & 1)) &&
+                            (i > 0 || mbar_test_wait(bar(BI::QFULL + qs), (k / C::QS) & 1))) {
+                            tc_fence_after();
+                            issue_s(g, s, qd);
+                            if (i == p.n_t - 1) umma_commit(bar(BI::QEMPTY + qs));
+                            s_done = true;
+                            continue;
+                        }
+                        if (clock64() - t0 > MLAKV_WAIT_TIMEOUT_CYCLES) {
+                            atomicOr(&g_decode_tc_status, kStatusMmaWait);
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!ok) break;
+                    pend = true;
+                    pend_g = g;
+                    pend_s = s;
+                    pend_first = i == 0;
+                    if (i == p.n_t - 1) {
+                        if (!mbar_wait_bounded(bar(BI::PREADY), g & 1, &g_decode_tc_status, kStatusMmaWait)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_pv(s, i == 0);
+                        pend = false;
+                    }
+                }
+                ++k;
+            }
+            // the last products finish before the block frees tensor memory
+            if (ok && g > 0) mbar_wait_bounded(bar(BI::PVDONE), (g - 1) & 1, &g_decode_tc_status, kStatusMmaWait);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int row = 32 * (warp & 3) + lane;           // token row, TMEM lane, value column
+        const int sw = warp - 2;
+        const int tid = threadIdx.x - 64;
+        const uint32_t lane_addr = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t t_o = tmem + lane_addr + 64;
+        constexpr int SHIFT = N == 32 ? 0 : 1;            // lane >> SHIFT: head held after a reduce
+        bool ok = true;
+        auto wait = [&](uint32_t b, uint32_t parity, unsigned code) {
+            if (ok && !mbar_wait_bounded(b, parity, &g_decode_tc_status, code)) ok = false;
+        };
+        // O (both halves) for this thread's value column, one half of 32 or 16 columns at a time
+        auto o_half = [&](int half, uint32_t (&o)[N]) { tmem_ld_row<N>(t_o + half * N, o); };
+        if (c == 0) {
+            // sequences with an empty cache own no tile: their output is zero
+            for (int b = 0; b < a.B; ++b)
+                if (prefix[b + 1] == prefix[b])
+                    for (int i = tid; i < a.Hq * DV / 4; i += kSoftmax)
+                        reinterpret_cast<float4 *>(a.out + (size_t)b * a.Hq * DV)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // Shared segments this block left a partial of (its first and last piece at most): their
+        // records in shared memory, the arrival count thread 0 saw in a register, read only at
+        // the end, so the counter's round trip never stalls the stream; the last arrival merges.
+        struct Shared {
+            long long fs;
+            int b, h0, seg, n_pieces, c0, sparse, first_odd;
+        };
+        Shared *shrec = reinterpret_cast<Shared *>(smem + C::SHREC_OFF);
+        int seen0 = 0, seen1 = 0, n_shared = 0;
+        int g = 0, k = 0;
+        Piece p;
+        while (walk.next(p)) {
+            float m[N], l[N];
+#pragma unroll
+            for (int h = 0; h < N; ++h) {
+                m[h] = -INFINITY;
+                l[h] = 0.f;
+            }
+            for (int i = 0; i < p.n_t; ++i, ++g) {
+                const int s = g % NS;
+                wait(bar(BI::SFULL + (g & 1)), (g >> 1) & 1, kStatusMmaWait);
+                tc_fence_after();
+                uint32_t sr[N];
+                tmem_ld_row<N>(tmem + lane_addr + 32 * (g & 1), sr);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BI::SFREE + (g & 1)));
+
+                const bool valid = (p.i0 + i) * TILE + row < p.S;
+                float x[N];
+#pragma unroll
+                for (int h = 0; h < N; ++h) x[h] = valid ? __uint_as_float(sr[h]) * a.scale_log2 : -INFINITY;
+                bool need = i == 0;
+                if (!need) {
+                    bool ex = false;
+#pragma unroll
+                    for (int h = 0; h < N; ++h) ex |= x[h] - m[h] > kRescaleLog2;
+                    need = bar_any(1, kSoftmax, ex);
+                }
+                if (need) {
+                    // new reference: the running maximum per head over all rows so far
+                    float v[N];
+#pragma unroll
+                    for (int h = 0; h < N; ++h) v[h] = x[h];
+                    const float wm = xpose_reduce<N, true>(v, lane);
+                    if ((lane & ((1 << SHIFT) - 1)) == 0) maxred[sw * N + (lane >> SHIFT)] = wm;
+                    bar_sync_named(1, kSoftmax);
+#pragma unroll
+                    for (int h = 0; h < N; ++h) {
+                        const float tm = fmaxf(fmaxf(maxred[h], maxred[N + h]), fmaxf(maxred[2 * N + h], maxred[3 * N + h]));
+                        const float mn = fmaxf(m[h], tm);
+                        v[h] = fast_exp2(m[h] - mn);      // the factor old → new reference
+                        m[h] = mn;
+                        l[h] *= v[h];
+                    }
+                    if (i > 0) {
+                        // O holds the tiles before this one: scale both halves to the new reference
+                        wait(bar(BI::PVDONE), (g - 1) & 1, kStatusMmaWait);
+                        tc_fence_after();
+#pragma unroll
+                        for (int ch = 0; ch < 2 * N / 16; ++ch) {      // 16 columns at a time
+                            uint32_t o[16];
+                            tmem_ld16_sync(t_o + ch * 16, o);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                o[j] = __float_as_uint(__uint_as_float(o[j]) * v[(ch * 16 + j) % N]);
+                            tmem_st16(t_o + ch * 16, o);
+                        }
+                        tmem_st_wait();
+                    }
+                }
+                // weights as bf16 head + bf16 residual; the sums take the two-part values
+                uint32_t pk[N / 2], pr[N / 2];
+#pragma unroll
+                for (int h = 0; h < N; h += 2) {
+                    const float p0 = fast_exp2(x[h] - m[h]), p1 = fast_exp2(x[h + 1] - m[h + 1]);
+                    const uint32_t w = pack_bf16x2(p0, p1);
+                    const uint32_t r = pack_bf16x2(p0 - bf16_lo(w), p1 - bf16_hi(w));
+                    pk[h / 2] = w;
+                    pr[h / 2] = r;
+                    l[h] += bf16_lo(w) + bf16_lo(r);
+                    l[h + 1] += bf16_hi(w) + bf16_hi(r);
+                }
+                // the weight buffer is free once P·V(g − 1) has completed
+                if (g >= 1) wait(bar(BI::PVDONE), (g - 1) & 1, kStatusMmaWait);
+                // row = [heads | residuals], 16-byte chunks swizzled (128-byte rows: chunk c at
+                // c ^ (row & 7); 64-byte rows: c ^ ((row >> 1) & 3))
+                uint8_t *prow = smem + C::P_OFF + row * C::P_ROW;
+                const int swz = N == 32 ? row & 7 : (row >> 1) & 3;
+#pragma unroll
+                for (int ch = 0; ch < N / 8; ++ch) {
+                    *reinterpret_cast<uint4 *>(prow + ((ch ^ swz) << 4)) =
+                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                    *reinterpret_cast<uint4 *>(prow + (((ch + N / 8) ^ swz) << 4)) =
+                        make_uint4(pr[4 * ch], pr[4 * ch + 1], pr[4 * ch + 2], pr[4 * ch + 3]);
+                }
+                if (!valid) {
+                    // a row past the sequence end: zero its value row (weight 0 · stale data)
+                    uint8_t *vr = smem + s * C::STAGE + C::V_OFF + row * 128;
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        *reinterpret_cast<uint4 *>(vr + ch * 16) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(vr + BOX + ch * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BI::PREADY));
+            }
+
+            // ---------------------------------------------------------- end of the piece
+            {
+                float v[N];
+#pragma unroll
+                for (int h = 0; h < N; ++h) v[h] = l[h];
+                const float ws = xpose_reduce<N, false>(v, lane);
+                if ((lane & ((1 << SHIFT) - 1)) == 0) lred[sw * N + (lane >> SHIFT)] = ws;
+            }
+            bar_sync_named(1, kSoftmax);
+            if (tid < N) {
+                const float L = lred[tid] + lred[N + tid] + lred[2 * N + tid] + lred[3 * N + tid];
+                float mh = m[0];
+#pragma unroll
+                for (int h = 1; h < N; ++h) mh = tid == h ? m[h] : mh;
+                stat[tid] = ok && L > 0.f ? 1.f / L : 0.f;
+                stat[N + tid] = ok && L > 0.f ? (mh + log2f(L)) * kLn2 : -INFINITY;
+            }
+            wait(bar(BI::PVDONE), (g - 1) & 1, kStatusMmaWait);
+            tc_fence_after();
+            uint32_t o[N], o2[N];
+            o_half(0, o);
+            o_half(1, o2);
+            tc_fence_before();
+            bar_sync_named(1, kSoftmax);
+            const int h0 = p.gi * a.G + p.hb * N;
+            const int slot = 2 * c + (k == 0 ? 0 : 1);
+            float *dst = p.whole ? a.out + ((size_t)p.b * a.Hq + h0) * DV : a.o_part + (size_t)slot * N * DV;
+#pragma unroll
+            for (int h = 0; h < N; ++h) dst[h * DV + row] = (__uint_as_float(o[h]) + __uint_as_float(o2[h])) * stat[h];
+            if (!p.whole) {
+                if (tid < N) a.lse_part[(size_t)slot * N + tid] = stat[N + tid];
+                // the partial slots of the blocks holding tiles of this segment: blocks c0 .. c1,
+                // or, with fewer tiles than blocks (each block then owns at most one tile), the
+                // owners of the segment's nb tiles
+                const int seg = p.b * a.seg_per_seq + p.gi * a.n_hblk + p.hb;
+                if (tid == 0) {
+                    Shared r;
+                    const int nb = stream_tiles(p.S, TILE);
+                    r.b = p.b;
+                    r.h0 = h0;
+                    r.seg = seg;
+                    r.fs = (long long)a.seg_per_seq * prefix[p.b] + (long long)(p.gi * a.n_hblk + p.hb) * nb;
+                    r.sparse = T < a.n_blocks;
+                    r.c0 = stream_block_of(r.fs, T, a.n_blocks);
+                    r.n_pieces = r.sparse ? nb : stream_block_of(r.fs + nb - 1, T, a.n_blocks) - r.c0 + 1;
+                    r.first_odd = stream_start(r.c0, T, a.n_blocks) < r.fs;
+                    shrec[n_shared] = r;
+                }
+                // publish: the partial's stores, ordered before thread 0's release by the
+                // barrier, are visible to whichever block later acquires the counter
+                bar_sync_named(1, kSoftmax);
+                if (tid == 0) {
+                    const int v = atomic_add_acq_rel_gpu(a.counters + seg, 1);
+                    if (n_shared == 0) seen0 = v; else seen1 = v;
+                }
+                ++n_shared;
+            }
+            ++k;
+        }
+
+        // ---------------------------------------------------------- merge the shared segments
+        // this block arrived last at
+        for (int j = 0; j < n_shared; ++j) {
+            bar_sync_named(1, kSoftmax);          // misc[1] and plist are free; records written
+            const Shared q = shrec[j];
+            if (tid == 0) {
+                const bool last = (j == 0 ? seen0 : seen1) == q.n_pieces - 1;
+                misc[1] = last;
+                if (last) a.counters[q.seg] = 0;
+            }
+            bar_sync_named(1, kSoftmax);
+            if (!misc[1]) continue;
+            // thread 0's acquire, then the barrier, order the loads below after every
+            // other block's release of its partial
+            const bool listed = q.n_pieces <= kPlist;
+            auto slot_of = [&](int i) {
+                if (q.sparse) return 2 * stream_block_of(q.fs + i, T, a.n_blocks);
+                if (i == 0) return 2 * q.c0 + q.first_odd;
+                return 2 * (q.c0 + i);
+            };
+            if (listed)
+                for (int i = tid; i < q.n_pieces; i += kSoftmax) plist[i] = slot_of(i);
+            bar_sync_named(1, kSoftmax);
+            auto slot_at = [&](int i) { return listed ? plist[i] : slot_of(i); };
+            // Warp w combines rows w, w + 4, ..., lane = float4 column block. The partials come
+            // PC at a time with their log-sum-exps, all rows' loads in flight together (one L2
+            // round trip per PC partials), folded in with a running maximum.
+            constexpr int RPW = N / 4, PC = 64 / N;
+            float M[RPW], W[RPW];
+            float4 acc[RPW];
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+                M[r] = -INFINITY;
+                W[r] = 0.f;
+                acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            for (int i0 = 0; i0 < q.n_pieces; i0 += PC) {
+                float lv[PC][RPW];
+                float4 xv[PC][RPW];
+#pragma unroll
+                for (int u = 0; u < PC; ++u) {
+                    const bool in = i0 + u < q.n_pieces;
+                    const size_t base = in ? (size_t)slot_at(i0 + u) * N : 0;
+#pragma unroll
+                    for (int r = 0; r < RPW; ++r) {
+                        const int rr = sw + 4 * r;
+                        lv[u][r] = in ? __ldcg(a.lse_part + base + rr) : -INFINITY;
+                        if (in) xv[u][r] = __ldcg(reinterpret_cast<const float4 *>(a.o_part + (base + rr) * DV) + lane);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < PC; ++u)
+#pragma unroll
+                    for (int r = 0; r < RPW; ++r) {
+                        if (lv[u][r] == -INFINITY) continue;
+                        const float mn = fmaxf(M[r], lv[u][r]);
+                        const float f = fast_exp2((M[r] - mn) * kLog2e);     // 0 while M = -inf
+                        const float w = fast_exp2((lv[u][r] - mn) * kLog2e);
+                        M[r] = mn;
+                        W[r] = W[r] * f + w;
+                        acc[r].x = fmaf(w, xv[u][r].x, acc[r].x * f);
+                        acc[r].y = fmaf(w, xv[u][r].y, acc[r].y * f);
+                        acc[r].z = fmaf(w, xv[u][r].z, acc[r].z * f);
+                        acc[r].w = fmaf(w, xv[u][r].w, acc[r].w * f);
+                    }
+            }
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+                const float inv = W[r] > 0.f ? 1.f / W[r] : 0.f;
+                reinterpret_cast<float4 *>(a.out + ((size_t)q.b * a.Hq + q.h0 + sw + 4 * r) * DV)[lane] =
+                    make_float4(acc[r].x * inv, acc[r].y * inv, acc[r].z * inv, acc[r].w * inv);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        n <= 0) {
+        cudaGetLastError();
+        return 148;
+    }
+    return n;
+}
+
+int heads_per_block(int G) { return G % 32 == 0 ? 32 : 16; }
+
+template <int KIND>
+size_t smem_for(int N, int B) {
+    return N == 32 ? Cfg<KIND, 32>::smem_bytes(B) : Cfg<KIND, 16>::smem_bytes(B);
+}
+
+// Segments (sequence, KV head, head block) and the grid over them. Aligned mode: when the
+// segments number between half the SMs and all of them, each gets a block of its own.
+struct Plan {
+    long long segs;
+    int n_blocks;
+    bool aligned;
+};
+
+Plan plan(long long segs, int n_split) {
+    Plan p{segs, 1, false};
+    const int sms = sm_count();
+    if (n_split == 0 && segs <= sms && 2 * segs >= sms) {
+        p.aligned = true;
+        p.n_blocks = (int)segs;
+        return p;
+    }
+    long long n = sms < kPlist ? sms : kPlist;
+    if (n_split > 0 && (long long)n_split * segs < n) n = (long long)n_split * segs;
+    p.n_blocks = (int)(n < 1 ? 1 : n);
+    return p;
+}
+
+size_t ws_bytes(const Plan &p, int N) {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    return up((size_t)2 * p.n_blocks * N * DV * 4) + up((size_t)2 * p.n_blocks * N * 4) + up((size_t)p.segs * 4);
+}
+
+TcArgs carve(const Plan &pl, int N, void *ws) {
+    TcArgs a{};
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    char *w = static_cast<char *>(ws);
+    a.o_part = reinterpret_cast<float *>(w);
+    a.lse_part = reinterpret_cast<float *>(w + up((size_t)2 * pl.n_blocks * N * DV * 4));
+    a.counters = reinterpret_cast<int *>(w + up((size_t)2 * pl.n_blocks * N * DV * 4) + up((size_t)2 * pl.n_blocks * N * 4));
+    a.n_blocks = pl.n_blocks;
+    a.aligned = pl.aligned ? 1 : 0;
+    return a;
+}
+
+template <int KIND, int N>
+cudaError_t launch(const CUtensorMap &km, const CUtensorMap &vm, const CUtensorMap &qm, const CUtensorMap &qrm,
+                   const TcArgs &a, cudaStream_t st) {
+    const size_t smem = Cfg<KIND, N>::smem_bytes(a.B);
+    auto kern = decode_tc_kernel<KIND, N>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(kern, dim3(a.n_blocks), dim3(kThreads), smem, st, km, vm, qm, qrm, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ GQA (D = 128, G % 16 == 0)
+
+bool decode_tc_gqa_eligible(int B, int Hq, int Hkv, int D) {
+    const int G = Hq / Hkv;
+    return D == 128 && G % 16 == 0 && smem_for<kGqa>(heads_per_block(G), B) <= 227 * 1024;
+}
+
+static Plan gqa_plan_tc(int B, int Hq, int Hkv, int n_split) {
+    const int G = Hq / Hkv;
+    return plan((long long)B * Hkv * (G / heads_per_block(G)), n_split);
+}
+
+int decode_tc_gqa_blocks(int B, int Hq, int Hkv, int n_split) { return gqa_plan_tc(B, Hq, Hkv, n_split).n_blocks; }
+
+size_t decode_tc_gqa_workspace(int B, int Hq, int Hkv, int n_split) {
+    return ws_bytes(gqa_plan_tc(B, Hq, Hkv, n_split), heads_per_block(Hq / Hkv));
+}
+
+cudaError_t launch_decode_tc_gqa(const void *q, const void *k, const void *v, const int *seq_lens, float *out, int B,
+                                 int Hq, int Hkv, float scale_log2, int S_max, int n_split, void *ws, cudaStream_t st) {
+    const int G = Hq / Hkv;
+    const int N = heads_per_block(G);
+    const Plan pl = gqa_plan_tc(B, Hq, Hkv, n_split);
+    TcArgs a = carve(pl, N, ws);
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.B = B;
+    a.Hq = Hq;
+    a.G = G;
+    a.n_hblk = G / N;
+    a.seg_per_seq = Hkv * a.n_hblk;
+    a.scale_log2 = scale_log2;
+    CUtensorMap km, vm, qm;
+    const uint64_t dims[4] = {128, (uint64_t)Hkv, (uint64_t)S_max, (uint64_t)B};
+    const uint64_t strides[3] = {256, (uint64_t)Hkv * 256, (uint64_t)S_max * Hkv * 256};
+    const uint32_t box[4] = {64, 1, TILE, 1};
+    cudaError_t e = encode_tensor_map(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k, dims, strides, box,
+                                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (e == cudaSuccess)
+        e = encode_tensor_map(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (e == cudaSuccess) {
+        const uint64_t qdims[3] = {128, (uint64_t)Hq, (uint64_t)B};
+        const uint64_t qstrides[2] = {256, (uint64_t)Hq * 256};
+        const uint32_t qbox[3] = {64, (uint32_t)N, 1};
+        e = encode_tensor_map(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, qdims, qstrides, qbox,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    }
+    if (e != cudaSuccess) return e;
+    return N == 32 ? launch<kGqa, 32>(km, vm, qm, qm, a, st) : launch<kGqa, 16>(km, vm, qm, qm, a, st);
+}
+
+// ------------------------------------------------------------------ MLA (r = 128, dr = 48, Hq % 16 == 0)
+
+bool decode_tc_mla_fits(int B, int Hq) { return smem_for<kMla>(heads_per_block(Hq), B) <= 227 * 1024; }
+
+static Plan mla_plan_tc(int B, int Hq, int n_split) {
+    return plan((long long)B * (Hq / heads_per_block(Hq)), n_split);
+}
+
+int decode_tc_mla_blocks(int B, int Hq, int n_split) { return mla_plan_tc(B, Hq, n_split).n_blocks; }
+
+size_t decode_tc_mla_workspace(int B, int Hq, int n_split) {
+    return ws_bytes(mla_plan_tc(B, Hq, n_split), heads_per_block(Hq));
+}
+
+cudaError_t launch_decode_tc_mla(const void *q_lat, const void *q_rope, const void *c_cache, const void *kr_cache,
+                                 const int *seq_lens, float *out, int B, int Hq, float scale_log2, int S_max,
+                                 int n_split, void *ws, cudaStream_t st) {
+    const int N = heads_per_block(Hq);
+    const Plan pl = mla_plan_tc(B, Hq, n_split);
+    TcArgs a = carve(pl, N, ws);
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.B = B;
+    a.Hq = Hq;
+    a.G = Hq;
+    a.n_hblk = Hq / N;
+    a.seg_per_seq = a.n_hblk;
+    a.scale_log2 = scale_log2;
+    CUtensorMap cm, krm, qm, qrm;
+    const uint64_t cdims[3] = {128, (uint64_t)S_max, (uint64_t)B};
+    const uint64_t cstrides[2] = {256, (uint64_t)S_max * 256};
+    const uint32_t cbox[3] = {64, TILE, 1};
+    cudaError_t e = encode_tensor_map(&cm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c_cache, cdims, cstrides, cbox,
+                                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (e == cudaSuccess) {
+        const uint64_t dims[3] = {48, (uint64_t)S_max, (uint64_t)B};
+        const uint64_t strides[2] = {96, (uint64_t)S_max * 96};
+        const uint32_t box[3] = {16, TILE, 1};
+        e = encode_tensor_map(&krm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kr_cache, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    }
+    if (e == cudaSuccess) {
+        const uint64_t dims[3] = {128, (uint64_t)Hq, (uint64_t)B};
+        const uint64_t strides[2] = {256, (uint64_t)Hq * 256};
+        const uint32_t box[3] = {64, (uint32_t)N, 1};
+        e = encode_tensor_map(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q_lat, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    }
+    if (e == cudaSuccess) {
+        const uint64_t dims[3] = {48, (uint64_t)Hq, (uint64_t)B};
+        const uint64_t strides[2] = {96, (uint64_t)Hq * 96};
+        const uint32_t box[3] = {16, (uint32_t)N, 1};
+        e = encode_tensor_map(&qrm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q_rope, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    }
+    if (e != cudaSuccess) return e;
+    return N == 32 ? launch<kMla, 32>(cm, krm, qm, qrm, a, st) : launch<kMla, 16>(cm, krm, qm, qrm, a, st);
+}
+
+int decode_tc_read_and_clear_status(cudaStream_t s, unsigned *flag) {
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(flag, g_decode_tc_status, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbolAsync(g_decode_tc_status, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return (int)e;
+}
+
+}  // namespace mlakv

@@ -26,4 +26,41 @@ __host__ __device__ __forceinline__ int stream_block_of(long long t, long long T
     return (int)(((t + 1) * n - 1) / T);
 }
 
+// One piece of a block's range: tiles [i0, i0 + n_t) of segment (b, gi, hb).
+struct Piece {
+    int b, gi, hb, S, i0, n_t;
+    bool whole;                 // the piece is the whole segment
+};
+
+// Walks the pieces of a block's tile range [t, t_end) using the tile prefix over sequences.
+struct PieceWalker {
+    const int *prefix;          // prefix[b] = Σ_{b' < b} tiles(S_b'), b = 0 .. B
+    const int *seq_lens;
+    int B, seg_per_seq, n_hblk, tile;
+    long long t, t_end;
+    __device__ bool next(Piece &p) {
+        if (t >= t_end) return false;
+        // the last b with seg_per_seq · prefix[b] <= t (sequences with no tiles are skipped)
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((long long)seg_per_seq * prefix[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        p.b = lo;
+        p.S = seq_lens[lo];
+        const int nb = stream_tiles(p.S, tile);
+        const long long fb = (long long)seg_per_seq * prefix[lo];
+        const int q = (int)((t - fb) / nb);
+        p.gi = q / n_hblk;
+        p.hb = q % n_hblk;
+        p.i0 = (int)((t - fb) % nb);
+        const long long seg_end = fb + (long long)(q + 1) * nb;
+        const long long end = seg_end < t_end ? seg_end : t_end;
+        p.n_t = (int)(end - t);
+        p.whole = p.i0 == 0 && end == seg_end;
+        t = end;
+        return true;
+    }
+};
+
 }  // namespace mlakv
