@@ -99,7 +99,7 @@ struct Cfg {
     static constexpr int STAT_OFF = LRED_OFF + 4 * N * 4;       // [N] 1/L, [N] lse
     static constexpr int MISC_OFF = STAT_OFF + 2 * N * 4;       // TMEM base, merge flag
     static constexpr int SHREC_OFF = MISC_OFF + 16;             // [2] shared-segment records
-    static constexpr int PLIST_OFF = SHREC_OFF + 2 * 48;
+    static constexpr int PLIST_OFF = SHREC_OFF + 2 * 64;
     static constexpr int PREFIX_OFF = PLIST_OFF + kPlist * 4;
     static_assert(STAGE % 1024 == 0 && Q_SLOT % 1024 == 0 && P_BYTES % 1024 == 0, "swizzle alignment");
     static_assert(N_BARS * 8 <= 256, "barrier area");
@@ -209,19 +209,30 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
     griddep_wait();
     griddep_launch_dependents();
     if (warp == 0) {
-        // tile prefix over the sequences (warp scan, 32 sequences at a time)
+        // tile prefix over the sequences (warp scan, 32 sequences at a time; the lengths of
+        // up to 128 sequences are loaded in one round trip)
         int carry = 0;
-        for (int base = 0; base < a.B; base += 32) {
-            const int b = base + lane;
-            const int v = b < a.B ? stream_tiles(a.seq_lens[b], TILE) : 0;
-            int x = v;
+        for (int base = 0; base < a.B; base += 128) {
+            int len[4];
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
+            for (int j = 0; j < 4; ++j) {
+                const int b = base + 32 * j + lane;
+                len[j] = b < a.B ? __ldg(a.seq_lens + b) : 0;
             }
-            if (b < a.B) prefix[b] = carry + x - v;
-            carry += __shfl_sync(0xffffffffu, x, 31);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (base + 32 * j >= a.B) break;
+                const int b = base + 32 * j + lane;
+                const int v = stream_tiles(len[j], TILE);
+                int x = v;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += y;
+                }
+                if (b < a.B) prefix[b] = carry + x - v;
+                carry += __shfl_sync(0xffffffffu, x, 31);
+            }
         }
         if (lane == 0) prefix[a.B] = carry;
     }
@@ -440,8 +451,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
         // records in shared memory, the arrival count thread 0 saw in a register, read only at
         // the end, so the counter's round trip never stalls the stream; the last arrival merges.
         struct Shared {
-            long long fs;
-            int b, h0, seg, n_pieces, c0, sparse, first_odd;
+            long long fs;                     // the segment's first tile in the stream
+            int b, h0, seg, nb;               // sequence, first query head, segment, its tiles
+            int c0, c1, first_odd;            // its first and last owner blocks (filled at the end)
         };
         Shared *shrec = reinterpret_cast<Shared *>(smem + C::SHREC_OFF);
         int seen0 = 0, seen1 = 0, n_shared = 0;
@@ -581,26 +593,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
                 // the partial slots of the blocks holding tiles of this segment: blocks c0 .. c1,
                 // or, with fewer tiles than blocks (each block then owns at most one tile), the
                 // owners of the segment's nb tiles
-                const int seg = p.b * a.seg_per_seq + p.gi * a.n_hblk + p.hb;
+                // publish: the partial's stores, ordered before thread 0's release by the
+                // barrier, are visible to whichever block later acquires the counter. Thread 0
+                // keeps the count it saw in a register of its own, read only at the end.
+                bar_sync_named(1, kSoftmax);
                 if (tid == 0) {
-                    Shared r;
-                    const int nb = stream_tiles(p.S, TILE);
+                    const int seg = p.b * a.seg_per_seq + p.gi * a.n_hblk + p.hb;
+                    if (n_shared == 0) seen0 = atomic_add_acq_rel_gpu(a.counters + seg, 1);
+                    else seen1 = atomic_add_acq_rel_gpu(a.counters + seg, 1);
+                    Shared &r = shrec[n_shared];
+                    r.nb = prefix[p.b + 1] - prefix[p.b];
+                    r.fs = (long long)a.seg_per_seq * prefix[p.b] + (long long)(p.gi * a.n_hblk + p.hb) * r.nb;
                     r.b = p.b;
                     r.h0 = h0;
                     r.seg = seg;
-                    r.fs = (long long)a.seg_per_seq * prefix[p.b] + (long long)(p.gi * a.n_hblk + p.hb) * nb;
-                    r.sparse = T < a.n_blocks;
-                    r.c0 = stream_block_of(r.fs, T, a.n_blocks);
-                    r.n_pieces = r.sparse ? nb : stream_block_of(r.fs + nb - 1, T, a.n_blocks) - r.c0 + 1;
-                    r.first_odd = stream_start(r.c0, T, a.n_blocks) < r.fs;
-                    shrec[n_shared] = r;
-                }
-                // publish: the partial's stores, ordered before thread 0's release by the
-                // barrier, are visible to whichever block later acquires the counter
-                bar_sync_named(1, kSoftmax);
-                if (tid == 0) {
-                    const int v = atomic_add_acq_rel_gpu(a.counters + seg, 1);
-                    if (n_shared == 0) seen0 = v; else seen1 = v;
                 }
                 ++n_shared;
             }
@@ -609,11 +615,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
 
         // ---------------------------------------------------------- merge the shared segments
         // this block arrived last at
+        const bool sparse = T < a.n_blocks;
         for (int j = 0; j < n_shared; ++j) {
             bar_sync_named(1, kSoftmax);          // misc[1] and plist are free; records written
-            const Shared q = shrec[j];
+            // the blocks holding tiles of this segment: c0 .. c1 (three divisions, one per warp);
+            // first_odd: block c0 started before the segment, so it holds it in its second slot
+            Shared &rs = shrec[j];
+            if (lane == 0 && sw == 0) rs.c0 = stream_block_of(rs.fs, T, a.n_blocks);
+            if (lane == 0 && sw == 1) rs.c1 = stream_block_of(rs.fs + rs.nb - 1, T, a.n_blocks);
+            if (lane == 0 && sw == 2) rs.first_odd = rs.fs > 0 && stream_block_of(rs.fs - 1, T, a.n_blocks) ==
+                                                                    stream_block_of(rs.fs, T, a.n_blocks);
+            bar_sync_named(1, kSoftmax);
+            const Shared q = rs;
+            // with fewer tiles than blocks each block owns at most one tile: one partial per tile
+            const int n_pieces = sparse ? q.nb : q.c1 - q.c0 + 1;
             if (tid == 0) {
-                const bool last = (j == 0 ? seen0 : seen1) == q.n_pieces - 1;
+                const bool last = (j == 0 ? seen0 : seen1) == n_pieces - 1;
                 misc[1] = last;
                 if (last) a.counters[q.seg] = 0;
             }
@@ -621,20 +638,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
             if (!misc[1]) continue;
             // thread 0's acquire, then the barrier, order the loads below after every
             // other block's release of its partial
-            const bool listed = q.n_pieces <= kPlist;
+            const bool listed = n_pieces <= kPlist;
             auto slot_of = [&](int i) {
-                if (q.sparse) return 2 * stream_block_of(q.fs + i, T, a.n_blocks);
+                if (sparse) return 2 * stream_block_of(q.fs + i, T, a.n_blocks);
                 if (i == 0) return 2 * q.c0 + q.first_odd;
                 return 2 * (q.c0 + i);
             };
             if (listed)
-                for (int i = tid; i < q.n_pieces; i += kSoftmax) plist[i] = slot_of(i);
+                for (int i = tid; i < n_pieces; i += kSoftmax) plist[i] = slot_of(i);
             bar_sync_named(1, kSoftmax);
             auto slot_at = [&](int i) { return listed ? plist[i] : slot_of(i); };
             // Warp w combines rows w, w + 4, ..., lane = float4 column block. The partials come
             // PC at a time with their log-sum-exps, all rows' loads in flight together (one L2
             // round trip per PC partials), folded in with a running maximum.
-            constexpr int RPW = N / 4, PC = 64 / N;
+            constexpr int RPW = N / 4, PC = 4;
             float M[RPW], W[RPW];
             float4 acc[RPW];
 #pragma unroll
@@ -643,12 +660,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
                 W[r] = 0.f;
                 acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            for (int i0 = 0; i0 < q.n_pieces; i0 += PC) {
+            for (int i0 = 0; i0 < n_pieces; i0 += PC) {
                 float lv[PC][RPW];
                 float4 xv[PC][RPW];
 #pragma unroll
                 for (int u = 0; u < PC; ++u) {
-                    const bool in = i0 + u < q.n_pieces;
+                    const bool in = i0 + u < n_pieces;
                     const size_t base = in ? (size_t)slot_at(i0 + u) * N : 0;
 #pragma unroll
                     for (int r = 0; r < RPW; ++r) {

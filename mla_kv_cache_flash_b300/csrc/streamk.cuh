@@ -48,7 +48,7 @@ struct PieceWalker {
         }
         p.b = lo;
         p.S = seq_lens[lo];
-        const int nb = stream_tiles(p.S, tile);
+        const int nb = prefix[lo + 1] - prefix[lo];     // = stream_tiles(p.S, tile)
         const long long fb = (long long)seg_per_seq * prefix[lo];
         const int q = (int)((t - fb) / nb);
         p.gi = q / n_hblk;
