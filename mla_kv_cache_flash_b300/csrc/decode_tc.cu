@@ -90,9 +90,12 @@ struct Cfg {
     static constexpr int P_BYTES = TILE * P_ROW;
     static constexpr uint32_t P_LAYOUT = N == 32 ? kSw128 : kSw64;
     static constexpr int Q_OFF = NS * STAGE;
-    static constexpr int P_OFF = Q_OFF + QS * Q_SLOT;           // weights, then their residuals
-    static constexpr int BAR_OFF = P_OFF + P_BYTES;
-    static constexpr int N_BARS = 2 * NS + 10;
+    // weight buffers: two (the softmax of tile g + 1 need not wait for P·V(g)) where shared
+    // memory allows
+    static constexpr int PB = N == 16 ? 2 : 1;
+    static constexpr int P_OFF = Q_OFF + QS * Q_SLOT;
+    static constexpr int BAR_OFF = P_OFF + PB * P_BYTES;
+    static constexpr int N_BARS = 2 * NS + 12;
     static constexpr int SCR_OFF = BAR_OFF + 256;
     static constexpr int MAXRED_OFF = SCR_OFF;                  // [4][N] per-warp tile maxima
     static constexpr int LRED_OFF = MAXRED_OFF + 4 * N * 4;     // [4][N] per-warp sums
@@ -110,7 +113,7 @@ struct Cfg {
 template <int NS>
 struct Bars {
     static constexpr int FULL = 0, EMPTY = NS, QFULL = 2 * NS, QEMPTY = 2 * NS + 2, SFULL = 2 * NS + 4,
-                         SFREE = 2 * NS + 6, PREADY = 2 * NS + 8, PVDONE = 2 * NS + 9;
+                         SFREE = 2 * NS + 6, PREADY = 2 * NS + 8, PVDONE = 2 * NS + 10;   // PREADY, PVDONE: one per weight buffer
 };
 
 struct TcArgs {
@@ -197,8 +200,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
             mbar_init(bar(BI::SFULL + i), 1);
             mbar_init(bar(BI::SFREE + i), 4);
         }
-        mbar_init(bar(BI::PREADY), 4);
-        mbar_init(bar(BI::PVDONE), 1);
+        for (int i = 0; i < C::PB; ++i) {
+            mbar_init(bar(BI::PREADY + i), 4);
+            mbar_init(bar(BI::PVDONE + i), 1);
+        }
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -360,19 +365,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
                 }
                 umma_commit(bar(BI::SFULL + (gg & 1)));
             };
-            auto issue_pv = [&](int s, bool first) {
+            auto issue_pv = [&](int gg, int s, bool first) {
                 const uint32_t v = sb + s * C::STAGE + C::V_OFF;
-                const uint32_t pb = sb + C::P_OFF;
+                const uint32_t pb = sb + C::P_OFF + (gg % C::PB) * C::P_BYTES;
                 // 16 tokens per MMA; columns [0, N) of O take the weights' heads, [N, 2N) their residuals
 #pragma unroll
                 for (int kk = 0; kk < TILE / 16; ++kk)
                     umma_ss(t_o, sdesc(v + kk * 2048, BOX, 1024, kSw128),
                             sdesc(pb + kk * 16 * C::P_ROW, C::P_BYTES, 8 * C::P_ROW, C::P_LAYOUT), idesc_o,
                             (!first || kk > 0) ? 1u : 0u);
-                umma_commit(bar(BI::PVDONE));
+                umma_commit(bar(BI::PVDONE + gg % C::PB));
                 umma_commit(bar(BI::EMPTY + s));
             };
-            auto ready_pv = [&](int gg) { return mbar_test_wait(bar(BI::PREADY), gg & 1); };
+            auto ready_pv = [&](int gg) { return mbar_test_wait(bar(BI::PREADY + gg % C::PB), (gg / C::PB) & 1); };
             int g = 0, k = 0;
             bool pend = false, pend_first = false;   // P·V of tile pend_g not yet issued
             int pend_g = 0, pend_s = 0;
@@ -387,7 +392,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
                     while (!s_done || pend) {
                         if (pend && ready_pv(pend_g)) {
                             tc_fence_after();
-                            issue_pv(pend_s, pend_first);
+                            issue_pv(pend_g, pend_s, pend_first);
                             pend = false;
                             continue;
                         }
@@ -412,19 +417,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
                     pend_s = s;
                     pend_first = i == 0;
                     if (i == p.n_t - 1) {
-                        if (!mbar_wait_bounded(bar(BI::PREADY), g & 1, &g_decode_tc_status, kStatusMmaWait)) {
+                        if (!mbar_wait_bounded(bar(BI::PREADY + g % C::PB), (g / C::PB) & 1, &g_decode_tc_status,
+                                               kStatusMmaWait)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        issue_pv(s, i == 0);
+                        issue_pv(g, s, i == 0);
                         pend = false;
                     }
                 }
                 ++k;
             }
             // the last products finish before the block frees tensor memory
-            if (ok && g > 0) mbar_wait_bounded(bar(BI::PVDONE), (g - 1) & 1, &g_decode_tc_status, kStatusMmaWait);
+            if (ok && g > 0)
+                mbar_wait_bounded(bar(BI::PVDONE + (g - 1) % C::PB), ((g - 1) / C::PB) & 1, &g_decode_tc_status,
+                                  kStatusMmaWait);
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
@@ -505,7 +513,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
                     }
                     if (i > 0) {
                         // O holds the tiles before this one: scale both halves to the new reference
-                        wait(bar(BI::PVDONE), (g - 1) & 1, kStatusMmaWait);
+                        wait(bar(BI::PVDONE + (g - 1) % C::PB), ((g - 1) / C::PB) & 1, kStatusMmaWait);
                         tc_fence_after();
 #pragma unroll
                         for (int ch = 0; ch < 2 * N / 16; ++ch) {      // 16 columns at a time
@@ -531,11 +539,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
                     l[h] += bf16_lo(w) + bf16_lo(r);
                     l[h + 1] += bf16_hi(w) + bf16_hi(r);
                 }
-                // the weight buffer is free once P·V(g − 1) has completed
-                if (g >= 1) wait(bar(BI::PVDONE), (g - 1) & 1, kStatusMmaWait);
+                // the weight buffer is free once P·V(g − PB) has completed
+                if (g >= C::PB) wait(bar(BI::PVDONE + g % C::PB), ((g / C::PB) - 1) & 1, kStatusMmaWait);
                 // row = [heads | residuals], 16-byte chunks swizzled (128-byte rows: chunk c at
                 // c ^ (row & 7); 64-byte rows: c ^ ((row >> 1) & 3))
-                uint8_t *prow = smem + C::P_OFF + row * C::P_ROW;
+                uint8_t *prow = smem + C::P_OFF + (g % C::PB) * C::P_BYTES + row * C::P_ROW;
                 const int swz = N == 32 ? row & 7 : (row >> 1) & 3;
 #pragma unroll
                 for (int ch = 0; ch < N / 8; ++ch) {
@@ -556,7 +564,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(BI::PREADY));
+                if (lane == 0) mbar_arrive(bar(BI::PREADY + g % C::PB));
             }
 
             // ---------------------------------------------------------- end of the piece
@@ -576,7 +584,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
                 stat[tid] = ok && L > 0.f ? 1.f / L : 0.f;
                 stat[N + tid] = ok && L > 0.f ? (mh + log2f(L)) * kLn2 : -INFINITY;
             }
-            wait(bar(BI::PVDONE), (g - 1) & 1, kStatusMmaWait);
+            wait(bar(BI::PVDONE + (g - 1) % C::PB), ((g - 1) / C::PB) & 1, kStatusMmaWait);
             tc_fence_after();
             uint32_t o[N], o2[N];
             o_half(0, o);
