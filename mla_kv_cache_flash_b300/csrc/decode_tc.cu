@@ -33,7 +33,7 @@
 // to `out`; a shared one leaves a normalised partial and ln Σ e^s in the block's slot, and the
 // last block to finish the segment (acquire-release arrival counter) combines them.
 //
-// Warp roles (192 threads, one block per SM):
+// Warp roles (192 threads, one block per SM; two for 16-head MLA):
 //   warp 0     TMA producer: per piece the query rows into a slot (two slots where shared
 //              memory allows), per tile the cache rows into an NS-stage ring (L2 evict-first).
 //   warp 1     allocates 128 TMEM columns (S double buffer at 0 and 32; O at 64: N columns
@@ -76,14 +76,17 @@ struct Cfg {
     static_assert(N == 16 || N == 32, "16 or 32 query heads per block");
     // ring stage: the key tile (2 boxes of K or c), then V (2 boxes) or kr (3 boxes)
     static constexpr int STAGE = 2 * BOX + (KIND == kGqa ? 2 * BOX : 3 * ROPE_BOX);
-    static constexpr int NS = KIND == kGqa ? 3 : 4;
+    // blocks per SM: two for 16-head MLA (two independent tile chains share the SM's tensor
+    // pipe and TMA engine, each filling the other's gaps), one otherwise
+    static constexpr int CPS = KIND == kMla && N == 16 ? 2 : 1;
+    static constexpr int NS = KIND == kGqa ? 3 : CPS == 2 ? 2 : 4;
     static constexpr int V_OFF = KIND == kGqa ? 2 * BOX : 0;     // value tile inside a stage
     static constexpr int Q_BOX = N * 128;                       // N query rows × 64 columns
     static constexpr int QR_BOX = N * 32;                       // N rows × 16 rope columns
     static constexpr int Q_BYTES = 2 * Q_BOX + (KIND == kMla ? 3 * QR_BOX : 0);
     static constexpr int Q_SLOT = (Q_BYTES + 1023) / 1024 * 1024;
     // query slots: two (the next piece's rows load early) where shared memory allows
-    static constexpr int QS = KIND == kGqa && N == 32 ? 1 : 2;
+    static constexpr int QS = (KIND == kGqa && N == 32) || CPS == 2 ? 1 : 2;
     // one token's weights as a row of 2N bf16: the N heads, then the N residuals; the P·V
     // product takes both as one N = 2N operand (one MMA chain instead of two)
     static constexpr int P_ROW = 2 * N * 2;
@@ -92,7 +95,7 @@ struct Cfg {
     static constexpr int Q_OFF = NS * STAGE;
     // weight buffers: two (the softmax of tile g + 1 need not wait for P·V(g)) where shared
     // memory allows
-    static constexpr int PB = N == 16 ? 2 : 1;
+    static constexpr int PB = N == 16 && CPS == 1 ? 2 : 1;
     static constexpr int P_OFF = Q_OFF + QS * Q_SLOT;
     static constexpr int BAR_OFF = P_OFF + PB * P_BYTES;
     static constexpr int N_BARS = 2 * NS + 12;
@@ -166,7 +169,7 @@ __device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint32_t (&r)[
 }
 
 template <int KIND, int N>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, Cfg<KIND, N>::CPS)
 decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (MLA)
                  const __grid_constant__ CUtensorMap vmap,    // V (GQA) or kr (MLA)
                  const __grid_constant__ CUtensorMap qmap,    // q (GQA) or q_lat (MLA)
@@ -732,16 +735,16 @@ size_t smem_for(int N, int B) {
 }
 
 // Segments (sequence, KV head, head block) and the grid over them. Aligned mode: when the
-// segments number between half the SMs and all of them, each gets a block of its own.
+// segments number between half the resident blocks and all of them, each gets a block.
 struct Plan {
     long long segs;
     int n_blocks;
     bool aligned;
 };
 
-Plan plan(long long segs, int n_split) {
+Plan plan(long long segs, int n_split, int cps) {
     Plan p{segs, 1, false};
-    const int sms = sm_count();
+    const int sms = cps * sm_count();          // resident blocks
     if (n_split == 0 && segs <= sms && 2 * segs >= sms) {
         p.aligned = true;
         p.n_blocks = (int)segs;
@@ -792,7 +795,8 @@ bool decode_tc_gqa_eligible(int B, int Hq, int Hkv, int D) {
 
 static Plan gqa_plan_tc(int B, int Hq, int Hkv, int n_split) {
     const int G = Hq / Hkv;
-    return plan((long long)B * Hkv * (G / heads_per_block(G)), n_split);
+    return plan((long long)B * Hkv * (G / heads_per_block(G)), n_split,
+                heads_per_block(G) == 32 ? Cfg<kGqa, 32>::CPS : Cfg<kGqa, 16>::CPS);
 }
 
 int decode_tc_gqa_blocks(int B, int Hq, int Hkv, int n_split) { return gqa_plan_tc(B, Hq, Hkv, n_split).n_blocks; }
@@ -840,7 +844,8 @@ cudaError_t launch_decode_tc_gqa(const void *q, const void *k, const void *v, co
 bool decode_tc_mla_fits(int B, int Hq) { return smem_for<kMla>(heads_per_block(Hq), B) <= 227 * 1024; }
 
 static Plan mla_plan_tc(int B, int Hq, int n_split) {
-    return plan((long long)B * (Hq / heads_per_block(Hq)), n_split);
+    return plan((long long)B * (Hq / heads_per_block(Hq)), n_split,
+                heads_per_block(Hq) == 32 ? Cfg<kMla, 32>::CPS : Cfg<kMla, 16>::CPS);
 }
 
 int decode_tc_mla_blocks(int B, int Hq, int n_split) { return mla_plan_tc(B, Hq, n_split).n_blocks; }
