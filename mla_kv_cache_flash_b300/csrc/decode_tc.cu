@@ -750,7 +750,15 @@ Plan plan(long long segs, int n_split, int cps) {
         p.n_blocks = (int)segs;
         return p;
     }
-    long long n = sms < kPlist ? sms : kPlist;
+    // A whole number k of blocks per segment when that fills at least 85 % of the resident
+    // slots: with segments of equal length every block then holds one piece of one segment
+    // (no block ends on a second, shared segment), which costs less than the last 15 % of
+    // slots gain (16-head MLA, 64 equal segments on B300: 256 blocks 25.4 us, 296 blocks
+    // 27.8 us, 259 blocks 28.6 us). Ragged lengths stay balanced either way. A merge over
+    // more than kPlist partials lists them on the fly.
+    long long n = sms;
+    const long long k = segs > 0 ? sms / segs : 0;
+    if (k >= 1 && 100 * k * segs >= 85LL * sms) n = k * segs;
     if (n_split > 0 && (long long)n_split * segs < n) n = (long long)n_split * segs;
     p.n_blocks = (int)(n < 1 ? 1 : n);
     return p;
