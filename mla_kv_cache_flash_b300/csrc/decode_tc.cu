@@ -649,15 +649,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
             if (!misc[1]) continue;
             // thread 0's acquire, then the barrier, order the loads below after every
             // other block's release of its partial
-            const bool listed = n_pieces <= kPlist;
+            // the partners' slots: consecutive blocks from c0 (their first slot; c0's second
+            // when it started before the segment), or, with more blocks than tiles, the owner
+            // of each tile, listed once in shared memory
+            const bool listed = sparse && n_pieces <= kPlist;
             auto slot_of = [&](int i) {
                 if (sparse) return 2 * stream_block_of(q.fs + i, T, a.n_blocks);
                 if (i == 0) return 2 * q.c0 + q.first_odd;
                 return 2 * (q.c0 + i);
             };
-            if (listed)
+            if (listed) {
                 for (int i = tid; i < n_pieces; i += kSoftmax) plist[i] = slot_of(i);
-            bar_sync_named(1, kSoftmax);
+                bar_sync_named(1, kSoftmax);
+            }
             auto slot_at = [&](int i) { return listed ? plist[i] : slot_of(i); };
             // Warp w combines rows w, w + 4, ..., lane = float4 column block. The partials come
             // PC at a time with their log-sum-exps, all rows' loads in flight together (one L2

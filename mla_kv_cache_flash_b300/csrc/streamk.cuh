@@ -18,11 +18,15 @@ namespace mlakv {
 __host__ __device__ __forceinline__ int stream_tiles(int len, int tile) { return (len + tile - 1) / tile; }
 
 __host__ __device__ __forceinline__ long long stream_start(int c, long long T, int n) {
+    if (T * n < (1LL << 32)) return (long long)((unsigned)c * (unsigned)T / (unsigned)n);
     return (long long)c * T / n;
 }
 
 // The block whose range holds tile t (0 <= t < T): the largest c with start(c) <= t.
+// In 32-bit arithmetic when T·n fits (the usual case: a 64-bit division is a long software
+// sequence on the GPU).
 __host__ __device__ __forceinline__ int stream_block_of(long long t, long long T, int n) {
+    if (T * n < (1LL << 32)) return (int)(((unsigned)(t + 1) * (unsigned)n - 1u) / (unsigned)T);
     return (int)(((t + 1) * n - 1) / T);
 }
 
