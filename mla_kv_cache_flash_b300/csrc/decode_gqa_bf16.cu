@@ -50,7 +50,6 @@ constexpr int kLseCache = 512;     // per warp: cached partial log-sum-exps of a
 // NC consumer warps (4 or 8) + 1 producer warp.
 template <int D, int MT, int HG, int NS, int NC>
 struct Cfg {
-    static constexpr int kConsumers = NC;
     static constexpr int kThreads = (NC + 1) * 32;
     static constexpr int TT = HG == 4 ? 32 : 16 * NC;   // tokens per tile
     static constexpr int WPH = NC / HG;             // warps per KV head

@@ -29,16 +29,7 @@ __device__ __forceinline__ void load8(const float *p, float (&x)[8]) {
     x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
-__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&x)[8]) {
-    const uint4 w = __ldg(reinterpret_cast<const uint4 *>(p));
-    x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x);
-    x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
-    x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z);
-    x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
-}
-
 __device__ __forceinline__ float to_f(float x) { return x; }
-__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 template <typename T, int D, int HB>
 __global__ void __launch_bounds__(128) decode_gqa_fma_kernel(const DecodeGqaArgs a) {

@@ -172,3 +172,22 @@ def test_merge_checks(L):
     assert L.attn_merge_partials(P, P, P, 4, 0, 64, S0) == SHAPE
     assert L.attn_merge_partials(P, P, P, 4, 2, 66, S0) == UNSUP
     assert L.attn_merge_partials(P, P, P, -1, 2, 64, S0) == SHAPE
+
+
+def test_tensor_core_plan(L):
+    # MQA / wide groups at D=128 and MLA go to the tensor-core decode: 148 SMs (the plan
+    # without a GPU assumes a 148-SM part), a whole number of blocks per segment when that
+    # fills at least 85% of the resident blocks
+    assert L.attn_decode_gqa_num_splits(64, 32, 1, 128, 8192, 1, 0) == 128       # 2 per sequence
+    assert L.attn_decode_mla_num_splits(64, 16, 128, 48, 4096, 0) == 256          # 2 per SM, 4 per seq
+    assert L.attn_decode_mla_num_splits(1, 16, 128, 48, 4096, 0) == 296           # one segment
+    assert L.attn_decode_gqa_num_splits(64, 32, 8, 128, 8192, 1, 0) == 148        # register-MMA path
+    # workspace: two partial slots of N heads x 128 fp32 per block, their lse, one counter per
+    # segment, each part 256-byte aligned
+    up = lambda x: (x + 255) // 256 * 256
+    n = 128
+    assert L.attn_decode_gqa_workspace_size(64, 32, 1, 128, 8192, 1, 0) == \
+        up(2 * n * 32 * 128 * 4) + up(2 * n * 32 * 4) + up(64 * 4)
+    n = 256
+    assert L.attn_decode_mla_workspace_size(64, 16, 128, 48, 4096, 0) == \
+        up(2 * n * 16 * 128 * 4) + up(2 * n * 16 * 4) + up(64 * 4)
