@@ -200,6 +200,15 @@ const char *attn_last_error(void);
  * wait since the last check, or ATTN_ERR_CUDA if the stream reported an error. */
 int attn_check_status(mlakv_stream_t stream);
 
+/* Failure-path self-test (no source page has a counterpart; it exists to test the library).
+ * Launches one thread that waits, bounded by `timeout_cycles` SM clock cycles (1e3 .. 1e9),
+ * on an mbarrier that nothing arrives on. The wait runs out, the kernel records it in its
+ * device status word and returns; the next attn_check_status on `stream` returns
+ * ATTN_ERR_TIMEOUT and clears it, and the context stays usable. Returns ATTN_OK once the
+ * kernel is launched, ATTN_ERR_SHAPE for a timeout outside the range, ATTN_ERR_CUDA if the
+ * launch fails. */
+int attn_selftest_bounded_wait(long long timeout_cycles, mlakv_stream_t stream);
+
 /* Library version string. */
 const char *attn_version(void);
 

@@ -24,10 +24,13 @@ __all__ = [
     "ATTN_F32", "ATTN_BF16", "MlakvError", "lib", "lib_path", "decode_gqa", "decode_gqa_workspace_size",
     "decode_gqa_num_splits", "decode_gqa_noalloc", "decode_mla_absorbed", "decode_mla_workspace_size", "decode_mla_num_splits",
     "prefill_gqa_causal", "merge_partials", "check_status", "last_error", "version",
+    "selftest_bounded_wait",
 ]
 
 ATTN_F32 = 0
 ATTN_BF16 = 1
+ATTN_OK, ATTN_ERR_NULL, ATTN_ERR_SHAPE, ATTN_ERR_UNSUPPORTED = 0, -1, -2, -3
+ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = -4, -5, -6
 _STATUS = {0: "ATTN_OK", -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_SHAPE", -3: "ATTN_ERR_UNSUPPORTED",
            -4: "ATTN_ERR_WORKSPACE", -5: "ATTN_ERR_CUDA", -6: "ATTN_ERR_TIMEOUT"}
 
@@ -57,6 +60,7 @@ _SIGNATURES = {
     "attn_last_error": (ctypes.c_char_p, []),
     "attn_check_status": (_c_int, [_vp]),
     "attn_version": (ctypes.c_char_p, []),
+    "attn_selftest_bounded_wait": (_c_int, [ctypes.c_longlong, _vp]),
 }
 
 
@@ -116,6 +120,12 @@ def _need(t, name, dtype, ndim, device=None):
 def check_status():
     """Synchronise the current stream and raise if a kernel reported a device-side error."""
     _check(lib().attn_check_status(_stream()))
+
+
+def selftest_bounded_wait(timeout_cycles=100_000):
+    """Launch a kernel whose bounded wait runs out on purpose (see attn_selftest_bounded_wait);
+    the next check_status() raises ATTN_ERR_TIMEOUT."""
+    _check(lib().attn_selftest_bounded_wait(int(timeout_cycles), _stream()))
 
 
 # ----------------------------------------------------------------------------- GQA decode

@@ -341,6 +341,7 @@ MLAKV_API int attn_check_status(mlakv_stream_t stream) {
     flag |= f;
     if (rc == 0) rc = decode_tc_read_and_clear_status(s, &f), flag |= f;
     if (rc == 0) rc = prefill_read_and_clear_status(s, &f), flag |= f;
+    if (rc == 0) rc = selftest_read_and_clear_status(s, &f), flag |= f;
     if (rc != 0) return cuda_fail((cudaError_t)rc, "attn_check_status: reading the device flags");
     if (flag != 0) return fail(ATTN_ERR_TIMEOUT, "a kernel gave up a bounded wait (flags 0x%x)", flag);
     return ok();

@@ -97,6 +97,7 @@ MLAKV_HIDDEN cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s);
 MLAKV_HIDDEN int decode_gqa_read_and_clear_status(cudaStream_t s, unsigned *flag);
 MLAKV_HIDDEN int decode_tc_read_and_clear_status(cudaStream_t s, unsigned *flag);
 MLAKV_HIDDEN int prefill_read_and_clear_status(cudaStream_t s, unsigned *flag);
+MLAKV_HIDDEN int selftest_read_and_clear_status(cudaStream_t s, unsigned *flag);
 
 // Launch `kern` on `s` with programmatic stream serialisation allowed: the kernel may start
 // before the previous kernel in the stream has finished, and must call griddep_wait() before

@@ -191,3 +191,9 @@ def test_tensor_core_plan(L):
     n = 256
     assert L.attn_decode_mla_workspace_size(64, 16, 128, 48, 4096, 0) == \
         up(2 * n * 16 * 128 * 4) + up(2 * n * 16 * 4) + up(64 * 4)
+
+
+@pytest.mark.parametrize("cycles", [0, 999, 10**9 + 1])
+def test_selftest_bounds(L, cycles):
+    # validated before any launch
+    assert L.attn_selftest_bounded_wait(cycles, S0) == SHAPE
