@@ -68,6 +68,18 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of `values` (floats) over all ranks of the default process group
+    (unchanged without one): the job's time is its slowest rank's. `device` holds the
+    reduction buffer (the GPU for NCCL, the CPU for gloo)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
 class ClockSampler:
     """Samples of the SM clock and the clock-event reasons taken while the timed region runs:
     NVML through pynvml when it is importable, else ``nvidia-smi --query-gpu ... -lms``."""
@@ -604,7 +616,6 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
-        wl = cls(w, torch.device("cpu"), 0, 0) if False else None
         # the oracle arm runs on the host only; inputs are generated on the CPU
         wl = _cpu_workload(cls, w)
         value, cores, sample, per_step = cpu_oracle_rate(wl, budget_s=120.0, steps=steps, warmup=args.warmup)
@@ -634,11 +645,7 @@ def main():
 
     with torch.cuda.stream(stream):
         res = run_workload(cls, w, device, rank, steps, args.warmup, l2, stream, barrier, want_e2e=True)
-    secs = torch.tensor([res["seconds"], res.get("e2e_seconds", 0.0)], dtype=torch.float64, device=device)
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(secs, op=dist.ReduceOp.MAX)
-    res["seconds"], res["e2e_seconds"] = float(secs[0]), float(secs[1])
+    res["seconds"], res["e2e_seconds"] = max_over_ranks([res["seconds"], res.get("e2e_seconds", 0.0)], device)
     head = summarize(res, steps, peaks, peak_src, world)
 
     also = []
