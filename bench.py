@@ -26,6 +26,7 @@ rank 0 prints the aggregate.
 """
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -206,6 +207,7 @@ def profiled_traffic(kernel_src, workload_name):
 class DecodeGqa:
     kind = "decode"
     kernel_src = "mla_kv_cache_flash_b300/csrc/decode_gqa_bf16.cu"
+    call = "attn_decode_gqa call: "
 
     def __init__(self, w, device, rank, l2_bytes):
         import mla_kv_cache_flash_b300 as mk
@@ -276,6 +278,7 @@ class DecodeGqa:
 
 class DecodeMla(DecodeGqa):
     kernel_src = "mla_kv_cache_flash_b300/csrc/decode_tc.cu"
+    call = "attn_decode_mla_absorbed call: "
 
     def __init__(self, w, device, rank, l2_bytes):
         import mla_kv_cache_flash_b300 as mk
@@ -337,6 +340,45 @@ class DecodeMla(DecodeGqa):
                 "l2": self.l2_note}
 
 
+class DecodeMlaStep(DecodeMla):
+    """The whole MLA decode step: W_UK absorbed into the query, the latent decode, W_UV on its
+    output (three launches). Algorithmic bytes: the cache rows read plus both weight tensors."""
+    call = "attn_mla_absorb_query + attn_decode_mla_absorbed + attn_mla_apply_uv; dominant: "
+
+    def __init__(self, w, device, rank, l2_bytes):
+        super().__init__(w, device, rank, l2_bytes)
+        self.bytes_per_step += (self.sets[0]["w_uk"].nbytes + self.sets[0]["w_uv"].nbytes)
+        self.out_lat = self.out
+        self.out = torch.empty((w.batch, w.n_q_heads, w.v_head_dim), dtype=torch.float32, device=device)
+        self.q_lat = torch.empty((w.batch, w.n_q_heads, w.kv_lora_rank), dtype=torch.bfloat16, device=device)
+        self.launches_per_step = 3
+
+    def _run(self, s):
+        mk = self.mk
+        mk.mla_absorb_query(s["q_nope"], s["w_uk"], q_lat=self.q_lat)
+        mk.decode_mla_absorbed(self.q_lat, s["q_rope"], s["c_cache"], s["kr_cache"], s["seq_lens"], self.w.scale,
+                               out_lat=self.out_lat, max_s=self.max_s, workspace=self.ws)
+        mk.mla_apply_uv(self.out_lat, s["w_uv"], out=self.out)
+
+    def step(self, i):
+        self._run(self.sets[i % len(self.sets)])
+
+    def host_inputs(self):
+        s = self.sets[0]
+        return {k: s[k].cpu().pin_memory() for k in ("q_nope", "q_rope", "c_cache", "kr_cache", "w_uk", "w_uv",
+                                                     "seq_lens")}
+
+    def e2e_step(self, host, dev_bufs, out_host):
+        for k, t in host.items():
+            dev_bufs[k].copy_(t, non_blocking=True)
+        self._run(dev_bufs)
+        out_host.copy_(self.out, non_blocking=True)
+
+    def describe(self):
+        return dict(super().describe(), workload=self.name, nope_dim=self.w.nope_dim, v_head_dim=self.w.v_head_dim,
+                    launches="absorb W_UK, latent decode, apply W_UV")
+
+
 class Prefill:
     kind = "prefill"
     kernel_src = "mla_kv_cache_flash_b300/csrc/prefill.cu"
@@ -383,11 +425,12 @@ WORKLOADS = {
     "llama_hkv8": lambda: (DecodeGqa, W.LLAMA3_8B[8]),
     "llama_hkv1": lambda: (DecodeGqa, W.LLAMA3_8B[1]),
     "mla": lambda: (DecodeMla, W.MINIMIND_MLA),
+    "mla_step": lambda: (DecodeMlaStep, dataclasses.replace(W.MINIMIND_MLA, name=W.MINIMIND_MLA.name + "_full_step")),
     "prefill": lambda: (Prefill, W.PREFILL_UNIFORM),
     "prefill_ragged": lambda: (Prefill, W.PREFILL_RAGGED),
 }
 DEFAULT_STEPS = {"minimind_gqa": 60000, "llama_hkv32": 400, "llama_hkv8": 2000, "llama_hkv1": 10000,
-                 "mla": 40000, "prefill": 2000, "prefill_ragged": 1500}
+                 "mla": 40000, "mla_step": 40000, "prefill": 2000, "prefill_ragged": 1500}
 
 
 # ============================================================================ timing
@@ -478,9 +521,7 @@ def summarize(res, steps, peaks, peak_src, world):
                 "traffic": profiled_traffic(wl.kernel_src, wl.name),
                 "peak_source": f"{peak_src} HBM copy bandwidth (MEASURED_PEAKS hbm_gbs)",
                 "algorithmic_bytes_per_launch": wl.bytes_per_step,
-                "kernel": ("attn_decode_gqa call: " if isinstance(wl, DecodeGqa) and not isinstance(wl, DecodeMla)
-                           else "attn_decode_mla_absorbed call: ") + os.path.basename(wl.kernel_src)
-                + " (one launch, split segments merged in-kernel)",
+                "kernel": wl.call + os.path.basename(wl.kernel_src) + " (one launch, split segments merged in-kernel)",
                 "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)}
         extra = {"tokens_per_s": round(wl.w.batch * world / per_step, 1),
                  "pct_of_8tbs": round(100 * achieved / NOMINAL_HBM_GBS, 2)}
@@ -650,7 +691,7 @@ def main():
 
     also = []
     if not args.no_also and world == 1:
-        for name in ("llama_hkv32", "llama_hkv8", "llama_hkv1", "mla", "prefill", "prefill_ragged"):
+        for name in ("llama_hkv32", "llama_hkv8", "llama_hkv1", "mla", "mla_step", "prefill", "prefill_ragged"):
             if name == args.workload:
                 continue
             c2, w2 = WORKLOADS[name]()
@@ -669,7 +710,7 @@ def main():
             torch.cuda.empty_cache()
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
+    if rank == 0 and world == 1 and not args.no_cpu and not isinstance(res["wl"], DecodeMlaStep):
         value, cores, sample, _ = cpu_oracle_rate(res["wl"], args.cpu_seconds)
         cpu = {"value": round(value, 4), "unit": head["unit"], "cores": cores, "kind": "oracle", "sample": sample}
 
@@ -702,8 +743,8 @@ def _cpu_workload(cls, w):
             self.lens = s["seq_lens"].numpy()
             self.n_split = None
             self.l2_note = "host memory"
-    if cls is Prefill:
-        raise SystemExit("the oracle arm covers the decode workloads")
+    if cls is Prefill or cls is DecodeMlaStep:
+        raise SystemExit("the oracle arm covers the single-call decode workloads")
     return HostOnly(w)
 
 

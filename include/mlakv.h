@@ -137,7 +137,7 @@ int attn_decode_gqa_noalloc(const void *q, const void *k_cache, const void *v_ca
  * latent row [c_t ‖ kr_t] and averages c_t itself:
  *   s_t = scale·(q_lat[b,h]·c_t + q_rope[b,h]·kr_t),  out_lat[b,h] = Σ_t softmax(s)_t c_t.
  * The caller forms q_lat[b,h] = W_UK[h]ᵀ q_nope[b,h] before the call and applies W_UV[h]
- * to out_lat after it.
+ * to out_lat after it (attn_mla_absorb_query and attn_mla_apply_uv below).
  *
  *   q_lat       [B, Hq, r]      bf16
  *   q_rope      [B, Hq, dr]     bf16 (RoPE already applied)
@@ -159,6 +159,33 @@ int attn_decode_mla_absorbed(const void *q_lat, const void *q_rope, const void *
                              int B, int Hq, int r, int dr, float scale,
                              int S_max, int max_S, int n_split,
                              void *workspace, size_t ws_bytes, mlakv_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * The two projections around the absorbed MLA decode [MLA section 2]: W_UK is folded into
+ * the query before the decode, W_UV is applied once to its latent output after it.
+ *
+ * attn_mla_absorb_query:  q_lat[b,h,:] = W_UK[h]ᵀ · q_nope[b,h,:], fp32 sums rounded to
+ *                         nearest-even bf16 (the decode's query operand).
+ *   q_nope  [B, Hq, d_nope]   bf16 (the non-RoPE part of the per-head query)
+ *   w_uk    [Hq, d_nope, r]   bf16 (key up-projection, latent index last)
+ *   q_lat   [B, Hq, r]        bf16, fully written.
+ *   r a multiple of 32 up to 256; d_nope 1 .. 512.
+ *
+ * attn_mla_apply_uv:      out[b,h,:] = W_UV[h] · o_lat[b,h,:], fp32.
+ *   o_lat   [B, Hq, r]        fp32 (attn_decode_mla_absorbed's out_lat)
+ *   w_uv    [Hq, d_v, r]      bf16 (value up-projection, latent index last)
+ *   out     [B, Hq, d_v]      fp32, fully written.
+ *   r a multiple of 32 up to 256; d_v 1 .. 256.
+ *
+ * Both: B, Hq >= 1; pointers 16-byte aligned; ATTN_ERR_NULL / _SHAPE / _UNSUPPORTED before
+ * any launch, ATTN_ERR_CUDA if the launch fails. Each may start before the previous kernel
+ * on the stream has finished and waits for it before reading its inputs.
+ * ------------------------------------------------------------------------------------- */
+int attn_mla_absorb_query(const void *q_nope, const void *w_uk, void *q_lat,
+                          int B, int Hq, int d_nope, int r, mlakv_stream_t stream);
+
+int attn_mla_apply_uv(const float *o_lat, const void *w_uv, float *out,
+                      int B, int Hq, int r, int d_v, mlakv_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * Causal GQA prefill over packed variable-length sequences [MQA&GQA, Attention.forward

@@ -24,7 +24,7 @@ __all__ = [
     "ATTN_F32", "ATTN_BF16", "MlakvError", "lib", "lib_path", "decode_gqa", "decode_gqa_workspace_size",
     "decode_gqa_num_splits", "decode_gqa_noalloc", "decode_mla_absorbed", "decode_mla_workspace_size", "decode_mla_num_splits",
     "prefill_gqa_causal", "merge_partials", "check_status", "last_error", "version",
-    "selftest_bounded_wait",
+    "selftest_bounded_wait", "mla_absorb_query", "mla_apply_uv", "decode_mla",
 ]
 
 ATTN_F32 = 0
@@ -55,6 +55,8 @@ _SIGNATURES = {
     "attn_decode_mla_workspace_size": (_c_size, [_c_int] * 6),
     "attn_decode_mla_num_splits": (_c_int, [_c_int] * 6),
     "attn_decode_mla_absorbed": (_c_int, [_vp] * 6 + [_c_int] * 4 + [_c_float] + [_c_int] * 3 + [_vp, _c_size, _vp]),
+    "attn_mla_absorb_query": (_c_int, [_vp] * 3 + [_c_int] * 4 + [_vp]),
+    "attn_mla_apply_uv": (_c_int, [_vp] * 3 + [_c_int] * 4 + [_vp]),
     "attn_prefill_gqa_causal": (_c_int, [_vp] * 5 + [_c_int] * 4 + [_c_float] + [_c_int] * 2 + [_vp]),
     "attn_merge_partials": (_c_int, [_vp] * 3 + [_c_int] * 3 + [_vp]),
     "attn_last_error": (ctypes.c_char_p, []),
@@ -249,6 +251,59 @@ def decode_mla_absorbed(q_lat, q_rope, c_cache, krope_cache, seq_lens, scale, ou
                                           _ptr(seq_lens), _ptr(out_lat), B, Hq, r, dr, float(scale), S_max,
                                           max_s, n_split, _ptr(workspace), ws_bytes, _stream()))
     return out_lat
+
+
+def mla_absorb_query(q_nope, w_uk, q_lat=None):
+    """q_lat[b, h] = W_UK[h]ᵀ · q_nope[b, h], fp32 sums rounded to bf16.
+
+    q_nope [B, Hq, d_nope] bf16, w_uk [Hq, d_nope, r] bf16. Returns q_lat [B, Hq, r] bf16.
+    """
+    bf = torch.bfloat16
+    _need(q_nope, "q_nope", bf, 3)
+    dev = q_nope.device
+    _need(w_uk, "w_uk", bf, 3, dev)
+    B, Hq, dn = q_nope.shape
+    r = w_uk.shape[2]
+    if w_uk.shape[:2] != (Hq, dn):
+        raise ValueError("w_uk must be [Hq, d_nope, r] for q_nope [B, Hq, d_nope]")
+    if q_lat is None:
+        q_lat = torch.empty((B, Hq, r), dtype=bf, device=dev)
+    else:
+        _need(q_lat, "q_lat", bf, 3, dev)
+        if q_lat.shape != (B, Hq, r):
+            raise ValueError("q_lat must be [B, Hq, r]")
+    _check(lib().attn_mla_absorb_query(_ptr(q_nope), _ptr(w_uk), _ptr(q_lat), B, Hq, dn, r, _stream()))
+    return q_lat
+
+
+def mla_apply_uv(o_lat, w_uv, out=None):
+    """out[b, h] = W_UV[h] · o_lat[b, h] (fp32). o_lat [B, Hq, r] fp32, w_uv [Hq, d_v, r] bf16."""
+    _need(o_lat, "o_lat", torch.float32, 3)
+    dev = o_lat.device
+    _need(w_uv, "w_uv", torch.bfloat16, 3, dev)
+    B, Hq, r = o_lat.shape
+    dv = w_uv.shape[1]
+    if w_uv.shape != (Hq, dv, r):
+        raise ValueError("w_uv must be [Hq, d_v, r] for o_lat [B, Hq, r]")
+    if out is None:
+        out = torch.empty((B, Hq, dv), dtype=torch.float32, device=dev)
+    else:
+        _need(out, "out", torch.float32, 3, dev)
+        if out.shape != (B, Hq, dv):
+            raise ValueError("out must be [B, Hq, d_v]")
+    _check(lib().attn_mla_apply_uv(_ptr(o_lat), _ptr(w_uv), _ptr(out), B, Hq, r, dv, _stream()))
+    return out
+
+
+def decode_mla(q_nope, q_rope, c_cache, krope_cache, w_uk, w_uv, seq_lens, scale, max_s=None, n_split=0,
+               workspace=None):
+    """One MLA decode step with both up-projections absorbed: W_UK into the query, the
+    latent attention over [c ‖ kr], W_UV on its output. Three launches on the current stream.
+    Returns out [B, Hq, d_v] fp32."""
+    q_lat = mla_absorb_query(q_nope, w_uk)
+    o_lat = decode_mla_absorbed(q_lat, q_rope, c_cache, krope_cache, seq_lens, scale, max_s=max_s,
+                                n_split=n_split, workspace=workspace)
+    return mla_apply_uv(o_lat, w_uv)
 
 
 # ----------------------------------------------------------------------------- prefill

@@ -223,4 +223,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Hint: bring the 128-byte line holding `p` into L2 (no data returned, no ordering implied).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// 16-byte global → shared copy that bypasses the registers (both addresses 16-byte aligned);
+// cp_async_wait_all() returns once every copy this thread committed has landed.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 }  // namespace mlakv

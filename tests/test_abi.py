@@ -142,6 +142,44 @@ def test_mla_workspace(L):
     assert mla(L, S_max=4096, max_S=4096, n_split=4) == WS
 
 
+def absorb(L, qn=P, wuk=P, ql=P, B=2, Hq=16, dn=96, r=128):
+    return L.attn_mla_absorb_query(qn, wuk, ql, B, Hq, dn, r, S0)
+
+
+def apply_uv(L, ol=P, wuv=P, out=P, B=2, Hq=16, r=128, dv=96):
+    return L.attn_mla_apply_uv(ol, wuv, out, B, Hq, r, dv, S0)
+
+
+@pytest.mark.parametrize("which", ["qn", "wuk", "ql"])
+def test_absorb_null_pointers(L, which):
+    assert absorb(L, **{which: N0}) == NULL
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(Hq=0), dict(dn=0), dict(r=0)])
+def test_absorb_bad_shapes(L, kw):
+    assert absorb(L, **kw) == SHAPE
+
+
+@pytest.mark.parametrize("kw", [dict(r=48), dict(r=288), dict(dn=513), dict(wuk=PU)])
+def test_absorb_unsupported(L, kw):
+    assert absorb(L, **kw) == UNSUP
+
+
+@pytest.mark.parametrize("which", ["ol", "wuv", "out"])
+def test_apply_uv_null_pointers(L, which):
+    assert apply_uv(L, **{which: N0}) == NULL
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(Hq=-1), dict(r=0), dict(dv=0)])
+def test_apply_uv_bad_shapes(L, kw):
+    assert apply_uv(L, **kw) == SHAPE
+
+
+@pytest.mark.parametrize("kw", [dict(r=48), dict(r=288), dict(dv=257), dict(out=PU)])
+def test_apply_uv_unsupported(L, kw):
+    assert apply_uv(L, **kw) == UNSUP
+
+
 def prefill(L, q=P, k=P, v=P, cu=P, out=P, B=2, Hq=8, Hkv=2, D=128, scale=0.088, max_seqlen=64, T=100):
     return L.attn_prefill_gqa_causal(q, k, v, cu, out, B, Hq, Hkv, D, scale, max_seqlen, T, S0)
 
