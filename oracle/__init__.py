@@ -1,6 +1,7 @@
 """CPU fp64 oracle for KV-cache attention: GQA/MHA/MQA decode, causal GQA prefill,
-MLA (absorbed and decompressed), the log-sum-exp merge of split partials, and the
-KV-cache byte/parameter accounting the pages print.
+MLA (absorbed and decompressed), the log-sum-exp merge of split partials, the rotary
+embedding and cache append of a decode step, and the KV-cache byte/parameter accounting
+the pages print.
 
 This package is TEST INFRASTRUCTURE. It is the plain, slow definition that the CUDA
 library is checked against. Only the test suite, ``__graft_entry__.smoke()`` and the
@@ -44,5 +45,10 @@ from .mla import (  # noqa: F401
     apply_uv,
     mla_decode_absorbed,
     mla_decode_naive,
+)
+from .rope import (  # noqa: F401
+    rope_rotate,
+    kv_append_rope,
+    mla_append_rope,
 )
 from . import accounting  # noqa: F401

@@ -355,3 +355,108 @@ def check_mla_is_mqa(mla_decode_absorbed, decode_gqa):
     vc = m["c"][:, :, None, :]
     ref = decode_gqa(q, kc, vc, m["lens"], 0.3)
     assert np.abs(o_lat - ref).max() <= TOL_EXACT
+
+
+# ----------------------------------------------------------------------------- RoPE + append
+
+def _unit_cis(angles):
+    return np.stack([np.cos(angles), np.sin(angles)], axis=-1)
+
+
+def check_rope_complex(rope_rotate):
+    """Consecutive pairs as complex numbers: torch.view_as_complex of a trailing axis of 2,
+    times torch.polar(1, φ), the complex multiplication the pages' cis table implies."""
+    rng = _rng(81)
+    x = rng.standard_normal((3, 4, 10))
+    ang = rng.uniform(-math.pi, math.pi, 5)
+    xc = torch.view_as_complex(torch.from_numpy(x).reshape(3, 4, 5, 2).contiguous())
+    cis = torch.polar(torch.ones(5, dtype=torch.float64), torch.from_numpy(ang))
+    ref = torch.view_as_real(xc * cis).reshape(3, 4, 10).numpy()
+    got = rope_rotate(x, _unit_cis(ang))
+    assert np.abs(got - ref).max() <= TOL_EXACT
+
+
+def check_rope_closed_forms(rope_rotate):
+    rng = _rng(82)
+    x = rng.standard_normal((2, 8))
+    assert np.array_equal(rope_rotate(x, _unit_cis(np.zeros(4))), x)                 # angle 0
+    quarter = np.tile(np.array([0.0, 1.0]), (4, 1))                                   # angle π/2
+    want = np.empty_like(x)
+    want[:, 0::2], want[:, 1::2] = -x[:, 1::2], x[:, 0::2]
+    assert np.array_equal(rope_rotate(x, quarter), want)
+    got = rope_rotate(x, _unit_cis(rng.uniform(0, 2 * math.pi, 4)))                  # |z| kept per pair
+    assert np.allclose(np.hypot(got[:, 0::2], got[:, 1::2]), np.hypot(x[:, 0::2], x[:, 1::2]), rtol=0, atol=1e-12)
+
+
+def check_rope_relative_position(rope_rotate):
+    """With angles p·θ_j the score of a rotated query and key depends on their offset only."""
+    rng = _rng(83)
+    w = 16
+    theta = 10000.0 ** (-np.arange(w // 2) * 2.0 / w)
+    table = lambda p: _unit_cis(p * theta)                       # noqa: E731
+    q, k = rng.standard_normal(w), rng.standard_normal(w)
+    for m, n, t in ((5, 2, 7), (0, 9, 31), (40, 40, 3)):
+        a = rope_rotate(q, table(m)) @ rope_rotate(k, table(n))
+        b = rope_rotate(q, table(m + t)) @ rope_rotate(k, table(n + t))
+        assert abs(a - b) <= 1e-9 * (1 + abs(a)), (m, n, t)
+
+
+def _cmul_pairs(vec, cis_row):
+    """Scalar loop: pair j of vec times cos + i·sin of row j, with Python complex numbers."""
+    out = []
+    for j in range(len(vec) // 2):
+        z = complex(vec[2 * j], vec[2 * j + 1]) * complex(cis_row[j][0], cis_row[j][1])
+        out += [z.real, z.imag]
+    return out
+
+
+def append_case(seed, bsz=4, n_q=4, n_kv=2, d=6, s_max=5, positions=(0, 4, 2, 5)):
+    rng = _rng(seed)
+    return dict(q=rng.standard_normal((bsz, n_q, d)), k_new=rng.standard_normal((bsz, n_kv, d)),
+                v_new=rng.standard_normal((bsz, n_kv, d)), pos=np.asarray(positions),
+                cis=_unit_cis(rng.uniform(-math.pi, math.pi, (s_max, d // 2))),
+                k=rng.standard_normal((bsz, s_max, n_kv, d)), v=rng.standard_normal((bsz, s_max, n_kv, d)))
+
+
+def check_append_brute(kv_append_rope):
+    a = append_case(84, positions=(0, 4, 2, 5))             # 5 = S_max: nothing appended
+    q_rot, k2, v2, lens = kv_append_rope(a["q"], a["k_new"], a["v_new"], a["pos"], a["cis"], a["k"], a["v"])
+    bsz, s_max = a["k"].shape[:2]
+    for b in range(bsz):
+        p = int(a["pos"][b])
+        ok = 0 <= p < s_max
+        assert lens[b] == (p + 1 if ok else 0)
+        for t in range(s_max):
+            for j in range(a["k"].shape[2]):
+                if ok and t == p:
+                    assert np.abs(np.array(_cmul_pairs(a["k_new"][b, j], a["cis"][p])) - k2[b, t, j]).max() <= TOL_EXACT
+                    assert list(v2[b, t, j]) == list(a["v_new"][b, j])
+                else:
+                    assert list(k2[b, t, j]) == list(a["k"][b, t, j])
+                    assert list(v2[b, t, j]) == list(a["v"][b, t, j])
+        for h in range(a["q"].shape[1]):
+            want = _cmul_pairs(a["q"][b, h], a["cis"][p]) if ok else [0.0] * a["q"].shape[2]
+            assert np.abs(np.array(want) - q_rot[b, h]).max() <= TOL_EXACT
+
+
+def check_mla_append_brute(mla_append_rope):
+    rng = _rng(85)
+    bsz, n_q, r, dr, s_max = 3, 4, 6, 4, 5
+    q_rope = rng.standard_normal((bsz, n_q, dr))
+    c_new, kr_new = rng.standard_normal((bsz, r)), rng.standard_normal((bsz, dr))
+    c, kr = rng.standard_normal((bsz, s_max, r)), rng.standard_normal((bsz, s_max, dr))
+    cis = _unit_cis(rng.uniform(-math.pi, math.pi, (s_max, dr // 2)))
+    pos = np.asarray([3, -1, 0])
+    q_rot, c2, kr2, lens = mla_append_rope(q_rope, c_new, kr_new, pos, cis, c, kr)
+    assert list(lens) == [4, 0, 1]
+    for b in range(bsz):
+        p = int(pos[b])
+        for t in range(s_max):
+            if t == p:
+                assert list(c2[b, t]) == list(c_new[b])                      # c is not rotated
+                assert np.abs(np.array(_cmul_pairs(kr_new[b], cis[p])) - kr2[b, t]).max() <= TOL_EXACT
+            else:
+                assert list(c2[b, t]) == list(c[b, t]) and list(kr2[b, t]) == list(kr[b, t])
+        for h in range(n_q):
+            want = _cmul_pairs(q_rope[b, h], cis[p]) if p >= 0 else [0.0] * dr
+            assert np.abs(np.array(want) - q_rot[b, h]).max() <= TOL_EXACT

@@ -130,3 +130,44 @@ def test_mla_naive_shared_rope_sign_error_is_caught(monkeypatch):
     monkeypatch.setattr(omla, "mla_decode_naive",
                         lambda qn, qr, c, kr, wuk, wuv, lens, scale: real(qn, qr, c, -kr, wuk, wuv, lens, scale))
     _fails(pins.check_mla_naive_brute, omla.mla_decode_naive)
+
+
+# ----------------------------------------------------------------------------- RoPE + append
+
+def _rope_pins(rot):
+    return [(pins.check_rope_complex, rot), (pins.check_rope_closed_forms, rot)]
+
+
+def test_rope_sin_sign_is_caught():
+    def rot(x, cis):
+        x, cis = np.asarray(x, float), np.asarray(cis, float)
+        c, s = cis[..., 0], cis[..., 1]
+        re, im = x[..., 0::2] * c + x[..., 1::2] * s, -x[..., 0::2] * s + x[..., 1::2] * c
+        return np.stack([re, im], -1).reshape(x.shape)
+    _any_fails(_rope_pins(rot))
+
+
+def test_rope_half_split_pairing_is_caught():
+    def rot(x, cis):                 # pairs (j, j + W/2) instead of (2j, 2j+1)
+        x, cis = np.asarray(x, float), np.asarray(cis, float)
+        c, s = cis[..., 0], cis[..., 1]
+        h = x.shape[-1] // 2
+        return np.concatenate([x[..., :h] * c - x[..., h:] * s, x[..., :h] * s + x[..., h:] * c], -1)
+    _any_fails(_rope_pins(rot))
+
+
+def test_append_position_off_by_one_is_caught(monkeypatch):
+    from oracle import rope as orope
+    real = orope._append
+    monkeypatch.setattr(orope, "_append", lambda q, kn, vn, pos, cis, kc, vc:
+                        real(q, kn, vn, np.asarray(pos) + 1, cis, kc, vc))
+    _fails(pins.check_append_brute, orope.kv_append_rope)
+    _fails(pins.check_mla_append_brute, orope.mla_append_rope)
+
+
+def test_append_rotating_the_value_is_caught():
+    from oracle import rope as orope
+    def bad(q, k_new, v_new, pos, cis, k, v):
+        rv = [orope.rope_rotate(v_new[b], cis[min(max(int(p), 0), cis.shape[0] - 1)]) for b, p in enumerate(pos)]
+        return orope.kv_append_rope(q, k_new, np.stack(rv), pos, cis, k, v)
+    _fails(pins.check_append_brute, bad)

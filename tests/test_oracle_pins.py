@@ -147,3 +147,25 @@ def test_minimind_gqa_vs_mla_floats():
     printed = float(g["compression_printed"].rstrip("x"))
     assert round(gqa / mla, g["compression_rounding_digits"]) == printed
     assert math.isclose(gqa / mla, 768 / 176)
+
+
+# ----------------------------------------------------------------------------- RoPE + append
+
+def test_rope_is_complex_multiplication_of_pairs():
+    pins.check_rope_complex(oracle.rope_rotate)
+
+
+def test_rope_closed_forms():
+    pins.check_rope_closed_forms(oracle.rope_rotate)
+
+
+def test_rope_relative_position():
+    pins.check_rope_relative_position(oracle.rope_rotate)
+
+
+def test_kv_append_brute_force():
+    pins.check_append_brute(oracle.kv_append_rope)
+
+
+def test_mla_append_brute_force():
+    pins.check_mla_append_brute(oracle.mla_append_rope)
