@@ -276,6 +276,51 @@ class DecodeGqa:
                 "l2": self.l2_note}
 
 
+class DecodeGqaStep(DecodeGqa):
+    """A whole GQA decode step: the new token's q and k rotated and k, v written into the
+    cache (attn_kv_append_rope), then the decode over the cache that holds it. Each sequence's
+    new token is its last cached row (position = length − 1), so the decode reads the same
+    bytes as the decode-only workload; the append's own bytes are added."""
+    call = "attn_kv_append_rope + attn_decode_gqa; dominant: "
+
+    def __init__(self, w, device, rank, l2_bytes):
+        super().__init__(w, device, rank, l2_bytes)
+        for i, s in enumerate(self.sets):
+            new = W.append_inputs(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.s_max, device,
+                                  seed=w.seed + 500 + i + 1000 * rank)
+            s.update(new)
+            s["pos"] = (s["seq_lens"] - 1).contiguous()
+        B, Hq, Hkv, D = w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim
+        self.bytes_per_step += B * (2 * Hq * D * 2 + 4 * Hkv * D * 2 + D * 4 + 8)
+        self.q_rot = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
+        self.new_lens = torch.empty(B, dtype=torch.int32, device=device)
+        self.launches_per_step = 2
+
+    def _run(self, s):
+        mk = self.mk
+        mk.kv_append_rope(s["q"], s["k_new"], s["v_new"], s["pos"], s["freqs_cis"], s["k_cache"], s["v_cache"],
+                          q_out=self.q_rot, new_lens=self.new_lens)
+        mk.decode_gqa(self.q_rot, s["k_cache"], s["v_cache"], self.new_lens, out=self.out, scale=self.w.scale,
+                      max_s=self.max_s, workspace=self.ws)
+
+    def step(self, i):
+        self._run(self.sets[i % len(self.sets)])
+
+    def host_inputs(self):
+        s = self.sets[0]
+        return {k: s[k].cpu().pin_memory() for k in ("q", "k_new", "v_new", "pos", "freqs_cis", "k_cache", "v_cache")}
+
+    def e2e_step(self, host, dev_bufs, out_host):
+        for k, t in host.items():
+            dev_bufs[k].copy_(t, non_blocking=True)
+        self._run(dev_bufs)
+        out_host.copy_(self.out, non_blocking=True)
+
+    def describe(self):
+        return dict(super().describe(), workload=self.name,
+                    launches="append the new token with RoPE at position length-1, then decode")
+
+
 class DecodeMla(DecodeGqa):
     kernel_src = "mla_kv_cache_flash_b300/csrc/decode_tc.cu"
     call = "attn_decode_mla_absorbed call: "
@@ -425,11 +470,12 @@ WORKLOADS = {
     "llama_hkv8": lambda: (DecodeGqa, W.LLAMA3_8B[8]),
     "llama_hkv1": lambda: (DecodeGqa, W.LLAMA3_8B[1]),
     "mla": lambda: (DecodeMla, W.MINIMIND_MLA),
+    "minimind_gqa_step": lambda: (DecodeGqaStep, dataclasses.replace(W.MINIMIND_GQA, name=W.MINIMIND_GQA.name + "_with_append")),
     "mla_step": lambda: (DecodeMlaStep, dataclasses.replace(W.MINIMIND_MLA, name=W.MINIMIND_MLA.name + "_full_step")),
     "prefill": lambda: (Prefill, W.PREFILL_UNIFORM),
     "prefill_ragged": lambda: (Prefill, W.PREFILL_RAGGED),
 }
-DEFAULT_STEPS = {"minimind_gqa": 60000, "llama_hkv32": 400, "llama_hkv8": 2000, "llama_hkv1": 10000,
+DEFAULT_STEPS = {"minimind_gqa": 60000, "minimind_gqa_step": 60000, "llama_hkv32": 400, "llama_hkv8": 2000, "llama_hkv1": 10000,
                  "mla": 40000, "mla_step": 40000, "prefill": 2000, "prefill_ragged": 1500}
 
 
@@ -691,7 +737,8 @@ def main():
 
     also = []
     if not args.no_also and world == 1:
-        for name in ("llama_hkv32", "llama_hkv8", "llama_hkv1", "mla", "mla_step", "prefill", "prefill_ragged"):
+        for name in ("minimind_gqa_step", "llama_hkv32", "llama_hkv8", "llama_hkv1", "mla", "mla_step", "prefill",
+                     "prefill_ragged"):
             if name == args.workload:
                 continue
             c2, w2 = WORKLOADS[name]()
@@ -710,7 +757,7 @@ def main():
             torch.cuda.empty_cache()
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu and not isinstance(res["wl"], DecodeMlaStep):
+    if rank == 0 and world == 1 and not args.no_cpu and not isinstance(res["wl"], (DecodeMlaStep, DecodeGqaStep)):
         value, cores, sample, _ = cpu_oracle_rate(res["wl"], args.cpu_seconds)
         cpu = {"value": round(value, 4), "unit": head["unit"], "cores": cores, "kind": "oracle", "sample": sample}
 
@@ -743,7 +790,7 @@ def _cpu_workload(cls, w):
             self.lens = s["seq_lens"].numpy()
             self.n_split = None
             self.l2_note = "host memory"
-    if cls is Prefill or cls is DecodeMlaStep:
+    if cls in (Prefill, DecodeMlaStep, DecodeGqaStep):
         raise SystemExit("the oracle arm covers the single-call decode workloads")
     return HostOnly(w)
 

@@ -188,6 +188,46 @@ int attn_mla_apply_uv(const float *o_lat, const void *w_uv, float *out,
                       int B, int Hq, int r, int d_v, mlakv_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * The cache write of one decode step, fused with the rotary embedding [MQA&GQA "代码":
+ * forward rotates the new q and k with the cis table, writes k and v at start_pos, then
+ * reads the cache; MLA section 3: q_rope and the shared rope key are rotated, c is not].
+ * A head vector of width W is rotated as W/2 consecutive pairs:
+ *   (x[2j] + i·x[2j+1]) · (cos + i·sin),  (cos, sin) = freqs_cis[pos, j],
+ * in fp32, the result rounded to nearest-even when the type is bf16.
+ *
+ * attn_kv_append_rope (GQA, decode: one new token per sequence)
+ *   q          [B, Hq, D]           dtype (the new token's query, before RoPE)
+ *   k_new      [B, Hkv, D]          dtype (before RoPE)
+ *   v_new      [B, Hkv, D]          dtype
+ *   positions  [B] int32 on the device: the row each sequence's token goes to (start_pos)
+ *   freqs_cis  [S_max, D/2, 2] fp32 (cos, sin) per position and pair
+ *   q_out      [B, Hq, D]           dtype, the rotated query (may be the same buffer as q)
+ *   k_cache, v_cache [B, S_max, Hkv, D] dtype: row positions[b] of sequence b is written,
+ *              nothing else is touched.
+ *   new_lens   [B] int32 or NULL: positions[b] + 1, the decode's seq_lens.
+ *   D a multiple of 8 (bf16) or 4 (fp32); Hq % Hkv == 0.
+ *
+ * attn_mla_append_rope (MLA, decode)
+ *   q_rope [B, Hq, dr], c_new [B, r], kr_new [B, dr] bf16; freqs_cis [S_max, dr/2, 2] fp32;
+ *   q_rope_out [B, Hq, dr] (may be q_rope); c_cache [B, S_max, r] gets c_new unrotated,
+ *   krope_cache [B, S_max, dr] the rotated kr_new; new_lens as above. r, dr multiples of 8.
+ *
+ * Both: a position outside [0, S_max) appends nothing for that sequence, writes its q_out
+ * rows as 0 and its new length as 0. Pointers 16-byte aligned. ATTN_ERR_NULL / _SHAPE /
+ * _UNSUPPORTED before any launch, ATTN_ERR_CUDA if the launch fails. The kernel may start
+ * before the previous kernel on the stream has finished and waits for it before reading.
+ * ------------------------------------------------------------------------------------- */
+int attn_kv_append_rope(const void *q, const void *k_new, const void *v_new, const int *positions,
+                        const float *freqs_cis, void *q_out, void *k_cache, void *v_cache,
+                        int *new_lens, int B, int Hq, int Hkv, int D, int S_max, attn_dtype dtype,
+                        mlakv_stream_t stream);
+
+int attn_mla_append_rope(const void *q_rope, const void *c_new, const void *kr_new,
+                         const int *positions, const float *freqs_cis, void *q_rope_out,
+                         void *c_cache, void *krope_cache, int *new_lens,
+                         int B, int Hq, int r, int dr, int S_max, mlakv_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * Causal GQA prefill over packed variable-length sequences [MQA&GQA, Attention.forward
  * with the causal mask; MLA code's is_causal=True]: row i of sequence b attends keys
  * 0 .. i of the same sequence.

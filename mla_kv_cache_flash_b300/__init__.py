@@ -24,7 +24,8 @@ __all__ = [
     "ATTN_F32", "ATTN_BF16", "MlakvError", "lib", "lib_path", "decode_gqa", "decode_gqa_workspace_size",
     "decode_gqa_num_splits", "decode_gqa_noalloc", "decode_mla_absorbed", "decode_mla_workspace_size", "decode_mla_num_splits",
     "prefill_gqa_causal", "merge_partials", "check_status", "last_error", "version",
-    "selftest_bounded_wait", "mla_absorb_query", "mla_apply_uv", "decode_mla",
+    "selftest_bounded_wait", "mla_absorb_query", "mla_apply_uv", "decode_mla", "kv_append_rope",
+    "mla_append_rope",
 ]
 
 ATTN_F32 = 0
@@ -55,6 +56,8 @@ _SIGNATURES = {
     "attn_decode_mla_workspace_size": (_c_size, [_c_int] * 6),
     "attn_decode_mla_num_splits": (_c_int, [_c_int] * 6),
     "attn_decode_mla_absorbed": (_c_int, [_vp] * 6 + [_c_int] * 4 + [_c_float] + [_c_int] * 3 + [_vp, _c_size, _vp]),
+    "attn_kv_append_rope": (_c_int, [_vp] * 9 + [_c_int] * 6 + [_vp]),
+    "attn_mla_append_rope": (_c_int, [_vp] * 9 + [_c_int] * 5 + [_vp]),
     "attn_mla_absorb_query": (_c_int, [_vp] * 3 + [_c_int] * 4 + [_vp]),
     "attn_mla_apply_uv": (_c_int, [_vp] * 3 + [_c_int] * 4 + [_vp]),
     "attn_prefill_gqa_causal": (_c_int, [_vp] * 5 + [_c_int] * 4 + [_c_float] + [_c_int] * 2 + [_vp]),
@@ -304,6 +307,80 @@ def decode_mla(q_nope, q_rope, c_cache, krope_cache, w_uk, w_uv, seq_lens, scale
     o_lat = decode_mla_absorbed(q_lat, q_rope, c_cache, krope_cache, seq_lens, scale, max_s=max_s,
                                 n_split=n_split, workspace=workspace)
     return mla_apply_uv(o_lat, w_uv)
+
+
+# ----------------------------------------------------------------------------- cache append + RoPE
+
+def _cis(freqs_cis, s_max, w, dev):
+    if freqs_cis.dtype == torch.complex64:
+        freqs_cis = torch.view_as_real(freqs_cis)
+    _need(freqs_cis, "freqs_cis", torch.float32, 3, dev)
+    if freqs_cis.shape != (s_max, w // 2, 2):
+        raise ValueError(f"freqs_cis must be [S_max={s_max}, {w // 2}, 2] (cos, sin), got {tuple(freqs_cis.shape)}")
+    return freqs_cis
+
+
+def kv_append_rope(q, k_new, v_new, positions, freqs_cis, k_cache, v_cache, q_out=None, new_lens=None):
+    """Rotate the new token's q and k at positions[b], write k and v into row positions[b]
+    of each sequence's cache. Returns (q_out, new_lens = positions + 1).
+
+    q [B, Hq, D], k_new/v_new [B, Hkv, D], caches [B, S_max, Hkv, D] (all bf16 or all fp32),
+    positions [B] int32, freqs_cis [S_max, D/2, 2] fp32 (cos, sin) or [S_max, D/2] complex64.
+    """
+    dt = q.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise TypeError("q must be bf16 or fp32")
+    _need(q, "q", dt, 3)
+    dev = q.device
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        _need(t, name, dt, 3, dev)
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _need(t, name, dt, 4, dev)
+    _need(positions, "positions", torch.int32, 1, dev)
+    B, Hq, D = q.shape
+    Hkv = k_new.shape[1]
+    S_max = k_cache.shape[1]
+    if (k_new.shape != (B, Hkv, D) or v_new.shape != k_new.shape or k_cache.shape != (B, S_max, Hkv, D)
+            or v_cache.shape != k_cache.shape or positions.shape[0] != B):
+        raise ValueError("inconsistent shapes for q, k_new, v_new, k_cache, v_cache, positions")
+    cis = _cis(freqs_cis, S_max, D, dev)
+    q_out = torch.empty_like(q) if q_out is None else q_out
+    _need(q_out, "q_out", dt, 3, dev)
+    new_lens = torch.empty(B, dtype=torch.int32, device=dev) if new_lens is None else new_lens
+    _need(new_lens, "new_lens", torch.int32, 1, dev)
+    _check(lib().attn_kv_append_rope(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(cis), _ptr(q_out),
+                                     _ptr(k_cache), _ptr(v_cache), _ptr(new_lens), B, Hq, Hkv, D, S_max,
+                                     ATTN_BF16 if dt == torch.bfloat16 else ATTN_F32, _stream()))
+    return q_out, new_lens
+
+
+def mla_append_rope(q_rope, c_new, kr_new, positions, freqs_cis, c_cache, krope_cache, q_rope_out=None,
+                    new_lens=None):
+    """MLA decode step's cache write: rotate q_rope and kr_new at positions[b], write kr and
+    the unrotated c_new into that row. Returns (q_rope_out, new_lens). All bf16."""
+    bf = torch.bfloat16
+    _need(q_rope, "q_rope", bf, 3)
+    dev = q_rope.device
+    _need(c_new, "c_new", bf, 2, dev)
+    _need(kr_new, "kr_new", bf, 2, dev)
+    _need(c_cache, "c_cache", bf, 3, dev)
+    _need(krope_cache, "krope_cache", bf, 3, dev)
+    _need(positions, "positions", torch.int32, 1, dev)
+    B, Hq, dr = q_rope.shape
+    r = c_new.shape[1]
+    S_max = c_cache.shape[1]
+    if (c_new.shape != (B, r) or kr_new.shape != (B, dr) or c_cache.shape != (B, S_max, r)
+            or krope_cache.shape != (B, S_max, dr) or positions.shape[0] != B):
+        raise ValueError("inconsistent shapes for q_rope, c_new, kr_new, c_cache, krope_cache, positions")
+    cis = _cis(freqs_cis, S_max, dr, dev)
+    q_rope_out = torch.empty_like(q_rope) if q_rope_out is None else q_rope_out
+    _need(q_rope_out, "q_rope_out", bf, 3, dev)
+    new_lens = torch.empty(B, dtype=torch.int32, device=dev) if new_lens is None else new_lens
+    _need(new_lens, "new_lens", torch.int32, 1, dev)
+    _check(lib().attn_mla_append_rope(_ptr(q_rope), _ptr(c_new), _ptr(kr_new), _ptr(positions), _ptr(cis),
+                                      _ptr(q_rope_out), _ptr(c_cache), _ptr(krope_cache), _ptr(new_lens), B, Hq, r,
+                                      dr, S_max, _stream()))
+    return q_rope_out, new_lens
 
 
 # ----------------------------------------------------------------------------- prefill

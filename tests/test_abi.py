@@ -180,6 +180,44 @@ def test_apply_uv_unsupported(L, kw):
     assert apply_uv(L, **kw) == UNSUP
 
 
+def append(L, q=P, kn=P, vn=P, pos=P, cis=P, qo=P, kc=P, vc=P, lens=N0, B=2, Hq=8, Hkv=4, D=96, S_max=64, dt=1):
+    return L.attn_kv_append_rope(q, kn, vn, pos, cis, qo, kc, vc, lens, B, Hq, Hkv, D, S_max, dt, S0)
+
+
+def mla_append(L, qr=P, cn=P, krn=P, pos=P, cis=P, qo=P, cc=P, krc=P, lens=N0, B=2, Hq=16, r=128, dr=48, S_max=64):
+    return L.attn_mla_append_rope(qr, cn, krn, pos, cis, qo, cc, krc, lens, B, Hq, r, dr, S_max, S0)
+
+
+@pytest.mark.parametrize("which", ["q", "kn", "vn", "pos", "cis", "qo", "kc", "vc"])
+def test_append_null_pointers(L, which):
+    assert append(L, **{which: N0}) == NULL
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(Hq=0), dict(Hkv=0), dict(D=0), dict(S_max=0), dict(Hq=8, Hkv=3)])
+def test_append_bad_shapes(L, kw):
+    assert append(L, **kw) == SHAPE
+
+
+@pytest.mark.parametrize("kw", [dict(D=100), dict(D=6, dt=0), dict(dt=2), dict(kc=PU), dict(lens=PU)])
+def test_append_unsupported(L, kw):
+    assert append(L, **kw) == UNSUP
+
+
+@pytest.mark.parametrize("which", ["qr", "cn", "krn", "pos", "cis", "qo", "cc", "krc"])
+def test_mla_append_null_pointers(L, which):
+    assert mla_append(L, **{which: N0}) == NULL
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(Hq=0), dict(r=0), dict(dr=0), dict(S_max=0)])
+def test_mla_append_bad_shapes(L, kw):
+    assert mla_append(L, **kw) == SHAPE
+
+
+@pytest.mark.parametrize("kw", [dict(r=100), dict(dr=50), dict(cc=PU)])
+def test_mla_append_unsupported(L, kw):
+    assert mla_append(L, **kw) == UNSUP
+
+
 def prefill(L, q=P, k=P, v=P, cu=P, out=P, B=2, Hq=8, Hkv=2, D=128, scale=0.088, max_seqlen=64, T=100):
     return L.attn_prefill_gqa_causal(q, k, v, cu, out, B, Hq, Hkv, D, scale, max_seqlen, T, S0)
 

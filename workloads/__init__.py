@@ -11,7 +11,9 @@ Recipe (every workload):
     workload keeps the float32 draws;
   * lengths: drawn on the host with ``numpy.random.default_rng(seed)``, integers
     uniform over the inclusive range, stored as int32;
-  * seeds: ``1000 + workload index``; a sub-case k of a workload adds ``10 * k``.
+  * seeds: ``1000 + workload index``; a sub-case k of a workload adds ``10 * k``;
+  * a decode step's new token (``append_inputs``): q, k_new, v_new drawn as above, and a
+    rotation table of (cos, sin) of angles uniform in [-π, π), one per position and pair.
 
 The shapes are those of the model layers the pages account for: the MiniMind hidden-768
 attention (8 Q heads, 4 KV heads of width 96; MLA rank 128 + RoPE 48), and the
@@ -181,6 +183,22 @@ def prefill_inputs(w, device="cpu", seed=None):
     v = _randn((total, w.n_kv_heads, w.head_dim), gen, device, "bf16")
     return {"q": q, "k": k, "v": v, "cu_seqlens": torch.from_numpy(cu).to(device),
             "lengths": lens, "max_seqlen": int(lens.max()) if len(lens) else 0}
+
+
+def append_inputs(batch, n_q_heads, n_kv_heads, head_dim, s_max, device="cpu", seed=0, dtype="bf16",
+                  rot_dim=None):
+    """The new token of one decode step: q [B,Hq,D], k_new/v_new [B,Hkv,D] (``dtype``), and a
+    rotation table freqs_cis [S_max, rot_dim/2, 2] fp32 of (cos, sin) of angles drawn
+    uniformly in [-π, π) (the table is an input of the method; its angles are arbitrary
+    here). ``rot_dim`` defaults to ``head_dim``."""
+    gen = _gen(device, seed)
+    rot_dim = head_dim if rot_dim is None else rot_dim
+    q = _randn((batch, n_q_heads, head_dim), gen, device, dtype)
+    k_new = _randn((batch, n_kv_heads, head_dim), gen, device, dtype)
+    v_new = _randn((batch, n_kv_heads, head_dim), gen, device, dtype)
+    ang = (torch.rand((s_max, rot_dim // 2), generator=gen, device=device, dtype=torch.float32) * 2 - 1) * math.pi
+    cis = torch.stack([torch.cos(ang), torch.sin(ang)], dim=-1).contiguous()
+    return {"q": q, "k_new": k_new, "v_new": v_new, "freqs_cis": cis}
 
 
 def to_f64(t):
