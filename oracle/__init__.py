@@ -1,7 +1,7 @@
 """CPU fp64 oracle for KV-cache attention: GQA/MHA/MQA decode, causal GQA prefill,
 MLA (absorbed and decompressed), the log-sum-exp merge of split partials, the rotary
-embedding and cache append of a decode step, and the KV-cache byte/parameter accounting
-the pages print.
+embedding and cache append of a decode step, decode over an fp8 (E4M3) cache, and the
+KV-cache byte/parameter accounting the pages print.
 
 This package is TEST INFRASTRUCTURE. It is the plain, slow definition that the CUDA
 library is checked against. Only the test suite, ``__graft_entry__.smoke()`` and the
@@ -50,5 +50,10 @@ from .rope import (  # noqa: F401
     rope_rotate,
     kv_append_rope,
     mla_append_rope,
+)
+from .fp8 import (  # noqa: F401
+    e4m3_to_float,
+    dequantize,
+    decode_gqa_fp8,
 )
 from . import accounting  # noqa: F401

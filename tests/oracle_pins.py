@@ -460,3 +460,53 @@ def check_mla_append_brute(mla_append_rope):
         for h in range(n_q):
             want = _cmul_pairs(q_rope[b, h], cis[p]) if p >= 0 else [0.0] * dr
             assert np.abs(np.array(want) - q_rot[b, h]).max() <= TOL_EXACT
+
+
+# ----------------------------------------------------------------------------- fp8 cache
+
+def check_e4m3_table(e4m3_to_float):
+    """All 256 codes against PyTorch's float8_e4m3fn widening (NaN where it gives NaN)."""
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = e4m3_to_float(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+
+
+def check_e4m3_closed_forms(e4m3_to_float):
+    v = e4m3_to_float(np.array([0x38, 0x7E, 0x01, 0x08, 0xB8, 0x00, 0x80, 0x7F], dtype=np.uint8))
+    assert list(v[:7]) == [1.0, 448.0, 2.0 ** -9, 2.0 ** -6, -1.0, 0.0, -0.0] and np.isnan(v[7])
+
+
+def fp8_case(seed, bsz=3, n_q=4, n_kv=2, d=8, s_max=9, lens=(9, 4, 0)):
+    rng = _rng(seed)
+    codes = lambda: rng.integers(0, 0x7F, size=(bsz, s_max, n_kv, d)).astype(np.uint8) | \
+        (rng.integers(0, 2, size=(bsz, s_max, n_kv, d)).astype(np.uint8) << 7)    # noqa: E731 (no NaN code)
+    return dict(q=rng.standard_normal((bsz, n_q, d)), k=codes(), v=codes(),
+                ks=rng.uniform(0.001, 0.01, (bsz, s_max, n_kv)), vs=rng.uniform(0.001, 0.01, (bsz, s_max, n_kv)),
+                lens=np.asarray(lens))
+
+
+def check_fp8_decode_identities(decode_gqa_fp8, e4m3_to_float, decode_gqa):
+    c = fp8_case(86)
+    ones = np.ones_like(c["ks"])
+    # unit scales: the decode over the decoded values
+    got = decode_gqa_fp8(c["q"], c["k"], c["v"], ones, ones, c["lens"], 0.01)
+    ref = decode_gqa(c["q"], e4m3_to_float(c["k"]), e4m3_to_float(c["v"]), c["lens"], 0.01)
+    assert np.abs(got - ref).max() <= TOL_EXACT
+    # a uniform V scale scales the output; a uniform K scale is a factor on the softmax scale
+    base = decode_gqa_fp8(c["q"], c["k"], c["v"], ones * 0.004, ones, c["lens"], 0.5)
+    assert np.abs(decode_gqa_fp8(c["q"], c["k"], c["v"], ones * 0.004, ones * 3.0, c["lens"], 0.5)
+                  - 3.0 * base).max() <= TOL_EXACT * 10
+    assert np.abs(decode_gqa_fp8(c["q"], c["k"], c["v"], ones, ones, c["lens"], 0.5 * 0.004) - base).max() <= TOL_EXACT
+    # per-row scales: brute force, one row at a time
+    got = decode_gqa_fp8(c["q"], c["k"], c["v"], c["ks"], c["vs"], c["lens"], 0.3)
+    kd = e4m3_to_float(c["k"])
+    vd = e4m3_to_float(c["v"])
+    for b, s in enumerate(c["lens"]):
+        for t in range(int(s)):
+            for j in range(kd.shape[2]):
+                kd[b, t, j] = [x * c["ks"][b, t, j] for x in kd[b, t, j]]
+                vd[b, t, j] = [x * c["vs"][b, t, j] for x in vd[b, t, j]]
+    assert np.abs(got - brute_decode(c["q"], kd, vd, c["lens"], 0.3)).max() <= TOL_EXACT

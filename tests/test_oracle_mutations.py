@@ -171,3 +171,30 @@ def test_append_rotating_the_value_is_caught():
         rv = [orope.rope_rotate(v_new[b], cis[min(max(int(p), 0), cis.shape[0] - 1)]) for b, p in enumerate(pos)]
         return orope.kv_append_rope(q, k_new, np.stack(rv), pos, cis, k, v)
     _fails(pins.check_append_brute, bad)
+
+
+# ----------------------------------------------------------------------------- fp8 cache
+
+def test_e4m3_exponent_bias_is_caught():
+    from oracle import fp8 as ofp8
+    def bad(codes):
+        return ofp8.e4m3_to_float(codes) * 0.5          # bias 8 instead of 7
+    _any_fails([(pins.check_e4m3_table, bad), (pins.check_e4m3_closed_forms, bad)])
+
+
+def test_e4m3_subnormals_as_normals_is_caught():
+    from oracle import fp8 as ofp8
+    def bad(codes):
+        c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+        v = ofp8.e4m3_to_float(codes)
+        exp, man = (c >> 3) & 0xF, c & 7
+        sign = np.where(c & 0x80, -1.0, 1.0)
+        return np.where(exp == 0, sign * (1 + man / 8.0) * 2.0 ** -7, v)
+    _any_fails([(pins.check_e4m3_table, bad), (pins.check_e4m3_closed_forms, bad)])
+
+
+def test_fp8_dropped_value_scale_is_caught():
+    from oracle import fp8 as ofp8
+    def bad(q, kc, vc, ks, vs, lens, scale):
+        return ofp8.decode_gqa_fp8(q, kc, vc, ks, np.ones_like(vs), lens, scale)
+    _fails(pins.check_fp8_decode_identities, bad, ofp8.e4m3_to_float, oracle.decode_gqa)

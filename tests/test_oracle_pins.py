@@ -169,3 +169,17 @@ def test_kv_append_brute_force():
 
 def test_mla_append_brute_force():
     pins.check_mla_append_brute(oracle.mla_append_rope)
+
+
+# ----------------------------------------------------------------------------- fp8 cache
+
+def test_e4m3_codes_match_torch():
+    pins.check_e4m3_table(oracle.e4m3_to_float)
+
+
+def test_e4m3_closed_forms():
+    pins.check_e4m3_closed_forms(oracle.e4m3_to_float)
+
+
+def test_fp8_decode_identities():
+    pins.check_fp8_decode_identities(oracle.decode_gqa_fp8, oracle.e4m3_to_float, oracle.decode_gqa)
