@@ -321,6 +321,53 @@ class DecodeGqaStep(DecodeGqa):
                     launches="append the new token with RoPE at position length-1, then decode")
 
 
+class DecodeGqaFp8(DecodeGqa):
+    """The MiniMind decode batch over an E4M3 cache with per-row fp32 K and V scales.
+    Algorithmic bytes: each live code once plus its row's scale."""
+    kernel_src = "mla_kv_cache_flash_b300/csrc/decode_gqa_fma.cu"
+    call = "attn_decode_gqa_fp8 call: "
+
+    def __init__(self, w, device, rank, l2_bytes):
+        import mla_kv_cache_flash_b300 as mk
+        self.mk, self.w, self.device, self.name = mk, w, device, w.name
+        first = W.fp8_decode_inputs(w, device, seed=w.seed + 1000 * rank)
+        self.lens = first["seq_lens"].cpu().numpy()
+        self.bytes_per_step = int(self.lens.sum()) * 2 * w.n_kv_heads * (w.head_dim + 4)
+        self.flops_per_step = 4 * w.head_dim * w.n_q_heads * int(self.lens.sum())
+        cache_bytes = 2 * (first["k_cache"].nbytes + first["k_scale"].nbytes)
+        n_sets = max(1, math.ceil(4 * l2_bytes / cache_bytes))
+        self.sets = [first] + [W.fp8_decode_inputs(w, device, seed=w.seed + 1000 * rank) for _ in range(n_sets - 1)]
+        self.max_s = int(self.lens.max())
+        self.out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.float32, device=device)
+        self.n_split = mk.decode_gqa_num_splits(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, self.max_s,
+                                                mk.ATTN_FP8_E4M3)
+        nb = mk.decode_gqa_workspace_size(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, self.max_s,
+                                          mk.ATTN_FP8_E4M3)
+        self.ws = torch.zeros(max(nb, 1), dtype=torch.uint8, device=device)
+        self.launches_per_step = 1 + (self.n_split > 1)
+        self.l2_note = f"rotating {n_sets} distinct fp8 caches ({n_sets * cache_bytes / 1e6:.0f} MB, L2 {l2_bytes / 1e6:.0f} MB)"
+
+    def _run(self, s):
+        self.mk.decode_gqa_fp8(s["q"], s["k_cache"], s["v_cache"], s["k_scale"], s["v_scale"], s["seq_lens"],
+                               out=self.out, scale=self.w.scale, max_s=self.max_s, workspace=self.ws)
+
+    def step(self, i):
+        self._run(self.sets[i % len(self.sets)])
+
+    def host_inputs(self):
+        s = self.sets[0]
+        return {k: s[k].cpu().pin_memory() for k in ("q", "k_cache", "v_cache", "k_scale", "v_scale", "seq_lens")}
+
+    def e2e_step(self, host, dev_bufs, out_host):
+        for k, t in host.items():
+            dev_bufs[k].copy_(t, non_blocking=True)
+        self._run(dev_bufs)
+        out_host.copy_(self.out, non_blocking=True)
+
+    def describe(self):
+        return dict(super().describe(), cache_dtype="fp8_e4m3 + fp32 scale per row")
+
+
 class DecodeMla(DecodeGqa):
     kernel_src = "mla_kv_cache_flash_b300/csrc/decode_tc.cu"
     call = "attn_decode_mla_absorbed call: "
@@ -470,12 +517,13 @@ WORKLOADS = {
     "llama_hkv8": lambda: (DecodeGqa, W.LLAMA3_8B[8]),
     "llama_hkv1": lambda: (DecodeGqa, W.LLAMA3_8B[1]),
     "mla": lambda: (DecodeMla, W.MINIMIND_MLA),
+    "minimind_gqa_fp8": lambda: (DecodeGqaFp8, dataclasses.replace(W.MINIMIND_GQA, name=W.MINIMIND_GQA.name + "_fp8")),
     "minimind_gqa_step": lambda: (DecodeGqaStep, dataclasses.replace(W.MINIMIND_GQA, name=W.MINIMIND_GQA.name + "_with_append")),
     "mla_step": lambda: (DecodeMlaStep, dataclasses.replace(W.MINIMIND_MLA, name=W.MINIMIND_MLA.name + "_full_step")),
     "prefill": lambda: (Prefill, W.PREFILL_UNIFORM),
     "prefill_ragged": lambda: (Prefill, W.PREFILL_RAGGED),
 }
-DEFAULT_STEPS = {"minimind_gqa": 60000, "minimind_gqa_step": 60000, "llama_hkv32": 400, "llama_hkv8": 2000, "llama_hkv1": 10000,
+DEFAULT_STEPS = {"minimind_gqa": 60000, "minimind_gqa_step": 60000, "minimind_gqa_fp8": 60000, "llama_hkv32": 400, "llama_hkv8": 2000, "llama_hkv1": 10000,
                  "mla": 40000, "mla_step": 40000, "prefill": 2000, "prefill_ragged": 1500}
 
 
@@ -737,7 +785,7 @@ def main():
 
     also = []
     if not args.no_also and world == 1:
-        for name in ("minimind_gqa_step", "llama_hkv32", "llama_hkv8", "llama_hkv1", "mla", "mla_step", "prefill",
+        for name in ("minimind_gqa_step", "minimind_gqa_fp8", "llama_hkv32", "llama_hkv8", "llama_hkv1", "mla", "mla_step", "prefill",
                      "prefill_ragged"):
             if name == args.workload:
                 continue
@@ -757,7 +805,8 @@ def main():
             torch.cuda.empty_cache()
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu and not isinstance(res["wl"], (DecodeMlaStep, DecodeGqaStep)):
+    if rank == 0 and world == 1 and not args.no_cpu and not isinstance(res["wl"], (DecodeMlaStep, DecodeGqaStep,
+                                                                                   DecodeGqaFp8)):
         value, cores, sample, _ = cpu_oracle_rate(res["wl"], args.cpu_seconds)
         cpu = {"value": round(value, 4), "unit": head["unit"], "cores": cores, "kind": "oracle", "sample": sample}
 
@@ -790,7 +839,7 @@ def _cpu_workload(cls, w):
             self.lens = s["seq_lens"].numpy()
             self.n_split = None
             self.l2_note = "host memory"
-    if cls in (Prefill, DecodeMlaStep, DecodeGqaStep):
+    if cls in (Prefill, DecodeMlaStep, DecodeGqaStep, DecodeGqaFp8):
         raise SystemExit("the oracle arm covers the single-call decode workloads")
     return HostOnly(w)
 

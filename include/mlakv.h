@@ -56,7 +56,7 @@ enum {
 };
 
 /* Element type of q and of the cache for attn_decode_gqa. */
-typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
+typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1, ATTN_FP8_E4M3 = 2 } attn_dtype;
 
 /* ---------------------------------------------------------------------------------------
  * GQA / MHA / MQA decode: one new query token per sequence over its cache.
@@ -131,6 +131,26 @@ int attn_decode_gqa_noalloc(const void *q, const void *k_cache, const void *v_ca
                             int B, int Hq, int Hkv, int D, float scale,
                             int S_max, int max_S, attn_dtype dtype, int n_split,
                             mlakv_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * GQA decode over an 8-bit floating-point cache [EBOOK: fp8 halves every cache byte]:
+ * attn_decode_gqa with the cached values e4m3(code)·scale, one fp32 scale per cached row
+ * (sequence, token, KV head) for K and for V. E4M3: 1 sign, 4 exponent (bias 7) and
+ * 3 mantissa bits, no infinities, largest finite 448; codes widen to fp32 exactly.
+ *
+ *   q          [B, Hq, D]           bf16
+ *   k_cache, v_cache [B, S_max, Hkv, D] uint8 E4M3 codes
+ *   k_scale, v_scale [B, S_max, Hkv]    fp32
+ *   seq_lens, out, scale, S_max, max_S, n_split, workspace: as attn_decode_gqa with
+ *   dtype = ATTN_FP8_E4M3 (use that dtype for the workspace and split queries). D in
+ *   {64, 96, 128}. attn_decode_gqa itself refuses ATTN_FP8_E4M3 (it has no scales).
+ * CUDA-core kernel: split partials merged by a second launch (as for fp32 caches).
+ * ------------------------------------------------------------------------------------- */
+int attn_decode_gqa_fp8(const void *q, const void *k_cache, const void *v_cache,
+                        const float *k_scale, const float *v_scale, const int *seq_lens,
+                        float *out, int B, int Hq, int Hkv, int D, float scale,
+                        int S_max, int max_S, int n_split,
+                        void *workspace, size_t ws_bytes, mlakv_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * MLA decode with W_UK absorbed [MLA sections 2, 3, 6]: every head attends the same cached

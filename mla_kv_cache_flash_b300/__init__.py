@@ -21,7 +21,7 @@ import os
 import torch
 
 __all__ = [
-    "ATTN_F32", "ATTN_BF16", "MlakvError", "lib", "lib_path", "decode_gqa", "decode_gqa_workspace_size",
+    "ATTN_F32", "ATTN_BF16", "ATTN_FP8_E4M3", "MlakvError", "decode_gqa_fp8", "lib", "lib_path", "decode_gqa", "decode_gqa_workspace_size",
     "decode_gqa_num_splits", "decode_gqa_noalloc", "decode_mla_absorbed", "decode_mla_workspace_size", "decode_mla_num_splits",
     "prefill_gqa_causal", "merge_partials", "check_status", "last_error", "version",
     "selftest_bounded_wait", "mla_absorb_query", "mla_apply_uv", "decode_mla", "kv_append_rope",
@@ -30,6 +30,7 @@ __all__ = [
 
 ATTN_F32 = 0
 ATTN_BF16 = 1
+ATTN_FP8_E4M3 = 2
 ATTN_OK, ATTN_ERR_NULL, ATTN_ERR_SHAPE, ATTN_ERR_UNSUPPORTED = 0, -1, -2, -3
 ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = -4, -5, -6
 _STATUS = {0: "ATTN_OK", -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_SHAPE", -3: "ATTN_ERR_UNSUPPORTED",
@@ -56,6 +57,7 @@ _SIGNATURES = {
     "attn_decode_mla_workspace_size": (_c_size, [_c_int] * 6),
     "attn_decode_mla_num_splits": (_c_int, [_c_int] * 6),
     "attn_decode_mla_absorbed": (_c_int, [_vp] * 6 + [_c_int] * 4 + [_c_float] + [_c_int] * 3 + [_vp, _c_size, _vp]),
+    "attn_decode_gqa_fp8": (_c_int, [_vp] * 7 + [_c_int] * 4 + [_c_float] + [_c_int] * 3 + [_vp, _c_size, _vp]),
     "attn_kv_append_rope": (_c_int, [_vp] * 9 + [_c_int] * 6 + [_vp]),
     "attn_mla_append_rope": (_c_int, [_vp] * 9 + [_c_int] * 5 + [_vp]),
     "attn_mla_absorb_query": (_c_int, [_vp] * 3 + [_c_int] * 4 + [_vp]),
@@ -180,6 +182,43 @@ def decode_gqa(q, k_cache, v_cache, seq_lens, out=None, scale=None, max_s=None, 
     _check(lib().attn_decode_gqa(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(out),
                                  B, Hq, Hkv, D, scale, S_max, max_s, code, n_split,
                                  _ptr(workspace), ws_bytes, _stream()))
+    return out
+
+
+def decode_gqa_fp8(q, k_cache, v_cache, k_scale, v_scale, seq_lens, out=None, scale=None, max_s=None, n_split=0,
+                   workspace=None):
+    """decode_gqa over an E4M3 cache: cached value = e4m3(code) · the row's scale.
+
+    q [B, Hq, D] bf16; k_cache, v_cache [B, S_max, Hkv, D] uint8 codes (or float8_e4m3fn);
+    k_scale, v_scale [B, S_max, Hkv] fp32; seq_lens [B] int32. Returns out [B, Hq, D] fp32.
+    """
+    _need(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    k_cache = k_cache.view(torch.uint8) if k_cache.dtype == torch.float8_e4m3fn else k_cache
+    v_cache = v_cache.view(torch.uint8) if v_cache.dtype == torch.float8_e4m3fn else v_cache
+    _need(k_cache, "k_cache", torch.uint8, 4, dev)
+    _need(v_cache, "v_cache", torch.uint8, 4, dev)
+    _need(k_scale, "k_scale", torch.float32, 3, dev)
+    _need(v_scale, "v_scale", torch.float32, 3, dev)
+    _need(seq_lens, "seq_lens", torch.int32, 1, dev)
+    B, Hq, D = q.shape
+    _, S_max, Hkv, Dk = k_cache.shape
+    if (k_cache.shape[0] != B or Dk != D or v_cache.shape != k_cache.shape or seq_lens.shape[0] != B
+            or k_scale.shape != (B, S_max, Hkv) or v_scale.shape != k_scale.shape):
+        raise ValueError("inconsistent shapes for q, k_cache, v_cache, k_scale, v_scale, seq_lens")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    max_s = S_max if max_s is None else int(max_s)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    else:
+        _need(out, "out", torch.float32, 3, dev)
+    need = decode_gqa_workspace_size(B, Hq, Hkv, D, max_s, ATTN_FP8_E4M3, n_split)
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _check(lib().attn_decode_gqa_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                     _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D, scale, S_max, max_s, n_split,
+                                     _ptr(workspace), ws_bytes, _stream()))
     return out
 
 

@@ -90,13 +90,15 @@ SplitPlan plan_splits(int max_S, int tile, long blocks_per_split, int n_split_re
 
 constexpr int kFmaTile = 128;
 
-bool gqa_use_fma(attn_dtype dtype) { return dtype == ATTN_F32; }
+bool gqa_use_fma(attn_dtype dtype) { return dtype == ATTN_F32 || dtype == ATTN_FP8_E4M3; }
 
 SplitPlan gqa_plan(int B, int Hq, int Hkv, int D, int max_S, attn_dtype dtype, int n_split) {
     const int G = Hq / Hkv;
     if (gqa_use_fma(dtype)) {
         const int hb = (G % 8 == 0) ? 8 : (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
-        return plan_splits(max_S, kFmaTile, (long)B * Hkv * (G / hb), n_split, 2);
+        // 128-thread blocks: up to 8 resident per SM for 1-2 stacked heads (≈40 registers a
+        // thread), 4 for 4-8 heads (≈110 registers)
+        return plan_splits(max_S, kFmaTile, (long)B * Hkv * (G / hb), n_split, 2, hb <= 2 ? 8 : 4);
     }
     // bf16: the balanced split; n_split reports the persistent grid size
     if (decode_tc_gqa_eligible(B, Hq, Hkv, D)) return SplitPlan{decode_tc_gqa_blocks(B, Hq, Hkv, n_split), 0};
@@ -122,8 +124,8 @@ int check_gqa_shapes(int B, int Hq, int Hkv, int D, int S_max, int max_S, attn_d
         return fail(ATTN_ERR_SHAPE, "n_split=%d must lie in [0, 256]", n_split);
     if (D != 64 && D != 96 && D != 128)
         return fail(ATTN_ERR_UNSUPPORTED, "head width D=%d not built (64, 96, 128)", D);
-    if (dtype != ATTN_F32 && dtype != ATTN_BF16)
-        return fail(ATTN_ERR_UNSUPPORTED, "dtype %d not built (ATTN_F32, ATTN_BF16)", (int)dtype);
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16 && dtype != ATTN_FP8_E4M3)
+        return fail(ATTN_ERR_UNSUPPORTED, "dtype %d not built (ATTN_F32, ATTN_BF16, ATTN_FP8_E4M3)", (int)dtype);
     if (Hq / Hkv > 128)
         return fail(ATTN_ERR_UNSUPPORTED, "group size Hq/Hkv=%d above 128", Hq / Hkv);
     return ATTN_OK;
@@ -168,6 +170,45 @@ MLAKV_API const char *attn_version(void) { return "mlakv 0.1.0 (sm_103a)"; }
 
 // ======================================================================== GQA decode
 
+namespace {
+
+// The CUDA-core decode (fp32 or E4M3 cache): split plan, workspace check, decode, merge.
+int decode_fma(DecodeGqaArgs a, int B, int Hq, int Hkv, int D, float scale, int S_max, int max_S,
+               attn_dtype dtype, int n_split, void *workspace, size_t ws_bytes, cudaStream_t s, const char *who) {
+    const SplitPlan p = gqa_plan(B, Hq, Hkv, D, max_S, dtype, n_split);
+    const size_t need = partials_bytes(B, Hq, D, p.n_split);
+    if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
+        return fail(ATTN_ERR_WORKSPACE, "%s: workspace of %zu bytes (16-byte aligned) needed, got %zu at %p", who,
+                    need, workspace ? ws_bytes : (size_t)0, workspace);
+    a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.D = D;
+    a.scale_log2 = scale * kLog2e;
+    a.S_max = S_max;
+    a.n_split = p.n_split;
+    a.split_len = p.split_len;
+    if (p.n_split > 1) {
+        const size_t rows = (size_t)B * Hq;
+        a.o_part = static_cast<float *>(workspace);
+        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                               align_up(rows * p.n_split * D * sizeof(float), 256));
+    }
+    char what[96];
+    cudaError_t e = dtype == ATTN_FP8_E4M3 ? launch_decode_gqa_fp8(a, s) : launch_decode_gqa_f32(a, s);
+    if (e != cudaSuccess) {
+        snprintf(what, sizeof(what), "%s: decode kernel launch", who);
+        return cuda_fail(e, what);
+    }
+    if (p.n_split > 1) {
+        e = launch_merge(a.o_part, a.lse_part, a.out, B * Hq, p.n_split, D, s);
+        if (e != cudaSuccess) {
+            snprintf(what, sizeof(what), "%s: merge kernel launch", who);
+            return cuda_fail(e, what);
+        }
+    }
+    return ok();
+}
+
+}  // namespace
+
 MLAKV_API int attn_decode_gqa_num_splits(int B, int Hq, int Hkv, int D, int max_S, attn_dtype dtype,
                                          int n_split) {
     const int rc = check_gqa_shapes(B, Hq, Hkv, D, max_S > 0 ? max_S : 1, max_S, dtype, n_split);
@@ -193,6 +234,8 @@ MLAKV_API int attn_decode_gqa(const void *q, const void *k_cache, const void *v_
         return fail(ATTN_ERR_NULL, "attn_decode_gqa: q, k_cache, v_cache, seq_lens and out must be non-NULL");
     int rc = check_gqa_shapes(B, Hq, Hkv, D, S_max, max_S, dtype, n_split);
     if (rc != ATTN_OK) return rc;
+    if (dtype == ATTN_FP8_E4M3)
+        return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_gqa: an fp8 cache needs its scales; call attn_decode_gqa_fp8");
     if (!isfinite(scale)) return fail(ATTN_ERR_SHAPE, "scale must be finite");
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(seq_lens))
         return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_gqa: every pointer must be 16-byte aligned");
@@ -228,32 +271,30 @@ MLAKV_API int attn_decode_gqa(const void *q, const void *k_cache, const void *v_
         if (e != cudaSuccess) return cuda_fail(e, "attn_decode_gqa: kernel launch");
         return ok();
     }
-    const SplitPlan p = gqa_plan(B, Hq, Hkv, D, max_S, dtype, n_split);
-    const size_t need = partials_bytes(B, Hq, D, p.n_split);
-    if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
-        return fail(ATTN_ERR_WORKSPACE, "attn_decode_gqa: workspace of %zu bytes (16-byte aligned) needed, "
-                    "got %zu at %p", need, workspace ? ws_bytes : (size_t)0, workspace);
-
     DecodeGqaArgs a{};
     a.q = q; a.k = k_cache; a.v = v_cache; a.seq_lens = seq_lens; a.out = out;
-    a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.D = D;
-    a.scale_log2 = scale * kLog2e;
-    a.S_max = S_max;
-    a.n_split = p.n_split;
-    a.split_len = p.split_len;
-    if (p.n_split > 1) {
-        const size_t rows = (size_t)B * Hq;
-        a.o_part = static_cast<float *>(workspace);
-        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                               align_up(rows * p.n_split * D * sizeof(float), 256));
-    }
-    cudaError_t e = launch_decode_gqa_f32(a, s);
-    if (e != cudaSuccess) return cuda_fail(e, "attn_decode_gqa: decode kernel launch");
-    if (p.n_split > 1) {
-        e = launch_merge(a.o_part, a.lse_part, out, B * Hq, p.n_split, D, s);
-        if (e != cudaSuccess) return cuda_fail(e, "attn_decode_gqa: merge kernel launch");
-    }
-    return ok();
+    return decode_fma(a, B, Hq, Hkv, D, scale, S_max, max_S, dtype, n_split, workspace, ws_bytes, s,
+                      "attn_decode_gqa");
+}
+
+MLAKV_API int attn_decode_gqa_fp8(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
+                                  const float *v_scale, const int *seq_lens, float *out, int B, int Hq, int Hkv,
+                                  int D, float scale, int S_max, int max_S, int n_split, void *workspace,
+                                  size_t ws_bytes, mlakv_stream_t stream) {
+    if (!q || !k_cache || !v_cache || !k_scale || !v_scale || !seq_lens || !out)
+        return fail(ATTN_ERR_NULL, "attn_decode_gqa_fp8: q, k_cache, v_cache, k_scale, v_scale, seq_lens and out "
+                    "must be non-NULL");
+    int rc = check_gqa_shapes(B, Hq, Hkv, D, S_max, max_S, ATTN_FP8_E4M3, n_split);
+    if (rc != ATTN_OK) return rc;
+    if (!isfinite(scale)) return fail(ATTN_ERR_SHAPE, "scale must be finite");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_scale) ||
+        !aligned16(v_scale) || !aligned16(out) || !aligned16(seq_lens))
+        return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_gqa_fp8: every pointer must be 16-byte aligned");
+    DecodeGqaArgs a{};
+    a.q = q; a.k = k_cache; a.v = v_cache; a.seq_lens = seq_lens; a.out = out;
+    a.k_scale = k_scale; a.v_scale = v_scale;
+    return decode_fma(a, B, Hq, Hkv, D, scale, S_max, max_S, ATTN_FP8_E4M3, n_split, workspace, ws_bytes,
+                      reinterpret_cast<cudaStream_t>(stream), "attn_decode_gqa_fp8");
 }
 
 // ======================================================================== MLA decode

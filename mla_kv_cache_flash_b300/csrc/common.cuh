@@ -27,6 +27,8 @@ struct DecodeGqaArgs {
     int S_max;
     int n_split;
     int split_len;          // tokens per split (multiple of the kernel's tile)
+    const float *k_scale;   // [B, S_max, Hkv] per-row scales of an E4M3 cache, else unused
+    const float *v_scale;
 };
 
 // GQA decode over a bf16 cache with the balanced ("stream-K") split of streamk.cuh.
@@ -65,6 +67,8 @@ struct PrefillArgs {
 
 // K1: split-KV GQA decode. Writes out directly when n_split == 1, else the partials.
 MLAKV_HIDDEN cudaError_t launch_decode_gqa_f32(const DecodeGqaArgs &a, cudaStream_t s);
+// K1 over an E4M3 cache with per-row K and V scales (bf16 query), same grid and partials.
+MLAKV_HIDDEN cudaError_t launch_decode_gqa_fp8(const DecodeGqaArgs &a, cudaStream_t s);
 // K1 (bf16, balanced): the persistent grid size and the workspace it needs; the decode kernel
 // also combines the segments it splits between blocks.
 MLAKV_HIDDEN int decode_gqa_stream_blocks(int B, int Hq, int Hkv, int D, int n_split);

@@ -1,7 +1,12 @@
-// K1 (CUDA-core form): split-KV decode for GQA/MHA/MQA over an fp32 cache, fp32 FMA.
+// K1 (CUDA-core form): split-KV decode for GQA/MHA/MQA over an fp32 cache, or over an
+// 8-bit E4M3 cache with one fp32 scale per cached row of K and of V ("MHA, MQA và GQA"
+// ebook: fp8 halves every byte of the cache), fp32 FMA.
 //
 // The fp32 cache stays off the tensor cores, which would round it (TF32 keeps 10 mantissa
-// bits) and break the fp32 tolerance; the bf16 cache has its own tensor-core kernel. One thread block handles one (sequence b, KV head j, split, block of HB query
+// bits) and break the fp32 tolerance; the bf16 cache has its own tensor-core kernel. E4M3
+// codes widen exactly to fp32; a row's K scale multiplies its finished dot products and its
+// V scale multiplies its softmax weight before P·V (the normaliser takes the unscaled
+// weight), so no element is rescaled. One thread block handles one (sequence b, KV head j, split, block of HB query
 // heads of j's group). The HB heads are stacked so each K/V element is loaded once per
 // block and feeds all HB heads ("模型架构｜MQA & GQA 调研", section "代码": repeat_kv
 // would instead re-read each K/V byte once per query head).
@@ -17,7 +22,10 @@
 // writes out = O / l; otherwise it writes the normalised partial and lse = ln Σ e^s for K2.
 #include "common.cuh"
 
+#include <cuda_fp8.h>
 #include <math.h>
+
+#include <type_traits>
 
 namespace mlakv {
 namespace {
@@ -29,10 +37,34 @@ __device__ __forceinline__ void load8(const float *p, float (&x)[8]) {
     x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
-__device__ __forceinline__ float to_f(float x) { return x; }
+// eight E4M3 codes (8-byte aligned) → fp32, exactly
+__device__ __forceinline__ void load8(const uint8_t *p, float (&x)[8]) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+    const uint32_t w[2] = {u.x, u.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+                static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * k)) & 0xffffu), __NV_E4M3);
+            const float2 f = __half22float2(__half2(hr));
+            x[4 * i + 2 * k] = f.x;
+            x[4 * i + 2 * k + 1] = f.y;
+        }
+    }
+}
 
-template <typename T, int D, int HB>
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float load1(const float *p) { return __ldg(p); }
+__device__ __forceinline__ float load1(const uint8_t *p) {
+    return __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(__ldg(p)), __NV_E4M3)));
+}
+
+// TQ: query type (fp32, or bf16 beside an E4M3 cache); T: cache element (fp32 or E4M3 code).
+template <typename TQ, typename T, int D, int HB>
 __global__ void __launch_bounds__(128) decode_gqa_fma_kernel(const DecodeGqaArgs a) {
+    constexpr bool kScaled = std::is_same<T, uint8_t>::value;
     constexpr int DPL = D / 32;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -51,7 +83,7 @@ __global__ void __launch_bounds__(128) decode_gqa_fma_kernel(const DecodeGqaArgs
     __shared__ float l_s[4][HB];
     __shared__ __align__(16) float o_s[4][HB][D];
 
-    const T *qg = static_cast<const T *>(a.q) + ((size_t)b * a.Hq + h0) * D;
+    const TQ *qg = static_cast<const TQ *>(a.q) + ((size_t)b * a.Hq + h0) * D;
     for (int i = threadIdx.x; i < HB * D; i += 128) q_s[i / D][i % D] = to_f(qg[i]) * a.scale_log2;
     __syncthreads();
 
@@ -74,6 +106,7 @@ __global__ void __launch_bounds__(128) decode_gqa_fma_kernel(const DecodeGqaArgs
         float s[HB];
 #pragma unroll
         for (int h = 0; h < HB; ++h) s[h] = 0.f;
+        float sv = 1.f;                         // the row's V scale (E4M3 cache)
         if (valid) {
             const T *kr = kb + (size_t)t * row_stride;
 #pragma unroll 2
@@ -84,6 +117,13 @@ __global__ void __launch_bounds__(128) decode_gqa_fma_kernel(const DecodeGqaArgs
                 for (int h = 0; h < HB; ++h)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) s[h] = fmaf(q_s[h][c + e], x[e], s[h]);
+            }
+            if constexpr (kScaled) {
+                const size_t srow = ((size_t)b * a.S_max + t) * a.Hkv + j;
+                const float sk = __ldg(a.k_scale + srow);
+                sv = __ldg(a.v_scale + srow);
+#pragma unroll
+                for (int h = 0; h < HB; ++h) s[h] *= sk;
             }
         }
         float p[HB];
@@ -103,10 +143,10 @@ __global__ void __launch_bounds__(128) decode_gqa_fma_kernel(const DecodeGqaArgs
             const T *vr = vb + (size_t)(t0 + tt) * row_stride;
             float vv[DPL];
 #pragma unroll
-            for (int i = 0; i < DPL; ++i) vv[i] = to_f(vr[lane + 32 * i]);
+            for (int i = 0; i < DPL; ++i) vv[i] = load1(vr + lane + 32 * i);
 #pragma unroll
             for (int h = 0; h < HB; ++h) {
-                const float pt = __shfl_sync(0xffffffffu, p[h], tt);
+                const float pt = __shfl_sync(0xffffffffu, kScaled ? p[h] * sv : p[h], tt);
 #pragma unroll
                 for (int i = 0; i < DPL; ++i) o[h][i] = fmaf(pt, vv[i], o[h][i]);
             }
@@ -152,32 +192,35 @@ __global__ void __launch_bounds__(128) decode_gqa_fma_kernel(const DecodeGqaArgs
     }
 }
 
-template <typename T, int D>
+template <typename TQ, typename T, int D>
 cudaError_t launch_d(const DecodeGqaArgs &a, cudaStream_t s) {
     const int G = a.Hq / a.Hkv;
     const int hb = (G % 8 == 0) ? 8 : (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
     const dim3 grid(a.n_split, a.Hkv * (G / hb), a.B);
     switch (hb) {
-        case 8: decode_gqa_fma_kernel<T, D, 8><<<grid, 128, 0, s>>>(a); break;
-        case 4: decode_gqa_fma_kernel<T, D, 4><<<grid, 128, 0, s>>>(a); break;
-        case 2: decode_gqa_fma_kernel<T, D, 2><<<grid, 128, 0, s>>>(a); break;
-        default: decode_gqa_fma_kernel<T, D, 1><<<grid, 128, 0, s>>>(a); break;
+        case 8: decode_gqa_fma_kernel<TQ, T, D, 8><<<grid, 128, 0, s>>>(a); break;
+        case 4: decode_gqa_fma_kernel<TQ, T, D, 4><<<grid, 128, 0, s>>>(a); break;
+        case 2: decode_gqa_fma_kernel<TQ, T, D, 2><<<grid, 128, 0, s>>>(a); break;
+        default: decode_gqa_fma_kernel<TQ, T, D, 1><<<grid, 128, 0, s>>>(a); break;
     }
     return cudaGetLastError();
 }
 
-template <typename T>
+template <typename TQ, typename T>
 cudaError_t launch_t(const DecodeGqaArgs &a, cudaStream_t s) {
     switch (a.D) {
-        case 64: return launch_d<T, 64>(a, s);
-        case 96: return launch_d<T, 96>(a, s);
-        case 128: return launch_d<T, 128>(a, s);
+        case 64: return launch_d<TQ, T, 64>(a, s);
+        case 96: return launch_d<TQ, T, 96>(a, s);
+        case 128: return launch_d<TQ, T, 128>(a, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_decode_gqa_f32(const DecodeGqaArgs &a, cudaStream_t s) { return launch_t<float>(a, s); }
+cudaError_t launch_decode_gqa_f32(const DecodeGqaArgs &a, cudaStream_t s) { return launch_t<float, float>(a, s); }
+cudaError_t launch_decode_gqa_fp8(const DecodeGqaArgs &a, cudaStream_t s) {
+    return launch_t<__nv_bfloat16, uint8_t>(a, s);
+}
 
 }  // namespace mlakv

@@ -83,7 +83,7 @@ def test_gqa_divisibility_message(L):
     assert "does not divide" in mk.last_error()
 
 
-@pytest.mark.parametrize("kw", [dict(D=80), dict(D=256), dict(dtype=2), dict(Hq=256, Hkv=1), dict(q=PU),
+@pytest.mark.parametrize("kw", [dict(D=80), dict(D=256), dict(dtype=2), dict(dtype=3), dict(Hq=256, Hkv=1), dict(q=PU),
                                 dict(k=PU), dict(out=PU)])
 def test_gqa_unsupported(L, kw):
     assert gqa(L, **kw) == UNSUP
@@ -140,6 +140,36 @@ def test_mla_workspace(L):
     need = L.attn_decode_mla_workspace_size(2, 16, 128, 48, 4096, 4)
     assert need >= 2 * 16 * 4 * 128 * 4
     assert mla(L, S_max=4096, max_S=4096, n_split=4) == WS
+
+
+def fp8(L, q=P, k=P, v=P, ks=P, vs=P, lens=P, out=P, B=2, Hq=8, Hkv=4, D=96, scale=0.1, S_max=128, max_S=128,
+        n_split=1, ws=N0, ws_bytes=0):
+    return L.attn_decode_gqa_fp8(q, k, v, ks, vs, lens, out, B, Hq, Hkv, D, scale, S_max, max_S, n_split, ws,
+                                 ws_bytes, S0)
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v", "ks", "vs", "lens", "out"])
+def test_fp8_null_pointers(L, which):
+    assert fp8(L, **{which: N0}) == NULL
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(Hq=8, Hkv=3), dict(max_S=129), dict(scale=float("inf"))])
+def test_fp8_bad_shapes(L, kw):
+    assert fp8(L, **kw) == SHAPE
+
+
+@pytest.mark.parametrize("kw", [dict(D=80), dict(ks=PU), dict(k=PU)])
+def test_fp8_unsupported(L, kw):
+    assert fp8(L, **kw) == UNSUP
+
+
+def test_fp8_workspace(L):
+    # the CUDA-core plan: partials for every split when there is more than one
+    n = L.attn_decode_gqa_num_splits(2, 8, 4, 96, 4096, 2, 0)
+    assert n > 1
+    assert L.attn_decode_gqa_workspace_size(2, 8, 4, 96, 4096, 2, 0) == \
+        L.attn_decode_gqa_workspace_size(2, 8, 4, 96, 4096, 0, 0)
+    assert fp8(L, S_max=4096, max_S=4096, n_split=0) == WS
 
 
 def absorb(L, qn=P, wuk=P, ql=P, B=2, Hq=16, dn=96, r=128):

@@ -12,6 +12,8 @@ Recipe (every workload):
   * lengths: drawn on the host with ``numpy.random.default_rng(seed)``, integers
     uniform over the inclusive range, stored as int32;
   * seeds: ``1000 + workload index``; a sub-case k of a workload adds ``10 * k``;
+  * an fp8 cache (``fp8_decode_inputs``): fp32 draws stored as E4M3 codes with one fp32
+    scale per cached row, the row's largest magnitude over 448;
   * a decode step's new token (``append_inputs``): q, k_new, v_new drawn as above, and a
     rotation table of (cos, sin) of angles uniform in [-π, π), one per position and pair.
 
@@ -199,6 +201,24 @@ def append_inputs(batch, n_q_heads, n_kv_heads, head_dim, s_max, device="cpu", s
     ang = (torch.rand((s_max, rot_dim // 2), generator=gen, device=device, dtype=torch.float32) * 2 - 1) * math.pi
     cis = torch.stack([torch.cos(ang), torch.sin(ang)], dim=-1).contiguous()
     return {"q": q, "k_new": k_new, "v_new": v_new, "freqs_cis": cis}
+
+
+def fp8_decode_inputs(w, device="cpu", seed=None):
+    """A decode workload with an E4M3 cache: q [B,Hq,D] bf16; the K and V rows are fp32
+    N(0,1) draws stored as E4M3 codes [B,S_max,Hkv,D] uint8 with one fp32 scale per row
+    [B,S_max,Hkv] (the row's largest magnitude over 448, so the codes span the format's
+    range; the conversion is torch's ``float8_e4m3fn`` cast); seq_lens as ``decode_inputs``."""
+    seed = w.seed if seed is None else seed
+    gen = _gen(device, seed)
+    q = _randn((w.batch, w.n_q_heads, w.head_dim), gen, device, "bf16")
+    out = {"q": q}
+    for name in ("k", "v"):
+        x = _randn((w.batch, w.s_max, w.n_kv_heads, w.head_dim), gen, device, "fp32")
+        sc = (x.abs().amax(dim=-1) / 448.0).clamp_min(1e-12)
+        out[name + "_cache"] = (x / sc[..., None]).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+        out[name + "_scale"] = sc.contiguous()
+    out["seq_lens"] = torch.from_numpy(draw_lengths(w.batch, w.lengths, w.length_range, seed)).to(device)
+    return out
 
 
 def to_f64(t):
