@@ -1,7 +1,8 @@
 """CPU fp64 oracle for KV-cache attention: GQA/MHA/MQA decode, causal GQA prefill,
 MLA (absorbed and decompressed), the log-sum-exp merge of split partials, the rotary
-embedding and cache append of a decode step, decode over an fp8 (E4M3) cache, and the
-KV-cache byte/parameter accounting the pages print.
+embedding and cache append of a decode step, decode over an fp8 (E4M3) cache, chunked
+prefill over an existing cache (GQA and MLA), and the KV-cache byte/parameter accounting
+the pages print.
 
 This package is TEST INFRASTRUCTURE. It is the plain, slow definition that the CUDA
 library is checked against. Only the test suite, ``__graft_entry__.smoke()`` and the
@@ -55,5 +56,10 @@ from .fp8 import (  # noqa: F401
     e4m3_to_float,
     dequantize,
     decode_gqa_fp8,
+)
+from .chunked import (  # noqa: F401
+    prefill_gqa_chunked,
+    mla_prefill_absorbed,
+    mla_prefill_naive,
 )
 from . import accounting  # noqa: F401

@@ -510,3 +510,88 @@ def check_fp8_decode_identities(decode_gqa_fp8, e4m3_to_float, decode_gqa):
                 kd[b, t, j] = [x * c["ks"][b, t, j] for x in kd[b, t, j]]
                 vd[b, t, j] = [x * c["vs"][b, t, j] for x in vd[b, t, j]]
     assert np.abs(got - brute_decode(c["q"], kd, vd, c["lens"], 0.3)).max() <= TOL_EXACT
+
+
+# ----------------------------------------------------------------------------- chunked prefill
+
+def chunk_case(seed, n_q=4, n_kv=2, d=6, s_max=12, chunks=((3, 4), (0, 5), (7, 1), (2, 0))):
+    """chunks: (start_pos, n_new) per sequence; the cache holds start_pos + n_new rows."""
+    rng = _rng(seed)
+    bsz = len(chunks)
+    cu = np.concatenate([[0], np.cumsum([n for _, n in chunks])])
+    return dict(q=rng.standard_normal((int(cu[-1]), n_q, d)), k=rng.standard_normal((bsz, s_max, n_kv, d)),
+                v=rng.standard_normal((bsz, s_max, n_kv, d)), cu=cu, start=np.array([s for s, _ in chunks]))
+
+
+def check_chunked_sdpa(prefill_gqa_chunked):
+    """torch SDPA in float64 over repeat_interleave'd heads, with the mask written as the rule
+    'new token i of a chunk at start_pos sees cached columns 0 .. start_pos + i'."""
+    c = chunk_case(87)
+    scale = 0.37
+    got = prefill_gqa_chunked(c["q"], c["k"], c["v"], c["cu"], c["start"], scale)
+    g = c["q"].shape[1] // c["k"].shape[2]
+    for b in range(len(c["start"])):
+        lo, hi, s = int(c["cu"][b]), int(c["cu"][b + 1]), int(c["start"][b])
+        if hi == lo:
+            continue
+        n, keys = hi - lo, s + hi - lo
+        q = torch.from_numpy(c["q"][lo:hi]).transpose(0, 1)                              # [Hq, n, D]
+        k = torch.from_numpy(c["k"][b, :keys]).repeat_interleave(g, dim=1).transpose(0, 1)
+        v = torch.from_numpy(c["v"][b, :keys]).repeat_interleave(g, dim=1).transpose(0, 1)
+        mask = torch.tensor([[col <= s + row for col in range(keys)] for row in range(n)])
+        ref = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale).transpose(0, 1).numpy()
+        assert np.abs(got[lo:hi] - ref).max() <= TOL_EXACT, b
+
+
+def check_chunked_ends(prefill_gqa_chunked, prefill_gqa_causal, decode_gqa):
+    """start_pos = 0 with the chunk as the whole cache is the causal prefill; each new token
+    is the decode step over the cache up to and including itself."""
+    c = chunk_case(88, chunks=((0, 5), (0, 3)))
+    k_packed = np.concatenate([c["k"][0, :5], c["k"][1, :3]])
+    v_packed = np.concatenate([c["v"][0, :5], c["v"][1, :3]])
+    got = prefill_gqa_chunked(c["q"], c["k"], c["v"], c["cu"], c["start"], 0.5)
+    assert np.abs(got - prefill_gqa_causal(c["q"], k_packed, v_packed, c["cu"], 0.5)).max() <= TOL_EXACT
+    c = chunk_case(89)
+    got = prefill_gqa_chunked(c["q"], c["k"], c["v"], c["cu"], c["start"], 0.5)
+    for b in range(len(c["start"])):
+        for i in range(int(c["cu"][b + 1] - c["cu"][b])):
+            row = int(c["cu"][b]) + i
+            lens = np.zeros(len(c["start"]), dtype=np.int64)
+            lens[b] = c["start"][b] + i + 1
+            dec = decode_gqa(np.broadcast_to(c["q"][row], (len(lens),) + c["q"].shape[1:]), c["k"], c["v"], lens, 0.5)
+            assert np.abs(got[row] - dec[b]).max() <= TOL_EXACT, (b, i)
+
+
+def check_mla_chunked(mla_prefill_absorbed, mla_prefill_naive, absorb_query, apply_uv, mla_decode_absorbed):
+    rng = _rng(90)
+    n_q, d_nope, r, dr, dv, s_max = 3, 4, 6, 4, 5, 10
+    chunks = ((4, 3), (0, 6), (9, 1))
+    cu = np.concatenate([[0], np.cumsum([n for _, n in chunks])])
+    start = np.array([s for s, _ in chunks])
+    T, bsz = int(cu[-1]), len(chunks)
+    q_nope, q_rope = rng.standard_normal((T, n_q, d_nope)), rng.standard_normal((T, n_q, dr))
+    c, kr = rng.standard_normal((bsz, s_max, r)), rng.standard_normal((bsz, s_max, dr))
+    w_uk, w_uv = rng.standard_normal((n_q, d_nope, r)) / 3, rng.standard_normal((n_q, dv, r)) / 3
+    scale = 1.0 / math.sqrt(d_nope + dr)
+    naive = mla_prefill_naive(q_nope, q_rope, c, kr, w_uk, w_uv, cu, start, scale)
+    # absorbed = decompressed (associativity), through the pinned absorption steps
+    q_lat = absorb_query(q_nope, w_uk)                 # the packed rows play the batch axis
+    o_lat = mla_prefill_absorbed(q_lat, q_rope, c, kr, cu, start, scale)
+    assert np.abs(apply_uv(o_lat, w_uv) - naive).max() <= 1e-10
+    # each new token is an absorbed decode step over the cache up to itself
+    for b in range(bsz):
+        for i in range(int(cu[b + 1] - cu[b])):
+            row = int(cu[b]) + i
+            lens = np.array([start[b] + i + 1])
+            dec = mla_decode_absorbed(q_lat[row][None], q_rope[row][None], c[b][None], kr[b][None], lens, scale)
+            assert np.abs(o_lat[row] - dec[0]).max() <= TOL_EXACT, (b, i)
+    # the article's own path for a whole prompt: SDPA with is_causal over the recombined heads
+    b = 1
+    lo, hi = int(cu[b]), int(cu[b + 1])
+    cb = torch.from_numpy(c[b, :hi - lo])
+    k = torch.stack([torch.cat([cb @ torch.from_numpy(w_uk[h]).T, torch.from_numpy(kr[b, :hi - lo])], 1)
+                     for h in range(n_q)])
+    v = torch.stack([cb @ torch.from_numpy(w_uv[h]).T for h in range(n_q)])
+    q = torch.from_numpy(np.concatenate([q_nope[lo:hi], q_rope[lo:hi]], axis=2)).transpose(0, 1)
+    ref = F.scaled_dot_product_attention(q, k, v, is_causal=True).transpose(0, 1).numpy()
+    assert np.abs(naive[lo:hi] - ref).max() <= TOL_EXACT

@@ -198,3 +198,24 @@ def test_fp8_dropped_value_scale_is_caught():
     def bad(q, kc, vc, ks, vs, lens, scale):
         return ofp8.decode_gqa_fp8(q, kc, vc, ks, np.ones_like(vs), lens, scale)
     _fails(pins.check_fp8_decode_identities, bad, ofp8.e4m3_to_float, oracle.decode_gqa)
+
+
+# ----------------------------------------------------------------------------- chunked prefill
+
+def test_chunked_top_left_mask_is_caught(monkeypatch):
+    from oracle import chunked as och
+    def top_left(q_len, k_len):      # is_causal's alignment: query i sees keys 0 .. i
+        return np.arange(k_len)[None, :] <= np.arange(q_len)[:, None]
+    monkeypatch.setattr(och, "causal_allowed", top_left)
+    _fails(pins.check_chunked_sdpa, och.prefill_gqa_chunked)
+    _fails(pins.check_mla_chunked, och.mla_prefill_absorbed, och.mla_prefill_naive, omla.absorb_query,
+           omla.apply_uv, omla.mla_decode_absorbed)
+
+
+def test_chunked_excluding_the_diagonal_is_caught(monkeypatch):
+    from oracle import chunked as och
+    def strict(q_len, k_len):
+        off = k_len - q_len
+        return np.arange(k_len)[None, :] < (np.arange(q_len)[:, None] + off) + (np.arange(k_len)[None, :] == 0)
+    monkeypatch.setattr(och, "causal_allowed", strict)
+    _fails(pins.check_chunked_ends, och.prefill_gqa_chunked, oracle.prefill_gqa_causal, oracle.decode_gqa)

@@ -183,3 +183,18 @@ def test_e4m3_closed_forms():
 
 def test_fp8_decode_identities():
     pins.check_fp8_decode_identities(oracle.decode_gqa_fp8, oracle.e4m3_to_float, oracle.decode_gqa)
+
+
+# ----------------------------------------------------------------------------- chunked prefill
+
+def test_chunked_prefill_matches_sdpa_with_offset_mask():
+    pins.check_chunked_sdpa(oracle.prefill_gqa_chunked)
+
+
+def test_chunked_prefill_ends_are_prefill_and_decode():
+    pins.check_chunked_ends(oracle.prefill_gqa_chunked, oracle.prefill_gqa_causal, oracle.decode_gqa)
+
+
+def test_mla_chunked_prefill():
+    pins.check_mla_chunked(oracle.mla_prefill_absorbed, oracle.mla_prefill_naive, oracle.absorb_query,
+                           oracle.apply_uv, oracle.mla_decode_absorbed)
