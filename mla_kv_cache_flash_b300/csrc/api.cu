@@ -33,7 +33,6 @@ int cuda_fail(cudaError_t e, const char *what) {
     return fail(ATTN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // SM count of the current device. The split plan must be the same for the workspace query
 // and the launch; both run on the caller's current device. Without a device (a host with
@@ -159,6 +158,7 @@ int check_mla_shapes(int B, int Hq, int r, int dr, int S_max, int max_S, int n_s
 
 // Lets other translation units report through attn_last_error().
 int report_error(int code, const char *message) { return fail(code, "%s", message); }
+int report_cuda_error(cudaError_t e, const char *what) { return cuda_fail(e, what); }
 
 }  // namespace mlakv
 

@@ -123,6 +123,11 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 // Sets the thread's attn_last_error() message and returns `code`.
 MLAKV_HIDDEN int report_error(int code, const char *message);
+// Sets the message to "<what>: <CUDA error name> (<description>)" and returns ATTN_ERR_CUDA.
+MLAKV_HIDDEN int report_cuda_error(cudaError_t e, const char *what);
+
+// Every pointer the C ABI takes must sit on a 16-byte boundary.
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ------------------------------------------------------------------ device helpers
 

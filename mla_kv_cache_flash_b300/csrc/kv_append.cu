@@ -102,17 +102,15 @@ __global__ void __launch_bounds__(128) append_rope_kernel(AppendArgs a) {
     }
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 int launch_append(const AppendArgs &a, int B, attn_dtype dtype, mlakv_stream_t stream, const char *who) {
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = dtype == ATTN_BF16 ? launch_pdl(append_rope_kernel<__nv_bfloat16>, dim3(B), dim3(128), 0, s, a)
                                        : launch_pdl(append_rope_kernel<float>, dim3(B), dim3(128), 0, s, a);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
-        char msg[256];
-        snprintf(msg, sizeof(msg), "%s: kernel launch: %s (%s)", who, cudaGetErrorName(e), cudaGetErrorString(e));
-        return report_error(ATTN_ERR_CUDA, msg);
+        char what[96];
+        snprintf(what, sizeof(what), "%s: kernel launch", who);
+        return report_cuda_error(e, what);
     }
     report_error(ATTN_OK, "");
     return ATTN_OK;

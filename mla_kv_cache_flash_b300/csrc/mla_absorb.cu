@@ -18,8 +18,6 @@
 #include "common.cuh"
 #include "ptx.cuh"
 
-#include <stdio.h>
-
 namespace mlakv {
 namespace {
 
@@ -184,14 +182,6 @@ __global__ void __launch_bounds__(kMaxThreads) apply_uv_kernel(const float *__re
     }
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-int cuda_error(cudaError_t e, const char *what) {
-    char msg[256];
-    snprintf(msg, sizeof(msg), "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
-    return report_error(ATTN_ERR_CUDA, msg);
-}
-
 }  // namespace
 }  // namespace mlakv
 
@@ -218,7 +208,7 @@ extern "C" __attribute__((visibility("default"))) int attn_mla_absorb_query(cons
                        reinterpret_cast<cudaStream_t>(stream), static_cast<const __nv_bfloat16 *>(q_nope),
                        static_cast<const __nv_bfloat16 *>(w_uk), static_cast<__nv_bfloat16 *>(q_lat), B, Hq, d_nope, r);
     if (e == cudaSuccess) e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_error(e, "attn_mla_absorb_query: kernel launch");
+    if (e != cudaSuccess) return report_cuda_error(e, "attn_mla_absorb_query: kernel launch");
     report_error(ATTN_OK, "");
     return ATTN_OK;
 }
@@ -244,7 +234,7 @@ extern "C" __attribute__((visibility("default"))) int attn_mla_apply_uv(const fl
                        reinterpret_cast<cudaStream_t>(stream), o_lat, static_cast<const __nv_bfloat16 *>(w_uv), out, B,
                        Hq, r, d_v);
     if (e == cudaSuccess) e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_error(e, "attn_mla_apply_uv: kernel launch");
+    if (e != cudaSuccess) return report_cuda_error(e, "attn_mla_apply_uv: kernel launch");
     report_error(ATTN_OK, "");
     return ATTN_OK;
 }
