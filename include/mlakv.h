@@ -266,6 +266,34 @@ int attn_prefill_gqa_causal(const void *q, const void *k, const void *v,
                             int total_tokens, mlakv_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Chunked prefill over an existing cache [MQA&GQA "代码": seqlen new tokens at start_pos,
+ * written into the cache first, see cached positions 0 .. start_pos + i]: new token i of
+ * sequence b attends rows 0 .. start_pos[b] + i of its cache (bottom-right causal).
+ *
+ *   q          [T, Hq, D]            dtype, the new tokens packed by sequence
+ *   k_cache, v_cache [B, S_max, Hkv, D] dtype, already holding the chunks
+ *   cu_q       [B+1] int32 on the device: 0, then running sums of the chunk lengths (= T)
+ *   start_pos  [B] int32 on the device: tokens cached before each chunk;
+ *              start_pos[b] + n_b <= S_max
+ *   out        [T, Hq, D] fp32, every row written.
+ *   max_kv     host-known bound on start_pos[b] + n_b (sizes the split), 0 .. S_max
+ *   dtype      ATTN_F32 or ATTN_BF16; D in {64, 96, 128}; 0 <= T <= 65535; T = 0 or
+ *              max_kv = 0 launches nothing.
+ *   n_split, workspace: as attn_decode_gqa with an fp32 cache (size from
+ *              attn_prefill_gqa_chunked_workspace_size).
+ * CUDA-core kernel (each new token is a decode over its visible cache), then the K2 merge.
+ * With n_b = 1 and start_pos = seq_lens − 1 this is one decode step.
+ * ------------------------------------------------------------------------------------- */
+size_t attn_prefill_gqa_chunked_workspace_size(int B, int T, int Hq, int Hkv, int D, int max_kv,
+                                               int n_split);
+
+int attn_prefill_gqa_chunked(const void *q, const void *k_cache, const void *v_cache,
+                             const int *cu_q, const int *start_pos, float *out,
+                             int B, int T, int Hq, int Hkv, int D, float scale,
+                             int S_max, int max_kv, attn_dtype dtype, int n_split,
+                             void *workspace, size_t ws_bytes, mlakv_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * Log-sum-exp merge of split partials (the combine step of split-KV decode):
  *   out[row] = Σ_i e^{lse[row,i] − M} o[row,i,:] / Σ_i e^{lse[row,i] − M},  M = max_i lse[row,i]
  * where o[row,i,:] is piece i's normalised output and lse[row,i] = ln Σ_t e^{s_t} over the

@@ -25,7 +25,7 @@ __all__ = [
     "decode_gqa_num_splits", "decode_gqa_noalloc", "decode_mla_absorbed", "decode_mla_workspace_size", "decode_mla_num_splits",
     "prefill_gqa_causal", "merge_partials", "check_status", "last_error", "version",
     "selftest_bounded_wait", "mla_absorb_query", "mla_apply_uv", "decode_mla", "kv_append_rope",
-    "mla_append_rope",
+    "mla_append_rope", "prefill_gqa_chunked",
 ]
 
 ATTN_F32 = 0
@@ -58,6 +58,8 @@ _SIGNATURES = {
     "attn_decode_mla_num_splits": (_c_int, [_c_int] * 6),
     "attn_decode_mla_absorbed": (_c_int, [_vp] * 6 + [_c_int] * 4 + [_c_float] + [_c_int] * 3 + [_vp, _c_size, _vp]),
     "attn_decode_gqa_fp8": (_c_int, [_vp] * 7 + [_c_int] * 4 + [_c_float] + [_c_int] * 3 + [_vp, _c_size, _vp]),
+    "attn_prefill_gqa_chunked_workspace_size": (_c_size, [_c_int] * 7),
+    "attn_prefill_gqa_chunked": (_c_int, [_vp] * 6 + [_c_int] * 5 + [_c_float] + [_c_int] * 4 + [_vp, _c_size, _vp]),
     "attn_kv_append_rope": (_c_int, [_vp] * 9 + [_c_int] * 6 + [_vp]),
     "attn_mla_append_rope": (_c_int, [_vp] * 9 + [_c_int] * 5 + [_vp]),
     "attn_mla_absorb_query": (_c_int, [_vp] * 3 + [_c_int] * 4 + [_vp]),
@@ -448,6 +450,45 @@ def prefill_gqa_causal(q, k, v, cu_seqlens, max_seqlen, out=None, scale=None):
         _need(out, "out", torch.float32, 3, dev)
     _check(lib().attn_prefill_gqa_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(out),
                                          B, Hq, Hkv, D, scale, int(max_seqlen), T, _stream()))
+    return out
+
+
+# ----------------------------------------------------------------------------- chunked prefill
+
+def prefill_gqa_chunked(q, k_cache, v_cache, cu_q, start_pos, max_kv, out=None, scale=None, n_split=0,
+                        workspace=None):
+    """New tokens over an existing cache, bottom-right causal: packed row i of sequence b
+    attends cache rows 0 .. start_pos[b] + i. q [T, Hq, D], caches [B, S_max, Hkv, D] (fp32 or
+    bf16, as q) already holding the chunks, cu_q [B+1] and start_pos [B] int32 on the device,
+    ``max_kv`` a host bound on start_pos + chunk length. Returns out [T, Hq, D] fp32."""
+    dt = q.dtype
+    if dt not in (torch.float32, torch.bfloat16):
+        raise TypeError("q must be float32 or bfloat16")
+    _need(q, "q", dt, 3)
+    dev = q.device
+    _need(k_cache, "k_cache", dt, 4, dev)
+    _need(v_cache, "v_cache", dt, 4, dev)
+    _need(cu_q, "cu_q", torch.int32, 1, dev)
+    _need(start_pos, "start_pos", torch.int32, 1, dev)
+    T, Hq, D = q.shape
+    B, S_max, Hkv, Dk = k_cache.shape
+    if Dk != D or v_cache.shape != k_cache.shape or cu_q.shape[0] != B + 1 or start_pos.shape[0] != B:
+        raise ValueError("inconsistent shapes for q, k_cache, v_cache, cu_q, start_pos")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    code = ATTN_F32 if dt == torch.float32 else ATTN_BF16
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=torch.float32, device=dev)
+    else:
+        _need(out, "out", torch.float32, 3, dev)
+    if T == 0:
+        return out                                   # nothing to attend (an empty tensor has no pointer)
+    need = int(lib().attn_prefill_gqa_chunked_workspace_size(B, T, Hq, Hkv, D, int(max_kv), n_split))
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _check(lib().attn_prefill_gqa_chunked(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_q), _ptr(start_pos),
+                                          _ptr(out), B, T, Hq, Hkv, D, scale, S_max, int(max_kv), code, n_split,
+                                          _ptr(workspace), ws_bytes, _stream()))
     return out
 
 

@@ -297,6 +297,80 @@ MLAKV_API int attn_decode_gqa_fp8(const void *q, const void *k_cache, const void
                       reinterpret_cast<cudaStream_t>(stream), "attn_decode_gqa_fp8");
 }
 
+// ======================================================================== chunked prefill
+
+namespace {
+
+constexpr int kMaxGridZ = 65535;
+
+int check_chunked(int B, int T, int Hq, int Hkv, int D, int S_max, int max_kv, attn_dtype dtype, int n_split,
+                  const char *who) {
+    if (T < 0 || T > kMaxGridZ)
+        return fail(ATTN_ERR_SHAPE, "%s: T=%d new tokens must lie in [0, %d]", who, T, kMaxGridZ);
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16)
+        return fail(ATTN_ERR_UNSUPPORTED, "%s: dtype must be ATTN_F32 or ATTN_BF16", who);
+    return check_gqa_shapes(B, Hq, Hkv, D, S_max, max_kv, dtype, n_split);
+}
+
+// Blocks per split: one per (query row, KV head, block of stacked heads), as for the
+// CUDA-core decode with the packed rows in place of the sequences.
+SplitPlan chunked_plan(int T, int Hq, int Hkv, int D, int max_kv, int n_split) {
+    return gqa_plan(T > 0 ? T : 1, Hq, Hkv, D, max_kv, ATTN_F32, n_split);
+}
+
+}  // namespace
+
+MLAKV_API size_t attn_prefill_gqa_chunked_workspace_size(int B, int T, int Hq, int Hkv, int D, int max_kv,
+                                                         int n_split) {
+    if (check_chunked(B, T, Hq, Hkv, D, max_kv > 0 ? max_kv : 1, max_kv, ATTN_F32, n_split,
+                      "attn_prefill_gqa_chunked_workspace_size") != ATTN_OK || T == 0)
+        return 0;
+    return partials_bytes(T, Hq, D, chunked_plan(T, Hq, Hkv, D, max_kv, n_split).n_split);
+}
+
+MLAKV_API int attn_prefill_gqa_chunked(const void *q, const void *k_cache, const void *v_cache, const int *cu_q,
+                                       const int *start_pos, float *out, int B, int T, int Hq, int Hkv, int D,
+                                       float scale, int S_max, int max_kv, attn_dtype dtype, int n_split,
+                                       void *workspace, size_t ws_bytes, mlakv_stream_t stream) {
+    const char *who = "attn_prefill_gqa_chunked";
+    if (!q || !k_cache || !v_cache || !cu_q || !start_pos || !out)
+        return fail(ATTN_ERR_NULL, "%s: q, k_cache, v_cache, cu_q, start_pos and out must be non-NULL", who);
+    const int rc = check_chunked(B, T, Hq, Hkv, D, S_max, max_kv, dtype, n_split, who);
+    if (rc != ATTN_OK) return rc;
+    if (!isfinite(scale)) return fail(ATTN_ERR_SHAPE, "scale must be finite");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(cu_q) || !aligned16(start_pos) ||
+        !aligned16(out))
+        return fail(ATTN_ERR_UNSUPPORTED, "%s: every pointer must be 16-byte aligned", who);
+    if (T == 0 || max_kv == 0) return ok();
+    const SplitPlan p = chunked_plan(T, Hq, Hkv, D, max_kv, n_split);
+    const size_t need = partials_bytes(T, Hq, D, p.n_split);
+    if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
+        return fail(ATTN_ERR_WORKSPACE, "%s: workspace of %zu bytes (16-byte aligned) needed, got %zu at %p", who,
+                    need, workspace ? ws_bytes : (size_t)0, workspace);
+    DecodeGqaArgs a{};
+    a.q = q; a.k = k_cache; a.v = v_cache; a.out = out;
+    a.cu_q = cu_q; a.start_pos = start_pos; a.n_seq = B;
+    a.B = T; a.Hq = Hq; a.Hkv = Hkv; a.D = D;
+    a.scale_log2 = scale * kLog2e;
+    a.S_max = S_max;
+    a.n_split = p.n_split;
+    a.split_len = p.split_len;
+    if (p.n_split > 1) {
+        const size_t rows = (size_t)T * Hq;
+        a.o_part = static_cast<float *>(workspace);
+        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                               align_up(rows * p.n_split * D * sizeof(float), 256));
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = dtype == ATTN_BF16 ? launch_prefill_chunked_bf16(a, s) : launch_decode_gqa_f32(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_prefill_gqa_chunked: kernel launch");
+    if (p.n_split > 1) {
+        e = launch_merge(a.o_part, a.lse_part, out, T * Hq, p.n_split, D, s);
+        if (e != cudaSuccess) return cuda_fail(e, "attn_prefill_gqa_chunked: merge kernel launch");
+    }
+    return ok();
+}
+
 // ======================================================================== MLA decode
 
 MLAKV_API int attn_decode_mla_num_splits(int B, int Hq, int r, int dr, int max_S, int n_split) {

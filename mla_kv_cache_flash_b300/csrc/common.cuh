@@ -29,6 +29,11 @@ struct DecodeGqaArgs {
     int split_len;          // tokens per split (multiple of the kernel's tile)
     const float *k_scale;   // [B, S_max, Hkv] per-row scales of an E4M3 cache, else unused
     const float *v_scale;
+    // chunked prefill (cu_q non-null): B counts the packed query rows, n_seq the sequences;
+    // row r of sequence b sees the cache up to start_pos[b] + (r - cu_q[b]) inclusive
+    const int *cu_q;        // [n_seq + 1]
+    const int *start_pos;   // [n_seq]
+    int n_seq;
 };
 
 // GQA decode over a bf16 cache with the balanced ("stream-K") split of streamk.cuh.
@@ -69,6 +74,9 @@ struct PrefillArgs {
 MLAKV_HIDDEN cudaError_t launch_decode_gqa_f32(const DecodeGqaArgs &a, cudaStream_t s);
 // K1 over an E4M3 cache with per-row K and V scales (bf16 query), same grid and partials.
 MLAKV_HIDDEN cudaError_t launch_decode_gqa_fp8(const DecodeGqaArgs &a, cudaStream_t s);
+// Chunked prefill (cu_q set) on the same kernel over a bf16 cache; an fp32 cache goes through
+// launch_decode_gqa_f32, which also takes cu_q.
+MLAKV_HIDDEN cudaError_t launch_prefill_chunked_bf16(const DecodeGqaArgs &a, cudaStream_t s);
 // K1 (bf16, balanced): the persistent grid size and the workspace it needs; the decode kernel
 // also combines the segments it splits between blocks.
 MLAKV_HIDDEN int decode_gqa_stream_blocks(int B, int Hq, int Hkv, int D, int n_split);

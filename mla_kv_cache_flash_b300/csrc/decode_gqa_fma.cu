@@ -1,15 +1,19 @@
 // K1 (CUDA-core form): split-KV decode for GQA/MHA/MQA over an fp32 cache, or over an
 // 8-bit E4M3 cache with one fp32 scale per cached row of K and of V ("MHA, MQA và GQA"
-// ebook: fp8 halves every byte of the cache), fp32 FMA.
+// ebook: fp8 halves every byte of the cache), fp32 FMA. The same kernel runs chunked
+// prefill ("模型架构｜MQA & GQA 调研", section "代码": new tokens at start_pos see the cache up
+// to their own position): each packed new-token row is a decode over its sequence's cache
+// with length start_pos + i + 1, for fp32 and bf16 caches.
 //
 // The fp32 cache stays off the tensor cores, which would round it (TF32 keeps 10 mantissa
-// bits) and break the fp32 tolerance; the bf16 cache has its own tensor-core kernel. E4M3
+// bits) and break the fp32 tolerance; the bf16 decode has its own tensor-core kernels. E4M3
 // codes widen exactly to fp32; a row's K scale multiplies its finished dot products and its
 // V scale multiplies its softmax weight before P·V (the normaliser takes the unscaled
-// weight), so no element is rescaled. One thread block handles one (sequence b, KV head j, split, block of HB query
-// heads of j's group). The HB heads are stacked so each K/V element is loaded once per
-// block and feeds all HB heads ("模型架构｜MQA & GQA 调研", section "代码": repeat_kv
-// would instead re-read each K/V byte once per query head).
+// weight), so no element is rescaled.
+//
+// One thread block handles one (query row, KV head j, split, block of HB query heads of j's
+// group). The HB heads are stacked so each K/V element is loaded once per block and feeds
+// all HB heads (repeat_kv would instead re-read each K/V byte once per query head).
 //
 // Per 128-token tile each of the 4 warps takes 32 tokens, one token per lane:
 //   scores   lane t computes s[h] = (scale·log2 e)·q_h·k_t for its token (q in shared memory,
@@ -54,15 +58,25 @@ __device__ __forceinline__ void load8(const uint8_t *p, float (&x)[8]) {
     }
 }
 
+// eight bf16 (16-byte aligned) → fp32, exactly
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&x)[8]) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) { x[2 * i] = bf16_lo(w[i]); x[2 * i + 1] = bf16_hi(w[i]); }
+}
+
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ float load1(const float *p) { return __ldg(p); }
+__device__ __forceinline__ float load1(const __nv_bfloat16 *p) { return __bfloat162float(p[0]); }
 __device__ __forceinline__ float load1(const uint8_t *p) {
     return __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(__ldg(p)), __NV_E4M3)));
 }
 
-// TQ: query type (fp32, or bf16 beside an E4M3 cache); T: cache element (fp32 or E4M3 code).
-template <typename TQ, typename T, int D, int HB>
+// TQ: query type (fp32, or bf16 beside a bf16 or E4M3 cache); T: cache element (fp32, bf16 or
+// E4M3 code); kChunk: rows are packed new tokens of chunked prefill (cu_q, start_pos).
+template <typename TQ, typename T, int D, int HB, bool kChunk>
 __global__ void __launch_bounds__(128) decode_gqa_fma_kernel(const DecodeGqaArgs a) {
     constexpr bool kScaled = std::is_same<T, uint8_t>::value;
     constexpr int DPL = D / 32;
@@ -72,9 +86,22 @@ __global__ void __launch_bounds__(128) decode_gqa_fma_kernel(const DecodeGqaArgs
     const int n_hblk = G / HB;
     const int j = blockIdx.y / n_hblk;
     const int h0 = j * G + (blockIdx.y % n_hblk) * HB;
-    const int b = blockIdx.z;
+    const int row = blockIdx.z;                 // query / output row
     const int split = blockIdx.x;
-    const int S = a.seq_lens[b];
+    int b = row, S;                             // cache batch index and visible length
+    if constexpr (kChunk) {
+        // chunked prefill: the sequence whose chunk holds packed row `row` is the b with
+        // cu_q[b] <= row < cu_q[b + 1] (cu_q non-decreasing, cu_q[0] = 0, cu_q[n_seq] = rows)
+        int lo = 0, hi = a.n_seq;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(a.cu_q + mid) <= row) lo = mid; else hi = mid;
+        }
+        b = lo;
+        S = __ldg(a.start_pos + b) + (row - __ldg(a.cu_q + b)) + 1;
+    } else {
+        S = a.seq_lens[row];
+    }
     const int t_begin = split * a.split_len;
     const int t_end = min(S, t_begin + a.split_len);
 
@@ -83,7 +110,7 @@ __global__ void __launch_bounds__(128) decode_gqa_fma_kernel(const DecodeGqaArgs
     __shared__ float l_s[4][HB];
     __shared__ __align__(16) float o_s[4][HB][D];
 
-    const TQ *qg = static_cast<const TQ *>(a.q) + ((size_t)b * a.Hq + h0) * D;
+    const TQ *qg = static_cast<const TQ *>(a.q) + ((size_t)row * a.Hq + h0) * D;
     for (int i = threadIdx.x; i < HB * D; i += 128) q_s[i / D][i % D] = to_f(qg[i]) * a.scale_log2;
     __syncthreads();
 
@@ -181,46 +208,51 @@ __global__ void __launch_bounds__(128) decode_gqa_fma_kernel(const DecodeGqaArgs
                 O = fmaf(o_s[w][h][d], f, O);
             }
         }
-        const size_t row = (size_t)b * a.Hq + h0 + h;
+        const size_t orow = (size_t)row * a.Hq + h0 + h;
         const float val = L > 0.f ? O / L : 0.f;
         if (a.n_split == 1) {
-            a.out[row * D + d] = val;
+            a.out[orow * D + d] = val;
         } else {
-            a.o_part[(row * a.n_split + split) * D + d] = val;
-            if (d == 0) a.lse_part[row * a.n_split + split] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+            a.o_part[(orow * a.n_split + split) * D + d] = val;
+            if (d == 0) a.lse_part[orow * a.n_split + split] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
         }
     }
 }
 
-template <typename TQ, typename T, int D>
+template <typename TQ, typename T, int D, bool kChunk>
 cudaError_t launch_d(const DecodeGqaArgs &a, cudaStream_t s) {
     const int G = a.Hq / a.Hkv;
     const int hb = (G % 8 == 0) ? 8 : (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
     const dim3 grid(a.n_split, a.Hkv * (G / hb), a.B);
     switch (hb) {
-        case 8: decode_gqa_fma_kernel<TQ, T, D, 8><<<grid, 128, 0, s>>>(a); break;
-        case 4: decode_gqa_fma_kernel<TQ, T, D, 4><<<grid, 128, 0, s>>>(a); break;
-        case 2: decode_gqa_fma_kernel<TQ, T, D, 2><<<grid, 128, 0, s>>>(a); break;
-        default: decode_gqa_fma_kernel<TQ, T, D, 1><<<grid, 128, 0, s>>>(a); break;
+        case 8: decode_gqa_fma_kernel<TQ, T, D, 8, kChunk><<<grid, 128, 0, s>>>(a); break;
+        case 4: decode_gqa_fma_kernel<TQ, T, D, 4, kChunk><<<grid, 128, 0, s>>>(a); break;
+        case 2: decode_gqa_fma_kernel<TQ, T, D, 2, kChunk><<<grid, 128, 0, s>>>(a); break;
+        default: decode_gqa_fma_kernel<TQ, T, D, 1, kChunk><<<grid, 128, 0, s>>>(a); break;
     }
     return cudaGetLastError();
 }
 
-template <typename TQ, typename T>
+template <typename TQ, typename T, bool kChunk>
 cudaError_t launch_t(const DecodeGqaArgs &a, cudaStream_t s) {
     switch (a.D) {
-        case 64: return launch_d<TQ, T, 64>(a, s);
-        case 96: return launch_d<TQ, T, 96>(a, s);
-        case 128: return launch_d<TQ, T, 128>(a, s);
+        case 64: return launch_d<TQ, T, 64, kChunk>(a, s);
+        case 96: return launch_d<TQ, T, 96, kChunk>(a, s);
+        case 128: return launch_d<TQ, T, 128, kChunk>(a, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_decode_gqa_f32(const DecodeGqaArgs &a, cudaStream_t s) { return launch_t<float, float>(a, s); }
+cudaError_t launch_decode_gqa_f32(const DecodeGqaArgs &a, cudaStream_t s) {
+    return a.cu_q ? launch_t<float, float, true>(a, s) : launch_t<float, float, false>(a, s);
+}
 cudaError_t launch_decode_gqa_fp8(const DecodeGqaArgs &a, cudaStream_t s) {
-    return launch_t<__nv_bfloat16, uint8_t>(a, s);
+    return launch_t<__nv_bfloat16, uint8_t, false>(a, s);
+}
+cudaError_t launch_prefill_chunked_bf16(const DecodeGqaArgs &a, cudaStream_t s) {
+    return launch_t<__nv_bfloat16, __nv_bfloat16, true>(a, s);
 }
 
 }  // namespace mlakv

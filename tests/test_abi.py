@@ -172,6 +172,37 @@ def test_fp8_workspace(L):
     assert fp8(L, S_max=4096, max_S=4096, n_split=0) == WS
 
 
+def chunked(L, q=P, k=P, v=P, cu=P, st=P, out=P, B=2, T=10, Hq=8, Hkv=4, D=96, scale=0.1, S_max=64, max_kv=64,
+            dt=1, n_split=1, ws=N0, ws_bytes=0):
+    return L.attn_prefill_gqa_chunked(q, k, v, cu, st, out, B, T, Hq, Hkv, D, scale, S_max, max_kv, dt, n_split, ws,
+                                      ws_bytes, S0)
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v", "cu", "st", "out"])
+def test_chunked_null_pointers(L, which):
+    assert chunked(L, **{which: N0}) == NULL
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(T=-1), dict(T=65536), dict(Hq=8, Hkv=3), dict(max_kv=65),
+                                dict(scale=float("nan"))])
+def test_chunked_bad_shapes(L, kw):
+    assert chunked(L, **kw) == SHAPE
+
+
+@pytest.mark.parametrize("kw", [dict(D=80), dict(dt=2), dict(cu=PU), dict(out=PU)])
+def test_chunked_unsupported(L, kw):
+    assert chunked(L, **kw) == UNSUP
+
+
+def test_chunked_empty_and_workspace(L):
+    assert chunked(L, T=0) == OK
+    assert chunked(L, max_kv=0) == OK
+    assert L.attn_prefill_gqa_chunked_workspace_size(2, 10, 8, 4, 96, 64, 1) == 0
+    need = L.attn_prefill_gqa_chunked_workspace_size(2, 10, 8, 4, 96, 4096, 4)
+    assert need >= 10 * 8 * 4 * 96 * 4
+    assert chunked(L, S_max=4096, max_kv=4096, n_split=4) == WS
+
+
 def absorb(L, qn=P, wuk=P, ql=P, B=2, Hq=16, dn=96, r=128):
     return L.attn_mla_absorb_query(qn, wuk, ql, B, Hq, dn, r, S0)
 

@@ -1,0 +1,81 @@
+"""Chunked prefill over an existing cache (attn_prefill_gqa_chunked) against the fp64 CPU
+oracle: new token i of a chunk at start_pos sees cache rows 0 .. start_pos + i.
+
+fp32 caches: max |Δ| ≤ 1e-5; bf16 caches: ≤ 3e-3 (bf16 inputs, fp32 arithmetic).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import mla_kv_cache_flash_b300 as mk
+import oracle
+import workloads as W
+from workloads import to_f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _case(chunks, hq, hkv, d, s_max, dtype, seed):
+    """chunks: (start_pos, n_new) per sequence; the cache already holds every chunk."""
+    w = W.DecodeWorkload("chunked", 6, len(chunks), hq, hkv, d, s_max, dtype, lengths=(1,) * len(chunks), sub=seed)
+    base = W.decode_inputs(w, DEV)                   # its caches serve as the sequences' caches
+    n = np.array([c for _, c in chunks])
+    cu = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    start = np.array([s for s, _ in chunks], dtype=np.int32)
+    g = torch.Generator(device=DEV).manual_seed(7000 + seed)
+    q = torch.randn((int(cu[-1]), hq, d), generator=g, device=DEV)
+    q = q.to(torch.bfloat16) if dtype == "bf16" else q
+    return q, base["k_cache"], base["v_cache"], cu, start, w.scale
+
+
+def _check(chunks, hq, hkv, d, s_max, dtype, seed, tol, n_splits=(0, 1, 3)):
+    q, k, v, cu, start, scale = _case(chunks, hq, hkv, d, s_max, dtype, seed)
+    ref = oracle.prefill_gqa_chunked(to_f64(q), to_f64(k), to_f64(v), cu, start, scale)
+    max_kv = int((start + np.diff(cu)).max())
+    for n_split in n_splits:
+        out = mk.prefill_gqa_chunked(q, k, v, torch.from_numpy(cu).to(DEV), torch.from_numpy(start).to(DEV), max_kv,
+                                     scale=scale, n_split=n_split)
+        torch.cuda.synchronize()
+        assert float(np.abs(to_f64(out) - ref).max()) <= tol, n_split
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(8, 4, 96), (8, 8, 64), (8, 1, 128), (32, 8, 128)])
+def test_chunked_fp32(hq, hkv, d):
+    # a chunk after a cached prefix, a chunk from the start, one token (a decode step), an
+    # empty chunk, and a chunk that ends at the cache's last row
+    _check(((300, 17), (0, 40), (999, 1), (5, 0), (200, 300)), hq, hkv, d, 1000, "fp32", hq + d, 1e-5)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(8, 4, 96), (32, 8, 128), (16, 1, 64)])
+def test_chunked_bf16(hq, hkv, d):
+    _check(((1000, 64), (0, 129), (2047, 1), (127, 128)), hq, hkv, d, 2048, "bf16", hq + 2 * d, 3e-3)
+
+
+def test_chunked_single_tokens_are_decode_steps():
+    """Chunks of one token at start_pos = length − 1 give the decode of that length."""
+    w = W.MINIMIND_GQA
+    inp = W.decode_inputs(w, DEV)
+    lens = inp["seq_lens"]
+    B = w.batch
+    cu = torch.arange(B + 1, dtype=torch.int32, device=DEV)
+    out = mk.prefill_gqa_chunked(inp["q"], inp["k_cache"], inp["v_cache"], cu, (lens - 1).contiguous(),
+                                 int(lens.max()), scale=w.scale)
+    dec = mk.decode_gqa(inp["q"], inp["k_cache"], inp["v_cache"], lens, scale=w.scale)
+    torch.cuda.synchronize()
+    ref = oracle.decode_gqa(to_f64(inp["q"]), to_f64(inp["k_cache"]), to_f64(inp["v_cache"]), lens.cpu().numpy(),
+                            w.scale)
+    assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3
+    assert float((out - dec).abs().max()) <= 3e-3
+
+
+def test_chunked_empty_batch_is_a_no_op():
+    q = torch.zeros((0, 8, 96), dtype=torch.bfloat16, device=DEV)
+    k = torch.zeros((2, 16, 4, 96), dtype=torch.bfloat16, device=DEV)
+    cu = torch.zeros(3, dtype=torch.int32, device=DEV)
+    st = torch.zeros(2, dtype=torch.int32, device=DEV)
+    out = mk.prefill_gqa_chunked(q, k, k, cu, st, 0)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 8, 96)
