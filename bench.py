@@ -368,6 +368,52 @@ class DecodeGqaFp8(DecodeGqa):
         return dict(super().describe(), cache_dtype="fp8_e4m3 + fp32 scale per row")
 
 
+class DecodeChunked(DecodeGqa):
+    """Chunks of 4 new tokens per sequence over the MiniMind caches (a speculative-decoding
+    style step): each sequence's last 4 cached rows are its chunk, so row i sees
+    length − 4 + i + 1 rows. Algorithmic bytes: each sequence's visible K/V once (as for the
+    decode of the full length); the kernel reads them once per new token."""
+    kernel_src = "mla_kv_cache_flash_b300/csrc/decode_gqa_fma.cu"
+    call = "attn_prefill_gqa_chunked call: "
+    n_new = 4
+
+    def __init__(self, w, device, rank, l2_bytes):
+        super().__init__(w, device, rank, l2_bytes)
+        B, n = w.batch, self.n_new
+        for i, s in enumerate(self.sets):
+            g = torch.Generator(device=device).manual_seed(w.seed + 700 + i + 1000 * rank)
+            s["q_chunk"] = torch.randn((B * n, w.n_q_heads, w.head_dim), generator=g, device=device).to(torch.bfloat16)
+            s["cu_q"] = torch.arange(0, B * n + 1, n, dtype=torch.int32, device=device)
+            s["start_pos"] = (s["seq_lens"] - n).clamp_min(0).contiguous()
+        self.out = torch.empty((B * n, w.n_q_heads, w.head_dim), dtype=torch.float32, device=device)
+        lib = self.mk.lib()
+        nb = int(lib.attn_prefill_gqa_chunked_workspace_size(B, B * n, w.n_q_heads, w.n_kv_heads, w.head_dim,
+                                                             self.max_s, 0))
+        self.ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=device)
+        self.launches_per_step = 2 if nb else 1
+
+    def _run(self, s):
+        self.mk.prefill_gqa_chunked(s["q_chunk"], s["k_cache"], s["v_cache"], s["cu_q"], s["start_pos"], self.max_s,
+                                    out=self.out, scale=self.w.scale, workspace=self.ws)
+
+    def step(self, i):
+        self._run(self.sets[i % len(self.sets)])
+
+    def host_inputs(self):
+        s = self.sets[0]
+        return {k: s[k].cpu().pin_memory() for k in ("q_chunk", "k_cache", "v_cache", "cu_q", "start_pos")}
+
+    def e2e_step(self, host, dev_bufs, out_host):
+        for k, t in host.items():
+            dev_bufs[k].copy_(t, non_blocking=True)
+        self._run(dev_bufs)
+        out_host.copy_(self.out, non_blocking=True)
+
+    def describe(self):
+        return dict(super().describe(), workload=self.name, new_tokens_per_sequence=self.n_new,
+                    launches="chunked prefill: 4 new tokens per sequence over its cache")
+
+
 class DecodeMla(DecodeGqa):
     kernel_src = "mla_kv_cache_flash_b300/csrc/decode_tc.cu"
     call = "attn_decode_mla_absorbed call: "
@@ -518,12 +564,14 @@ WORKLOADS = {
     "llama_hkv1": lambda: (DecodeGqa, W.LLAMA3_8B[1]),
     "mla": lambda: (DecodeMla, W.MINIMIND_MLA),
     "minimind_gqa_fp8": lambda: (DecodeGqaFp8, dataclasses.replace(W.MINIMIND_GQA, name=W.MINIMIND_GQA.name + "_fp8")),
+    "minimind_gqa_chunk4": lambda: (DecodeChunked, dataclasses.replace(W.MINIMIND_GQA, name=W.MINIMIND_GQA.name + "_chunk4")),
     "minimind_gqa_step": lambda: (DecodeGqaStep, dataclasses.replace(W.MINIMIND_GQA, name=W.MINIMIND_GQA.name + "_with_append")),
     "mla_step": lambda: (DecodeMlaStep, dataclasses.replace(W.MINIMIND_MLA, name=W.MINIMIND_MLA.name + "_full_step")),
     "prefill": lambda: (Prefill, W.PREFILL_UNIFORM),
     "prefill_ragged": lambda: (Prefill, W.PREFILL_RAGGED),
 }
-DEFAULT_STEPS = {"minimind_gqa": 60000, "minimind_gqa_step": 60000, "minimind_gqa_fp8": 60000, "llama_hkv32": 400, "llama_hkv8": 2000, "llama_hkv1": 10000,
+DEFAULT_STEPS = {"minimind_gqa": 60000, "minimind_gqa_step": 60000, "minimind_gqa_fp8": 60000,
+                 "minimind_gqa_chunk4": 20000, "llama_hkv32": 400, "llama_hkv8": 2000, "llama_hkv1": 10000,
                  "mla": 40000, "mla_step": 40000, "prefill": 2000, "prefill_ragged": 1500}
 
 
@@ -785,7 +833,7 @@ def main():
 
     also = []
     if not args.no_also and world == 1:
-        for name in ("minimind_gqa_step", "minimind_gqa_fp8", "llama_hkv32", "llama_hkv8", "llama_hkv1", "mla", "mla_step", "prefill",
+        for name in ("minimind_gqa_step", "minimind_gqa_fp8", "minimind_gqa_chunk4", "llama_hkv32", "llama_hkv8", "llama_hkv1", "mla", "mla_step", "prefill",
                      "prefill_ragged"):
             if name == args.workload:
                 continue
@@ -800,13 +848,13 @@ def main():
                              "tokens_per_s": s2.get("tokens_per_s"), "clocks": s2["clocks"],
                              "config": s2["config"]})
                 del r2
-            except mk.MlakvError as e:
-                also.append({"workload": w2.name, "error": str(e)})
+            except Exception as e:   # a secondary line must not cost the headline line
+                also.append({"workload": w2.name, "error": f"{type(e).__name__}: {e}"})
             torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu and not isinstance(res["wl"], (DecodeMlaStep, DecodeGqaStep,
-                                                                                   DecodeGqaFp8)):
+                                                                                   DecodeGqaFp8, DecodeChunked)):
         value, cores, sample, _ = cpu_oracle_rate(res["wl"], args.cpu_seconds)
         cpu = {"value": round(value, 4), "unit": head["unit"], "cores": cores, "kind": "oracle", "sample": sample}
 
@@ -839,7 +887,7 @@ def _cpu_workload(cls, w):
             self.lens = s["seq_lens"].numpy()
             self.n_split = None
             self.l2_note = "host memory"
-    if cls in (Prefill, DecodeMlaStep, DecodeGqaStep, DecodeGqaFp8):
+    if cls in (Prefill, DecodeMlaStep, DecodeGqaStep, DecodeGqaFp8, DecodeChunked):
         raise SystemExit("the oracle arm covers the single-call decode workloads")
     return HostOnly(w)
 

@@ -1,0 +1,53 @@
+"""bench.py's workload classes build on the CPU with the byte counts their roofline lines
+state (the GPU timing itself runs only on a GPU)."""
+
+
+import pytest
+
+import bench
+
+
+def _make(name):
+    cls, w = bench.WORKLOADS[name]()
+    return cls(w, "cpu", 0, 1), w
+
+
+def test_step_with_append_counts_the_cache_and_the_new_token():
+    wl, w = _make("minimind_gqa_step")
+    B, Hq, Hkv, D = w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim
+    cache = int(wl.lens.sum()) * 2 * Hkv * D * 2
+    assert wl.bytes_per_step == cache + B * (2 * Hq * D * 2 + 4 * Hkv * D * 2 + D * 4 + 8)
+    assert wl.launches_per_step == 2
+    s = wl.sets[0]
+    assert (s["pos"] == s["seq_lens"] - 1).all()
+
+
+def test_fp8_counts_codes_and_row_scales():
+    wl, w = _make("minimind_gqa_fp8")
+    assert wl.bytes_per_step == int(wl.lens.sum()) * 2 * w.n_kv_heads * (w.head_dim + 4)
+    assert wl.sets[0]["k_cache"].dtype.itemsize == 1
+    assert wl.describe()["workload"].endswith("_fp8")
+
+
+def test_chunked_counts_each_visible_row_once():
+    wl, w = _make("minimind_gqa_chunk4")
+    assert wl.bytes_per_step == int(wl.lens.sum()) * 2 * w.n_kv_heads * w.head_dim * 2
+    s = wl.sets[0]
+    assert s["q_chunk"].shape == (w.batch * 4, w.n_q_heads, w.head_dim)
+    assert s["cu_q"].tolist() == list(range(0, w.batch * 4 + 1, 4))
+    assert ((s["start_pos"] + 4) == s["seq_lens"]).all()
+
+
+def test_mla_full_step_counts_cache_and_weights():
+    wl, w = _make("mla_step")
+    cache = int(wl.lens.sum()) * (w.kv_lora_rank + w.rope_dim) * 2
+    weights = 2 * w.n_q_heads * w.nope_dim * w.kv_lora_rank * 2
+    assert wl.bytes_per_step == cache + weights
+    assert wl.launches_per_step == 3
+
+
+@pytest.mark.parametrize("name", ["minimind_gqa_step", "minimind_gqa_fp8", "minimind_gqa_chunk4", "mla_step"])
+def test_multi_launch_lines_have_no_oracle_arm(name):
+    cls, w = bench.WORKLOADS[name]()
+    with pytest.raises(SystemExit):
+        bench._cpu_workload(cls, w)
