@@ -1,7 +1,6 @@
 """bench.py's workload classes build on the CPU with the byte counts their roofline lines
 state (the GPU timing itself runs only on a GPU)."""
 
-
 import pytest
 
 import bench

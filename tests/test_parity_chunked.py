@@ -79,3 +79,22 @@ def test_chunked_empty_batch_is_a_no_op():
     out = mk.prefill_gqa_chunked(q, k, k, cu, st, 0)
     torch.cuda.synchronize()
     assert out.shape == (0, 8, 96)
+
+
+def test_chunked_minimind_four_new_tokens():
+    """The bench's chunked line: the MiniMind caches with each sequence's last 4 rows as its
+    chunk, every output against the oracle."""
+    w = W.MINIMIND_GQA
+    inp = W.decode_inputs(w, DEV)
+    lens = inp["seq_lens"]
+    B, n = w.batch, 4
+    g = torch.Generator(device=DEV).manual_seed(w.seed + 700)
+    q = torch.randn((B * n, w.n_q_heads, w.head_dim), generator=g, device=DEV).to(torch.bfloat16)
+    cu = torch.arange(0, B * n + 1, n, dtype=torch.int32, device=DEV)
+    start = (lens - n).contiguous()
+    out = mk.prefill_gqa_chunked(q, inp["k_cache"], inp["v_cache"], cu, start, int(lens.max()), scale=w.scale)
+    torch.cuda.synchronize()
+    ref = oracle.prefill_gqa_chunked(to_f64(q), to_f64(inp["k_cache"]), to_f64(inp["v_cache"]), cu.cpu().numpy(),
+                                     start.cpu().numpy(), w.scale)
+    assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3
+

@@ -137,3 +137,21 @@ def test_full_step_is_the_three_calls():
     torch.cuda.synchronize()
     assert torch.equal(out, out2)
     mk.check_status()
+
+
+def test_full_mla_step_at_the_bench_size_sampled():
+    """The bench's MLA step (B=64, S=4096, 16 heads) in its launch configuration; eight
+    sequences' outputs against the decompress-then-attend oracle."""
+    w = W.MINIMIND_MLA
+    inp = W.mla_inputs(w, DEV)
+    out = mk.decode_mla(inp["q_nope"], inp["q_rope"], inp["c_cache"], inp["kr_cache"], inp["w_uk"], inp["w_uv"],
+                        inp["seq_lens"], w.scale)
+    torch.cuda.synchronize()
+    pick = [0, 9, 18, 27, 36, 45, 54, 63]
+    sub = {k: (v[pick] if k not in ("w_uk", "w_uv") else v) for k, v in inp.items()}
+    ref = oracle.mla_decode_naive(to_f64(sub["q_nope"]), to_f64(sub["q_rope"]), to_f64(sub["c_cache"]),
+                                  to_f64(sub["kr_cache"]), to_f64(sub["w_uk"]), to_f64(sub["w_uv"]),
+                                  sub["seq_lens"].cpu().numpy(), w.scale)
+    err = np.abs(to_f64(out[pick]) - ref)
+    assert np.all(err <= _full_step_tolerance(sub, w.scale))
+
