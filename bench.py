@@ -208,6 +208,7 @@ class DecodeGqa:
     kind = "decode"
     kernel_src = "mla_kv_cache_flash_b300/csrc/decode_gqa_bf16.cu"
     call = "attn_decode_gqa call: "
+    launch_note = " (one launch, split segments merged in-kernel)"
 
     def __init__(self, w, device, rank, l2_bytes):
         import mla_kv_cache_flash_b300 as mk
@@ -326,6 +327,7 @@ class DecodeGqaFp8(DecodeGqa):
     Algorithmic bytes: each live code once plus its row's scale."""
     kernel_src = "mla_kv_cache_flash_b300/csrc/decode_gqa_fma.cu"
     call = "attn_decode_gqa_fp8 call: "
+    launch_note = " (CUDA-core decode, then the merge launch when the plan splits)"
 
     def __init__(self, w, device, rank, l2_bytes):
         import mla_kv_cache_flash_b300 as mk
@@ -375,6 +377,7 @@ class DecodeChunked(DecodeGqa):
     decode of the full length); the kernel reads them once per new token."""
     kernel_src = "mla_kv_cache_flash_b300/csrc/decode_gqa_fma.cu"
     call = "attn_prefill_gqa_chunked call: "
+    launch_note = " (CUDA-core decode, then the merge launch when the plan splits)"
     n_new = 4
 
     def __init__(self, w, device, rank, l2_bytes):
@@ -663,7 +666,7 @@ def summarize(res, steps, peaks, peak_src, world):
                 "traffic": profiled_traffic(wl.kernel_src, wl.name),
                 "peak_source": f"{peak_src} HBM copy bandwidth (MEASURED_PEAKS hbm_gbs)",
                 "algorithmic_bytes_per_launch": wl.bytes_per_step,
-                "kernel": wl.call + os.path.basename(wl.kernel_src) + " (one launch, split segments merged in-kernel)",
+                "kernel": wl.call + os.path.basename(wl.kernel_src) + wl.launch_note,
                 "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)}
         extra = {"tokens_per_s": round(wl.w.batch * world / per_step, 1),
                  "pct_of_8tbs": round(100 * achieved / NOMINAL_HBM_GBS, 2)}

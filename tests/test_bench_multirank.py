@@ -25,6 +25,7 @@ class _Wl:
     kind = "decode"
     kernel_src = "mla_kv_cache_flash_b300/csrc/decode_gqa_bf16.cu"
     call = "attn_decode_gqa call: "
+    launch_note = ""
     name = "test"
     launches_per_step = 1
 
