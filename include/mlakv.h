@@ -55,7 +55,9 @@ enum {
     ATTN_ERR_TIMEOUT = -6      /* a kernel's bounded wait gave up (from attn_check_status) */
 };
 
-/* Element type of q and of the cache for attn_decode_gqa. */
+/* Element type of q and of the cache for attn_decode_gqa (ATTN_F32, ATTN_BF16) and of the
+ * cache for attn_decode_gqa_fp8 (ATTN_FP8_E4M3, whose query is bf16; attn_decode_gqa
+ * refuses it). The workspace and split queries take all three. */
 typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1, ATTN_FP8_E4M3 = 2 } attn_dtype;
 
 /* ---------------------------------------------------------------------------------------
@@ -72,7 +74,7 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1, ATTN_FP8_E4M3 = 2 } attn_dtype;
  *   S_max    cache capacity (the row stride of the cache, in tokens).
  *   max_S    host-known upper bound on seq_lens; sizes the split-KV plan. Passing S_max is
  *            always valid.
- *   n_split  fp32 cache: number of pieces each sequence's cache is cut into (each piece is
+ *   n_split  fp32 (and E4M3) cache: number of pieces each sequence's cache is cut into (each piece is
  *            processed by its own thread block and the pieces are merged by log-sum-exp);
  *            0 lets the library choose from B, Hkv, max_S and the device's SM count.
  *            bf16 cache: the work is always balanced over one persistent thread block per SM
