@@ -334,3 +334,18 @@ def test_tensor_core_plan(L):
 def test_selftest_bounds(L, cycles):
     # validated before any launch
     assert L.attn_selftest_bounded_wait(cycles, S0) == SHAPE
+
+
+def test_binding_signatures_cover_the_header():
+    # the ctypes binding declares argument types for every entry point of the header
+    assert set(declared_functions()) == set(mk._SIGNATURES)
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    # no library, no result: the binding raises instead of computing anything itself
+    monkeypatch.setattr(mk, "_lib", None)
+    monkeypatch.setattr(mk, "lib_path", os.path.join(os.path.dirname(mk.lib_path), "absent", "libmlakv.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        mk.lib()
+    with pytest.raises(RuntimeError, match="no fallback"):
+        mk.version()
