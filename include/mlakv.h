@@ -296,6 +296,28 @@ int attn_prefill_gqa_chunked(const void *q, const void *k_cache, const void *v_c
                              void *workspace, size_t ws_bytes, mlakv_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * MLA chunked prefill with W_UK absorbed [MLA sections 2, 3 and 6, with the chunk mask of
+ * MQA&GQA "代码"]: new token i of sequence b attends latent rows 0 .. start_pos[b] + i:
+ *   s_t = scale·(q_lat·c_t + q_rope·kr_t),  out_lat = Σ_t softmax(s)_t c_t.
+ *
+ *   q_lat       [T, Hq, r]       bf16 (W_UK absorbed, e.g. by attn_mla_absorb_query)
+ *   q_rope      [T, Hq, dr]      bf16 (RoPE applied)
+ *   c_cache     [B, S_max, r]    bf16, krope_cache [B, S_max, dr] bf16, holding the chunks
+ *   cu_q, start_pos, max_kv, n_split, workspace: as attn_prefill_gqa_chunked (workspace
+ *               size from attn_prefill_mla_chunked_workspace_size).
+ *   out_lat     [T, Hq, r] fp32, every row written (apply W_UV with attn_mla_apply_uv).
+ *   r = 128, dr = 48; 1 <= Hq <= 128; 0 <= T <= 65535.
+ * CUDA-core kernel (each new token a decode over its visible latent rows), then the K2 merge.
+ * ------------------------------------------------------------------------------------- */
+size_t attn_prefill_mla_chunked_workspace_size(int B, int T, int Hq, int max_kv, int n_split);
+
+int attn_prefill_mla_chunked(const void *q_lat, const void *q_rope, const void *c_cache,
+                             const void *krope_cache, const int *cu_q, const int *start_pos,
+                             float *out_lat, int B, int T, int Hq, int r, int dr, float scale,
+                             int S_max, int max_kv, int n_split,
+                             void *workspace, size_t ws_bytes, mlakv_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * Log-sum-exp merge of split partials (the combine step of split-KV decode):
  *   out[row] = Σ_i e^{lse[row,i] − M} o[row,i,:] / Σ_i e^{lse[row,i] − M},  M = max_i lse[row,i]
  * where o[row,i,:] is piece i's normalised output and lse[row,i] = ln Σ_t e^{s_t} over the

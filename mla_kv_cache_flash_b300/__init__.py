@@ -25,7 +25,7 @@ __all__ = [
     "decode_gqa_num_splits", "decode_gqa_noalloc", "decode_mla_absorbed", "decode_mla_workspace_size", "decode_mla_num_splits",
     "prefill_gqa_causal", "merge_partials", "check_status", "last_error", "version",
     "selftest_bounded_wait", "mla_absorb_query", "mla_apply_uv", "decode_mla", "kv_append_rope",
-    "mla_append_rope", "prefill_gqa_chunked",
+    "mla_append_rope", "prefill_gqa_chunked", "prefill_mla_chunked",
 ]
 
 ATTN_F32 = 0
@@ -60,6 +60,8 @@ _SIGNATURES = {
     "attn_decode_gqa_fp8": (_c_int, [_vp] * 7 + [_c_int] * 4 + [_c_float] + [_c_int] * 3 + [_vp, _c_size, _vp]),
     "attn_prefill_gqa_chunked_workspace_size": (_c_size, [_c_int] * 7),
     "attn_prefill_gqa_chunked": (_c_int, [_vp] * 6 + [_c_int] * 5 + [_c_float] + [_c_int] * 4 + [_vp, _c_size, _vp]),
+    "attn_prefill_mla_chunked_workspace_size": (_c_size, [_c_int] * 5),
+    "attn_prefill_mla_chunked": (_c_int, [_vp] * 7 + [_c_int] * 5 + [_c_float] + [_c_int] * 3 + [_vp, _c_size, _vp]),
     "attn_kv_append_rope": (_c_int, [_vp] * 9 + [_c_int] * 6 + [_vp]),
     "attn_mla_append_rope": (_c_int, [_vp] * 9 + [_c_int] * 5 + [_vp]),
     "attn_mla_absorb_query": (_c_int, [_vp] * 3 + [_c_int] * 4 + [_vp]),
@@ -490,6 +492,42 @@ def prefill_gqa_chunked(q, k_cache, v_cache, cu_q, start_pos, max_kv, out=None, 
                                           _ptr(out), B, T, Hq, Hkv, D, scale, S_max, int(max_kv), code, n_split,
                                           _ptr(workspace), ws_bytes, _stream()))
     return out
+
+
+def prefill_mla_chunked(q_lat, q_rope, c_cache, krope_cache, cu_q, start_pos, max_kv, scale, out_lat=None,
+                        n_split=0, workspace=None):
+    """MLA over an existing latent cache, bottom-right causal: packed row i of sequence b
+    attends latent rows 0 .. start_pos[b] + i with key [c ‖ kr] and value c. q_lat [T, Hq, r],
+    q_rope [T, Hq, dr], c_cache [B, S_max, r], krope_cache [B, S_max, dr] (bf16), cu_q [B+1],
+    start_pos [B] int32. Returns out_lat [T, Hq, r] fp32."""
+    bf = torch.bfloat16
+    _need(q_lat, "q_lat", bf, 3)
+    dev = q_lat.device
+    _need(q_rope, "q_rope", bf, 3, dev)
+    _need(c_cache, "c_cache", bf, 3, dev)
+    _need(krope_cache, "krope_cache", bf, 3, dev)
+    _need(cu_q, "cu_q", torch.int32, 1, dev)
+    _need(start_pos, "start_pos", torch.int32, 1, dev)
+    T, Hq, r = q_lat.shape
+    dr = q_rope.shape[2]
+    B, S_max, _ = c_cache.shape
+    if (q_rope.shape[:2] != (T, Hq) or c_cache.shape != (B, S_max, r) or krope_cache.shape != (B, S_max, dr)
+            or cu_q.shape[0] != B + 1 or start_pos.shape[0] != B):
+        raise ValueError("inconsistent shapes for q_lat, q_rope, c_cache, krope_cache, cu_q, start_pos")
+    if out_lat is None:
+        out_lat = torch.empty((T, Hq, r), dtype=torch.float32, device=dev)
+    else:
+        _need(out_lat, "out_lat", torch.float32, 3, dev)
+    if T == 0:
+        return out_lat
+    need = int(lib().attn_prefill_mla_chunked_workspace_size(B, T, Hq, int(max_kv), n_split))
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _check(lib().attn_prefill_mla_chunked(_ptr(q_lat), _ptr(q_rope), _ptr(c_cache), _ptr(krope_cache), _ptr(cu_q),
+                                          _ptr(start_pos), _ptr(out_lat), B, T, Hq, r, dr, float(scale), S_max,
+                                          int(max_kv), n_split, _ptr(workspace), ws_bytes, _stream()))
+    return out_lat
 
 
 # ----------------------------------------------------------------------------- merge

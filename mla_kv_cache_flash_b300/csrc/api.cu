@@ -371,6 +371,59 @@ MLAKV_API int attn_prefill_gqa_chunked(const void *q, const void *k_cache, const
     return ok();
 }
 
+MLAKV_API size_t attn_prefill_mla_chunked_workspace_size(int B, int T, int Hq, int max_kv, int n_split) {
+    if (check_chunked(B, T, Hq, 1, 128, max_kv > 0 ? max_kv : 1, max_kv, ATTN_BF16, n_split,
+                      "attn_prefill_mla_chunked_workspace_size") != ATTN_OK || T == 0)
+        return 0;
+    return partials_bytes(T, Hq, kMlaRank, chunked_plan(T, Hq, 1, kMlaRank, max_kv, n_split).n_split);
+}
+
+MLAKV_API int attn_prefill_mla_chunked(const void *q_lat, const void *q_rope, const void *c_cache,
+                                       const void *krope_cache, const int *cu_q, const int *start_pos, float *out_lat,
+                                       int B, int T, int Hq, int r, int dr, float scale, int S_max, int max_kv,
+                                       int n_split, void *workspace, size_t ws_bytes, mlakv_stream_t stream) {
+    const char *who = "attn_prefill_mla_chunked";
+    if (!q_lat || !q_rope || !c_cache || !krope_cache || !cu_q || !start_pos || !out_lat)
+        return fail(ATTN_ERR_NULL, "%s: q_lat, q_rope, c_cache, krope_cache, cu_q, start_pos and out_lat must be "
+                    "non-NULL", who);
+    const int rc = check_chunked(B, T, Hq, 1, 128, S_max, max_kv, ATTN_BF16, n_split, who);
+    if (rc != ATTN_OK) return rc;
+    if (r != kMlaRank || dr != kMlaRope)
+        return fail(ATTN_ERR_UNSUPPORTED, "%s: MLA rank r=%d, rope width dr=%d not built (r=128, dr=48)", who, r, dr);
+    if (!isfinite(scale)) return fail(ATTN_ERR_SHAPE, "scale must be finite");
+    if (!aligned16(q_lat) || !aligned16(q_rope) || !aligned16(c_cache) || !aligned16(krope_cache) ||
+        !aligned16(cu_q) || !aligned16(start_pos) || !aligned16(out_lat))
+        return fail(ATTN_ERR_UNSUPPORTED, "%s: every pointer must be 16-byte aligned", who);
+    if (T == 0 || max_kv == 0) return ok();
+    const SplitPlan p = chunked_plan(T, Hq, 1, kMlaRank, max_kv, n_split);
+    const size_t need = partials_bytes(T, Hq, kMlaRank, p.n_split);
+    if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
+        return fail(ATTN_ERR_WORKSPACE, "%s: workspace of %zu bytes (16-byte aligned) needed, got %zu at %p", who,
+                    need, workspace ? ws_bytes : (size_t)0, workspace);
+    DecodeGqaArgs a{};
+    a.q = q_lat; a.q2 = q_rope; a.k = c_cache; a.v = c_cache; a.k2 = krope_cache; a.out = out_lat;
+    a.cu_q = cu_q; a.start_pos = start_pos; a.n_seq = B;
+    a.B = T; a.Hq = Hq; a.Hkv = 1; a.D = kMlaRank;
+    a.scale_log2 = scale * kLog2e;
+    a.S_max = S_max;
+    a.n_split = p.n_split;
+    a.split_len = p.split_len;
+    if (p.n_split > 1) {
+        const size_t rows = (size_t)T * Hq;
+        a.o_part = static_cast<float *>(workspace);
+        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                               align_up(rows * p.n_split * kMlaRank * sizeof(float), 256));
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_prefill_chunked_mla(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_prefill_mla_chunked: kernel launch");
+    if (p.n_split > 1) {
+        e = launch_merge(a.o_part, a.lse_part, out_lat, T * Hq, p.n_split, kMlaRank, s);
+        if (e != cudaSuccess) return cuda_fail(e, "attn_prefill_mla_chunked: merge kernel launch");
+    }
+    return ok();
+}
+
 // ======================================================================== MLA decode
 
 MLAKV_API int attn_decode_mla_num_splits(int B, int Hq, int r, int dr, int max_S, int n_split) {

@@ -34,6 +34,10 @@ struct DecodeGqaArgs {
     const int *cu_q;        // [n_seq + 1]
     const int *start_pos;   // [n_seq]
     int n_seq;
+    // MLA chunked prefill: q = q_lat [rows, Hq, 128], q2 = q_rope [rows, Hq, 48],
+    // k = v = c [n_seq, S_max, 128], k2 = kr [n_seq, S_max, 48], Hkv = 1, D = 128
+    const void *q2;
+    const void *k2;
 };
 
 // GQA decode over a bf16 cache with the balanced ("stream-K") split of streamk.cuh.
@@ -77,6 +81,8 @@ MLAKV_HIDDEN cudaError_t launch_decode_gqa_fp8(const DecodeGqaArgs &a, cudaStrea
 // Chunked prefill (cu_q set) on the same kernel over a bf16 cache; an fp32 cache goes through
 // launch_decode_gqa_f32, which also takes cu_q.
 MLAKV_HIDDEN cudaError_t launch_prefill_chunked_bf16(const DecodeGqaArgs &a, cudaStream_t s);
+// Chunked prefill over the MLA latent cache (key [c ‖ kr], value c), bf16.
+MLAKV_HIDDEN cudaError_t launch_prefill_chunked_mla(const DecodeGqaArgs &a, cudaStream_t s);
 // K1 (bf16, balanced): the persistent grid size and the workspace it needs; the decode kernel
 // also combines the segments it splits between blocks.
 MLAKV_HIDDEN int decode_gqa_stream_blocks(int B, int Hq, int Hkv, int D, int n_split);

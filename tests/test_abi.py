@@ -203,6 +203,34 @@ def test_chunked_empty_and_workspace(L):
     assert chunked(L, S_max=4096, max_kv=4096, n_split=4) == WS
 
 
+def mla_chunked(L, ql=P, qr=P, c=P, kr=P, cu=P, st=P, out=P, B=2, T=10, Hq=16, r=128, dr=48, scale=1 / 12,
+                S_max=64, max_kv=64, n_split=1, ws=N0, ws_bytes=0):
+    return L.attn_prefill_mla_chunked(ql, qr, c, kr, cu, st, out, B, T, Hq, r, dr, scale, S_max, max_kv, n_split,
+                                      ws, ws_bytes, S0)
+
+
+@pytest.mark.parametrize("which", ["ql", "qr", "c", "kr", "cu", "st", "out"])
+def test_mla_chunked_null_pointers(L, which):
+    assert mla_chunked(L, **{which: N0}) == NULL
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(T=70000), dict(Hq=0), dict(max_kv=65), dict(scale=float("inf"))])
+def test_mla_chunked_bad_shapes(L, kw):
+    assert mla_chunked(L, **kw) == SHAPE
+
+
+@pytest.mark.parametrize("kw", [dict(r=64), dict(dr=64), dict(Hq=129), dict(kr=PU)])
+def test_mla_chunked_unsupported(L, kw):
+    assert mla_chunked(L, **kw) == UNSUP
+
+
+def test_mla_chunked_empty_and_workspace(L):
+    assert mla_chunked(L, T=0) == OK
+    assert L.attn_prefill_mla_chunked_workspace_size(2, 10, 16, 64, 1) == 0
+    assert L.attn_prefill_mla_chunked_workspace_size(2, 10, 16, 4096, 4) >= 10 * 16 * 4 * 128 * 4
+    assert mla_chunked(L, S_max=4096, max_kv=4096, n_split=4) == WS
+
+
 def absorb(L, qn=P, wuk=P, ql=P, B=2, Hq=16, dn=96, r=128):
     return L.attn_mla_absorb_query(qn, wuk, ql, B, Hq, dn, r, S0)
 
@@ -349,3 +377,32 @@ def test_missing_library_fails_loudly(monkeypatch):
         mk.lib()
     with pytest.raises(RuntimeError, match="no fallback"):
         mk.version()
+
+
+def _kind(param):
+    param = param.strip()
+    if "*" in param or param.startswith("mlakv_stream_t"):
+        return "ptr"
+    if param.startswith("float"):
+        return "float"
+    if param.startswith("size_t"):
+        return "size"
+    if param.startswith("long long"):
+        return "longlong"
+    return "int"          # int, attn_dtype
+
+
+_CTYPE_KIND = {ctypes.c_void_p: "ptr", ctypes.c_float: "float", ctypes.c_size_t: "size",
+               ctypes.c_longlong: "longlong", ctypes.c_int: "int"}
+
+
+def test_binding_argument_kinds_match_the_prototypes():
+    # every ctypes argument list has the header prototype's length and kinds, in order
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER, encoding="utf-8").read(), flags=re.S)
+    protos = dict(re.findall(r"\b(attn_\w+)\s*\(([^)]*)\)\s*;", text))
+    assert set(protos) == set(mk._SIGNATURES)
+    for name, args in protos.items():
+        params = [] if args.strip() in ("", "void") else args.split(",")
+        want = [_kind(p) for p in params]
+        got = [_CTYPE_KIND[t] for t in mk._SIGNATURES[name][1]]
+        assert got == want, name

@@ -98,3 +98,50 @@ def test_chunked_minimind_four_new_tokens():
                                      start.cpu().numpy(), w.scale)
     assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3
 
+
+
+# --------------------------------------------------------------------------------- MLA
+
+def _mla_case(chunks, hq, s_max, seed):
+    w = W.MlaWorkload("mla_chunked", 6, len(chunks), hq, 96, 128, 48, 96, s_max, lengths=(1,) * len(chunks),
+                      sub=seed)
+    inp = W.mla_inputs(w, DEV)                       # its latent caches serve as the sequences' caches
+    n = np.array([c for _, c in chunks])
+    cu = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    start = np.array([s for s, _ in chunks], dtype=np.int32)
+    g = torch.Generator(device=DEV).manual_seed(8000 + seed)
+    T = int(cu[-1])
+    q_lat = torch.randn((T, hq, 128), generator=g, device=DEV).to(torch.bfloat16)
+    q_rope = torch.randn((T, hq, 48), generator=g, device=DEV).to(torch.bfloat16)
+    return q_lat, q_rope, inp["c_cache"], inp["kr_cache"], cu, start, w.scale
+
+
+@pytest.mark.parametrize("hq", [16, 8, 32, 3])
+def test_mla_chunked(hq):
+    chunks = ((300, 17), (0, 40), (999, 1), (5, 0), (200, 300))
+    q_lat, q_rope, c, kr, cu, start, scale = _mla_case(chunks, hq, 1000, hq)
+    ref = oracle.mla_prefill_absorbed(to_f64(q_lat), to_f64(q_rope), to_f64(c), to_f64(kr), cu, start, scale)
+    max_kv = int((start + np.diff(cu)).max())
+    for n_split in (0, 1, 3):
+        out = mk.prefill_mla_chunked(q_lat, q_rope, c, kr, torch.from_numpy(cu).to(DEV),
+                                     torch.from_numpy(start).to(DEV), max_kv, scale, n_split=n_split)
+        torch.cuda.synchronize()
+        assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3, n_split
+
+
+def test_mla_chunked_single_tokens_are_decode_steps():
+    """One-token chunks at start_pos = length − 1 give the absorbed MLA decode."""
+    lens = (1, 129, 700, 2000)
+    w = W.MlaWorkload("mla_chunk1", 6, len(lens), 16, 96, 128, 48, 96, 2000, lengths=lens, sub=40)
+    inp = W.mla_inputs(w, DEV)
+    q_lat = mk.mla_absorb_query(inp["q_nope"], inp["w_uk"])
+    B = len(lens)
+    cu = torch.arange(B + 1, dtype=torch.int32, device=DEV)
+    out = mk.prefill_mla_chunked(q_lat, inp["q_rope"], inp["c_cache"], inp["kr_cache"], cu,
+                                 (inp["seq_lens"] - 1).contiguous(), max(lens), w.scale)
+    dec = mk.decode_mla_absorbed(q_lat, inp["q_rope"], inp["c_cache"], inp["kr_cache"], inp["seq_lens"], w.scale)
+    torch.cuda.synchronize()
+    ref = oracle.mla_decode_absorbed(to_f64(q_lat), to_f64(inp["q_rope"]), to_f64(inp["c_cache"]),
+                                     to_f64(inp["kr_cache"]), inp["seq_lens"].cpu().numpy(), w.scale)
+    assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3
+    assert float((out - dec).abs().max()) <= 3e-3
