@@ -520,6 +520,53 @@ class DecodeMlaStep(DecodeMla):
                     launches="absorb W_UK, latent decode, apply W_UV")
 
 
+class MlaChunked(DecodeMla):
+    """MLA chunked prefill, 4 new tokens per sequence over the MiniMind MLA latent caches
+    (each sequence's last 4 rows are its chunk). Algorithmic bytes: each visible latent row
+    once, as for the decode of the full length."""
+    kernel_src = "mla_kv_cache_flash_b300/csrc/prefill_chunked_mla.cu"
+    call = "attn_prefill_mla_chunked call: "
+    launch_note = " (CUDA-core decode form, then the merge launch when the plan splits)"
+    n_new = 4
+
+    def __init__(self, w, device, rank, l2_bytes):
+        super().__init__(w, device, rank, l2_bytes)
+        B, n = w.batch, self.n_new
+        for i, s in enumerate(self.sets):
+            g = torch.Generator(device=device).manual_seed(w.seed + 800 + i + 1000 * rank)
+            s["q_lat_chunk"] = torch.randn((B * n, w.n_q_heads, w.kv_lora_rank), generator=g,
+                                           device=device).to(torch.bfloat16)
+            s["q_rope_chunk"] = torch.randn((B * n, w.n_q_heads, w.rope_dim), generator=g,
+                                            device=device).to(torch.bfloat16)
+            s["cu_q"] = torch.arange(0, B * n + 1, n, dtype=torch.int32, device=device)
+            s["start_pos"] = (s["seq_lens"] - n).clamp_min(0).contiguous()
+        self.out = torch.empty((B * n, w.n_q_heads, w.kv_lora_rank), dtype=torch.float32, device=device)
+        nb = int(self.mk.lib().attn_prefill_mla_chunked_workspace_size(B, B * n, w.n_q_heads, self.max_s, 0))
+        self.ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=device)
+        self.launches_per_step = 2 if nb else 1
+
+    def _run(self, s):
+        self.mk.prefill_mla_chunked(s["q_lat_chunk"], s["q_rope_chunk"], s["c_cache"], s["kr_cache"], s["cu_q"],
+                                    s["start_pos"], self.max_s, self.w.scale, out_lat=self.out, workspace=self.ws)
+
+    def step(self, i):
+        self._run(self.sets[i % len(self.sets)])
+
+    def host_inputs(self):
+        s = self.sets[0]
+        return {k: s[k].cpu().pin_memory() for k in ("q_lat_chunk", "q_rope_chunk", "c_cache", "kr_cache", "cu_q",
+                                                     "start_pos")}
+
+    def e2e_step(self, host, dev_bufs, out_host):
+        for k, t in host.items():
+            dev_bufs[k].copy_(t, non_blocking=True)
+        self._run(dev_bufs)
+        out_host.copy_(self.out, non_blocking=True)
+
+    def describe(self):
+        return dict(super().describe(), workload=self.name, new_tokens_per_sequence=self.n_new)
+
+
 class Prefill:
     kind = "prefill"
     kernel_src = "mla_kv_cache_flash_b300/csrc/prefill.cu"
@@ -569,13 +616,14 @@ WORKLOADS = {
     "minimind_gqa_fp8": lambda: (DecodeGqaFp8, dataclasses.replace(W.MINIMIND_GQA, name=W.MINIMIND_GQA.name + "_fp8")),
     "minimind_gqa_chunk4": lambda: (DecodeChunked, dataclasses.replace(W.MINIMIND_GQA, name=W.MINIMIND_GQA.name + "_chunk4")),
     "minimind_gqa_step": lambda: (DecodeGqaStep, dataclasses.replace(W.MINIMIND_GQA, name=W.MINIMIND_GQA.name + "_with_append")),
+    "mla_chunk4": lambda: (MlaChunked, dataclasses.replace(W.MINIMIND_MLA, name=W.MINIMIND_MLA.name + "_chunk4")),
     "mla_step": lambda: (DecodeMlaStep, dataclasses.replace(W.MINIMIND_MLA, name=W.MINIMIND_MLA.name + "_full_step")),
     "prefill": lambda: (Prefill, W.PREFILL_UNIFORM),
     "prefill_ragged": lambda: (Prefill, W.PREFILL_RAGGED),
 }
 DEFAULT_STEPS = {"minimind_gqa": 60000, "minimind_gqa_step": 60000, "minimind_gqa_fp8": 60000,
                  "minimind_gqa_chunk4": 20000, "llama_hkv32": 400, "llama_hkv8": 2000, "llama_hkv1": 10000,
-                 "mla": 40000, "mla_step": 40000, "prefill": 2000, "prefill_ragged": 1500}
+                 "mla": 40000, "mla_step": 40000, "mla_chunk4": 8000, "prefill": 2000, "prefill_ragged": 1500}
 
 
 # ============================================================================ timing
@@ -836,8 +884,8 @@ def main():
 
     also = []
     if not args.no_also and world == 1:
-        for name in ("minimind_gqa_step", "minimind_gqa_fp8", "minimind_gqa_chunk4", "llama_hkv32", "llama_hkv8", "llama_hkv1", "mla", "mla_step", "prefill",
-                     "prefill_ragged"):
+        for name in ("minimind_gqa_step", "minimind_gqa_fp8", "minimind_gqa_chunk4", "llama_hkv32", "llama_hkv8",
+                     "llama_hkv1", "mla", "mla_step", "mla_chunk4", "prefill", "prefill_ragged"):
             if name == args.workload:
                 continue
             c2, w2 = WORKLOADS[name]()
@@ -856,8 +904,8 @@ def main():
             torch.cuda.empty_cache()
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu and not isinstance(res["wl"], (DecodeMlaStep, DecodeGqaStep,
-                                                                                   DecodeGqaFp8, DecodeChunked)):
+    if rank == 0 and world == 1 and not args.no_cpu and not isinstance(
+            res["wl"], (DecodeMlaStep, DecodeGqaStep, DecodeGqaFp8, DecodeChunked, MlaChunked)):
         value, cores, sample, _ = cpu_oracle_rate(res["wl"], args.cpu_seconds)
         cpu = {"value": round(value, 4), "unit": head["unit"], "cores": cores, "kind": "oracle", "sample": sample}
 
@@ -890,7 +938,7 @@ def _cpu_workload(cls, w):
             self.lens = s["seq_lens"].numpy()
             self.n_split = None
             self.l2_note = "host memory"
-    if cls in (Prefill, DecodeMlaStep, DecodeGqaStep, DecodeGqaFp8, DecodeChunked):
+    if cls in (Prefill, DecodeMlaStep, DecodeGqaStep, DecodeGqaFp8, DecodeChunked, MlaChunked):
         raise SystemExit("the oracle arm covers the single-call decode workloads")
     return HostOnly(w)
 

@@ -45,7 +45,16 @@ def test_mla_full_step_counts_cache_and_weights():
     assert wl.launches_per_step == 3
 
 
-@pytest.mark.parametrize("name", ["minimind_gqa_step", "minimind_gqa_fp8", "minimind_gqa_chunk4", "mla_step"])
+def test_mla_chunked_counts_each_visible_latent_row_once():
+    wl, w = _make("mla_chunk4")
+    assert wl.bytes_per_step == int(wl.lens.sum()) * (w.kv_lora_rank + w.rope_dim) * 2
+    s = wl.sets[0]
+    assert s["q_lat_chunk"].shape == (w.batch * 4, w.n_q_heads, w.kv_lora_rank)
+    assert ((s["start_pos"] + 4) == s["seq_lens"]).all()
+
+
+@pytest.mark.parametrize("name", ["minimind_gqa_step", "minimind_gqa_fp8", "minimind_gqa_chunk4", "mla_step",
+                                  "mla_chunk4"])
 def test_multi_launch_lines_have_no_oracle_arm(name):
     cls, w = bench.WORKLOADS[name]()
     with pytest.raises(SystemExit):
