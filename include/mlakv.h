@@ -30,6 +30,14 @@
  *     (seq_lens, cu_seqlens) are trusted to lie within the bounds stated.
  *   - Calls are reentrant. A workspace must not be shared by two calls that can run at
  *     the same time (different streams); calls on one stream are ordered by the stream.
+ *   - Workspaces. Every workspace starts with a fixed 64 KiB region that holds only the
+ *     arrival counters of the kernels that merge split segments themselves (bf16 GQA
+ *     decode, MLA decode); split partials always lie after it. Zero-fill a workspace once
+ *     before its first use: every call that completes leaves its counters zero again, so
+ *     one buffer then serves any sequence of calls of any entry point, shape and dtype, as
+ *     long as it is large enough for each. A call with more than 16384 counters zeroes its
+ *     own (one memset on `stream`) before its launch. After attn_check_status reports
+ *     ATTN_ERR_TIMEOUT, zero-fill any workspace the failed calls used before reusing it.
  */
 #ifndef MLAKV_H
 #define MLAKV_H
@@ -88,8 +96,9 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1, ATTN_FP8_E4M3 = 2 } attn_dtype;
  *   workspace, ws_bytes: scratch for the split partials, at least
  *            attn_decode_gqa_workspace_size(...) bytes with the same arguments; may be
  *            NULL when that size is 0. For a bf16 cache the workspace also holds one arrival
- *            counter per segment: it must be zero-filled before its first use, and every
- *            call that completes leaves it zero-filled again.
+ *            counter per segment in its counter region (see "Workspaces" above): it must be
+ *            zero-filled before its first use, and every call that completes leaves the
+ *            counters zero again.
  * Returns ATTN_OK or an error code.
  * ------------------------------------------------------------------------------------- */
 size_t attn_decode_gqa_workspace_size(int B, int Hq, int Hkv, int D, int max_S,
@@ -119,11 +128,15 @@ int attn_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
  *   - Sizes whose partials need more than that return ATTN_ERR_WORKSPACE (ask for fewer
  *     splits, or use attn_decode_gqa).
  *   - The first call on a device looks up the array's device address on that device (the
- *     device must be current); make that first call before any stream capture.
- *   - Every call uses the same array. It starts zero-filled when the library loads, and a
- *     call that completes leaves its counters at zero again (the partials it also holds
- *     need no initial value). Calls whose kernels can overlap on the GPU — other streams,
- *     other host threads — race on it; order them.
+ *     device must be current); make that first call before any stream capture. The address
+ *     is kept until the process exits, so the device's primary context must live as long
+ *     (no cudaDeviceReset in between).
+ *   - Every call uses the same array, laid out like any workspace of this library (see
+ *     "Workspaces" above). It starts zero-filled when the library loads, and a call that
+ *     completes leaves its counters at zero again, so any sequence of shapes and dtypes
+ *     is served correctly. When attn_check_status reports ATTN_ERR_TIMEOUT it also zeroes
+ *     the array's counters on the current device. Calls whose kernels can overlap on the
+ *     GPU — other streams, other host threads — race on it; order them.
  * Results are identical to attn_decode_gqa with the same arguments.
  * ------------------------------------------------------------------------------------- */
 size_t attn_decode_gqa_noalloc_max_scratch(void);

@@ -218,7 +218,7 @@ def decode_gqa_fp8(q, k_cache, v_cache, k_scale, v_scale, seq_lens, out=None, sc
         _need(out, "out", torch.float32, 3, dev)
     need = decode_gqa_workspace_size(B, Hq, Hkv, D, max_s, ATTN_FP8_E4M3, n_split)
     if need and (workspace is None or workspace.numel() < need):
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() if workspace is not None else 0
     _check(lib().attn_decode_gqa_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                      _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D, scale, S_max, max_s, n_split,
@@ -486,7 +486,7 @@ def prefill_gqa_chunked(q, k_cache, v_cache, cu_q, start_pos, max_kv, out=None, 
         return out                                   # nothing to attend (an empty tensor has no pointer)
     need = int(lib().attn_prefill_gqa_chunked_workspace_size(B, T, Hq, Hkv, D, int(max_kv), n_split))
     if need and (workspace is None or workspace.numel() < need):
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() if workspace is not None else 0
     _check(lib().attn_prefill_gqa_chunked(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_q), _ptr(start_pos),
                                           _ptr(out), B, T, Hq, Hkv, D, scale, S_max, int(max_kv), code, n_split,
@@ -522,7 +522,7 @@ def prefill_mla_chunked(q_lat, q_rope, c_cache, krope_cache, cu_q, start_pos, ma
         return out_lat
     need = int(lib().attn_prefill_mla_chunked_workspace_size(B, T, Hq, int(max_kv), n_split))
     if need and (workspace is None or workspace.numel() < need):
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() if workspace is not None else 0
     _check(lib().attn_prefill_mla_chunked(_ptr(q_lat), _ptr(q_rope), _ptr(c_cache), _ptr(krope_cache), _ptr(cu_q),
                                           _ptr(start_pos), _ptr(out_lat), B, T, Hq, r, dr, float(scale), S_max,

@@ -104,10 +104,21 @@ SplitPlan gqa_plan(int B, int Hq, int Hkv, int D, int max_S, attn_dtype dtype, i
     return SplitPlan{decode_gqa_stream_blocks(B, Hq, Hkv, D, n_split), 0};
 }
 
+// Partials of the CUDA-core decode (merged by a second launch): o_part then lse_part, after
+// the workspace's counter region (which this path leaves alone, so that a workspace shared
+// with the bf16 kernels keeps its counters zero).
 size_t partials_bytes(int B, int Hq, int Dv, int n_split) {
     if (n_split <= 1) return 0;
     const size_t rows = (size_t)B * Hq;
-    return align_up(rows * n_split * Dv * sizeof(float), 256) + align_up(rows * n_split * sizeof(float), 256);
+    return kCounterRegionBytes + align_up(rows * n_split * Dv * sizeof(float), 256) +
+           align_up(rows * n_split * sizeof(float), 256);
+}
+
+void carve_partials(void *workspace, int B, int Hq, int Dv, int n_split, float **o_part, float **lse_part) {
+    const size_t rows = (size_t)B * Hq;
+    char *w = static_cast<char *>(workspace) + kCounterRegionBytes;
+    *o_part = reinterpret_cast<float *>(w);
+    *lse_part = reinterpret_cast<float *>(w + align_up(rows * n_split * Dv * sizeof(float), 256));
 }
 
 int check_gqa_shapes(int B, int Hq, int Hkv, int D, int S_max, int max_S, attn_dtype dtype, int n_split) {
@@ -185,12 +196,7 @@ int decode_fma(DecodeGqaArgs a, int B, int Hq, int Hkv, int D, float scale, int 
     a.S_max = S_max;
     a.n_split = p.n_split;
     a.split_len = p.split_len;
-    if (p.n_split > 1) {
-        const size_t rows = (size_t)B * Hq;
-        a.o_part = static_cast<float *>(workspace);
-        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                               align_up(rows * p.n_split * D * sizeof(float), 256));
-    }
+    if (p.n_split > 1) carve_partials(workspace, B, Hq, D, p.n_split, &a.o_part, &a.lse_part);
     char what[96];
     cudaError_t e = dtype == ATTN_FP8_E4M3 ? launch_decode_gqa_fp8(a, s) : launch_decode_gqa_f32(a, s);
     if (e != cudaSuccess) {
@@ -261,13 +267,16 @@ MLAKV_API int attn_decode_gqa(const void *q, const void *k_cache, const void *v_
         a.S_max = S_max;
         a.n_blocks = decode_gqa_stream_blocks(B, Hq, Hkv, D, n_split);
         a.aligned = decode_gqa_stream_aligned(B, Hq, Hkv, n_split) ? 1 : 0;
-        // the partial outputs come first in the workspace, their log-sum-exps after them
-        a.o_part = static_cast<float *>(workspace);
-        const size_t o_bytes = decode_gqa_stream_o_bytes(B, Hq, Hkv, D, n_split);
-        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_bytes);
-        a.counters = reinterpret_cast<int *>(static_cast<char *>(workspace) + o_bytes +
-                                             decode_gqa_stream_lse_bytes(B, Hq, Hkv, D, n_split));
-        const cudaError_t e = launch_decode_gqa_stream(a, s);
+        // the arrival counters first, then the partial outputs, then their log-sum-exps
+        const size_t n_cnt = decode_gqa_stream_counters(B, Hq, Hkv);
+        char *w = static_cast<char *>(workspace);
+        a.counters = reinterpret_cast<int *>(w);
+        a.o_part = reinterpret_cast<float *>(w + counter_region_bytes(n_cnt));
+        a.lse_part = reinterpret_cast<float *>(w + counter_region_bytes(n_cnt) +
+                                               decode_gqa_stream_o_bytes(B, Hq, Hkv, D, n_split));
+        cudaError_t e = clear_overflow_counters(a.counters, n_cnt, s);
+        if (e != cudaSuccess) return cuda_fail(e, "attn_decode_gqa: clearing the arrival counters");
+        e = launch_decode_gqa_stream(a, s);
         if (e != cudaSuccess) return cuda_fail(e, "attn_decode_gqa: kernel launch");
         return ok();
     }
@@ -355,12 +364,7 @@ MLAKV_API int attn_prefill_gqa_chunked(const void *q, const void *k_cache, const
     a.S_max = S_max;
     a.n_split = p.n_split;
     a.split_len = p.split_len;
-    if (p.n_split > 1) {
-        const size_t rows = (size_t)T * Hq;
-        a.o_part = static_cast<float *>(workspace);
-        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                               align_up(rows * p.n_split * D * sizeof(float), 256));
-    }
+    if (p.n_split > 1) carve_partials(workspace, T, Hq, D, p.n_split, &a.o_part, &a.lse_part);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = dtype == ATTN_BF16 ? launch_prefill_chunked_bf16(a, s) : launch_decode_gqa_f32(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "attn_prefill_gqa_chunked: kernel launch");
@@ -408,12 +412,7 @@ MLAKV_API int attn_prefill_mla_chunked(const void *q_lat, const void *q_rope, co
     a.S_max = S_max;
     a.n_split = p.n_split;
     a.split_len = p.split_len;
-    if (p.n_split > 1) {
-        const size_t rows = (size_t)T * Hq;
-        a.o_part = static_cast<float *>(workspace);
-        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                               align_up(rows * p.n_split * kMlaRank * sizeof(float), 256));
-    }
+    if (p.n_split > 1) carve_partials(workspace, T, Hq, kMlaRank, p.n_split, &a.o_part, &a.lse_part);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = launch_prefill_chunked_mla(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "attn_prefill_mla_chunked: kernel launch");
@@ -511,6 +510,12 @@ MLAKV_API int attn_check_status(mlakv_stream_t stream) {
     if (rc == 0) rc = prefill_read_and_clear_status(s, &f), flag |= f;
     if (rc == 0) rc = selftest_read_and_clear_status(s, &f), flag |= f;
     if (rc != 0) return cuda_fail((cudaError_t)rc, "attn_check_status: reading the device flags");
-    if (flag != 0) return fail(ATTN_ERR_TIMEOUT, "a kernel gave up a bounded wait (flags 0x%x)", flag);
+    if (flag != 0) {
+        // a decode that gave up may have left arrival counters set in the built-in scratch
+        rc = noalloc_clear_counters(s);
+        if (rc != 0) return cuda_fail((cudaError_t)rc, "attn_check_status: clearing the no-alloc counters");
+        return fail(ATTN_ERR_TIMEOUT, "a kernel gave up a bounded wait (flags 0x%x); zero-fill any workspace "
+                    "it used before reusing it", flag);
+    }
     return ok();
 }

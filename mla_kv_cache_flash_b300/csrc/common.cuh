@@ -57,7 +57,7 @@ struct DecodeStreamArgs {
     int n_hblk;             // head blocks per KV head: ceil(G / (16·MT))
     int hg;                 // KV heads streamed together in one tile (1, 2 or 4)
     int tile_tokens;        // tokens per tile
-    int *counters;          // [B · Hkv · n_hblk], zero between calls
+    int *counters;          // [B · Hkv · n_hblk] at the workspace's start, zero between calls
     int aligned;            // 1: block c streams exactly segment c (no segment is shared)
 };
 
@@ -90,6 +90,7 @@ MLAKV_HIDDEN bool decode_gqa_stream_aligned(int B, int Hq, int Hkv, int n_split)
 MLAKV_HIDDEN size_t decode_gqa_stream_workspace(int B, int Hq, int Hkv, int D, int n_split);
 MLAKV_HIDDEN size_t decode_gqa_stream_o_bytes(int B, int Hq, int Hkv, int D, int n_split);
 MLAKV_HIDDEN size_t decode_gqa_stream_lse_bytes(int B, int Hq, int Hkv, int D, int n_split);
+MLAKV_HIDDEN size_t decode_gqa_stream_counters(int B, int Hq, int Hkv);
 MLAKV_HIDDEN cudaError_t launch_decode_gqa_stream(const DecodeStreamArgs &a, cudaStream_t s);
 // K2: log-sum-exp merge of the split partials.
 MLAKV_HIDDEN cudaError_t launch_merge(const float *o_part, const float *lse_part, float *out,
@@ -116,6 +117,9 @@ MLAKV_HIDDEN int decode_gqa_read_and_clear_status(cudaStream_t s, unsigned *flag
 MLAKV_HIDDEN int decode_tc_read_and_clear_status(cudaStream_t s, unsigned *flag);
 MLAKV_HIDDEN int prefill_read_and_clear_status(cudaStream_t s, unsigned *flag);
 MLAKV_HIDDEN int selftest_read_and_clear_status(cudaStream_t s, unsigned *flag);
+// Zeroes the counter region of the built-in no-alloc scratch on the current device (after a
+// timeout); synchronous.
+MLAKV_HIDDEN int noalloc_clear_counters(cudaStream_t s);
 
 // Launch `kern` on `s` with programmatic stream serialisation allowed: the kernel may start
 // before the previous kernel in the stream has finished, and must call griddep_wait() before
@@ -133,6 +137,28 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// ------------------------------------------------------------------ workspace layout
+//
+// Every workspace any entry point takes starts with one fixed region that only arrival
+// counters ever occupy; split partials always come after it. The kernels that merge split
+// segments in-kernel find their counters at the workspace's start, and a call that completes
+// leaves them zero. Because no partial is ever written into the region, one zero-filled
+// workspace serves any sequence of calls, whatever their shapes. A call with more counters
+// than the region holds extends it past the region and zeroes its counters itself (one
+// memset on its stream) before its launch, since partials of other shapes may lie there.
+constexpr size_t kCounterRegionBytes = size_t(64) << 10;   // 16384 int32 counters
+
+inline size_t counter_region_bytes(size_t n_counters) {
+    const size_t c = (n_counters * sizeof(int) + 255) / 256 * 256;
+    return c > kCounterRegionBytes ? c : kCounterRegionBytes;
+}
+
+// The counters of a call that overflow the fixed region are zeroed by the call itself.
+inline cudaError_t clear_overflow_counters(int *counters, size_t n_counters, cudaStream_t s) {
+    if (n_counters * sizeof(int) <= kCounterRegionBytes) return cudaSuccess;
+    return cudaMemsetAsync(counters, 0, n_counters * sizeof(int), s);
 }
 
 // Sets the thread's attn_last_error() message and returns `code`.

@@ -695,17 +695,16 @@ size_t decode_gqa_stream_lse_bytes(int B, int Hq, int Hkv, int D, int n_split) {
     return (stream_part_rows(B, Hq, Hkv, D, n_split) * sizeof(float) + 255) / 256 * 256;
 }
 
-// Per-segment arrival counters after the partials.
-static size_t stream_counter_bytes(int B, int Hq, int Hkv) {
+// One arrival counter per (sequence, KV head, head block), at the workspace's start.
+size_t decode_gqa_stream_counters(int B, int Hq, int Hkv) {
     const int G = Hq / Hkv;
     const int MT = mt_for(G);
-    const size_t segs = (size_t)B * Hkv * ((G + 16 * MT - 1) / (16 * MT));   // one per KV head
-    return (segs * sizeof(int) + 255) / 256 * 256;
+    return (size_t)B * Hkv * ((G + 16 * MT - 1) / (16 * MT));
 }
 
 size_t decode_gqa_stream_workspace(int B, int Hq, int Hkv, int D, int n_split) {
-    return decode_gqa_stream_o_bytes(B, Hq, Hkv, D, n_split) + decode_gqa_stream_lse_bytes(B, Hq, Hkv, D, n_split) +
-           stream_counter_bytes(B, Hq, Hkv);
+    return counter_region_bytes(decode_gqa_stream_counters(B, Hq, Hkv)) +
+           decode_gqa_stream_o_bytes(B, Hq, Hkv, D, n_split) + decode_gqa_stream_lse_bytes(B, Hq, Hkv, D, n_split);
 }
 
 cudaError_t launch_decode_gqa_stream(const DecodeStreamArgs &a0, cudaStream_t st) {

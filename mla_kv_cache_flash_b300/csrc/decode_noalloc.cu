@@ -12,12 +12,19 @@
 // loads the library holds it until the process exits. In host code its name only stands in
 // for the symbol; its device address is looked up with cudaGetSymbolAddress once per device,
 // with that device current, on the first call made on that device. That first call should
-// therefore come before any stream capture. All calls share the one array. It is zero when
-// the library loads; the bf16 kernels keep per-segment arrival counters in it that must
-// start at zero, and every call that completes leaves them at zero again (the partials need
-// no initial value: each is written before it is read). Two calls whose kernels can overlap
-// on the GPU (different streams, or different host threads) race on the array and must be
-// ordered by the caller.
+// therefore come before any stream capture. The address is kept for the life of the process:
+// it assumes the device's primary context (which the CUDA runtime uses) is not destroyed and
+// recreated in between (cudaDeviceReset would do that). All calls share the one array. It is
+// zero when the library loads. Like every workspace of this library it starts with a fixed
+// region that holds only the bf16 kernels' per-segment arrival counters; the split partials
+// (written before they are read, so they need no initial value) always lie after it. Every
+// call that completes leaves its counters at zero, so calls of any sequence of shapes and
+// dtypes find theirs at zero; a call with more counters than the region holds zeroes its own
+// (a memset on the caller's stream, which allocates nothing). A call whose kernel gave up a
+// bounded wait leaves counters set: attn_check_status, when it reports that timeout, zeroes
+// this array's counter region on the current device again. Two calls whose kernels can
+// overlap on the GPU (different streams, or different host threads) race on the array and
+// must be ordered by the caller.
 #include "../../include/mlakv.h"
 #include "common.cuh"
 
@@ -61,6 +68,23 @@ int scratch_address(void **out) {
 }
 
 }  // namespace
+
+// Zeroes the array's counter region on the current device (once a kernel has given up a wait
+// and may have left counters set); nothing to do where the array was never used. Synchronous.
+int noalloc_clear_counters(cudaStream_t s) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return (int)cudaGetLastError();
+    void *p = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        p = g_addr[dev];
+    }
+    if (!p) return 0;
+    cudaError_t e = cudaMemsetAsync(p, 0, kCounterRegionBytes, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return (int)e;
+}
+
 }  // namespace mlakv
 
 extern "C" __attribute__((visibility("default"))) size_t attn_decode_gqa_noalloc_max_scratch(void) {

@@ -124,7 +124,7 @@ struct TcArgs {
     float *out;             // [B, Hq, 128]
     float *o_part;          // [2·n_blocks, N, 128]
     float *lse_part;        // [2·n_blocks, N]
-    int *counters;          // [segments], zero between calls
+    int *counters;          // [segments] at the workspace's start, zero between calls
     int B, Hq, G;           // G: query heads per KV head (MLA: all Hq)
     int seg_per_seq;        // segments per sequence: KV heads × head blocks
     int n_hblk;             // head blocks of N per KV head
@@ -768,18 +768,22 @@ Plan plan(long long segs, int n_split, int cps) {
     return p;
 }
 
+// Workspace: one arrival counter per segment at the start (the library's counter region),
+// then two partial slots of N rows × DV floats per block, then their log-sum-exps.
 size_t ws_bytes(const Plan &p, int N) {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-    return up((size_t)2 * p.n_blocks * N * DV * 4) + up((size_t)2 * p.n_blocks * N * 4) + up((size_t)p.segs * 4);
+    return counter_region_bytes((size_t)p.segs) + up((size_t)2 * p.n_blocks * N * DV * 4) +
+           up((size_t)2 * p.n_blocks * N * 4);
 }
 
 TcArgs carve(const Plan &pl, int N, void *ws) {
     TcArgs a{};
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     char *w = static_cast<char *>(ws);
+    a.counters = reinterpret_cast<int *>(w);
+    w += counter_region_bytes((size_t)pl.segs);
     a.o_part = reinterpret_cast<float *>(w);
     a.lse_part = reinterpret_cast<float *>(w + up((size_t)2 * pl.n_blocks * N * DV * 4));
-    a.counters = reinterpret_cast<int *>(w + up((size_t)2 * pl.n_blocks * N * DV * 4) + up((size_t)2 * pl.n_blocks * N * 4));
     a.n_blocks = pl.n_blocks;
     a.aligned = pl.aligned ? 1 : 0;
     return a;
@@ -847,6 +851,7 @@ cudaError_t launch_decode_tc_gqa(const void *q, const void *k, const void *v, co
         e = encode_tensor_map(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, qdims, qstrides, qbox,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     }
+    if (e == cudaSuccess) e = clear_overflow_counters(a.counters, (size_t)pl.segs, st);
     if (e != cudaSuccess) return e;
     return N == 32 ? launch<kGqa, 32>(km, vm, qm, qm, a, st) : launch<kGqa, 16>(km, vm, qm, qm, a, st);
 }
@@ -907,6 +912,7 @@ cudaError_t launch_decode_tc_mla(const void *q_lat, const void *q_rope, const vo
         e = encode_tensor_map(&qrm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q_rope, dims, strides, box,
                               CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     }
+    if (e == cudaSuccess) e = clear_overflow_counters(a.counters, (size_t)pl.segs, st);
     if (e != cudaSuccess) return e;
     return N == 32 ? launch<kMla, 32>(cm, krm, qm, qrm, a, st) : launch<kMla, 16>(cm, krm, qm, qrm, a, st);
 }

@@ -347,15 +347,31 @@ def test_tensor_core_plan(L):
     assert L.attn_decode_mla_num_splits(64, 16, 128, 48, 4096, 0) == 256          # 2 per SM, 4 per seq
     assert L.attn_decode_mla_num_splits(1, 16, 128, 48, 4096, 0) == 296           # one segment
     assert L.attn_decode_gqa_num_splits(64, 32, 8, 128, 8192, 1, 0) == 148        # register-MMA path
-    # workspace: two partial slots of N heads x 128 fp32 per block, their lse, one counter per
-    # segment, each part 256-byte aligned
+    # workspace: the fixed 64 KiB counter region (one counter per segment), then two partial
+    # slots of N heads x 128 fp32 per block and their lse, each part 256-byte aligned
     up = lambda x: (x + 255) // 256 * 256
+    region = 64 << 10
     n = 128
     assert L.attn_decode_gqa_workspace_size(64, 32, 1, 128, 8192, 1, 0) == \
-        up(2 * n * 32 * 128 * 4) + up(2 * n * 32 * 4) + up(64 * 4)
+        region + up(2 * n * 32 * 128 * 4) + up(2 * n * 32 * 4)
     n = 256
     assert L.attn_decode_mla_workspace_size(64, 16, 128, 48, 4096, 0) == \
-        up(2 * n * 16 * 128 * 4) + up(2 * n * 16 * 4) + up(64 * 4)
+        region + up(2 * n * 16 * 128 * 4) + up(2 * n * 16 * 4)
+
+
+def test_workspace_counter_region(L):
+    # every workspace that holds partials starts with the same 64 KiB counter region, so one
+    # buffer serves calls of any shape: the fp32 path's partials lie after it too
+    region = 64 << 10
+    up = lambda x: (x + 255) // 256 * 256
+    B, Hq, D, n = 2, 8, 64, 2
+    assert L.attn_decode_gqa_workspace_size(B, Hq, 2, D, 128, 0, n) == \
+        region + up(B * Hq * n * D * 4) + up(B * Hq * n * 4)
+    # more segments than the region's 16384 counters: the region grows to hold them
+    B, Hq, Hkv = 1024, 32, 32
+    segs = B * Hkv
+    need = L.attn_decode_gqa_workspace_size(B, Hq, Hkv, 128, 64, 1, 0)
+    assert need >= up(segs * 4) > region
 
 
 @pytest.mark.parametrize("cycles", [0, 999, 10**9 + 1])
