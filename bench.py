@@ -3,20 +3,27 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
-Headline workload (default): MiniMind-shaped GQA decode — B=32, Hq=8, Hkv=4, D=96, bf16
-cache, one new query token per sequence, cache lengths uniform in [512, 2048] from the
-seed. A step is one ``attn_decode_gqa`` call (one balanced split-KV decode launch that also
-merges the segments it splits) over the whole batch. ``value`` = algorithmic KV bytes read per step (each cached K/V
-element of the live lengths once) ÷ the device time per step, in GB/s, with the inputs
-resident in HBM; the timed steps cycle through enough distinct cache sets that they
-cannot be served from L2 (≥ 4 × the L2 size in total).
+Headline workload (default): the Llama-3-8B-shaped layer decode with 8 KV heads (GQA) —
+B=64, Hq=32, Hkv=8, D=128, bf16 cache, 8192 cached tokens per sequence, one new query token
+per sequence; a step is one ``attn_decode_gqa`` call over the whole batch. ``value`` =
+algorithmic KV bytes read per step (each cached K/V element once) ÷ the device time per
+step, in GB/s, with the inputs resident in HBM (the 2 GiB cache is 16× the L2; smaller
+workloads cycle through enough distinct input sets to cover ≥ 4× the L2).
 
-The line also carries: ``roofline`` (the decode call's achieved GB/s against the measured
-HBM copy bandwidth), ``e2e`` (same metric through the Python API with pinned host inputs
-copied in and the output copied back inside the timed region), ``cpu_baseline`` (the fp64
-CPU oracle on the host cores, bounded sample), ``clocks`` (NVML samples taken during the
-timed region), ``gpu_launches`` and ``also`` (the other workloads: Llama-3-8B-shaped decode
-with Hkv 32/8/1, MLA absorbed decode, causal prefill, each with its own roofline).
+Timing: the calls are captured in a CUDA graph and replayed; each of 5 timed runs covers at
+least ``--steps`` calls and at least 50 ms, timed with CUDA events on the launching stream;
+the median run gives ``ms_per_step`` (``timing`` in the line says how many calls a run
+held). Clocks are sampled during the runs.
+
+The line also carries: ``roofline`` (the achieved GB/s against the measured HBM copy
+bandwidth, and the DRAM traffic per launch from the committed ncu summary when the kernel
+source is unchanged), ``e2e`` (the same metric through the Python API with the inputs copied
+in from pinned host memory and the output copied back inside the timed region),
+``cpu_baseline`` (the fp64 CPU oracle on the host cores, bounded sample), ``clocks``,
+``gpu_launches`` and, last, ``also``: one short entry per other workload (the Llama layer
+with 32 and 1 KV heads, the MiniMind GQA decode alone, with its cache append, over an fp8
+cache and as a 4-token chunk, MLA decode alone, its full step and a 4-token chunk, and
+causal prefill uniform and ragged), each with its own roofline fraction and oracle rate.
 
 ``--impl reference`` times the fp64 CPU oracle (the only reference this path has) on the
 same workload and metric, on the host cores, and prints the same line with
@@ -47,6 +54,10 @@ import workloads as W  # noqa: E402
 
 METRIC = "decode attn KV-read HBM GB/s (% of ~8 TB/s), tokens/s; prefill TFLOP/s"
 NOMINAL_HBM_GBS = 8000.0
+HEADLINE = "llama_hkv8"
+MIN_RUN_S = 0.05          # each timed run lasts at least this long
+N_RUNS = 5                # timed runs per workload; the median is reported
+ORACLE_HOST_BYTES = 512 << 20   # fp32 host copies handed to the oracle, per workload
 FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
@@ -204,6 +215,15 @@ def profiled_traffic(kernel_src, workload_name):
 
 # ============================================================================ workloads
 
+def _f32(t):
+    """Host fp32 copy of a tensor's exact values (bf16 widens exactly), for the oracle."""
+    return t.detach().to("cpu", torch.float32).numpy()
+
+
+def _host(t):
+    return t.detach().cpu().numpy()
+
+
 class DecodeGqa:
     kind = "decode"
     kernel_src = "mla_kv_cache_flash_b300/csrc/decode_gqa_bf16.cu"
@@ -255,18 +275,24 @@ class DecodeGqa:
                            out=self.out, scale=self.w.scale, max_s=self.max_s, workspace=self.ws)
         out_host.copy_(self.out, non_blocking=True)
 
-    def oracle_units(self):
-        return [(b, j) for b in range(self.w.batch) for j in range(self.w.n_kv_heads)]
+    oracle_kind = "decode"
 
-    def unit_bytes(self, unit):
-        b, _ = unit
-        elt = 2 if self.w.dtype == "bf16" else 4
-        return int(self.lens[b]) * 2 * self.w.head_dim * elt
+    def _oracle_seqs(self, per_seq_bytes):
+        """How many sequences (the first ones) the oracle gets: all of them, or as many as fit
+        in ORACLE_HOST_BYTES of host copies (the workloads this cuts have equal lengths)."""
+        return int(max(1, min(self.w.batch, ORACLE_HOST_BYTES // max(per_seq_bytes, 1))))
 
-    def host_arrays(self):
+    def oracle_payload(self):
+        """(host arrays, units, sequences covered) for the oracle; one unit = (sequence, KV head)."""
         s = self.sets[0]
-        return {"q": s["q"].float().cpu().numpy(), "k": s["k_cache"].float().cpu().numpy(),
-                "v": s["v_cache"].float().cpu().numpy(), "lens": self.lens, "scale": self.w.scale}
+        n = self._oracle_seqs(2 * s["k_cache"][0].numel() * 4)
+        arrays = {"q": _f32(s["q"][:n]), "k": _f32(s["k_cache"][:n]), "v": _f32(s["v_cache"][:n]),
+                  "lens": self.lens[:n]}
+        return arrays, [(b, j) for b in range(n) for j in range(self.w.n_kv_heads)], n
+
+    def unit_work(self, unit):
+        elt = 2 if self.w.dtype == "bf16" else 4
+        return int(self.lens[unit[0]]) * 2 * self.w.head_dim * elt
 
     def describe(self):
         w = self.w
@@ -317,6 +343,20 @@ class DecodeGqaStep(DecodeGqa):
         self._run(dev_bufs)
         out_host.copy_(self.out, non_blocking=True)
 
+    oracle_kind = "step"
+
+    def oracle_payload(self):
+        s = self.sets[0]
+        n = self._oracle_seqs(2 * s["k_cache"][0].numel() * 4)
+        arrays = {k: _f32(s[k][:n]) for k in ("q", "k_new", "v_new", "k_cache", "v_cache")}
+        arrays.update(pos=_host(s["pos"][:n]), freqs_cis=_f32(s["freqs_cis"]))
+        return arrays, [(b,) for b in range(n)], n
+
+    def unit_work(self, unit):
+        w = self.w
+        append = 2 * w.n_q_heads * w.head_dim * 2 + 4 * w.n_kv_heads * w.head_dim * 2 + w.head_dim * 4 + 8
+        return int(self.lens[unit[0]]) * 2 * w.n_kv_heads * w.head_dim * 2 + append
+
     def describe(self):
         return dict(super().describe(), workload=self.name,
                     launches="append the new token with RoPE at position length-1, then decode")
@@ -366,6 +406,17 @@ class DecodeGqaFp8(DecodeGqa):
         self._run(dev_bufs)
         out_host.copy_(self.out, non_blocking=True)
 
+    oracle_kind = "fp8"
+
+    def oracle_payload(self):
+        s = self.sets[0]
+        arrays = {"q": _f32(s["q"]), "k": _host(s["k_cache"]), "v": _host(s["v_cache"]),
+                  "k_scale": _host(s["k_scale"]), "v_scale": _host(s["v_scale"]), "lens": self.lens}
+        return arrays, [(b, j) for b in range(self.w.batch) for j in range(self.w.n_kv_heads)], self.w.batch
+
+    def unit_work(self, unit):
+        return int(self.lens[unit[0]]) * 2 * (self.w.head_dim + 4)
+
     def describe(self):
         return dict(super().describe(), cache_dtype="fp8_e4m3 + fp32 scale per row")
 
@@ -411,6 +462,17 @@ class DecodeChunked(DecodeGqa):
             dev_bufs[k].copy_(t, non_blocking=True)
         self._run(dev_bufs)
         out_host.copy_(self.out, non_blocking=True)
+
+    oracle_kind = "chunk"
+
+    def oracle_payload(self):
+        s = self.sets[0]
+        arrays = {"q": _f32(s["q_chunk"]), "k": _f32(s["k_cache"]), "v": _f32(s["v_cache"]),
+                  "cu_q": _host(s["cu_q"]), "start_pos": _host(s["start_pos"])}
+        return arrays, [(b,) for b in range(self.w.batch)], self.w.batch
+
+    def unit_work(self, unit):
+        return int(self.lens[unit[0]]) * 2 * self.w.n_kv_heads * self.w.head_dim * 2
 
     def describe(self):
         return dict(super().describe(), workload=self.name, new_tokens_per_sequence=self.n_new,
@@ -462,17 +524,16 @@ class DecodeMla(DecodeGqa):
                                     out_lat=self.out, max_s=self.max_s, workspace=self.ws)
         out_host.copy_(self.out, non_blocking=True)
 
-    def oracle_units(self):
-        return [(b, 0) for b in range(self.w.batch)]
+    oracle_kind = "mla"
 
-    def unit_bytes(self, unit):
-        return int(self.lens[unit[0]]) * (self.w.kv_lora_rank + self.w.rope_dim) * 2
-
-    def host_arrays(self):
+    def oracle_payload(self):
         s = self.sets[0]
-        return {"q_lat": s["q_lat"].float().cpu().numpy(), "q_rope": s["q_rope"].float().cpu().numpy(),
-                "c": s["c_cache"].float().cpu().numpy(), "kr": s["kr_cache"].float().cpu().numpy(),
-                "lens": self.lens, "scale": self.w.scale}
+        arrays = {"q_lat": _f32(s["q_lat"]), "q_rope": _f32(s["q_rope"]), "c": _f32(s["c_cache"]),
+                  "kr": _f32(s["kr_cache"]), "lens": self.lens}
+        return arrays, [(b,) for b in range(self.w.batch)], self.w.batch
+
+    def unit_work(self, unit):
+        return int(self.lens[unit[0]]) * (self.w.kv_lora_rank + self.w.rope_dim) * 2
 
     def describe(self):
         w = self.w
@@ -514,6 +575,19 @@ class DecodeMlaStep(DecodeMla):
             dev_bufs[k].copy_(t, non_blocking=True)
         self._run(dev_bufs)
         out_host.copy_(self.out, non_blocking=True)
+
+    oracle_kind = "mla_step"
+
+    def oracle_payload(self):
+        s = self.sets[0]
+        arrays = {k: _f32(s[k]) for k in ("q_nope", "q_rope", "w_uk", "w_uv")}
+        arrays.update(c=_f32(s["c_cache"]), kr=_f32(s["kr_cache"]), lens=self.lens)
+        return arrays, [(b,) for b in range(self.w.batch)], self.w.batch
+
+    def unit_work(self, unit):
+        s = self.sets[0]
+        weights = (s["w_uk"].nbytes + s["w_uv"].nbytes) // self.w.batch
+        return int(self.lens[unit[0]]) * (self.w.kv_lora_rank + self.w.rope_dim) * 2 + weights
 
     def describe(self):
         return dict(super().describe(), workload=self.name, nope_dim=self.w.nope_dim, v_head_dim=self.w.v_head_dim,
@@ -563,6 +637,14 @@ class MlaChunked(DecodeMla):
         self._run(dev_bufs)
         out_host.copy_(self.out, non_blocking=True)
 
+    oracle_kind = "mla_chunk"
+
+    def oracle_payload(self):
+        s = self.sets[0]
+        arrays = {"q_lat": _f32(s["q_lat_chunk"]), "q_rope": _f32(s["q_rope_chunk"]), "c": _f32(s["c_cache"]),
+                  "kr": _f32(s["kr_cache"]), "cu_q": _host(s["cu_q"]), "start_pos": _host(s["start_pos"])}
+        return arrays, [(b,) for b in range(self.w.batch)], self.w.batch
+
     def describe(self):
         return dict(super().describe(), workload=self.name, new_tokens_per_sequence=self.n_new)
 
@@ -601,6 +683,20 @@ class Prefill:
                                    self.sets[0]["max_seqlen"], out=self.out, scale=self.w.scale)
         out_host.copy_(self.out, non_blocking=True)
 
+    oracle_kind = "prefill"
+
+    def oracle_payload(self):
+        """The first sequence of the batch (1 of 8): its packed rows, one unit per query head."""
+        s = self.sets[0]
+        n = int(self.lens[0])
+        arrays = {"q": _f32(s["q"][:n]), "k": _f32(s["k"][:n]), "v": _f32(s["v"][:n]),
+                  "cu": np.array([0, n], dtype=np.int64)}
+        return arrays, [(0, h) for h in range(self.w.n_q_heads)], 1
+
+    def unit_work(self, unit):
+        n = int(self.lens[0])
+        return 4 * self.w.head_dim * n * (n + 1) // 2
+
     def describe(self):
         w = self.w
         return {"workload": w.name, "B": w.batch, "Hq": w.n_q_heads, "Hkv": w.n_kv_heads, "D": w.head_dim,
@@ -621,91 +717,80 @@ WORKLOADS = {
     "prefill": lambda: (Prefill, W.PREFILL_UNIFORM),
     "prefill_ragged": lambda: (Prefill, W.PREFILL_RAGGED),
 }
-DEFAULT_STEPS = {"minimind_gqa": 60000, "minimind_gqa_step": 60000, "minimind_gqa_fp8": 60000,
-                 "minimind_gqa_chunk4": 20000, "llama_hkv32": 400, "llama_hkv8": 2000, "llama_hkv1": 10000,
-                 "mla": 40000, "mla_step": 40000, "mla_chunk4": 8000, "prefill": 2000, "prefill_ragged": 1500}
+ALSO = ("llama_hkv32", "llama_hkv1", "minimind_gqa", "minimind_gqa_step", "minimind_gqa_fp8",
+        "minimind_gqa_chunk4", "mla", "mla_step", "mla_chunk4", "prefill", "prefill_ragged")
 
 
 # ============================================================================ timing
 
-def time_device(run, steps, warmup, graph_len, stream):
-    """Device time of `steps` calls of run(i): CUDA graphs of `graph_len` calls replayed back to
-    back (so host launch cost is off the clock), CUDA events on the launching stream."""
+def time_workload(wl, steps, warmup, stream, barrier, sampler_index):
+    """Median device time per call of wl.step.
+
+    The calls are captured in one CUDA graph of L calls (cycling through the workload's input
+    sets, so host launch cost is off the clock), replayed R times per timed run with R chosen
+    so that a run covers at least `steps` calls and lasts at least MIN_RUN_S; N_RUNS runs are
+    timed with CUDA events on the launching stream, bracketed by a barrier and a device
+    synchronisation, and the median run gives the time per call. Clocks are sampled during
+    the runs."""
     for i in range(warmup):
-        run(i)
+        wl.step(i)
     torch.cuda.synchronize()
-    graph_len = max(1, min(graph_len, steps))
-    reps, rem = divmod(steps, graph_len)
-    g_full = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_full, stream=stream):
-        for i in range(graph_len):
-            run(i)
-    g_rem = None
-    if rem:
-        g_rem = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_rem, stream=stream):
-            for i in range(rem):
-                run(i)
-    g_full.replay()  # warm the graph itself
+    n_sets = len(getattr(wl, "sets", [0]))
+    L = n_sets * max(1, 64 // n_sets) if wl.kind == "decode" else max(n_sets, 8 // n_sets * n_sets)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(L):
+            wl.step(i)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g.replay()      # warm the graph itself
+    ev0.record(stream)
+    g.replay()
+    ev1.record(stream)
     torch.cuda.synchronize()
-    return reps, g_full, g_rem
+    est = max(ev0.elapsed_time(ev1) / 1e3, 1e-6)
+    reps = max(math.ceil(steps / L), math.ceil(MIN_RUN_S / est))
+    per_call, total = [], 0.0
+    with ClockSampler(sampler_index) as clk:
+        for _ in range(N_RUNS):
+            barrier()
+            torch.cuda.synchronize()
+            ev0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            barrier()
+            t = ev0.elapsed_time(ev1) / 1e3
+            total += t
+            per_call.append(t / (reps * L))
+    del g
+    return {"seconds_per_call": statistics.median(per_call), "calls_per_run": reps * L, "runs": N_RUNS,
+            "timed_s": total, "spread": (min(per_call), max(per_call)), "clocks": clk.summary()}
 
 
-def timed_region(reps, g_full, g_rem, stream, barrier):
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
+def time_e2e(wl, device, barrier, n=20):
+    """The same workload end to end through the Python API: every call first copies its inputs
+    from pinned host memory and ends by copying the output back and waiting for it."""
+    host = wl.host_inputs()
+    dev_bufs = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    out_host = torch.empty(wl.out.shape, dtype=wl.out.dtype, pin_memory=True)
+    for _ in range(3):
+        wl.e2e_step(host, dev_bufs, out_host)
+    torch.cuda.synchronize()
     barrier()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(reps):
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        end.record(stream)
-    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        wl.e2e_step(host, dev_bufs, out_host)
+        torch.cuda.current_stream().synchronize()   # the result is read on the host each call
+    wall = time.perf_counter() - t0
     barrier()
-    return start.elapsed_time(end) / 1e3
-
-
-def run_workload(cls, w, device, rank, steps, warmup, l2, stream, barrier, want_e2e):
-    wl = cls(w, device, rank, l2)
-    graph_len = len(getattr(wl, "sets", [0])) * max(1, 256 // max(1, len(getattr(wl, "sets", [0]))))
-    if wl.kind == "prefill":
-        graph_len = min(graph_len, 8)
-    reps, g_full, g_rem = time_device(wl.step, steps, warmup, graph_len, stream)
-    with ClockSampler(device.index) as clk:
-        t = timed_region(reps, g_full, g_rem, stream, barrier)
-    res = {"wl": wl, "seconds": t, "clocks": clk.summary()}
-    del g_full, g_rem
-    if want_e2e and hasattr(wl, "e2e_step"):
-        host = wl.host_inputs()
-        dev_bufs = {k: torch.empty_like(v, device=device) for k, v in host.items()}
-        out_host = torch.empty(wl.out.shape, dtype=wl.out.dtype, pin_memory=True)
-        n_e2e = 20
-        for _ in range(3):
-            wl.e2e_step(host, dev_bufs, out_host)
-        torch.cuda.synchronize()
-        barrier()
-        t0 = time.perf_counter()
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        start.record()
-        for _ in range(n_e2e):
-            wl.e2e_step(host, dev_bufs, out_host)
-            torch.cuda.current_stream().synchronize()   # the result is read on the host each step
-        end.record()
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
-        barrier()
-        res["e2e_seconds"] = wall / n_e2e
-        res["e2e_h2d"] = sum(v.nbytes for v in host.values())
-        res["e2e_d2h"] = out_host.nbytes
+    res = {"seconds": wall / n, "h2d": sum(v.nbytes for v in host.values()), "d2h": out_host.nbytes}
+    del dev_bufs, host
     return res
 
 
-def summarize(res, steps, peaks, peak_src, world):
-    wl = res["wl"]
-    per_step = res["seconds"] / steps
+def summarize(wl, t, peaks, peak_src, world):
+    per_step = t["seconds_per_call"]
     if wl.kind == "decode":
         achieved = wl.bytes_per_step / per_step / 1e9
         value, unit = achieved * world, "GB/s"
@@ -728,122 +813,215 @@ def summarize(res, steps, peaks, peak_src, world):
                 "algorithmic_flops_per_launch": wl.flops_per_step, "kernel": "attn_prefill_gqa_causal"}
         extra = {"tokens_per_s": round(float(np.sum(wl.lens)) * world / per_step, 1)}
     out = {"value": round(value, 2), "unit": unit, "ms_per_step": round(per_step * 1e3, 5), "roofline": roof,
-           "gpu_launches": steps * wl.launches_per_step, "config": wl.describe(), "clocks": res["clocks"]}
+           "gpu_launches": t["runs"] * t["calls_per_run"] * wl.launches_per_step, "config": wl.describe(),
+           "clocks": t["clocks"],
+           "timing": {"calls_per_run": t["calls_per_run"], "runs": t["runs"], "statistic": "median",
+                      "ms_per_call_min_max": [round(x * 1e3, 5) for x in t["spread"]],
+                      "timed_s": round(t["timed_s"], 3)}}
     out.update(extra)
-    if res.get("e2e_seconds"):
-        e = res["e2e_seconds"]
-        ev = (wl.bytes_per_step / e / 1e9) if wl.kind == "decode" else (wl.flops_per_step / e / 1e12)
-        out["e2e"] = {"value": round(ev * world, 3), "unit": unit, "h2d_bytes_per_step": res["e2e_h2d"],
-                      "d2h_bytes_per_step": res["e2e_d2h"], "ms_per_step": round(e * 1e3, 3)}
     return out
 
 
+def e2e_line(wl, seconds, h2d, d2h, world):
+    """The e2e entry: the workload's metric over the slowest rank's end-to-end time per call."""
+    if wl.kind == "decode":
+        v, unit = wl.bytes_per_step / seconds / 1e9, "GB/s"
+    else:
+        v, unit = wl.flops_per_step / seconds / 1e12, "TFLOP/s"
+    return {"value": round(v * world, 3), "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(seconds * 1e3, 3)}
+
+
 # ============================================================================ CPU oracle timing
+#
+# The oracle (the fp64 CPU definition the tests check the kernels against) timed on the host
+# cores over the same inputs. The pool of worker processes is started with "spawn" before the
+# first GPU call; each workload's host copies go to .npy files that the workers map read-only.
 
-def _oracle_worker_init(path):
-    global _ARR
-    _ARR = dict(np.load(path, allow_pickle=False))
+_MAPPED = {}
 
 
-def _oracle_decode_units(units):
+def _load(path):
+    if path not in _MAPPED:
+        _MAPPED.clear()
+        with open(os.path.join(path, "meta.json")) as f:
+            meta = json.load(f)
+        arr = {k: np.load(os.path.join(path, k + ".npy"), mmap_mode="r") for k in meta["arrays"]}
+        arr["_meta"] = meta
+        _MAPPED[path] = arr
+    return _MAPPED[path]
+
+
+def _oracle_unit(a, kind, unit, scale):
     import oracle
-    a = _ARR
-    done = 0
-    if "q_lat" in a:
-        for b, _ in units:
-            s = int(a["lens"][b])
-            q = np.concatenate([a["q_lat"][b], a["q_rope"][b]], axis=1)
-            k = np.concatenate([a["c"][b, :s], a["kr"][b, :s]], axis=1)
-            oracle.attend(q, k, a["c"][b, :s], float(a["scale"]))
-            done += 1
-        return done
-    g = a["q"].shape[1] // a["k"].shape[2]
-    for b, j in units:
+    if kind in ("decode", "fp8"):
+        b, j = unit
+        g = a["q"].shape[1] // a["k"].shape[2]
         s = int(a["lens"][b])
-        oracle.attend(a["q"][b, j * g:(j + 1) * g], a["k"][b, :s, j], a["v"][b, :s, j], float(a["scale"]))
-        done += 1
-    return done
+        if kind == "decode":
+            k, v = a["k"][b, :s, j], a["v"][b, :s, j]
+        else:
+            k = oracle.dequantize(a["k"][b, :s, j], a["k_scale"][b, :s, j])
+            v = oracle.dequantize(a["v"][b, :s, j], a["v_scale"][b, :s, j])
+        oracle.attend(a["q"][b, j * g:(j + 1) * g], k, v, scale)
+    elif kind == "step":
+        b = unit[0]
+        q_rot, kc, vc, lens = oracle.kv_append_rope(a["q"][b:b + 1], a["k_new"][b:b + 1], a["v_new"][b:b + 1],
+                                                    a["pos"][b:b + 1], a["freqs_cis"], a["k_cache"][b:b + 1],
+                                                    a["v_cache"][b:b + 1])
+        oracle.decode_gqa(q_rot, kc, vc, lens, scale)
+    elif kind in ("mla", "mla_step"):
+        b = unit[0]
+        s = int(a["lens"][b])
+        if kind == "mla":
+            q_lat = a["q_lat"][b]
+        else:
+            q_lat = oracle.absorb_query(a["q_nope"][b:b + 1], a["w_uk"])[0]
+        q = np.concatenate([q_lat, a["q_rope"][b]], axis=1)
+        k = np.concatenate([a["c"][b, :s], a["kr"][b, :s]], axis=1)
+        o_lat = oracle.attend(q, k, a["c"][b, :s], scale)
+        if kind == "mla_step":
+            oracle.apply_uv(o_lat[None], a["w_uv"])
+    elif kind in ("chunk", "mla_chunk"):
+        b = unit[0]
+        lo, hi = int(a["cu_q"][b]), int(a["cu_q"][b + 1])
+        cu, start = np.array([0, hi - lo]), a["start_pos"][b:b + 1]
+        if kind == "chunk":
+            oracle.prefill_gqa_chunked(a["q"][lo:hi], a["k"][b:b + 1], a["v"][b:b + 1], cu, start, scale)
+        else:
+            oracle.mla_prefill_absorbed(a["q_lat"][lo:hi], a["q_rope"][lo:hi], a["c"][b:b + 1], a["kr"][b:b + 1],
+                                        cu, start, scale)
+    elif kind == "prefill":
+        b, h = unit
+        lo, hi = int(a["cu"][b]), int(a["cu"][b + 1])
+        j = h // (a["q"].shape[1] // a["k"].shape[1])
+        oracle.attend(a["q"][lo:hi, h], a["k"][lo:hi, j], a["v"][lo:hi, j], scale,
+                      oracle.attention.causal_allowed(hi - lo, hi - lo))
+    else:
+        raise ValueError(kind)
 
 
-def cpu_oracle_rate(wl, budget_s, steps=None, warmup=0):
-    """Time the fp64 oracle on the host cores over a bounded sample of the workload's units
-    (one unit = one sequence and KV head). Returns (value in GB/s of KV read, cores used,
-    sample description, seconds per step or None)."""
-    import multiprocessing as mp
-    import tempfile
-    global _ARR
-    cores = len(os.sched_getaffinity(0))
-    arrays = {k: np.asarray(v) for k, v in wl.host_arrays().items()}
-    units = wl.oracle_units()
-    order = [units[i] for i in np.random.default_rng(0).permutation(len(units))]
-    _ARR = arrays
-    t0 = time.perf_counter()
-    _oracle_decode_units(order[:min(8, len(order))])
-    per_unit = (time.perf_counter() - t0) / min(8, len(order))
-    tmp = tempfile.NamedTemporaryFile(suffix=".npz", delete=False)
-    tmp.close()
-    np.savez(tmp.name, **arrays)
-    ctx = mp.get_context("spawn")
-    try:
-        with ctx.Pool(cores, initializer=_oracle_worker_init, initargs=(tmp.name,)) as pool:
-            pool.map(_oracle_decode_units, [[order[0]]] * cores)   # workers up and loaded
+def _oracle_task(job):
+    path, units = job
+    a = _load(path)
+    meta = a["_meta"]
+    for u in units:
+        _oracle_unit(a, meta["kind"], tuple(u), meta["scale"])
+    return len(units)
+
+
+class OraclePool:
+    """Worker processes (spawned, one per host core) that run oracle units."""
+
+    def __init__(self):
+        import multiprocessing as mp
+        self.cores = len(os.sched_getaffinity(0))
+        # one BLAS thread per worker: the workers already use every core
+        saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        os.environ.update({k: "1" for k in saved})
+        try:
+            self.pool = mp.get_context("spawn").Pool(self.cores)
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+
+    def rate(self, wl, budget_s, steps=None, warmup=0):
+        """Oracle throughput over the workload's units (see each workload's oracle_payload):
+        (value in the workload's unit, workers used, sample description, seconds per step).
+        Without `steps`: as many whole passes over the units as fit in budget_s. With `steps`
+        (the reference arm): each step a bounded sample of the units, sized so that warmup +
+        steps fit in budget_s."""
+        import shutil
+        import tempfile
+        arrays, units, n_seq = wl.oracle_payload()
+        tmp = tempfile.mkdtemp(prefix="oracle_")
+        try:
+            for k, v in arrays.items():
+                np.save(os.path.join(tmp, k + ".npy"), np.ascontiguousarray(v))
+            with open(os.path.join(tmp, "meta.json"), "w") as f:
+                json.dump({"kind": wl.oracle_kind, "scale": float(wl.w.scale), "arrays": sorted(arrays)}, f)
+            order = [units[i] for i in np.random.default_rng(0).permutation(len(units))]
+            # size the sample from the time of a few units in this process
+            t0 = time.perf_counter()
+            n_probe = min(len(order), 2)
+            _oracle_task((tmp, order[:n_probe]))
+            per_unit = (time.perf_counter() - t0) / n_probe
+            self.pool.map(_oracle_task, [(tmp, [order[0]])] * self.cores)     # workers map the files
+            scale_work = 1e9 if wl.kind == "decode" else 1e12
             if steps is None:
-                passes = max(1, int(budget_s / max(per_unit * len(units) / cores, 1e-9)))
+                passes = max(1, int(budget_s / max(per_unit * len(units) / self.cores, 1e-9)))
                 sample = order * passes
+                workers = min(self.cores, len(sample))
                 t0 = time.perf_counter()
-                pool.map(_oracle_decode_units, [sample[i::cores] for i in range(cores)])
+                self.pool.map(_oracle_task, [(tmp, sample[i::workers]) for i in range(workers)])
                 wall = time.perf_counter() - t0
-                nbytes = passes * sum(wl.unit_bytes(u) for u in units)
-                return (nbytes / wall / 1e9, cores,
-                        f"{passes} full pass(es) over all {len(units)} (sequence, kv-head) units, fp64 oracle.attend, "
-                        f"{cores} worker processes", None)
+                work = passes * sum(wl.unit_work(u) for u in units)
+                covered = "all" if n_seq == wl.w.batch else f"the first {n_seq} of the {wl.w.batch}"
+                what = (f"{passes} pass(es) over {len(units)} units ({covered} sequences"
+                        f"{', one unit per query head' if wl.kind == 'prefill' else ''}), fp64 oracle, "
+                        f"{workers} worker processes")
+                return work / wall / scale_work, workers, what, None
             per_step_budget = budget_s / max(1, steps + warmup)
-            n_units = int(min(len(order), max(1, per_step_budget / per_unit * cores)))
-            workers = min(cores, n_units)
+            n_units = int(min(len(order), max(1, per_step_budget / per_unit * self.cores)))
+            workers = min(self.cores, n_units)
             cursor = 0
 
             def one_step():
                 nonlocal cursor
                 sample = [order[(cursor + i) % len(order)] for i in range(n_units)]
                 cursor += n_units
-                if workers == 1:
-                    _oracle_decode_units(sample)
-                else:
-                    pool.map(_oracle_decode_units, [sample[i::workers] for i in range(workers)])
-                return sum(wl.unit_bytes(u) for u in sample)
+                self.pool.map(_oracle_task, [(tmp, sample[i::workers]) for i in range(workers)])
+                return sum(wl.unit_work(u) for u in sample)
 
             for _ in range(warmup):
                 one_step()
             t0 = time.perf_counter()
-            nbytes = sum(one_step() for _ in range(steps))
+            work = sum(one_step() for _ in range(steps))
             wall = time.perf_counter() - t0
-    finally:
-        os.unlink(tmp.name)
-    what = "all" if n_units == len(units) else f"{n_units} of the"
-    return (nbytes / wall / 1e9, workers,
-            f"each step {what} {len(units)} (sequence, kv-head) units of the workload, fp64 oracle.attend, "
-            f"{workers} worker processes", wall / steps)
+            what = (f"each step {n_units} of {len(units)} units of the workload's first {n_seq} sequence(s), "
+                    f"fp64 oracle, {workers} worker processes")
+            return work / wall / scale_work, workers, what, wall / steps
+        finally:
+            shutil.rmtree(tmp, ignore_errors=True)
 
 
 # ============================================================================ main
 
+def compact(name, s, cpu):
+    """One secondary line, kept short so the whole list survives in a log's last lines."""
+    c = s["clocks"]
+    return {"workload": name, "value": s["value"], "unit": s["unit"], "ms_per_step": s["ms_per_step"],
+            "frac": s["roofline"]["frac"], "traffic": s["roofline"]["traffic"], "cpu": cpu,
+            "sm_mhz": c.get("sm_mhz"), "reasons": c.get("reasons")}
+
+
 def main():
     ap = argparse.ArgumentParser(description="KV-cache attention benchmark (one JSON line)")
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="minimind_gqa")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
     ap.add_argument("--no-also", action="store_true", help="time only the headline workload")
-    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baselines")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle budget for the headline line")
+    ap.add_argument("--also-cpu-seconds", type=float, default=3.0, help="oracle budget per secondary line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
     world, rank, local = dist_env()
     if args.gpus != world:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch N>1 with torchrun")
-    steps = args.steps or DEFAULT_STEPS[args.workload]
+    steps = args.steps
     peaks, peak_src = load_peaks()
     cls, w = WORKLOADS[args.workload]()
 
@@ -852,17 +1030,32 @@ def main():
             return 0
         # the oracle arm runs on the host only; inputs are generated on the CPU
         wl = _cpu_workload(cls, w)
-        value, cores, sample, per_step = cpu_oracle_rate(wl, budget_s=120.0, steps=steps, warmup=args.warmup)
-        line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        pool = OraclePool()
+        try:
+            value, cores, sample, per_step = pool.rate(wl, budget_s=120.0, steps=steps, warmup=args.warmup)
+        finally:
+            pool.close()
+        unit = "GB/s" if wl.kind == "decode" else "TFLOP/s"
+        line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": unit, "n_gpus": world,
                 "steps": steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 3),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": wl.describe(),
-                "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": cores, "kind": "oracle",
                                  "sample": sample},
-                "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+                "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return 0
 
+    # the oracle's worker processes start before the first GPU call
+    pool = OraclePool() if (rank == 0 and world == 1 and not args.no_cpu) else None
+    try:
+        return run_gpu(args, world, rank, local, steps, peaks, peak_src, cls, w, pool)
+    finally:
+        if pool is not None:
+            pool.close()
+
+
+def run_gpu(args, world, rank, local, steps, peaks, peak_src, cls, w, pool):
     if world > 1:
         import torch.distributed as dist
         torch.cuda.set_device(local)
@@ -878,46 +1071,54 @@ def main():
     stream = torch.cuda.Stream(device)
 
     with torch.cuda.stream(stream):
-        res = run_workload(cls, w, device, rank, steps, args.warmup, l2, stream, barrier, want_e2e=True)
-    res["seconds"], res["e2e_seconds"] = max_over_ranks([res["seconds"], res.get("e2e_seconds", 0.0)], device)
-    head = summarize(res, steps, peaks, peak_src, world)
+        wl = cls(w, device, rank, l2)
+        t = time_workload(wl, steps, args.warmup, stream, barrier, device.index)
+        e2e = time_e2e(wl, device, barrier) if hasattr(wl, "e2e_step") else None
+    t["seconds_per_call"], e2e_s = max_over_ranks([t["seconds_per_call"], e2e["seconds"] if e2e else 0.0], device)
+    head = summarize(wl, t, peaks, peak_src, world)
+    if e2e:
+        head["e2e"] = e2e_line(wl, e2e_s, e2e["h2d"], e2e["d2h"], world)
+    cpu = None
+    if pool is not None:
+        value, cores, sample, _ = pool.rate(wl, args.cpu_seconds)
+        cpu = {"value": round(value, 4), "unit": head["unit"], "cores": cores, "kind": "oracle", "sample": sample}
+    del wl
+    torch.cuda.empty_cache()
 
-    also = []
+    also, launches = [], head["gpu_launches"]
     if not args.no_also and world == 1:
-        for name in ("minimind_gqa_step", "minimind_gqa_fp8", "minimind_gqa_chunk4", "llama_hkv32", "llama_hkv8",
-                     "llama_hkv1", "mla", "mla_step", "mla_chunk4", "prefill", "prefill_ragged"):
+        for name in ALSO:
             if name == args.workload:
                 continue
             c2, w2 = WORKLOADS[name]()
             try:
                 with torch.cuda.stream(stream):
-                    r2 = run_workload(c2, w2, device, rank, max(3, DEFAULT_STEPS[name] // 4), 3, l2, stream,
-                                      barrier, want_e2e=False)
-                s2 = summarize(r2, max(3, DEFAULT_STEPS[name] // 4), peaks, peak_src, 1)
-                also.append({"workload": w2.name, "value": s2["value"], "unit": s2["unit"],
-                             "ms_per_step": s2["ms_per_step"], "roofline": s2["roofline"],
-                             "tokens_per_s": s2.get("tokens_per_s"), "clocks": s2["clocks"],
-                             "config": s2["config"]})
-                del r2
+                    wl2 = c2(w2, device, rank, l2)
+                    t2 = time_workload(wl2, steps, 3, stream, barrier, device.index)
+                s2 = summarize(wl2, t2, peaks, peak_src, 1)
+                launches += s2["gpu_launches"]
+                cpu2 = None
+                if pool is not None:
+                    cpu2 = round(pool.rate(wl2, args.also_cpu_seconds)[0], 4)
+                also.append(compact(name, s2, cpu2))
+                del wl2
             except Exception as e:   # a secondary line must not cost the headline line
-                also.append({"workload": w2.name, "error": f"{type(e).__name__}: {e}"})
+                also.append({"workload": name, "error": f"{type(e).__name__}: {e}"[:200]})
             torch.cuda.empty_cache()
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu and not isinstance(
-            res["wl"], (DecodeMlaStep, DecodeGqaStep, DecodeGqaFp8, DecodeChunked, MlaChunked)):
-        value, cores, sample, _ = cpu_oracle_rate(res["wl"], args.cpu_seconds)
-        cpu = {"value": round(value, 4), "unit": head["unit"], "cores": cores, "kind": "oracle", "sample": sample}
 
     if rank == 0:
         line = {"metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world, "steps": steps,
                 "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": dict(head["config"], parallelism=f"replicas x{world} (independent sequences per GPU)"),
-                "tokens_per_s": head.get("tokens_per_s"), "pct_of_8tbs": head.get("pct_of_8tbs"),
-                "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": head.get("e2e"),
-                "gpu_launches": head["gpu_launches"], "clocks": head["clocks"], "also": also}
-        print(json.dumps(line), flush=True)
+                "timing": head["timing"], "tokens_per_s": head.get("tokens_per_s"),
+                "pct_of_8tbs": head.get("pct_of_8tbs"), "roofline": head["roofline"], "cpu_baseline": cpu,
+                "e2e": head.get("e2e"), "gpu_launches": launches, "clocks": head["clocks"],
+                "also_note": "also: workload, value, unit, ms_per_step, roofline frac and traffic (DRAM bytes per "
+                             "launch from profiles/, null if none), cpu = the fp64 oracle on this host in the same "
+                             "unit, SM clock median and throttle reasons; timed like the headline",
+                "also": also}
+        print(json.dumps(line, separators=(",", ":")), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -929,17 +1130,23 @@ def _cpu_workload(cls, w):
     class HostOnly(cls):
         def __init__(self, w):
             self.w, self.name = w, w.name
-            if cls is DecodeMla:
+            if issubclass(cls, DecodeMla):
                 s = W.mla_inputs(w, "cpu")
                 s["q_lat"] = torch.einsum("hnr,bhn->bhr", s["w_uk"].float(), s["q_nope"].float()).to(torch.bfloat16).contiguous()
+            elif cls is Prefill:
+                s = W.prefill_inputs(w, "cpu")
+                self.lens = s["lengths"]
             else:
                 s = W.decode_inputs(w, "cpu")
             self.sets = [s]
-            self.lens = s["seq_lens"].numpy()
+            if cls is not Prefill:
+                self.lens = s["seq_lens"].numpy()
             self.n_split = None
             self.l2_note = "host memory"
-    if cls in (Prefill, DecodeMlaStep, DecodeGqaStep, DecodeGqaFp8, DecodeChunked, MlaChunked):
-        raise SystemExit("the oracle arm covers the single-call decode workloads")
+            self.flops_per_step = sum(4 * w.head_dim * w.n_q_heads * int(x) * (int(x) + 1) // 2
+                                      for x in self.lens) if cls is Prefill else None
+    if cls not in (DecodeGqa, DecodeMla, Prefill):
+        raise SystemExit("the oracle arm covers the single-call decode and prefill workloads")
     return HostOnly(w)
 
 

@@ -45,13 +45,14 @@ def _rank_main(rank, world, port, out):
         w = W.MINIMIND_GQA
         inp = W.decode_inputs(w, "cpu", seed=w.seed + 1000 * rank)
         checksum = float(inp["k_cache"][:2, :8].float().sum())
-        # rank r "took" 1 + r seconds for 10 steps, and 0.5 + r seconds end to end
-        secs, e2e = bench.max_over_ranks([1.0 + rank, 0.5 + rank], torch.device("cpu"))
-        res = {"wl": _Wl(), "seconds": secs, "e2e_seconds": e2e, "e2e_h2d": 0, "e2e_d2h": 0,
-               "clocks": None}
+        # rank r "took" (1 + r) / 10 seconds per step, and 0.5 + r seconds end to end
+        secs, e2e = bench.max_over_ranks([(1.0 + rank) / 10, 0.5 + rank], torch.device("cpu"))
+        t = {"seconds_per_call": secs, "calls_per_run": 10, "runs": 5, "timed_s": 5 * 10 * secs,
+             "spread": (secs, secs), "clocks": None}
         peaks = {"hbm_gbs": 6500.0, "bf16_tflops": 1700.0}
-        head = bench.summarize(res, 10, peaks, "test", world)
-        out[rank] = (secs, e2e, head["value"], head["e2e"]["value"], checksum)
+        head = bench.summarize(_Wl(), t, peaks, "test", world)
+        e2e_line = bench.e2e_line(_Wl(), e2e, 0, 0, world)
+        out[rank] = (secs, e2e, head["value"], e2e_line["value"], checksum)
     finally:
         dist.destroy_process_group()
 
@@ -64,7 +65,7 @@ def test_two_gloo_ranks():
     mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
     (s0, e0, v0, ev0, c0), (s1, e1, v1, ev1, c1) = out[0], out[1]
     # both ranks agree on the slowest rank's times
-    assert s0 == s1 == 2.0 and e0 == e1 == 1.5
+    assert s0 == s1 == 0.2 and e0 == e1 == 1.5
     # whole-job throughput: world x bytes per step / slowest time per step
     assert v0 == v1 == pytest.approx(world * 1e9 / (2.0 / 10) / 1e9, rel=1e-6)
     assert ev0 == pytest.approx(world * 1e9 / 1.5 / 1e9, rel=1e-3)

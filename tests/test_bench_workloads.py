@@ -59,3 +59,26 @@ def test_multi_launch_lines_have_no_oracle_arm(name):
     cls, w = bench.WORKLOADS[name]()
     with pytest.raises(SystemExit):
         bench._cpu_workload(cls, w)
+
+
+@pytest.mark.parametrize("name", ["minimind_gqa", "minimind_gqa_step", "minimind_gqa_fp8", "minimind_gqa_chunk4",
+                                  "mla", "mla_step", "mla_chunk4", "prefill"])
+def test_oracle_leg_runs_every_kind_and_counts_the_line_work(name, tmp_path):
+    # the CPU baseline beside each line: the oracle runs one unit of the workload from the
+    # files the worker processes map, and the units' work adds up to the line's own count
+    import json
+    import numpy as np
+    wl, w = _make(name)
+    arrays, units, n_seq = wl.oracle_payload()
+    for k, v in arrays.items():
+        np.save(tmp_path / (k + ".npy"), np.ascontiguousarray(v))
+    (tmp_path / "meta.json").write_text(json.dumps({"kind": wl.oracle_kind, "scale": w.scale,
+                                                    "arrays": sorted(arrays)}))
+    assert bench._oracle_task((str(tmp_path), [units[-1]])) == 1
+    work = sum(wl.unit_work(u) for u in units)
+    if wl.kind == "prefill":
+        s0 = int(wl.lens[0])
+        assert work == 4 * w.head_dim * w.n_q_heads * s0 * (s0 + 1) // 2
+    else:
+        assert n_seq == w.batch
+        assert work == wl.bytes_per_step
