@@ -294,13 +294,17 @@ int attn_prefill_gqa_causal(const void *q, const void *k, const void *v,
  *   max_kv     host-known bound on start_pos[b] + n_b (sizes the split), 0 .. S_max
  *   dtype      ATTN_F32 or ATTN_BF16; D in {64, 96, 128}; 0 <= T <= 65535; T = 0 or
  *              max_kv = 0 launches nothing.
- *   n_split, workspace: as attn_decode_gqa with an fp32 cache (size from
- *              attn_prefill_gqa_chunked_workspace_size).
- * CUDA-core kernel (each new token is a decode over its visible cache), then the K2 merge.
- * With n_b = 1 and start_pos = seq_lens − 1 this is one decode step.
+ *   n_split, workspace: size from attn_prefill_gqa_chunked_workspace_size with the same
+ *              dtype; zero-filled before its first use (see "Workspaces").
+ * Kernels: a bf16 cache with Hq/Hkv a multiple of 16 at D = 128 runs on the tcgen05 decode
+ * kernel, 4 new tokens × 16 query heads per thread block, so each cached row a block reads
+ * feeds all of them (n_split > 0 caps the blocks at n_split per segment); other shapes run on
+ * the CUDA-core kernel, each new token a decode over its visible cache (n_split as for an
+ * fp32 cache), then the K2 merge. With n_b = 1 and start_pos = seq_lens − 1 this is one decode
+ * step.
  * ------------------------------------------------------------------------------------- */
 size_t attn_prefill_gqa_chunked_workspace_size(int B, int T, int Hq, int Hkv, int D, int max_kv,
-                                               int n_split);
+                                               attn_dtype dtype, int n_split);
 
 int attn_prefill_gqa_chunked(const void *q, const void *k_cache, const void *v_cache,
                              const int *cu_q, const int *start_pos, float *out,
@@ -320,7 +324,10 @@ int attn_prefill_gqa_chunked(const void *q, const void *k_cache, const void *v_c
  *               size from attn_prefill_mla_chunked_workspace_size).
  *   out_lat     [T, Hq, r] fp32, every row written (apply W_UV with attn_mla_apply_uv).
  *   r = 128, dr = 48; 1 <= Hq <= 128; 0 <= T <= 65535.
- * CUDA-core kernel (each new token a decode over its visible latent rows), then the K2 merge.
+ * Kernels: Hq a multiple of 16 runs on the tcgen05 MLA decode kernel, 4 new tokens × 16
+ * heads per thread block reading each latent row once (n_split > 0 caps the blocks at n_split
+ * per segment); other head counts on the CUDA-core kernel (each new token a decode over its
+ * visible latent rows), then the K2 merge.
  * ------------------------------------------------------------------------------------- */
 size_t attn_prefill_mla_chunked_workspace_size(int B, int T, int Hq, int max_kv, int n_split);
 

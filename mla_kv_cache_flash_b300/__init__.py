@@ -58,7 +58,7 @@ _SIGNATURES = {
     "attn_decode_mla_num_splits": (_c_int, [_c_int] * 6),
     "attn_decode_mla_absorbed": (_c_int, [_vp] * 6 + [_c_int] * 4 + [_c_float] + [_c_int] * 3 + [_vp, _c_size, _vp]),
     "attn_decode_gqa_fp8": (_c_int, [_vp] * 7 + [_c_int] * 4 + [_c_float] + [_c_int] * 3 + [_vp, _c_size, _vp]),
-    "attn_prefill_gqa_chunked_workspace_size": (_c_size, [_c_int] * 7),
+    "attn_prefill_gqa_chunked_workspace_size": (_c_size, [_c_int] * 8),
     "attn_prefill_gqa_chunked": (_c_int, [_vp] * 6 + [_c_int] * 5 + [_c_float] + [_c_int] * 4 + [_vp, _c_size, _vp]),
     "attn_prefill_mla_chunked_workspace_size": (_c_size, [_c_int] * 5),
     "attn_prefill_mla_chunked": (_c_int, [_vp] * 7 + [_c_int] * 5 + [_c_float] + [_c_int] * 3 + [_vp, _c_size, _vp]),
@@ -484,7 +484,7 @@ def prefill_gqa_chunked(q, k_cache, v_cache, cu_q, start_pos, max_kv, out=None, 
         _need(out, "out", torch.float32, 3, dev)
     if T == 0:
         return out                                   # nothing to attend (an empty tensor has no pointer)
-    need = int(lib().attn_prefill_gqa_chunked_workspace_size(B, T, Hq, Hkv, D, int(max_kv), n_split))
+    need = int(lib().attn_prefill_gqa_chunked_workspace_size(B, T, Hq, Hkv, D, int(max_kv), code, n_split))
     if need and (workspace is None or workspace.numel() < need):
         workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() if workspace is not None else 0

@@ -327,13 +327,22 @@ SplitPlan chunked_plan(int T, int Hq, int Hkv, int D, int max_kv, int n_split) {
     return gqa_plan(T > 0 ? T : 1, Hq, Hkv, D, max_kv, ATTN_F32, n_split);
 }
 
+// bf16 caches whose query groups are a multiple of 16 heads at D = 128 (and every MLA cache
+// with Hq a multiple of 16) run chunks on the tcgen05 kernel: 4 new tokens × 16 heads per
+// block read each cached row once. Other shapes use the CUDA-core form, one new token per block.
+bool chunk_on_tc_gqa(int B, int Hq, int Hkv, int D, attn_dtype dtype) {
+    return dtype == ATTN_BF16 && decode_tc_gqa_chunk_eligible(B, Hq, Hkv, D);
+}
+bool chunk_on_tc_mla(int B, int Hq) { return Hq % 16 == 0 && Hq <= 128 && decode_tc_mla_chunk_fits(B); }
+
 }  // namespace
 
 MLAKV_API size_t attn_prefill_gqa_chunked_workspace_size(int B, int T, int Hq, int Hkv, int D, int max_kv,
-                                                         int n_split) {
-    if (check_chunked(B, T, Hq, Hkv, D, max_kv > 0 ? max_kv : 1, max_kv, ATTN_F32, n_split,
+                                                         attn_dtype dtype, int n_split) {
+    if (check_chunked(B, T, Hq, Hkv, D, max_kv > 0 ? max_kv : 1, max_kv, dtype, n_split,
                       "attn_prefill_gqa_chunked_workspace_size") != ATTN_OK || T == 0)
         return 0;
+    if (chunk_on_tc_gqa(B, Hq, Hkv, D, dtype)) return decode_tc_gqa_chunk_workspace(B, T, Hq, Hkv, n_split);
     return partials_bytes(T, Hq, D, chunked_plan(T, Hq, Hkv, D, max_kv, n_split).n_split);
 }
 
@@ -351,6 +360,17 @@ MLAKV_API int attn_prefill_gqa_chunked(const void *q, const void *k_cache, const
         !aligned16(out))
         return fail(ATTN_ERR_UNSUPPORTED, "%s: every pointer must be 16-byte aligned", who);
     if (T == 0 || max_kv == 0) return ok();
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (chunk_on_tc_gqa(B, Hq, Hkv, D, dtype)) {
+        const size_t need = decode_tc_gqa_chunk_workspace(B, T, Hq, Hkv, n_split);
+        if (!workspace || ws_bytes < need || !aligned16(workspace))
+            return fail(ATTN_ERR_WORKSPACE, "%s: workspace of %zu bytes (16-byte aligned) needed, got %zu at %p",
+                        who, need, workspace ? ws_bytes : (size_t)0, workspace);
+        const cudaError_t e = launch_decode_tc_gqa_chunk(q, k_cache, v_cache, cu_q, start_pos, out, B, T, Hq, Hkv,
+                                                         scale * kLog2e, S_max, n_split, workspace, s);
+        if (e != cudaSuccess) return cuda_fail(e, "attn_prefill_gqa_chunked: kernel launch");
+        return ok();
+    }
     const SplitPlan p = chunked_plan(T, Hq, Hkv, D, max_kv, n_split);
     const size_t need = partials_bytes(T, Hq, D, p.n_split);
     if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
@@ -365,7 +385,6 @@ MLAKV_API int attn_prefill_gqa_chunked(const void *q, const void *k_cache, const
     a.n_split = p.n_split;
     a.split_len = p.split_len;
     if (p.n_split > 1) carve_partials(workspace, T, Hq, D, p.n_split, &a.o_part, &a.lse_part);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = dtype == ATTN_BF16 ? launch_prefill_chunked_bf16(a, s) : launch_decode_gqa_f32(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "attn_prefill_gqa_chunked: kernel launch");
     if (p.n_split > 1) {
@@ -379,6 +398,7 @@ MLAKV_API size_t attn_prefill_mla_chunked_workspace_size(int B, int T, int Hq, i
     if (check_chunked(B, T, Hq, 1, 128, max_kv > 0 ? max_kv : 1, max_kv, ATTN_BF16, n_split,
                       "attn_prefill_mla_chunked_workspace_size") != ATTN_OK || T == 0)
         return 0;
+    if (chunk_on_tc_mla(B, Hq)) return decode_tc_mla_chunk_workspace(B, T, Hq, n_split);
     return partials_bytes(T, Hq, kMlaRank, chunked_plan(T, Hq, 1, kMlaRank, max_kv, n_split).n_split);
 }
 
@@ -399,6 +419,17 @@ MLAKV_API int attn_prefill_mla_chunked(const void *q_lat, const void *q_rope, co
         !aligned16(cu_q) || !aligned16(start_pos) || !aligned16(out_lat))
         return fail(ATTN_ERR_UNSUPPORTED, "%s: every pointer must be 16-byte aligned", who);
     if (T == 0 || max_kv == 0) return ok();
+    if (chunk_on_tc_mla(B, Hq)) {
+        const size_t need = decode_tc_mla_chunk_workspace(B, T, Hq, n_split);
+        if (!workspace || ws_bytes < need || !aligned16(workspace))
+            return fail(ATTN_ERR_WORKSPACE, "%s: workspace of %zu bytes (16-byte aligned) needed, got %zu at %p",
+                        who, need, workspace ? ws_bytes : (size_t)0, workspace);
+        const cudaError_t e = launch_decode_tc_mla_chunk(q_lat, q_rope, c_cache, krope_cache, cu_q, start_pos, out_lat,
+                                                         B, T, Hq, scale * kLog2e, S_max, n_split, workspace,
+                                                         reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "attn_prefill_mla_chunked: kernel launch");
+        return ok();
+    }
     const SplitPlan p = chunked_plan(T, Hq, 1, kMlaRank, max_kv, n_split);
     const size_t need = partials_bytes(T, Hq, kMlaRank, p.n_split);
     if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))

@@ -110,6 +110,22 @@ MLAKV_HIDDEN size_t decode_tc_mla_workspace(int B, int Hq, int n_split);
 MLAKV_HIDDEN cudaError_t launch_decode_tc_mla(const void *q_lat, const void *q_rope, const void *c_cache,
                                               const void *kr_cache, const int *seq_lens, float *out, int B, int Hq,
                                               float scale_log2, int S_max, int n_split, void *ws, cudaStream_t st);
+// Chunked prefill on the same tcgen05 kernel: 4 new tokens × 16 query heads per block, each
+// token with its own key limit (bottom-right causal); the workspace as for the decode.
+MLAKV_HIDDEN bool decode_tc_gqa_chunk_eligible(int B, int Hq, int Hkv, int D);
+MLAKV_HIDDEN size_t decode_tc_gqa_chunk_workspace(int B, int T, int Hq, int Hkv, int n_split);
+MLAKV_HIDDEN int decode_tc_gqa_chunk_blocks(int B, int T, int Hq, int Hkv, int n_split);
+MLAKV_HIDDEN cudaError_t launch_decode_tc_gqa_chunk(const void *q, const void *k, const void *v, const int *cu_q,
+                                                    const int *start_pos, float *out, int B, int T, int Hq, int Hkv,
+                                                    float scale_log2, int S_max, int n_split, void *ws,
+                                                    cudaStream_t st);
+MLAKV_HIDDEN bool decode_tc_mla_chunk_fits(int B);
+MLAKV_HIDDEN size_t decode_tc_mla_chunk_workspace(int B, int T, int Hq, int n_split);
+MLAKV_HIDDEN int decode_tc_mla_chunk_blocks(int B, int T, int Hq, int n_split);
+MLAKV_HIDDEN cudaError_t launch_decode_tc_mla_chunk(const void *q_lat, const void *q_rope, const void *c_cache,
+                                                    const void *kr_cache, const int *cu_q, const int *start_pos,
+                                                    float *out, int B, int T, int Hq, float scale_log2, int S_max,
+                                                    int n_split, void *ws, cudaStream_t st);
 // K4: causal GQA prefill (D = 128).
 MLAKV_HIDDEN cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s);
 // Device error flags of the TUs that have bounded waits: read-and-clear (synchronous).

@@ -86,7 +86,7 @@ Layout layout(int q_rows, int heads, int B, int n_blocks) {
     L.stats = L.fac + (C::WPH > 1 ? HG * heads * (C::WPH + 1) * 4 : 0);
     L.plist = L.stats + 2 * HG * heads * 4 + 16;
     L.prefix = L.plist + kConsumers * (n_blocks + kLseCache) * 4;
-    L.total = L.prefix + (B + 1) * 4 + 1024;
+    L.total = L.prefix + 2 * (B + 1) * 4 + 1024;      // tile prefix [B+1], lengths [B]
     return L;
 }
 
@@ -120,6 +120,7 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
     int *plist = reinterpret_cast<int *>(smem + L.plist);     // per warp: partial rows of a merge,
                                                               // then kLseCache cached lse values
     int *prefix = reinterpret_cast<int *>(smem + L.prefix);   // [B+1]
+    int *lens = prefix + (a.B + 1);                            // [B] a copy of seq_lens
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -140,6 +141,14 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
     for (int i = threadIdx.x; i < 2 * L.q_buf / 16; i += kThreads)
         reinterpret_cast<uint4 *>(smem + C::Q_OFF)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
+    uint64_t pol = 0;                         // producer: L2 evict-first for the streamed rows
+    if (warp == kConsumers && lane == 0) {
+        // the descriptors are kernel parameters, which no earlier kernel writes
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+        prefetch_tensormap(&qmap);
+        pol = l2_evict_first_policy();
+    }
 
     // everything above overlaps the previous kernel in the stream; the inputs are read below
     griddep_wait();
@@ -149,7 +158,9 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
         int carry = 0;
         for (int base = 0; base < a.B; base += 32) {
             const int b = base + lane;
-            const int v = b < a.B ? stream_tiles(a.seq_lens[b], TT) : 0;
+            const int len = b < a.B ? __ldg(a.seq_lens + b) : 0;
+            if (b < a.B) lens[b] = len;
+            const int v = stream_tiles(len, TT);
             int x = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -173,11 +184,11 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
                 for (int i = threadIdx.x; i < a.Hq * D / 4; i += kConsumers * 32)
                     reinterpret_cast<float4 *>(a.out + (size_t)b * a.Hq * D)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    PieceWalker walk{prefix, a.seq_lens, a.B, seg_per_seq, a.n_hblk, TT, 0, 0};
+    PieceWalker walk{prefix, lens, a.B, seg_per_seq, a.n_hblk, TT, 0, 0};
     if (a.aligned) {
         // block c streams segment c whole
         const int b = c / seg_per_seq, q = c % seg_per_seq;
-        const int nb = stream_tiles(a.seq_lens[b], TT);
+        const int nb = stream_tiles(lens[b], TT);
         walk.t = (long long)seg_per_seq * prefix[b] + (long long)q * nb;
         walk.t_end = walk.t + nb;
     } else if (T > 0) {
@@ -188,10 +199,6 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
     if (warp == kConsumers) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && walk.t < walk.t_end) {
-            prefetch_tensormap(&kmap);
-            prefetch_tensormap(&vmap);
-            prefetch_tensormap(&qmap);
-            const uint64_t pol = l2_evict_first_policy();
             int g = 0, k = 0;
             bool ok = true;
             Piece p;

@@ -30,6 +30,19 @@ __host__ __device__ __forceinline__ int stream_block_of(long long t, long long T
     return (int)(((t + 1) * n - 1) / T);
 }
 
+// off = q·nb + i0 with 0 <= i0 < nb: in 32 bits when off fits (a 64-bit division is a long
+// software sequence on the GPU, and the walkers run it at every piece start).
+__host__ __device__ __forceinline__ void split_offset(long long off, int nb, int &q, int &i0) {
+    if (off < (1LL << 31)) {
+        const unsigned u = (unsigned)off;
+        q = (int)(u / (unsigned)nb);
+        i0 = (int)(u - (unsigned)q * (unsigned)nb);
+    } else {
+        q = (int)(off / nb);
+        i0 = (int)(off - (long long)q * nb);
+    }
+}
+
 // One piece of a block's range: tiles [i0, i0 + n_t) of segment (b, gi, hb).
 struct Piece {
     int b, gi, hb, S, i0, n_t;
@@ -54,10 +67,45 @@ struct PieceWalker {
         p.S = seq_lens[lo];
         const int nb = prefix[lo + 1] - prefix[lo];     // = stream_tiles(p.S, tile)
         const long long fb = (long long)seg_per_seq * prefix[lo];
-        const int q = (int)((t - fb) / nb);
+        int q, i0;
+        split_offset(t - fb, nb, q, i0);
         p.gi = q / n_hblk;
         p.hb = q % n_hblk;
-        p.i0 = (int)((t - fb) % nb);
+        p.i0 = i0;
+        const long long seg_end = fb + (long long)(q + 1) * nb;
+        const long long end = seg_end < t_end ? seg_end : t_end;
+        p.n_t = (int)(end - t);
+        p.whole = p.i0 == 0 && end == seg_end;
+        t = end;
+        return true;
+    }
+};
+
+// Chunked prefill: sequence b owns nseg_b segments (its query blocks × KV heads × head
+// blocks), each over the same lens[b] keys (the keys its last new token sees); prefix[b]
+// counts the tiles of the sequences before b with that multiplicity. A piece's `gi` is its
+// segment's index within the sequence (hb = 0); the kernel splits it.
+struct ChunkPieceWalker {
+    const int *prefix;          // [B+1] Σ_{b' < b} nseg_b' · tiles(lens[b'])
+    const int *lens;            // [B]
+    int B, tile;
+    long long t, t_end;
+    __device__ bool next(Piece &p) {
+        if (t >= t_end) return false;
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((long long)prefix[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        p.b = lo;
+        p.S = lens[lo];
+        const int nb = stream_tiles(p.S, tile);
+        const long long fb = prefix[lo];
+        int q, i0;
+        split_offset(t - fb, nb, q, i0);
+        p.gi = q;
+        p.hb = 0;
+        p.i0 = i0;
         const long long seg_end = fb + (long long)(q + 1) * nb;
         const long long end = seg_end < t_end ? seg_end : t_end;
         p.n_t = (int)(end - t);

@@ -197,10 +197,20 @@ def test_chunked_unsupported(L, kw):
 def test_chunked_empty_and_workspace(L):
     assert chunked(L, T=0) == OK
     assert chunked(L, max_kv=0) == OK
-    assert L.attn_prefill_gqa_chunked_workspace_size(2, 10, 8, 4, 96, 64, 1) == 0
-    need = L.attn_prefill_gqa_chunked_workspace_size(2, 10, 8, 4, 96, 4096, 4)
+    assert L.attn_prefill_gqa_chunked_workspace_size(2, 10, 8, 4, 96, 64, 0, 1) == 0
+    need = L.attn_prefill_gqa_chunked_workspace_size(2, 10, 8, 4, 96, 4096, 0, 4)
     assert need >= 10 * 8 * 4 * 96 * 4
     assert chunked(L, S_max=4096, max_kv=4096, n_split=4) == WS
+
+
+def test_chunked_tensor_core_workspace(L):
+    # bf16, D = 128 and 16 query heads per KV head: the tcgen05 form, whose workspace always
+    # holds the arrival counters' region and the partial slots of one block per SM
+    need = L.attn_prefill_gqa_chunked_workspace_size(2, 10, 32, 2, 128, 4096, 1, 0)
+    assert need >= (64 << 10) + 2 * 148 * 64 * 128 * 4
+    assert chunked(L, Hq=32, Hkv=2, D=128, dt=1, S_max=4096, max_kv=4096, n_split=0) == WS
+    # the same shape over an fp32 cache stays on the CUDA-core form
+    assert L.attn_prefill_gqa_chunked_workspace_size(2, 10, 32, 2, 128, 4096, 0, 1) == 0
 
 
 def mla_chunked(L, ql=P, qr=P, c=P, kr=P, cu=P, st=P, out=P, B=2, T=10, Hq=16, r=128, dr=48, scale=1 / 12,
@@ -226,9 +236,11 @@ def test_mla_chunked_unsupported(L, kw):
 
 def test_mla_chunked_empty_and_workspace(L):
     assert mla_chunked(L, T=0) == OK
-    assert L.attn_prefill_mla_chunked_workspace_size(2, 10, 16, 64, 1) == 0
-    assert L.attn_prefill_mla_chunked_workspace_size(2, 10, 16, 4096, 4) >= 10 * 16 * 4 * 128 * 4
+    # 16 heads: the tcgen05 form, with its counter region and one block per SM
+    assert L.attn_prefill_mla_chunked_workspace_size(2, 10, 16, 64, 1) >= (64 << 10) + 2 * 64 * 128 * 4
+    assert L.attn_prefill_mla_chunked_workspace_size(2, 10, 16, 4096, 0) >= (64 << 10) + 2 * 148 * 64 * 128 * 4
     assert mla_chunked(L, S_max=4096, max_kv=4096, n_split=4) == WS
+    assert mla_chunked(L) == WS
 
 
 def absorb(L, qn=P, wuk=P, ql=P, B=2, Hq=16, dn=96, r=128):

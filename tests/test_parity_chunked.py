@@ -49,9 +49,27 @@ def test_chunked_fp32(hq, hkv, d):
     _check(((300, 17), (0, 40), (999, 1), (5, 0), (200, 300)), hq, hkv, d, 1000, "fp32", hq + d, 1e-5)
 
 
-@pytest.mark.parametrize("hq,hkv,d", [(8, 4, 96), (32, 8, 128), (16, 1, 64)])
+# (32, 2, 128), (32, 1, 128) and (64, 2, 128): 16 or 32 query heads per KV head at D = 128,
+# the tcgen05 form (4 new tokens × 16 heads per block); the others the CUDA-core form
+@pytest.mark.parametrize("hq,hkv,d", [(8, 4, 96), (32, 8, 128), (16, 1, 64), (32, 2, 128), (32, 1, 128),
+                                      (64, 2, 128)])
 def test_chunked_bf16(hq, hkv, d):
     _check(((1000, 64), (0, 129), (2047, 1), (127, 128)), hq, hkv, d, 2048, "bf16", hq + 2 * d, 3e-3)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(32, 1, 128), (8, 4, 96)])
+def test_chunked_bf16_ragged_small_chunks(hq, hkv, d):
+    # chunk lengths that are not multiples of 4 (the tcgen05 form's token block), a chunk at
+    # the cache's start, empty chunks between others, and a last chunk ending at S_max
+    _check(((0, 1), (3, 2), (10, 3), (0, 0), (77, 5), (250, 6), (4, 7), (999, 9), (1015, 9)), hq, hkv, d, 1024,
+           "bf16", 50 + hq, 3e-3, n_splits=(0, 1, 2, 7))
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 1), (8, 4)])
+def test_chunked_bf16_long_chunk(hq, hkv):
+    # 512-token chunks, from the start and after a cached prefix
+    _check(((0, 512), (700, 512), (3000, 48)), hq, hkv, 128 if hkv == 1 else 96, 4096, "bf16", 60 + hq, 3e-3,
+           n_splits=(0, 3))
 
 
 def test_chunked_single_tokens_are_decode_steps():
@@ -145,3 +163,36 @@ def test_mla_chunked_single_tokens_are_decode_steps():
                                      to_f64(inp["kr_cache"]), inp["seq_lens"].cpu().numpy(), w.scale)
     assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3
     assert float((out - dec).abs().max()) <= 3e-3
+
+
+def test_mla_chunked_ragged_and_long():
+    # the tcgen05 form's edge cases: chunks of 1 .. 9 tokens (not multiples of 4), an empty
+    # chunk, a 512-token chunk and one ending at S_max, with the split plan forced several ways
+    chunks = ((0, 1), (3, 2), (10, 3), (0, 0), (77, 5), (1200, 9), (0, 512), (1528, 512))
+    q_lat, q_rope, c, kr, cu, start, scale = _mla_case(chunks, 16, 2040, 41)
+    ref = oracle.mla_prefill_absorbed(to_f64(q_lat), to_f64(q_rope), to_f64(c), to_f64(kr), cu, start, scale)
+    max_kv = int((start + np.diff(cu)).max())
+    for n_split in (0, 1, 2, 5):
+        out = mk.prefill_mla_chunked(q_lat, q_rope, c, kr, torch.from_numpy(cu).to(DEV),
+                                     torch.from_numpy(start).to(DEV), max_kv, scale, n_split=n_split)
+        torch.cuda.synchronize()
+        assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3, n_split
+
+
+def test_mla_chunked_four_new_tokens_bench_size():
+    """The bench's MLA chunked line: the MiniMind MLA caches (B = 64, 4096 rows) with each
+    sequence's last 4 rows as its chunk, every output against the oracle."""
+    w = W.MINIMIND_MLA
+    inp = W.mla_inputs(w, DEV)
+    B, n = w.batch, 4
+    g = torch.Generator(device=DEV).manual_seed(w.seed + 800)
+    q_lat = torch.randn((B * n, w.n_q_heads, w.kv_lora_rank), generator=g, device=DEV).to(torch.bfloat16)
+    q_rope = torch.randn((B * n, w.n_q_heads, w.rope_dim), generator=g, device=DEV).to(torch.bfloat16)
+    cu = torch.arange(0, B * n + 1, n, dtype=torch.int32, device=DEV)
+    start = (inp["seq_lens"] - n).contiguous()
+    out = mk.prefill_mla_chunked(q_lat, q_rope, inp["c_cache"], inp["kr_cache"], cu, start,
+                                 int(inp["seq_lens"].max()), w.scale)
+    torch.cuda.synchronize()
+    ref = oracle.mla_prefill_absorbed(to_f64(q_lat), to_f64(q_rope), to_f64(inp["c_cache"]),
+                                      to_f64(inp["kr_cache"]), cu.cpu().numpy(), start.cpu().numpy(), w.scale)
+    assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3
