@@ -333,6 +333,11 @@ SplitPlan chunked_plan(int T, int Hq, int Hkv, int D, int max_kv, int n_split) {
 bool chunk_on_tc_gqa(int B, int Hq, int Hkv, int D, attn_dtype dtype) {
     return dtype == ATTN_BF16 && decode_tc_gqa_chunk_eligible(B, Hq, Hkv, D);
 }
+// other bf16 caches with up to 16 query heads per KV head: the register-MMA decode kernel,
+// 16 / G new tokens × G heads per MMA tile
+bool chunk_on_stream(int B, int Hq, int Hkv, int D, attn_dtype dtype) {
+    return dtype == ATTN_BF16 && !chunk_on_tc_gqa(B, Hq, Hkv, D, dtype) && decode_gqa_stream_chunk_eligible(Hq, Hkv);
+}
 bool chunk_on_tc_mla(int B, int Hq) { return Hq % 16 == 0 && Hq <= 128 && decode_tc_mla_chunk_fits(B); }
 
 }  // namespace
@@ -343,6 +348,7 @@ MLAKV_API size_t attn_prefill_gqa_chunked_workspace_size(int B, int T, int Hq, i
                       "attn_prefill_gqa_chunked_workspace_size") != ATTN_OK || T == 0)
         return 0;
     if (chunk_on_tc_gqa(B, Hq, Hkv, D, dtype)) return decode_tc_gqa_chunk_workspace(B, T, Hq, Hkv, n_split);
+    if (chunk_on_stream(B, Hq, Hkv, D, dtype)) return decode_gqa_stream_chunk_workspace(B, T, Hq, Hkv, D, n_split);
     return partials_bytes(T, Hq, D, chunked_plan(T, Hq, Hkv, D, max_kv, n_split).n_split);
 }
 
@@ -368,6 +374,16 @@ MLAKV_API int attn_prefill_gqa_chunked(const void *q, const void *k_cache, const
                         who, need, workspace ? ws_bytes : (size_t)0, workspace);
         const cudaError_t e = launch_decode_tc_gqa_chunk(q, k_cache, v_cache, cu_q, start_pos, out, B, T, Hq, Hkv,
                                                          scale * kLog2e, S_max, n_split, workspace, s);
+        if (e != cudaSuccess) return cuda_fail(e, "attn_prefill_gqa_chunked: kernel launch");
+        return ok();
+    }
+    if (chunk_on_stream(B, Hq, Hkv, D, dtype)) {
+        const size_t need = decode_gqa_stream_chunk_workspace(B, T, Hq, Hkv, D, n_split);
+        if (!workspace || ws_bytes < need || !aligned16(workspace))
+            return fail(ATTN_ERR_WORKSPACE, "%s: workspace of %zu bytes (16-byte aligned) needed, got %zu at %p",
+                        who, need, workspace ? ws_bytes : (size_t)0, workspace);
+        const cudaError_t e = launch_decode_gqa_stream_chunk(q, k_cache, v_cache, cu_q, start_pos, out, B, T, Hq,
+                                                             Hkv, D, scale * kLog2e, S_max, n_split, workspace, s);
         if (e != cudaSuccess) return cuda_fail(e, "attn_prefill_gqa_chunked: kernel launch");
         return ok();
     }

@@ -59,6 +59,11 @@ struct DecodeStreamArgs {
     int tile_tokens;        // tokens per tile
     int *counters;          // [B · Hkv · n_hblk] at the workspace's start, zero between calls
     int aligned;            // 1: block c streams exactly segment c (no segment is shared)
+    // chunked prefill: q is [T, Hq, D] packed by sequence; sequence b's cu_q[b+1] − cu_q[b]
+    // new tokens see keys up to start_pos[b] + i; nt new tokens per segment
+    const int *cu_q;        // [B+1]
+    const int *start_pos;   // [B]
+    int nt, T;
 };
 
 struct PrefillArgs {
@@ -92,6 +97,15 @@ MLAKV_HIDDEN size_t decode_gqa_stream_o_bytes(int B, int Hq, int Hkv, int D, int
 MLAKV_HIDDEN size_t decode_gqa_stream_lse_bytes(int B, int Hq, int Hkv, int D, int n_split);
 MLAKV_HIDDEN size_t decode_gqa_stream_counters(int B, int Hq, int Hkv);
 MLAKV_HIDDEN cudaError_t launch_decode_gqa_stream(const DecodeStreamArgs &a, cudaStream_t s);
+// Chunked prefill on the same kernel for query groups of up to 16 heads: 16 / G new tokens ×
+// G heads per MMA tile, each token with its own key limit.
+MLAKV_HIDDEN bool decode_gqa_stream_chunk_eligible(int Hq, int Hkv);
+MLAKV_HIDDEN int decode_gqa_stream_chunk_blocks(int B, int T, int Hq, int Hkv, int n_split);
+MLAKV_HIDDEN size_t decode_gqa_stream_chunk_workspace(int B, int T, int Hq, int Hkv, int D, int n_split);
+MLAKV_HIDDEN cudaError_t launch_decode_gqa_stream_chunk(const void *q, const void *k, const void *v,
+                                                        const int *cu_q, const int *start_pos, float *out, int B,
+                                                        int T, int Hq, int Hkv, int D, float scale_log2, int S_max,
+                                                        int n_split, void *ws, cudaStream_t st);
 // K2: log-sum-exp merge of the split partials.
 MLAKV_HIDDEN cudaError_t launch_merge(const float *o_part, const float *lse_part, float *out,
                                       int rows, int n_split, int Dv, cudaStream_t s);

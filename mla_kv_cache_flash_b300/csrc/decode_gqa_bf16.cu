@@ -73,7 +73,7 @@ struct Layout {
 };
 
 template <int D, int MT, int HG, int NS, int NC>
-Layout layout(int q_rows, int heads, int B, int n_blocks) {
+Layout layout(int q_rows, int heads, int B, int n_blocks, bool chunked) {
     using C = Cfg<D, MT, HG, NS, NC>;
     constexpr int kConsumers = NC;
     Layout L;
@@ -86,7 +86,9 @@ Layout layout(int q_rows, int heads, int B, int n_blocks) {
     L.stats = L.fac + (C::WPH > 1 ? HG * heads * (C::WPH + 1) * 4 : 0);
     L.plist = L.stats + 2 * HG * heads * 4 + 16;
     L.prefix = L.plist + kConsumers * (n_blocks + kLseCache) * 4;
-    L.total = L.prefix + 2 * (B + 1) * 4 + 1024;      // tile prefix [B+1], lengths [B]
+    // tile prefix [B+1], keys per sequence [B]; chunked prefill also the first new-token rows
+    // [B+1] and the segment prefix [B+1]
+    L.total = L.prefix + (chunked ? 4 : 2) * (B + 1) * 4 + 1024;
     return L;
 }
 
@@ -97,7 +99,10 @@ __device__ __forceinline__ uint32_t sw64(int row, int cidx) {
     return row * 64 + ((((cidx & 3) ^ ((row >> 1) & 3))) << 4);
 }
 
-template <int D, int MT, int HG, int NS, int NC>
+// CH: chunked prefill. The M rows of a KV head's MMA tile are then NT = a.nt new tokens × G
+// query heads (row i·G + g), each token with its own key limit (bottom-right causal); the
+// query rows of a KV-head group arrive as one box of NT tokens × HG·G heads.
+template <int D, int MT, int HG, int NS, int NC, bool CH>
 __global__ void __launch_bounds__((NC + 1) * 32, 1)
 decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                        const __grid_constant__ CUtensorMap qmap, const DecodeStreamArgs a, const Layout L,
@@ -120,7 +125,9 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
     int *plist = reinterpret_cast<int *>(smem + L.plist);     // per warp: partial rows of a merge,
                                                               // then kLseCache cached lse values
     int *prefix = reinterpret_cast<int *>(smem + L.prefix);   // [B+1]
-    int *lens = prefix + (a.B + 1);                            // [B] a copy of seq_lens
+    int *lens = prefix + (a.B + 1);                            // [B] keys per sequence
+    int *cu = lens + (a.B + 1);                                // chunked: [B+1] first new-token row
+    int *segpre = cu + (a.B + 1);                              // chunked: [B+1] segments before b
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -153,7 +160,45 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
     // everything above overlaps the previous kernel in the stream; the inputs are read below
     griddep_wait();
     griddep_launch_dependents();
-    if (warp == 0) {
+    const int ntok = CH ? a.nt : 1;                // new tokens per segment
+    if (CH && warp == 0) {
+        // per sequence: n new tokens at rows cu_q[b] .., seeing keys up to start_pos[b] + n;
+        // ceil(n / nt) query blocks of Hkv / HG segments each, every one over those keys
+        const int per_qb = a.Hkv / HG;
+        int carry = 0, scarry = 0;
+        for (int base = 0; base < a.B; base += 32) {
+            const int b = base + lane;
+            int n = 0, st = 0, c0 = 0;
+            if (b < a.B) {
+                c0 = __ldg(a.cu_q + b);
+                n = __ldg(a.cu_q + b + 1) - c0;
+                st = __ldg(a.start_pos + b);
+            }
+            const int keys = n > 0 ? st + n : 0;
+            const int nseg = (n + ntok - 1) / ntok * per_qb;
+            const int v = nseg * stream_tiles(keys, TT);
+            int x = v, y = nseg;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int xu = __shfl_up_sync(0xffffffffu, x, o);
+                const int yu = __shfl_up_sync(0xffffffffu, y, o);
+                if (lane >= o) x += xu, y += yu;
+            }
+            if (b < a.B) {
+                prefix[b] = carry + x - v;
+                segpre[b] = scarry + y - nseg;
+                lens[b] = keys;
+                cu[b] = c0;
+            }
+            carry += __shfl_sync(0xffffffffu, x, 31);
+            scarry += __shfl_sync(0xffffffffu, y, 31);
+        }
+        if (lane == 0) {
+            prefix[a.B] = carry;
+            segpre[a.B] = scarry;
+            cu[a.B] = __ldg(a.cu_q + a.B);
+        }
+    } else if (warp == 0) {
         // tile prefix over the sequences (warp scan, 32 sequences at a time)
         int carry = 0;
         for (int base = 0; base < a.B; base += 32) {
@@ -174,10 +219,10 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
     }
     __syncthreads();
 
-    const int seg_per_seq = (a.Hkv / HG) * a.n_hblk;
-    const long long T = (long long)seg_per_seq * prefix[a.B];
+    const int seg_per_seq = (a.Hkv / HG) * a.n_hblk;      // chunked: per query block
+    const long long T = CH ? (long long)prefix[a.B] : (long long)seg_per_seq * prefix[a.B];
     const int c = blockIdx.x;
-    if (c == 0 && warp < kConsumers) {
+    if (!CH && c == 0 && warp < kConsumers) {
         // sequences with an empty cache own no tile: their output is zero
         for (int b = 0; b < a.B; ++b)
             if (prefix[b + 1] == prefix[b])
@@ -185,7 +230,7 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
                     reinterpret_cast<float4 *>(a.out + (size_t)b * a.Hq * D)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     PieceWalker walk{prefix, lens, a.B, seg_per_seq, a.n_hblk, TT, 0, 0};
-    if (a.aligned) {
+    if (!CH && a.aligned) {
         // block c streams segment c whole
         const int b = c / seg_per_seq, q = c % seg_per_seq;
         const int nb = stream_tiles(lens[b], TT);
@@ -195,26 +240,79 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
         walk.t = stream_start(c, T, a.n_blocks);
         walk.t_end = stream_start(c + 1, T, a.n_blocks);
     }
+    ChunkPieceWalker cwalk{prefix, lens, a.B, TT, walk.t, walk.t_end};
+    AlignedChunkWalker awalk{0, 0, a.Hkv / HG, 0, 0, TT, 0};
+    if (CH && a.aligned) {
+        // block c: sequence c / Hkv, KV head c % Hkv (HG = 1), all of its query blocks
+        awalk.b = c / a.Hkv;
+        awalk.j = c % a.Hkv;
+        if (awalk.b < a.B) {
+            const int n = cu[awalk.b + 1] - cu[awalk.b];
+            awalk.nqb = (n + ntok - 1) / ntok;
+            awalk.S = lens[awalk.b];
+        }
+    }
+    auto next_piece = [&](Piece &p) {
+        if constexpr (CH) return a.aligned ? awalk.next(p) : cwalk.next(p);
+        else return walk.next(p);
+    };
+    // A piece's segment: KV-head group gi, head block hb, index q within the sequence (and the
+    // arrival counter seg); decode rows are heads of sequence b, chunked-prefill rows are the
+    // query block's new tokens at packed rows row0 .., nvalid of them, seeing keys < kbase + i + 1.
+    struct SegG {
+        int gi, hb, q, seg, row0, nvalid, kbase;
+    };
+    auto seg_info = [&](const Piece &p) {
+        SegG r;
+        if constexpr (CH) {
+            r.q = p.gi;
+            const int qb = r.q / seg_per_seq;
+            r.gi = r.q % seg_per_seq;
+            r.hb = 0;
+            const int n = cu[p.b + 1] - cu[p.b];
+            r.row0 = cu[p.b] + qb * ntok;
+            r.nvalid = min(ntok, n - qb * ntok);
+            r.kbase = lens[p.b] - n + qb * ntok;
+            r.seg = segpre[p.b] + r.q;
+        } else {
+            r.gi = p.gi;
+            r.hb = p.hb;
+            r.q = p.gi * a.n_hblk + p.hb;
+            r.seg = p.b * seg_per_seq + r.q;
+            r.row0 = p.b;
+            r.nvalid = 1;
+            r.kbase = 0;
+        }
+        return r;
+    };
+    // Output row of query row h (0 .. heads-1) of KV head jj: decode, head jj·G + hb·HEADS + h of
+    // sequence b; chunked prefill, head jj·G + h % G of packed row row0 + h / G
+    auto out_row = [&](const SegG &si, int jj, int h) {
+        if constexpr (CH) return (size_t)(si.row0 + h / G) * a.Hq + jj * G + h % G;
+        else return (size_t)si.row0 * a.Hq + jj * G + si.hb * C::HEADS + h;
+    };
+    auto row_valid = [&](const SegG &si, int h) { return !CH || h / G < si.nvalid; };
 
     if (warp == kConsumers) {
         // ------------------------------------------------------------ producer
-        if (lane == 0 && walk.t < walk.t_end) {
+        if (lane == 0 && (walk.t < walk.t_end || (CH && a.aligned && awalk.nqb > 0))) {
             int g = 0, k = 0;
             bool ok = true;
             Piece p;
-            while (ok && walk.next(p)) {
+            while (ok && next_piece(p)) {
                 const int qb = k & 1;
                 if (k >= 2 && !mbar_wait_bounded(qempty0 + 8 * qb, ((k >> 1) - 1) & 1, &g_decode_gqa_status,
                                                  kStatusEmptyWait)) {
                     ok = false;
                     break;
                 }
-                const int j0 = p.gi * HG;
-                const int h0 = j0 * G + p.hb * C::HEADS;
+                const SegG si = seg_info(p);
+                const int j0 = si.gi * HG;
+                const int h0 = j0 * G + si.hb * C::HEADS;
                 mbar_arrive_expect_tx(qfull0 + 8 * qb, C::NB * q_rows_loaded * 64);
 #pragma unroll
                 for (int bx = 0; bx < C::NB; ++bx)
-                    tma_load_3d(sbase + C::Q_OFF + qb * L.q_buf + bx * L.q_box, &qmap, bx * 32, h0, p.b,
+                    tma_load_3d(sbase + C::Q_OFF + qb * L.q_buf + bx * L.q_box, &qmap, bx * 32, h0, si.row0,
                                 qfull0 + 8 * qb, pol);
                 for (int i = 0; i < p.n_t; ++i, ++g) {
                     const int s = g % NS;
@@ -256,22 +354,39 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
     const int cq = lane & 3;      // column pair inside an MMA fragment
     const int mi = lane >> 3;     // ldmatrix: which 8x8 matrix this lane addresses
     const int ri = lane & 7;      // ldmatrix: which row of it
-    const int qrow0 = a.n_hblk == 1 ? hw * G : 0;     // this head's first query row in the buffer
+    // the query-buffer row of this lane's ldmatrix row (m = (mi & 1)·8 + ri of each 16-row MMA
+    // tile): decode, the head's rows from qrow0; chunked prefill, token m / G of the box's
+    // [token][HG·G heads] rows, or a zero padding row past the block's tokens
+    const int qrow0 = a.n_hblk == 1 ? hw * G : 0;
+    const int qm = (mi & 1) * 8 + ri;
+    const int my_qrow = !CH ? qrow0 + qm
+                      : qm < ntok * G ? (qm / G) * (HG * G) + hw * G + qm % G : ntok * HG * G;
     bool ok = true;               // false once a wait has given up: the warp then only keeps
                                   // step with its partners at the named barriers
     int g = 0, k = 0;
     Piece p;
-    while (walk.next(p)) {
+    while (next_piece(p)) {
+        const SegG si = seg_info(p);
         const int qb = k & 1;
         const uint32_t qbase = sbase + C::Q_OFF + qb * L.q_buf;
         if (ok && !mbar_wait_bounded(qfull0 + 8 * qb, (k >> 1) & 1, &g_decode_gqa_status, kStatusFullWait)) ok = false;
         float o[MT][D / 8][4];
         float m[MT][2], l[MT][2];
+        // chunked prefill: the key limit of this thread's two rows (g8 and g8 + 8: tokens
+        // (g8) / G and (g8 + 8) / G of the block; 0 for rows past its new tokens). Their running
+        // maxima start at −1e30 rather than −∞: a row may see no visible key in a slice or a
+        // whole piece, and 2^(−∞ − (−1e30)) = 0 is then its weight, where −∞ − (−∞) is NaN.
+        int lim[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int tok = (r * 8 + g8) / G;
+            lim[r] = CH && r * 8 + g8 < ntok * G && tok < si.nvalid ? si.kbase + tok + 1 : 0;
+        }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                m[mt][r] = -INFINITY;
+                m[mt][r] = CH ? -1e30f : -INFINITY;
                 l[mt][r] = 0.f;
             }
 #pragma unroll
@@ -321,14 +436,16 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
                         for (int mt = 0; mt < MT; ++mt) {
                             uint32_t a0, a1, a2, a3;
                             const int ca = 2 * kk + (mi >> 1);
-                            ldsm_x4(qbase + (ca >> 2) * L.q_box + sw64(qrow0 + mt * 16 + (mi & 1) * 8 + ri, ca), a0, a1,
-                                    a2, a3);
+                            ldsm_x4(qbase + (ca >> 2) * L.q_box + sw64(my_qrow + mt * 16, ca), a0, a1, a2, a3);
                             mma_bf16_16816(sc[mt][0], a0, a1, a2, a3, b0, b1);
                             mma_bf16_16816(sc[mt][1], a0, a1, a2, a3, b2, b3);
                         }
                     }
                     // online softmax (base 2) and P in bf16 as the A operand of P·V
-                    uint32_t pa[MT][4];
+                    // chunked prefill also keeps each weight's bf16 residual (p − bf16(p)) and
+                    // multiplies it with V as well: rows of a chunk near a sequence's start see
+                    // only a few keys, where a 2^-9 rounding of each weight does not average away
+                    uint32_t pa[MT][4], pres[MT][4];
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
@@ -339,7 +456,9 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
 #pragma unroll
                                 for (int e = 0; e < 2; ++e) {
                                     const int tok = nt * 8 + 2 * cq + e;
-                                    x[nt * 2 + e] = tok < n_valid ? sc[mt][nt][2 * r + e] * a.scale_log2 : -INFINITY;
+                                    const bool vis = tok < n_valid &&
+                                                     (!CH || (p.i0 + i) * TT + r0 + tok < lim[r]);
+                                    x[nt * 2 + e] = vis ? sc[mt][nt][2 * r + e] * a.scale_log2 : -INFINITY;
                                 }
                             float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
                             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -355,7 +474,14 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
                             pa[mt][r] = lo;
                             pa[mt][2 + r] = hi;
                             // the row sum uses the rounded weights, so Σ weights = 1 after normalising
-                            const float ps = bf16_lo(lo) + bf16_hi(lo) + bf16_lo(hi) + bf16_hi(hi);
+                            float ps = bf16_lo(lo) + bf16_hi(lo) + bf16_lo(hi) + bf16_hi(hi);
+                            if constexpr (CH) {
+                                const uint32_t lo2 = pack_bf16x2(pr[0] - bf16_lo(lo), pr[1] - bf16_hi(lo));
+                                const uint32_t hi2 = pack_bf16x2(pr[2] - bf16_lo(hi), pr[3] - bf16_hi(hi));
+                                pres[mt][r] = lo2;
+                                pres[mt][2 + r] = hi2;
+                                ps += bf16_lo(lo2) + bf16_hi(lo2) + bf16_lo(hi2) + bf16_hi(hi2);
+                            }
                             l[mt][r] = l[mt][r] * alpha + ps;
 #pragma unroll
                             for (int nd = 0; nd < D / 8; ++nd) {
@@ -374,6 +500,11 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
                         for (int mt = 0; mt < MT; ++mt) {
                             mma_bf16_16816(o[mt][2 * pq], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], b0, b1);
                             mma_bf16_16816(o[mt][2 * pq + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], b2, b3);
+                            if constexpr (CH) {
+                                mma_bf16_16816(o[mt][2 * pq], pres[mt][0], pres[mt][1], pres[mt][2], pres[mt][3], b0, b1);
+                                mma_bf16_16816(o[mt][2 * pq + 1], pres[mt][0], pres[mt][1], pres[mt][2], pres[mt][3], b2,
+                                               b3);
+                            }
                         }
                     }
                 }
@@ -385,9 +516,9 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
         __syncwarp();
         if (lane == 0) mbar_arrive(qempty0 + 8 * qb);
 
-        const int j = p.gi * HG + hw;                          // this warp's KV head
-        const int n_rows = min(heads, G - p.hb * C::HEADS);    // its query heads in this block
-        const size_t out_row0 = (size_t)p.b * a.Hq + j * G + p.hb * C::HEADS;
+        const int j = si.gi * HG + hw;                         // this warp's KV head
+        // its query rows in this block: heads (decode) or new tokens × heads (chunked prefill)
+        const int n_rows = CH ? heads : min(heads, G - si.hb * C::HEADS);
         const int slot = 2 * c + (k == 0 ? 0 : 1);
         const size_t part_row0 = (size_t)slot * HG * heads + hw * heads;
         if constexpr (WPH == 1) {
@@ -400,9 +531,9 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
                     lr += __shfl_xor_sync(0xffffffffu, lr, 1);
                     lr += __shfl_xor_sync(0xffffffffu, lr, 2);
                     const int h = mt * 16 + r * 8 + g8;
-                    if (h >= n_rows) continue;
+                    if (h >= n_rows || (p.whole && !row_valid(si, h))) continue;
                     const float inv = ok && lr > 0.f ? 1.f / lr : 0.f;
-                    float *dst = p.whole ? a.out + (out_row0 + h) * D : a.o_part + (part_row0 + h) * D;
+                    float *dst = p.whole ? a.out + out_row(si, j, h) * D : a.o_part + (part_row0 + h) * D;
 #pragma unroll
                     for (int nd = 0; nd < D / 8; ++nd)
                         *reinterpret_cast<float2 *>(dst + nd * 8 + 2 * cq) =
@@ -461,9 +592,9 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
 #pragma unroll
                 for (int w = 0; w < WPH; ++w)
                     val = fmaf(scr[((hh * WPH + w) * heads + h) * (D + 2) + d], fac[fi * (WPH + 1) + w], val);
-                const int jj = p.gi * HG + hh;
+                const int jj = si.gi * HG + hh;
                 if (p.whole) {
-                    a.out[((size_t)p.b * a.Hq + jj * G + p.hb * C::HEADS + h) * D + d] = val;
+                    if (row_valid(si, h)) a.out[out_row(si, jj, h) * D + d] = val;
                 } else {
                     const size_t pr = (size_t)slot * HG * heads + hh * heads + h;
                     a.o_part[pr * D + d] = val;
@@ -480,7 +611,9 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
         if (!p.whole) {
             const Piece &q = p;
             const int nb = stream_tiles(q.S, TT);
-            const long long fs = (long long)seg_per_seq * prefix[q.b] + (long long)(q.gi * a.n_hblk + q.hb) * nb;
+            // the segment's first tile in the stream
+            const long long fs = (CH ? (long long)prefix[q.b] : (long long)seg_per_seq * prefix[q.b]) +
+                                 (long long)si.q * nb;
             // the partial slots of all blocks holding tiles of this segment: blocks c0 .. c1, or,
             // with fewer tiles than blocks (each block then owns at most one tile), the owners of
             // the segment's nb tiles
@@ -492,7 +625,7 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
                 if (i == 0) return stream_start(c0, T, a.n_blocks) < fs ? 2 * c0 + 1 : 2 * c0;
                 return 2 * (c0 + i);
             };
-            const int seg = q.b * seg_per_seq + q.gi * a.n_hblk + q.hb;
+            const int seg = si.seg;
             // rows of heads hh0 .. hh0+n_hh-1 of the group, merged by n_thr threads from t0:
             // partial row bases cached in wl, their lse values in wc
             auto merge_rows = [&](int hh0, int n_hh, int t0, int n_thr, int *wl, float *wc) {
@@ -533,10 +666,11 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
                             }
                     }
                     const float inv = W > 0.f ? 1.f / W : 0.f;
-                    const int jj = q.gi * HG + hh0 + r / n_rows;
-                    float4 *dst = reinterpret_cast<float4 *>(
-                        a.out + ((size_t)q.b * a.Hq + jj * G + q.hb * C::HEADS + r % n_rows) * D);
-                    dst[col] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                    const int jj = si.gi * HG + hh0 + r / n_rows;
+                    if (row_valid(si, r % n_rows)) {
+                        float4 *dst = reinterpret_cast<float4 *>(a.out + out_row(si, jj, r % n_rows) * D);
+                        dst[col] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                    }
                 }
             };
             if constexpr (WPH == 1) {
@@ -577,11 +711,12 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
 }
 
 // Ring depth per configuration: about 192 KB of K/V in flight per SM, less where the
-// combine scratch of warps sharing a head needs room.
-template <int D, int MT, int HG, int NC>
+// combine scratch of warps sharing a head needs room, or (chunked prefill) the query buffers
+// hold several new tokens of every head of the group.
+template <int D, int MT, int HG, int NC, bool CH>
 constexpr int ring_depth() {
     constexpr int stage = 2 * (D / 32) * HG * (HG == 4 ? 32 : 16 * NC) * 64;
-    constexpr int budget = HG == 4 ? 192 * 1024 : MT == 2 ? 128 * 1024 : 176 * 1024;
+    constexpr int budget = (HG == 4 ? 192 * 1024 : MT == 2 ? 128 * 1024 : 176 * 1024) - (CH ? 40 * 1024 : 0);
     constexpr int n = budget / stage;
     return n < 2 ? 2 : n;
 }
@@ -607,16 +742,18 @@ int sm_count() {
     return n;
 }
 
-template <int D, int MT, int HG, int NC>
+template <int D, int MT, int HG, int NC, bool CH>
 cudaError_t launch_cfg(const DecodeStreamArgs &a, cudaStream_t st) {
-    constexpr int NS = ring_depth<D, MT, HG, NC>();
+    constexpr int NS = ring_depth<D, MT, HG, NC, CH>();
     using C = Cfg<D, MT, HG, NS, NC>;
     const int G = a.Hq / a.Hkv;
     // query rows: the group's HG·G rows (one head block when n_hblk > 1), plus the padding
-    // the last head's 16·MT-row MMA tile reaches past them
-    const int q_loaded = a.n_hblk == 1 ? HG * G : a.heads;
-    const int q_rows = ((a.n_hblk == 1 ? (HG - 1) * G : 0) + 16 * MT + 7) / 8 * 8;
-    const Layout L = layout<D, MT, HG, NS, NC>(q_rows, a.heads, a.B, a.n_blocks);
+    // the last head's 16·MT-row MMA tile reaches past them; chunked prefill, nt tokens × HG·G
+    // heads, plus one zero row that stands for the rows past the block's tokens
+    const int q_loaded = CH ? a.nt * HG * G : a.n_hblk == 1 ? HG * G : a.heads;
+    const int q_rows = CH ? (q_loaded + 1 + 7) / 8 * 8
+                          : ((a.n_hblk == 1 ? (HG - 1) * G : 0) + 16 * MT + 7) / 8 * 8;
+    const Layout L = layout<D, MT, HG, NS, NC>(q_rows, a.heads, a.B, a.n_blocks, CH);
     if (L.total > 227 * 1024) return cudaErrorInvalidValue;
     CUtensorMap km, vm, qm;
     const uint64_t dims[4] = {(uint64_t)D, (uint64_t)a.Hkv, (uint64_t)a.S_max, (uint64_t)a.B};
@@ -628,14 +765,16 @@ cudaError_t launch_cfg(const DecodeStreamArgs &a, cudaStream_t st) {
         e = encode_tensor_map(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.v, dims, strides, box,
                               CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (e == cudaSuccess) {
-        const uint64_t qdims[3] = {(uint64_t)D, (uint64_t)a.Hq, (uint64_t)a.B};
+        // decode: [B, Hq, D], a box of q_loaded heads of one sequence; chunked prefill:
+        // [T, Hq, D], a box of HG·G heads × nt packed rows
+        const uint64_t qdims[3] = {(uint64_t)D, (uint64_t)a.Hq, (uint64_t)(CH ? a.T : a.B)};
         const uint64_t qstrides[2] = {(uint64_t)D * 2, (uint64_t)a.Hq * D * 2};
-        const uint32_t qbox[3] = {32, (uint32_t)q_loaded, 1};
+        const uint32_t qbox[3] = {32, (uint32_t)(CH ? HG * G : q_loaded), (uint32_t)(CH ? a.nt : 1)};
         e = encode_tensor_map(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, qdims, qstrides, qbox,
                               CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     }
     if (e != cudaSuccess) return e;
-    auto kern = decode_gqa_bf16_kernel<D, MT, HG, NS, NC>;
+    auto kern = decode_gqa_bf16_kernel<D, MT, HG, NS, NC, CH>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
     if (e != cudaSuccess) return e;
     e = launch_pdl(kern, dim3(a.n_blocks), dim3(C::kThreads), L.total, st, km, vm, qm, a, L, q_loaded);
@@ -645,18 +784,24 @@ cudaError_t launch_cfg(const DecodeStreamArgs &a, cudaStream_t st) {
 // One KV head per tile with a single MMA row tile per head: 7 consumer warps over 112-token
 // tiles, for nearly twice the latency hiding per SM (8 warps in all keep 255 registers per
 // thread available; the combine scratch of 32-row heads would not fit beside them).
-template <int D, int MT>
+template <int D, int MT, bool CH>
 cudaError_t launch_mt(const DecodeStreamArgs &a, cudaStream_t st) {
     switch (a.hg) {
-        case 4: return launch_cfg<D, MT, 4, 4>(a, st);
-        case 2: return launch_cfg<D, MT, 2, 4>(a, st);
-        default: return MT == 1 ? launch_cfg<D, MT, 1, 7>(a, st) : launch_cfg<D, MT, 1, 4>(a, st);
+        case 4: return launch_cfg<D, MT, 4, 4, CH>(a, st);
+        case 2: return launch_cfg<D, MT, 2, 4, CH>(a, st);
+        default: return MT == 1 ? launch_cfg<D, MT, 1, 7, CH>(a, st) : launch_cfg<D, MT, 1, 4, CH>(a, st);
     }
 }
 
 template <int D>
 cudaError_t launch_d(const DecodeStreamArgs &a, cudaStream_t st) {
-    return mt_for(a.Hq / a.Hkv) == 1 ? launch_mt<D, 1>(a, st) : launch_mt<D, 2>(a, st);
+    return mt_for(a.Hq / a.Hkv) == 1 ? launch_mt<D, 1, false>(a, st) : launch_mt<D, 2, false>(a, st);
+}
+
+// Chunked prefill: one 16-row MMA tile per KV head (MT = 1) holds 16 / G new tokens.
+template <int D>
+cudaError_t launch_d_chunk(const DecodeStreamArgs &a, cudaStream_t st) {
+    return launch_mt<D, 1, true>(a, st);
 }
 
 }  // namespace
@@ -730,6 +875,81 @@ cudaError_t launch_decode_gqa_stream(const DecodeStreamArgs &a0, cudaStream_t st
         default: return cudaErrorInvalidValue;
     }
     return e;
+}
+
+// ------------------------------------------------------------------ chunked prefill
+// Query groups of up to 16 heads: 16 / G new tokens × G heads fill one 16-row MMA tile per KV
+// head, and every cached row a block reads feeds all of them. The grid is one block per SM
+// over the balanced split (the segments depend on the device-side chunk lengths); at most
+// ceil((T + B·(nt − 1)) / nt) query blocks of Hkv / HG segments each.
+static int chunk_tokens(int G) { return 16 / G; }
+
+bool decode_gqa_stream_chunk_eligible(int Hq, int Hkv) { return Hq / Hkv <= 16; }
+
+static long long stream_chunk_segs(int B, int T, int Hq, int Hkv) {
+    const int G = Hq / Hkv, nt = chunk_tokens(G);
+    return (T + (long long)B * (nt - 1)) / nt * (Hkv / hg_for(Hkv, G));
+}
+
+// Aligned chunk plan: when the (sequence, KV head) pairs number between half the SMs and all
+// of them, each gets a block that walks its query blocks itself (one pass over the cache for a
+// chunk of up to 16 / G tokens) and nothing is shared or merged, as for the decode.
+static bool stream_chunk_aligned(int B, int Hkv, int n_split) {
+    const long long pairs = (long long)B * Hkv;
+    const int sms = sm_count();
+    return n_split == 0 && pairs <= sms && 2 * pairs >= sms;
+}
+
+int decode_gqa_stream_chunk_blocks(int B, int T, int Hq, int Hkv, int n_split) {
+    if (stream_chunk_aligned(B, Hkv, n_split)) return B * Hkv;
+    long long n = sm_count();
+    if (n_split > 0) {
+        const long long cap = (long long)n_split * stream_chunk_segs(B, T, Hq, Hkv);
+        if (cap < n) n = cap;
+    }
+    return (int)(n < 1 ? 1 : n);
+}
+
+// Workspace: one arrival counter per (segment, KV head of its group) in the counter region,
+// then two partial slots of HG·(nt·G) rows per block and their log-sum-exps.
+size_t decode_gqa_stream_chunk_workspace(int B, int T, int Hq, int Hkv, int D, int n_split) {
+    const int G = Hq / Hkv, hg = hg_for(Hkv, G);        // (the aligned plan needs no more)
+    const size_t rows = 2 * (size_t)decode_gqa_stream_chunk_blocks(B, T, Hq, Hkv, n_split) * hg * chunk_tokens(G) * G;
+    const size_t n_cnt = (size_t)stream_chunk_segs(B, T, Hq, Hkv) * hg;
+    return counter_region_bytes(n_cnt) + (rows * D * sizeof(float) + 255) / 256 * 256 +
+           (rows * sizeof(float) + 255) / 256 * 256;
+}
+
+cudaError_t launch_decode_gqa_stream_chunk(const void *q, const void *k, const void *v, const int *cu_q,
+                                           const int *start_pos, float *out, int B, int T, int Hq, int Hkv, int D,
+                                           float scale_log2, int S_max, int n_split, void *ws, cudaStream_t st) {
+    DecodeStreamArgs a{};
+    const int G = Hq / Hkv;
+    a.q = q; a.k = k; a.v = v; a.out = out; a.cu_q = cu_q; a.start_pos = start_pos;
+    a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.T = T;
+    a.scale_log2 = scale_log2;
+    a.S_max = S_max;
+    a.nt = chunk_tokens(G);
+    a.heads = a.nt * G;
+    a.n_hblk = 1;
+    a.aligned = stream_chunk_aligned(B, Hkv, n_split) ? 1 : 0;
+    a.hg = a.aligned ? 1 : hg_for(Hkv, G);
+    a.tile_tokens = a.hg == 4 ? 32 : a.hg == 1 ? 112 : 64;
+    a.n_blocks = decode_gqa_stream_chunk_blocks(B, T, Hq, Hkv, n_split);
+    const size_t rows = 2 * (size_t)a.n_blocks * a.hg * a.heads;
+    const size_t n_cnt = (size_t)stream_chunk_segs(B, T, Hq, Hkv) * a.hg;
+    char *w = static_cast<char *>(ws);
+    a.counters = reinterpret_cast<int *>(w);
+    a.o_part = reinterpret_cast<float *>(w + counter_region_bytes(n_cnt));
+    a.lse_part = reinterpret_cast<float *>(w + counter_region_bytes(n_cnt) + (rows * D * sizeof(float) + 255) / 256 * 256);
+    cudaError_t e = clear_overflow_counters(a.counters, n_cnt, st);
+    if (e != cudaSuccess) return e;
+    switch (D) {
+        case 64: return launch_d_chunk<64>(a, st);
+        case 96: return launch_d_chunk<96>(a, st);
+        case 128: return launch_d_chunk<128>(a, st);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 int decode_gqa_read_and_clear_status(cudaStream_t s, unsigned *flag) {

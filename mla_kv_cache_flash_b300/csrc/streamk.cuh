@@ -115,4 +115,22 @@ struct ChunkPieceWalker {
     }
 };
 
+// Chunked prefill with one block per (sequence b, KV head j): the block's pieces are the
+// segments of its query blocks, q = qb·per_qb + j for qb = 0 .. nqb − 1, each whole.
+struct AlignedChunkWalker {
+    int b, j, per_qb, nqb, S, tile, qb;
+    __device__ bool next(Piece &p) {
+        if (qb >= nqb) return false;
+        p.b = b;
+        p.gi = qb * per_qb + j;
+        p.hb = 0;
+        p.S = S;
+        p.i0 = 0;
+        p.n_t = stream_tiles(S, tile);
+        p.whole = true;
+        ++qb;
+        return true;
+    }
+};
+
 }  // namespace mlakv

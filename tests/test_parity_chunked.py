@@ -50,9 +50,11 @@ def test_chunked_fp32(hq, hkv, d):
 
 
 # (32, 2, 128), (32, 1, 128) and (64, 2, 128): 16 or 32 query heads per KV head at D = 128,
-# the tcgen05 form (4 new tokens × 16 heads per block); the others the CUDA-core form
+# the tcgen05 form (4 new tokens × 16 heads per block); the others, up to 16 heads per KV
+# head, the register-MMA form (16 / G new tokens × G heads per 16-row MMA tile: 8 × 2, 4 × 4,
+# 1 × 16, 5 × 3 with a spare row, 2 × 8, and KV-head groups of 4, 2 and 1)
 @pytest.mark.parametrize("hq,hkv,d", [(8, 4, 96), (32, 8, 128), (16, 1, 64), (32, 2, 128), (32, 1, 128),
-                                      (64, 2, 128)])
+                                      (64, 2, 128), (12, 4, 64), (6, 3, 96), (64, 8, 128), (16, 2, 96)])
 def test_chunked_bf16(hq, hkv, d):
     _check(((1000, 64), (0, 129), (2047, 1), (127, 128)), hq, hkv, d, 2048, "bf16", hq + 2 * d, 3e-3)
 
