@@ -365,9 +365,9 @@ class DecodeGqaStep(DecodeGqa):
 class DecodeGqaFp8(DecodeGqa):
     """The MiniMind decode batch over an E4M3 cache with per-row fp32 K and V scales.
     Algorithmic bytes: each live code once plus its row's scale."""
-    kernel_src = "mla_kv_cache_flash_b300/csrc/decode_gqa_fma.cu"
+    kernel_src = "mla_kv_cache_flash_b300/csrc/decode_fp8.cu"
     call = "attn_decode_gqa_fp8 call: "
-    launch_note = " (CUDA-core decode, then the merge launch when the plan splits)"
+    launch_note = " (tensor-core fp8 decode over persistent blocks, shared segments merged in-kernel)"
 
     def __init__(self, w, device, rank, l2_bytes):
         import mla_kv_cache_flash_b300 as mk
@@ -386,7 +386,7 @@ class DecodeGqaFp8(DecodeGqa):
         nb = mk.decode_gqa_workspace_size(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, self.max_s,
                                           mk.ATTN_FP8_E4M3)
         self.ws = torch.zeros(max(nb, 1), dtype=torch.uint8, device=device)
-        self.launches_per_step = 1 + (self.n_split > 1)
+        self.launches_per_step = 1      # two query heads per KV head: the one-launch tensor-core kernel
         self.l2_note = f"rotating {n_sets} distinct fp8 caches ({n_sets * cache_bytes / 1e6:.0f} MB, L2 {l2_bytes / 1e6:.0f} MB)"
 
     def _run(self, s):

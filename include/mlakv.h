@@ -159,7 +159,14 @@ int attn_decode_gqa_noalloc(const void *q, const void *k_cache, const void *v_ca
  *   seq_lens, out, scale, S_max, max_S, n_split, workspace: as attn_decode_gqa with
  *   dtype = ATTN_FP8_E4M3 (use that dtype for the workspace and split queries). D in
  *   {64, 96, 128}. attn_decode_gqa itself refuses ATTN_FP8_E4M3 (it has no scales).
- * CUDA-core kernel: split partials merged by a second launch (as for fp32 caches).
+ * Up to 16 query heads per KV head: one launch on the tensor cores (mma.sync, codes widened
+ * exactly to fp16 in registers, the weights times each row's V scale split into two fp16
+ * parts so the products keep fp32 accuracy), the work balanced over persistent thread
+ * blocks as for bf16 caches (n_split > 0 caps the blocks at n_split per (sequence, KV
+ * head)); the workspace then holds one arrival counter per (sequence, KV head) in its
+ * counter region, under the bf16 rules (zero-filled before first use, left zero by every
+ * completed call). More query heads per KV head: the CUDA-core kernel, split partials
+ * merged by a second launch (as for fp32 caches).
  * ------------------------------------------------------------------------------------- */
 int attn_decode_gqa_fp8(const void *q, const void *k_cache, const void *v_cache,
                         const float *k_scale, const float *v_scale, const int *seq_lens,

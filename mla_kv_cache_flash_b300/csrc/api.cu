@@ -91,8 +91,16 @@ constexpr int kFmaTile = 128;
 
 bool gqa_use_fma(attn_dtype dtype) { return dtype == ATTN_F32 || dtype == ATTN_FP8_E4M3; }
 
+// E4M3 caches with up to 16 query heads per KV head run on the tensor-core fp8 kernel (the
+// balanced split over persistent blocks, merged in-kernel); others on the CUDA-core kernel.
+bool fp8_on_mma(int B, int Hq, int Hkv, int D, attn_dtype dtype) {
+    return dtype == ATTN_FP8_E4M3 && decode_fp8_mma_eligible(B, Hq, Hkv, D);
+}
+
 SplitPlan gqa_plan(int B, int Hq, int Hkv, int D, int max_S, attn_dtype dtype, int n_split) {
     const int G = Hq / Hkv;
+    // the fp8 tensor-core kernel: n_split reports the persistent grid size
+    if (fp8_on_mma(B, Hq, Hkv, D, dtype)) return SplitPlan{decode_fp8_blocks(B, Hq, Hkv, D, n_split), 0};
     if (gqa_use_fma(dtype)) {
         const int hb = (G % 8 == 0) ? 8 : (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
         // 128-thread blocks: up to 8 resident per SM for 1-2 stacked heads (≈40 registers a
@@ -228,6 +236,7 @@ MLAKV_API size_t attn_decode_gqa_workspace_size(int B, int Hq, int Hkv, int D, i
     if (!gqa_use_fma(dtype))
         return decode_tc_gqa_eligible(B, Hq, Hkv, D) ? decode_tc_gqa_workspace(B, Hq, Hkv, n_split)
                                                      : decode_gqa_stream_workspace(B, Hq, Hkv, D, n_split);
+    if (fp8_on_mma(B, Hq, Hkv, D, dtype)) return decode_fp8_workspace(B, Hq, Hkv, D, n_split);
     const SplitPlan p = gqa_plan(B, Hq, Hkv, D, max_S, dtype, n_split);
     return partials_bytes(B, Hq, D, p.n_split);
 }
@@ -299,6 +308,17 @@ MLAKV_API int attn_decode_gqa_fp8(const void *q, const void *k_cache, const void
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_scale) ||
         !aligned16(v_scale) || !aligned16(out) || !aligned16(seq_lens))
         return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_gqa_fp8: every pointer must be 16-byte aligned");
+    if (fp8_on_mma(B, Hq, Hkv, D, ATTN_FP8_E4M3)) {
+        const size_t need = decode_fp8_workspace(B, Hq, Hkv, D, n_split);
+        if (!workspace || ws_bytes < need || !aligned16(workspace))
+            return fail(ATTN_ERR_WORKSPACE, "attn_decode_gqa_fp8: workspace of %zu bytes (16-byte aligned) needed, "
+                        "got %zu at %p", need, workspace ? ws_bytes : (size_t)0, workspace);
+        const cudaError_t e = launch_decode_fp8_mma(q, k_cache, v_cache, k_scale, v_scale, seq_lens, out, B, Hq, Hkv,
+                                                    D, scale * kLog2e, S_max, n_split, workspace,
+                                                    reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "attn_decode_gqa_fp8: kernel launch");
+        return ok();
+    }
     DecodeGqaArgs a{};
     a.q = q; a.k = k_cache; a.v = v_cache; a.seq_lens = seq_lens; a.out = out;
     a.k_scale = k_scale; a.v_scale = v_scale;
@@ -556,6 +576,7 @@ MLAKV_API int attn_check_status(mlakv_stream_t stream) {
     if (rc == 0) rc = decode_tc_read_and_clear_status(s, &f), flag |= f;
     if (rc == 0) rc = prefill_read_and_clear_status(s, &f), flag |= f;
     if (rc == 0) rc = selftest_read_and_clear_status(s, &f), flag |= f;
+    if (rc == 0) rc = decode_fp8_read_and_clear_status(s, &f), flag |= f;
     if (rc != 0) return cuda_fail((cudaError_t)rc, "attn_check_status: reading the device flags");
     if (flag != 0) {
         // a decode that gave up may have left arrival counters set in the built-in scratch

@@ -106,6 +106,16 @@ MLAKV_HIDDEN cudaError_t launch_decode_gqa_stream_chunk(const void *q, const voi
                                                         const int *cu_q, const int *start_pos, float *out, int B,
                                                         int T, int Hq, int Hkv, int D, float scale_log2, int S_max,
                                                         int n_split, void *ws, cudaStream_t st);
+// K1 over an E4M3 cache on the tensor cores (mma.sync, up to 16 query heads per KV head): TMA
+// code tiles widened to fp16 in shared memory, the balanced split over persistent blocks, shared
+// segments merged in-kernel (arrival counters in the workspace's counter region).
+MLAKV_HIDDEN bool decode_fp8_mma_eligible(int B, int Hq, int Hkv, int D);
+MLAKV_HIDDEN int decode_fp8_blocks(int B, int Hq, int Hkv, int D, int n_split);
+MLAKV_HIDDEN size_t decode_fp8_workspace(int B, int Hq, int Hkv, int D, int n_split);
+MLAKV_HIDDEN cudaError_t launch_decode_fp8_mma(const void *q, const void *k, const void *v, const float *k_scale,
+                                               const float *v_scale, const int *seq_lens, float *out, int B, int Hq,
+                                               int Hkv, int D, float scale_log2, int S_max, int n_split, void *ws,
+                                               cudaStream_t st);
 // K2: log-sum-exp merge of the split partials.
 MLAKV_HIDDEN cudaError_t launch_merge(const float *o_part, const float *lse_part, float *out,
                                       int rows, int n_split, int Dv, cudaStream_t s);
@@ -147,6 +157,7 @@ MLAKV_HIDDEN int decode_gqa_read_and_clear_status(cudaStream_t s, unsigned *flag
 MLAKV_HIDDEN int decode_tc_read_and_clear_status(cudaStream_t s, unsigned *flag);
 MLAKV_HIDDEN int prefill_read_and_clear_status(cudaStream_t s, unsigned *flag);
 MLAKV_HIDDEN int selftest_read_and_clear_status(cudaStream_t s, unsigned *flag);
+MLAKV_HIDDEN int decode_fp8_read_and_clear_status(cudaStream_t s, unsigned *flag);
 // Zeroes the counter region of the built-in no-alloc scratch on the current device (after a
 // timeout); synchronous.
 MLAKV_HIDDEN int noalloc_clear_counters(cudaStream_t s);

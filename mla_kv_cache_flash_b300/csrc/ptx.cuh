@@ -22,6 +22,7 @@ enum : unsigned {
     kStatusEmptyWait = 2u,    // the producer gave up waiting for a stage to be released
     kStatusDrainWait = 4u,    // the producer gave up draining its last copies
     kStatusMmaWait = 8u,      // a tensor-core commit never arrived
+    kStatusPublishWait = 16u, // a block's producer gave up waiting for its consumers' partial rows
     kStatusSelfTest = 0x100u  // the self-test wait ran out (expected)
 };
 
@@ -121,6 +122,11 @@ __device__ __forceinline__ bool bar_any(int id, int nthreads, bool v) {
 
 __device__ __forceinline__ void bar_sync_named(int id, int nthreads) {
     asm volatile("barrier.cta.sync.aligned %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Arrive on named barrier `id` (of `nthreads` threads) without waiting for it.
+__device__ __forceinline__ void bar_arrive_named(int id, int nthreads) {
+    asm volatile("barrier.cta.arrive.aligned %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // 4-D tiled TMA load into shared memory, completing `bytes` on `bar`.

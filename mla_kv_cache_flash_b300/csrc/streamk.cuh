@@ -81,6 +81,62 @@ struct PieceWalker {
     }
 };
 
+// The same walk, incremental: the start position (sequence b, segment q of it, tile i0 of
+// that) is found once, lane-parallel, by seq_walk_start; each further piece then follows from
+// the previous one without a search or a division (a search and two divisions cost a single
+// thread about a thousand cycles, paid at every piece start on the critical path).
+struct SeqWalker {
+    const int *prefix;          // prefix[b] = Σ_{b' < b} tiles(S_b'), b = 0 .. B
+    const int *seq_lens;
+    int B, seg_per_seq;
+    int b, q, i0;
+    long long t, t_end;
+    __device__ bool next(Piece &p) {
+        if (t >= t_end) return false;
+        const int nb = prefix[b + 1] - prefix[b];
+        const long long left = t_end - t;
+        const int n_t = left < nb - i0 ? (int)left : nb - i0;
+        p.b = b;
+        p.S = seq_lens[b];
+        p.gi = q;
+        p.hb = 0;
+        p.i0 = i0;
+        p.n_t = n_t;
+        p.whole = i0 == 0 && n_t == nb;
+        t += n_t;
+        i0 += n_t;
+        if (i0 == nb) {
+            i0 = 0;
+            if (++q == seg_per_seq) {
+                q = 0;
+                do {
+                    ++b;
+                } while (b < B && prefix[b + 1] == prefix[b]);
+            }
+        }
+        return true;
+    }
+};
+
+// Start position of tile t0 < T for a SeqWalker, by all 32 lanes of a warp: the sequence whose
+// tiles hold t0 by a ballot over 32 sequences at a time, then one division. Every lane
+// returns the same (b, q, i0).
+__device__ __forceinline__ void seq_walk_start(const int *prefix, int B, int seg_per_seq, long long t0, int lane,
+                                               int &b, int &q, int &i0) {
+    b = 0;
+    for (int base = 0; base < B; base += 32) {
+        const int bb = base + lane;
+        const bool hit = bb < B && (long long)seg_per_seq * prefix[bb] <= t0 &&
+                         t0 < (long long)seg_per_seq * prefix[bb + 1];
+        const unsigned m = __ballot_sync(0xffffffffu, hit);
+        if (m) {
+            b = base + __ffs(m) - 1;
+            break;
+        }
+    }
+    split_offset(t0 - (long long)seg_per_seq * prefix[b], prefix[b + 1] - prefix[b], q, i0);
+}
+
 // Chunked prefill: sequence b owns nseg_b segments (its query blocks × KV heads × head
 // blocks), each over the same lens[b] keys (the keys its last new token sees); prefix[b]
 // counts the tiles of the sequences before b with that multiplicity. A piece's `gi` is its

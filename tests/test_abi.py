@@ -164,11 +164,15 @@ def test_fp8_unsupported(L, kw):
 
 
 def test_fp8_workspace(L):
-    # the CUDA-core plan: partials for every split when there is more than one
+    # the tensor-core fp8 plan: persistent blocks, three resident per SM (148 SMs without a
+    # GPU), each with two partial slots of G rows after the counter region; n_split > 0 caps
+    # the blocks at n_split per (sequence, KV head)
     n = L.attn_decode_gqa_num_splits(2, 8, 4, 96, 4096, 2, 0)
-    assert n > 1
+    assert n == 3 * 148
+    assert L.attn_decode_gqa_num_splits(2, 8, 4, 96, 4096, 2, 5) == 5 * 2 * 4
+    up = lambda x: (x + 255) // 256 * 256
     assert L.attn_decode_gqa_workspace_size(2, 8, 4, 96, 4096, 2, 0) == \
-        L.attn_decode_gqa_workspace_size(2, 8, 4, 96, 4096, 0, 0)
+        (64 << 10) + up(2 * n * 2 * 96 * 4) + up(2 * n * 2 * 4)
     assert fp8(L, S_max=4096, max_S=4096, n_split=0) == WS
 
 

@@ -1,8 +1,11 @@
 """GQA decode over an E4M3 cache with per-row K and V scales (attn_decode_gqa_fp8) against
 the fp64 CPU oracle.
 
-The codes widen to fp32 exactly and the bf16 query is exact in fp32, so the kernel does the
-fp32 cache path's arithmetic on exact inputs; the bound is that path's, max |Δ| ≤ 1e-5.
+The codes widen exactly (to fp32, or to fp16 for the tensor-core kernel), the bf16 query is
+exact in fp32 (in fp16 too for |q| in [2^-14, 65504], within 2^-25 below), so the scores are
+products summed in fp32; the tensor-core kernel multiplies V by each weight times its row's V
+scale (and 2^10) split into an fp16 head and residual, which leaves about 2^-22 of the weight.
+The bound is the fp32 cache path's, max |Δ| ≤ 1e-5.
 """
 
 import numpy as np
@@ -33,7 +36,10 @@ def _ref(inp, scale):
                                  scale)
 
 
-@pytest.mark.parametrize("hq,hkv,d", [(8, 4, 96), (8, 8, 64), (8, 1, 128), (32, 8, 128), (6, 3, 96)])
+# up to 16 query heads per KV head: the tensor-core kernel (one 8-column block of heads up
+# to 8, two up to 16); (32, 1, 128), (24, 1, 64), (64, 1, 64): the CUDA-core kernel
+@pytest.mark.parametrize("hq,hkv,d", [(8, 4, 96), (8, 8, 64), (8, 1, 128), (32, 8, 128), (6, 3, 96), (16, 1, 128),
+                                      (12, 1, 96), (32, 1, 128), (24, 1, 64), (64, 1, 64)])
 def test_fp8_ragged(hq, hkv, d):
     lens = (0, 1, 127, 128, 129, 300, 1000)
     w = W.DecodeWorkload("fp8_ragged", 5, len(lens), hq, hkv, d, 1000, "bf16", lengths=lens, sub=hq + d)
@@ -45,13 +51,23 @@ def test_fp8_ragged(hq, hkv, d):
         assert torch.all(out[0] == 0)
 
 
-def test_fp8_single_token_is_the_scaled_value_row():
-    # one token: weight 1, so out = fp32(e4m3(v) · v_scale) exactly
-    w = W.DecodeWorkload("fp8_one", 5, 3, 8, 4, 96, 8, "bf16", lengths=(1, 1, 1), sub=1)
+@pytest.mark.parametrize("hq,hkv", [(8, 4), (64, 1)])
+def test_fp8_single_token_is_the_scaled_value_row(hq, hkv):
+    # One token: weight 1, so out = e4m3(v) · v_scale. The CUDA-core kernel (64 heads per KV
+    # head) forms that product once in fp32: exact equality. The tensor-core kernel multiplies
+    # the code by the scale (times 2^10) split into an fp16 head and an fp16 residual, which
+    # sum to it within 2^-22 of it, and adds the two exact products in the MMA's fp32
+    # accumulator (one more rounding, up to 2^-23), then divides by 2^10 exactly: within
+    # 2^-21 of |v|, checked against 2^-20 of |v| per element.
+    w = W.DecodeWorkload("fp8_one", 5, 3, hq, hkv, 96 if hkv == 4 else 64, 8, "bf16", lengths=(1, 1, 1), sub=1)
     inp = W.fp8_decode_inputs(w, DEV)
     out = _run(inp, w.scale)
     v = inp["v_cache"][:, 0].view(torch.float8_e4m3fn).float() * inp["v_scale"][:, 0, :, None]
-    assert torch.equal(out, v.repeat_interleave(2, dim=1))
+    v = v.repeat_interleave(hq // hkv, dim=1)
+    if hq // hkv > 16:
+        assert torch.equal(out, v)
+    else:
+        assert bool(((out - v).abs() <= 2.0 ** -20 * v.abs()).all())
 
 
 def test_fp8_minimind_full_size():
@@ -60,3 +76,24 @@ def test_fp8_minimind_full_size():
     inp = W.fp8_decode_inputs(w, DEV)
     out = _run(inp, w.scale, max_s=int(inp["seq_lens"].max()))
     assert float(np.abs(to_f64(out) - _ref(inp, w.scale)).max()) <= TOL
+
+
+def test_fp8_one_workspace_across_calls():
+    """Calls of different shapes on one zero-filled workspace: each finds its arrival counters
+    at zero (the counter region is left zero by every call) and gives the same bits as a call
+    on a fresh workspace."""
+    shapes = [W.MINIMIND_GQA,
+              W.DecodeWorkload("fp8_ws_b", 5, 7, 16, 1, 128, 1000, "bf16", lengths=(0, 1, 127, 300, 1000, 64, 65),
+                               sub=7),
+              W.MINIMIND_GQA]
+    sizes = [mk.decode_gqa_workspace_size(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.s_max, mk.ATTN_FP8_E4M3, 0)
+             for w in shapes]
+    ws = torch.zeros(max(sizes), dtype=torch.uint8, device=DEV)
+    for w in shapes:
+        inp = W.fp8_decode_inputs(w, DEV)
+        fresh = torch.zeros(max(sizes), dtype=torch.uint8, device=DEV)
+        ref = _run(inp, w.scale, workspace=fresh)
+        out = _run(inp, w.scale, workspace=ws)
+        assert torch.equal(out, ref)
+        assert int(ws[:64 << 10].count_nonzero()) == 0
+        assert float(np.abs(to_f64(out) - _ref(inp, w.scale)).max()) <= TOL
