@@ -326,8 +326,8 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 for (int i = lane; i < a.Hq * D / 4; i += 32)
                     reinterpret_cast<float4 *>(a.out + (size_t)b * a.Hq * D)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    SeqWalker walk{prefix, lens, a.B, seg_per_seq, walk_start[0], walk_start[1], walk_start[2], walk_range[0],
-                   walk_range[1]};
+    SeqWalker walk{prefix, lens, a.B, seg_per_seq, 1, 0, 0, 0, 0, 0, 0};
+    walk.set(walk_start[0], walk_start[1], walk_start[2], walk_range[0], walk_range[1]);
     const SeqWalker walk0 = walk;
 
     if (warp == kConsumers) {

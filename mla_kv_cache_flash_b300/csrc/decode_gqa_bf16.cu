@@ -87,8 +87,8 @@ Layout layout(int q_rows, int heads, int B, int n_blocks, bool chunked) {
     L.plist = L.stats + 2 * HG * heads * 4 + 16;
     L.prefix = L.plist + kConsumers * (n_blocks + kLseCache) * 4;
     // tile prefix [B+1], keys per sequence [B]; chunked prefill also the first new-token rows
-    // [B+1] and the segment prefix [B+1]
-    L.total = L.prefix + (chunked ? 4 : 2) * (B + 1) * 4 + 1024;
+    // [B+1] and the segment prefix [B+1]; then the walk's start (b, q, i0)
+    L.total = L.prefix + (chunked ? 4 : 2) * (B + 1) * 4 + 16 + 1024;
     return L;
 }
 
@@ -128,6 +128,7 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
     int *lens = prefix + (a.B + 1);                            // [B] keys per sequence
     int *cu = lens + (a.B + 1);                                // chunked: [B+1] first new-token row
     int *segpre = cu + (a.B + 1);                              // chunked: [B+1] segments before b
+    int *wstart = prefix + (CH ? 4 : 2) * (a.B + 1);           // decode: the walk's start b, q, i0
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -216,6 +217,20 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
             carry += __shfl_sync(0xffffffffu, x, 31);
         }
         if (lane == 0) prefix[a.B] = carry;
+        __syncwarp();
+        // where this block's tile range starts (streamed split): found once, lane-parallel
+        const int spp = (a.Hkv / HG) * a.n_hblk;
+        const long long T0 = (long long)spp * carry;
+        int b0 = 0, q0 = 0, i00 = 0;
+        if (!a.aligned && T0 > 0) {
+            const long long t0 = stream_start(blockIdx.x, T0, a.n_blocks);
+            if (t0 < stream_start(blockIdx.x + 1, T0, a.n_blocks)) seq_walk_start(prefix, a.B, spp, t0, lane, b0, q0, i00);
+        }
+        if (lane == 0) {
+            wstart[0] = b0;
+            wstart[1] = q0;
+            wstart[2] = i00;
+        }
     }
     __syncthreads();
 
@@ -223,22 +238,26 @@ decode_gqa_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_co
     const long long T = CH ? (long long)prefix[a.B] : (long long)seg_per_seq * prefix[a.B];
     const int c = blockIdx.x;
     if (!CH && c == 0 && warp < kConsumers) {
-        // sequences with an empty cache own no tile: their output is zero
-        for (int b = 0; b < a.B; ++b)
+        // sequences with an empty cache own no tile: their output is zero (a warp per sequence)
+        for (int b = warp; b < a.B; b += kConsumers)
             if (prefix[b + 1] == prefix[b])
-                for (int i = threadIdx.x; i < a.Hq * D / 4; i += kConsumers * 32)
+                for (int i = lane; i < a.Hq * D / 4; i += 32)
                     reinterpret_cast<float4 *>(a.out + (size_t)b * a.Hq * D)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    PieceWalker walk{prefix, lens, a.B, seg_per_seq, a.n_hblk, TT, 0, 0};
+    SeqWalker walk{prefix, lens, a.B, a.Hkv / HG, a.n_hblk, 0, 0, 0, 0, 0, 0};
     if (!CH && a.aligned) {
         // block c streams segment c whole
         const int b = c / seg_per_seq, q = c % seg_per_seq;
         const int nb = stream_tiles(lens[b], TT);
-        walk.t = (long long)seg_per_seq * prefix[b] + (long long)q * nb;
-        walk.t_end = walk.t + nb;
+        const long long t = (long long)seg_per_seq * prefix[b] + (long long)q * nb;
+        walk.set(b, q, 0, t, t + nb);
     } else if (T > 0) {
-        walk.t = stream_start(c, T, a.n_blocks);
-        walk.t_end = stream_start(c + 1, T, a.n_blocks);
+        if constexpr (CH) {
+            walk.t = stream_start(c, T, a.n_blocks);
+            walk.t_end = stream_start(c + 1, T, a.n_blocks);
+        } else {
+            walk.set(wstart[0], wstart[1], wstart[2], stream_start(c, T, a.n_blocks), stream_start(c + 1, T, a.n_blocks));
+        }
     }
     ChunkPieceWalker cwalk{prefix, lens, a.B, TT, walk.t, walk.t_end};
     AlignedChunkWalker awalk{0, 0, a.Hkv / HG, 0, 0, TT, 0};

@@ -128,7 +128,8 @@ struct Cfg {
     static_assert(N_BARS * 8 <= 256, "barrier area");
     // after the tile prefix [B+1]: the keys per sequence [B] (decode: seq_lens), then for
     // chunked prefill the first new-token row [B+1] and the segment prefix [B+1]
-    static size_t smem_bytes(int B) { return PREFIX_OFF + (size_t)(B + 1) * 4 * (CH ? 4 : 2) + 1024; }
+    // the prefix arrays, then the walk's start (b, q, i0)
+    static size_t smem_bytes(int B) { return PREFIX_OFF + (size_t)(B + 1) * 4 * (CH ? 4 : 2) + 16 + 1024; }
 };
 
 // Barrier indices.
@@ -241,6 +242,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
     int *klen = prefix + (a.B + 1);       // keys per sequence (decode: a copy of seq_lens)
     int *cu = klen + (a.B + 1);           //   first new-token row per sequence, [B+1]
     int *segpre = cu + (a.B + 1);         //   segments before each sequence, [B+1]
+    int *wstart = prefix + (CH ? 4 : 2) * (a.B + 1);   // decode: the walk's start b, q, i0
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -342,6 +344,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
             }
         }
         if (lane == 0) prefix[a.B] = carry;
+        __syncwarp();
+        // where this block's tile range starts (streamed split): found once, lane-parallel
+        const long long T0 = (long long)a.seg_per_seq * carry;
+        int b0 = 0, q0 = 0, i00 = 0;
+        if (!a.aligned && T0 > 0) {
+            const long long t0 = stream_start(blockIdx.x, T0, a.n_blocks);
+            if (t0 < stream_start(blockIdx.x + 1, T0, a.n_blocks))
+                seq_walk_start(prefix, a.B, a.seg_per_seq, t0, lane, b0, q0, i00);
+        }
+        if (lane == 0) {
+            wstart[0] = b0;
+            wstart[1] = q0;
+            wstart[2] = i00;
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -351,16 +367,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,    // K (GQA) or c (M
     // tiles of all segments, laid end to end
     const long long T = CH ? (long long)prefix[a.B] : (long long)a.seg_per_seq * prefix[a.B];
     const int c = blockIdx.x;
-    PieceWalker walk{prefix, klen, a.B, a.seg_per_seq, a.n_hblk, TILE, 0, 0};
+    SeqWalker walk{prefix, klen, a.B, a.seg_per_seq / a.n_hblk, a.n_hblk, 0, 0, 0, 0, 0, 0};
     if (!CH && a.aligned) {
         // block c streams segment c whole
         const int b = c / a.seg_per_seq, q = c % a.seg_per_seq;
         const int nb = stream_tiles(klen[b], TILE);
-        walk.t = (long long)a.seg_per_seq * prefix[b] + (long long)q * nb;
-        walk.t_end = walk.t + nb;
+        const long long t = (long long)a.seg_per_seq * prefix[b] + (long long)q * nb;
+        walk.set(b, q, 0, t, t + nb);
     } else if (T > 0) {
-        walk.t = stream_start(c, T, a.n_blocks);
-        walk.t_end = stream_start(c + 1, T, a.n_blocks);
+        if constexpr (CH) {
+            walk.t = stream_start(c, T, a.n_blocks);
+            walk.t_end = stream_start(c + 1, T, a.n_blocks);
+        } else {
+            walk.set(wstart[0], wstart[1], wstart[2], stream_start(c, T, a.n_blocks), stream_start(c + 1, T, a.n_blocks));
+        }
     }
     ChunkPieceWalker cwalk{prefix, klen, a.B, TILE, walk.t, walk.t_end};
     auto next_piece = [&](Piece &p) {

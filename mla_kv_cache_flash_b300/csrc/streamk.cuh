@@ -88,9 +88,18 @@ struct PieceWalker {
 struct SeqWalker {
     const int *prefix;          // prefix[b] = Σ_{b' < b} tiles(S_b'), b = 0 .. B
     const int *seq_lens;
-    int B, seg_per_seq;
-    int b, q, i0;
+    int B, n_groups, n_hblk;    // a sequence's segments: n_groups KV-head groups × n_hblk head blocks
+    int b, gi, hb, i0;          // the next piece's segment (b, gi, hb) and first tile
     long long t, t_end;
+    // position from seq_walk_start's (b, q, i0), q = gi·n_hblk + hb
+    __device__ void set(int b_, int q, int i0_, long long t_, long long t_end_) {
+        b = b_;
+        gi = n_hblk == 1 ? q : q / n_hblk;
+        hb = n_hblk == 1 ? 0 : q - gi * n_hblk;
+        i0 = i0_;
+        t = t_;
+        t_end = t_end_;
+    }
     __device__ bool next(Piece &p) {
         if (t >= t_end) return false;
         const int nb = prefix[b + 1] - prefix[b];
@@ -98,8 +107,8 @@ struct SeqWalker {
         const int n_t = left < nb - i0 ? (int)left : nb - i0;
         p.b = b;
         p.S = seq_lens[b];
-        p.gi = q;
-        p.hb = 0;
+        p.gi = gi;
+        p.hb = hb;
         p.i0 = i0;
         p.n_t = n_t;
         p.whole = i0 == 0 && n_t == nb;
@@ -107,11 +116,14 @@ struct SeqWalker {
         i0 += n_t;
         if (i0 == nb) {
             i0 = 0;
-            if (++q == seg_per_seq) {
-                q = 0;
-                do {
-                    ++b;
-                } while (b < B && prefix[b + 1] == prefix[b]);
+            if (++hb == n_hblk) {
+                hb = 0;
+                if (++gi == n_groups) {
+                    gi = 0;
+                    do {
+                        ++b;
+                    } while (b < B && prefix[b + 1] == prefix[b]);
+                }
             }
         }
         return true;
