@@ -426,9 +426,10 @@ class DecodeChunked(DecodeGqa):
     style step): each sequence's last 4 cached rows are its chunk, so row i sees
     length − 4 + i + 1 rows. Algorithmic bytes: each sequence's visible K/V once (as for the
     decode of the full length); the kernel reads them once per new token."""
-    kernel_src = "mla_kv_cache_flash_b300/csrc/decode_gqa_fma.cu"
+    kernel_src = "mla_kv_cache_flash_b300/csrc/decode_gqa_bf16.cu"
     call = "attn_prefill_gqa_chunked call: "
-    launch_note = " (CUDA-core decode, then the merge launch when the plan splits)"
+    launch_note = (" (register-MMA decode kernel: 16/G new tokens x G heads per MMA tile, balanced over persistent"
+                   " blocks, shared segments merged in-kernel)")
     n_new = 4
 
     def __init__(self, w, device, rank, l2_bytes):
@@ -444,7 +445,7 @@ class DecodeChunked(DecodeGqa):
         nb = int(lib.attn_prefill_gqa_chunked_workspace_size(B, B * n, w.n_q_heads, w.n_kv_heads, w.head_dim,
                                                              self.max_s, self.mk.ATTN_BF16, 0))
         self.ws = torch.zeros(max(nb, 1), dtype=torch.uint8, device=device)
-        self.launches_per_step = 2 if nb else 1
+        self.launches_per_step = 1          # one launch; the workspace holds counters and partials
 
     def _run(self, s):
         self.mk.prefill_gqa_chunked(s["q_chunk"], s["k_cache"], s["v_cache"], s["cu_q"], s["start_pos"], self.max_s,
@@ -598,9 +599,10 @@ class MlaChunked(DecodeMla):
     """MLA chunked prefill, 4 new tokens per sequence over the MiniMind MLA latent caches
     (each sequence's last 4 rows are its chunk). Algorithmic bytes: each visible latent row
     once, as for the decode of the full length."""
-    kernel_src = "mla_kv_cache_flash_b300/csrc/prefill_chunked_mla.cu"
+    kernel_src = "mla_kv_cache_flash_b300/csrc/decode_tc.cu"
     call = "attn_prefill_mla_chunked call: "
-    launch_note = " (CUDA-core decode form, then the merge launch when the plan splits)"
+    launch_note = (" (tcgen05 MLA decode kernel: 4 new tokens x 16 heads per block, balanced over persistent"
+                   " blocks, shared segments merged in-kernel)")
     n_new = 4
 
     def __init__(self, w, device, rank, l2_bytes):
@@ -617,7 +619,7 @@ class MlaChunked(DecodeMla):
         self.out = torch.empty((B * n, w.n_q_heads, w.kv_lora_rank), dtype=torch.float32, device=device)
         nb = int(self.mk.lib().attn_prefill_mla_chunked_workspace_size(B, B * n, w.n_q_heads, self.max_s, 0))
         self.ws = torch.zeros(max(nb, 1), dtype=torch.uint8, device=device)
-        self.launches_per_step = 2 if nb else 1
+        self.launches_per_step = 1          # one launch; the workspace holds counters and partials
 
     def _run(self, s):
         self.mk.prefill_mla_chunked(s["q_lat_chunk"], s["q_rope_chunk"], s["c_cache"], s["kr_cache"], s["cu_q"],
