@@ -131,10 +131,9 @@ def test_llama3_8b_full(hkv):
     inp = W.decode_inputs(w, DEV)
     out = mk.decode_gqa(inp["q"], inp["k_cache"], inp["v_cache"], inp["seq_lens"], scale=w.scale)
     torch.cuda.synchronize()
-    # MHA holds 8 GiB of cache: the oracle checks a fixed sample of 8 sequences there
-    batches = None if hkv != 32 else [0, 9, 18, 27, 36, 45, 54, 63]
-    ref = _oracle_decode(inp, w.scale, batches)
-    assert _max_err(out, ref, batches) <= TOL_BF16
+    # every output; the oracle widens one sequence's cache at a time (MHA holds 8 GiB of it)
+    ref = _oracle_decode(inp, w.scale)
+    assert _max_err(out, ref) <= TOL_BF16
     del inp
     torch.cuda.empty_cache()
 

@@ -12,6 +12,7 @@ import torch
 import mla_kv_cache_flash_b300 as mk
 import oracle
 import workloads as W
+from tests import mla_bounds as mb
 from workloads import to_f64
 
 pytestmark = pytest.mark.gpu
@@ -66,7 +67,9 @@ def test_single_token_is_c0():
 
 def test_decompressed_output_close_to_naive():
     # kernel + W_UV applied in fp64 vs the oracle's decompress-then-attend path on the same
-    # bf16 inputs: differs only by the bf16 rounding of q_lat and fp32 accumulation
+    # bf16 inputs: they differ by the bf16 rounding of the fp32 q_lat (bounded per score,
+    # then per latent average) and the decode's own tolerance, each mapped through W_UV
+    # (tests/mla_bounds.py states the derivation)
     w = W.MlaWorkload("mla_naive", 3, 4, 16, 96, 128, 48, 96, 256, lengths=(256, 100, 17, 200))
     inp = W.mla_inputs(w, DEV)
     q_lat, out = _run(inp, w.scale)
@@ -74,4 +77,4 @@ def test_decompressed_output_close_to_naive():
     ref = oracle.mla_decode_naive(to_f64(inp["q_nope"]), to_f64(inp["q_rope"]), to_f64(inp["c_cache"]),
                                   to_f64(inp["kr_cache"]), to_f64(inp["w_uk"]), to_f64(inp["w_uv"]),
                                   inp["seq_lens"].cpu().numpy(), w.scale)
-    assert np.abs(o - ref).max() <= 2e-2
+    assert np.all(np.abs(o - ref) <= mb.full_step_tolerance(inp, w.scale, oracle))

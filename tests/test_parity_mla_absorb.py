@@ -19,14 +19,13 @@ import torch
 import mla_kv_cache_flash_b300 as mk
 import oracle
 import workloads as W
+from tests import mla_bounds as mb
 from workloads import to_f64
 
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
-U_BF16 = 2.0 ** -8
-U_F32 = 2.0 ** -24
-DECODE_TOL = 3e-3
+U_F32 = mb.U_F32
 
 
 def _rand(shape, seed, std=1.0):
@@ -34,11 +33,7 @@ def _rand(shape, seed, std=1.0):
     return (torch.randn(shape, generator=g, device=DEV) * std).to(torch.bfloat16)
 
 
-def _absorb_bound(qn, wuk, ref):
-    # qn [B,H,dn], wuk [H,dn,r] fp64; Σ_n |q_n w_n| per output element
-    mag = np.einsum("hnr,bhn->bhr", np.abs(wuk), np.abs(qn))
-    gamma = qn.shape[2] * U_F32 * mag
-    return U_BF16 * (np.abs(ref) + gamma) + gamma + 1e-30
+_absorb_bound = mb.absorb_bound
 
 
 @pytest.mark.parametrize("B,H,dn,r", [(1, 16, 96, 128), (17, 16, 96, 128), (33, 3, 1, 32), (5, 128, 96, 128),
@@ -87,24 +82,7 @@ def test_apply_uv(B, H, r, dv):
 
 
 def _full_step_tolerance(inp, scale):
-    """Per-(b, h, v) bound for the product path against the decompress-then-attend oracle."""
-    q64, w64 = to_f64(inp["q_nope"]), to_f64(inp["w_uk"])
-    x = oracle.absorb_query(q64, w64)                               # exact q_lat, [B,H,r]
-    dq = _absorb_bound(q64, w64, x)                                 # bound on |q_lat − x|
-    c = to_f64(inp["c_cache"])                                      # [B,S,r]
-    lens = inp["seq_lens"].cpu().numpy()
-    B, H, r = x.shape
-    wsum = np.abs(to_f64(inp["w_uv"])).sum(2)                       # [H, dv]
-    tol = np.zeros((B, H, wsum.shape[1]))
-    for b in range(B):
-        s = int(lens[b])
-        if s == 0:
-            continue
-        cb = np.abs(c[b, :s])                                       # [s, r]
-        delta = scale * (cb @ dq[b].T).max(0)                       # [H]
-        olat_tol = np.expm1(2 * delta) * cb.max() + DECODE_TOL      # [H]
-        tol[b] = olat_tol[:, None] * wsum[None, :]
-    return tol
+    return mb.full_step_tolerance(inp, scale, oracle)
 
 
 @pytest.mark.parametrize("lens,hq,n_split", [((0, 1, 127, 128, 129, 1000, 2049), 16, 0),
@@ -139,19 +117,20 @@ def test_full_step_is_the_three_calls():
     mk.check_status()
 
 
-def test_full_mla_step_at_the_bench_size_sampled():
-    """The bench's MLA step (B=64, S=4096, 16 heads) in its launch configuration; eight
-    sequences' outputs against the decompress-then-attend oracle."""
+def test_full_mla_step_at_the_bench_size():
+    """The bench's MLA step (B=64, S=4096, 16 heads) in its launch configuration; every
+    sequence's outputs against the decompress-then-attend oracle, eight sequences at a time."""
     w = W.MINIMIND_MLA
     inp = W.mla_inputs(w, DEV)
     out = mk.decode_mla(inp["q_nope"], inp["q_rope"], inp["c_cache"], inp["kr_cache"], inp["w_uk"], inp["w_uv"],
                         inp["seq_lens"], w.scale)
     torch.cuda.synchronize()
-    pick = [0, 9, 18, 27, 36, 45, 54, 63]
-    sub = {k: (v[pick] if k not in ("w_uk", "w_uv") else v) for k, v in inp.items()}
-    ref = oracle.mla_decode_naive(to_f64(sub["q_nope"]), to_f64(sub["q_rope"]), to_f64(sub["c_cache"]),
-                                  to_f64(sub["kr_cache"]), to_f64(sub["w_uk"]), to_f64(sub["w_uv"]),
-                                  sub["seq_lens"].cpu().numpy(), w.scale)
-    err = np.abs(to_f64(out[pick]) - ref)
-    assert np.all(err <= _full_step_tolerance(sub, w.scale))
+    for b0 in range(0, w.batch, 8):
+        pick = list(range(b0, min(b0 + 8, w.batch)))
+        sub = {k: (v[pick] if k not in ("w_uk", "w_uv") else v) for k, v in inp.items()}
+        ref = oracle.mla_decode_naive(to_f64(sub["q_nope"]), to_f64(sub["q_rope"]), to_f64(sub["c_cache"]),
+                                      to_f64(sub["kr_cache"]), to_f64(sub["w_uk"]), to_f64(sub["w_uv"]),
+                                      sub["seq_lens"].cpu().numpy(), w.scale)
+        err = np.abs(to_f64(out[pick]) - ref)
+        assert np.all(err <= _full_step_tolerance(sub, w.scale)), pick
 

@@ -1,9 +1,9 @@
 """Causal GQA prefill on the GPU (tcgen05 kernel) against the fp64 CPU oracle.
 
 Tolerance: max |Δ| ≤ 3e-3 over every output element compared (bf16 inputs, fp32
-accumulation, fp32 output). Small cases compare every row and head; the full-size
+accumulation, fp32 output). Every case compares every row of every head, the full-size
 workloads (8 × 2048 tokens, and 8 ragged sequences of 256 to 4096 tokens, Hq=32, Hkv=8,
-D=128) compare every row of a fixed sample of query heads, one from each KV group.
+D=128) included.
 """
 
 import numpy as np
@@ -91,12 +91,15 @@ def test_deterministic_under_full_occupancy():
 
 
 @pytest.mark.parametrize("wl", [W.PREFILL_UNIFORM, W.PREFILL_RAGGED], ids=["uniform", "ragged"])
-def test_full_size_sampled_heads(wl):
+def test_full_size_every_head(wl):
+    """The bench's prefill workloads in the bench's launch configuration, every output row of
+    every head against the oracle (four heads at a time, to bound the host memory)."""
     inp = W.prefill_inputs(wl, DEV)
     out = _run(inp, wl.scale)
-    g = wl.n_q_heads // wl.n_kv_heads
-    heads = [j * g + (j % g) for j in range(wl.n_kv_heads)]     # one head of every KV group
-    err = _err(out, _ref(inp, wl.scale, heads=heads), heads)
-    print(f"{wl.name} heads={heads} max|err|={err:.3e}")
+    err = 0.0
+    for h0 in range(0, wl.n_q_heads, 4):
+        heads = list(range(h0, min(h0 + 4, wl.n_q_heads)))
+        err = max(err, _err(out, _ref(inp, wl.scale, heads=heads), heads))
+    print(f"{wl.name} max|err|={err:.3e}")
     assert err <= TOL
     assert torch.isfinite(out).all()
