@@ -546,6 +546,7 @@ MLAKV_API int attn_prefill_gqa_causal(const void *q, const void *k, const void *
     a.q = q; a.k = k; a.v = v; a.cu_seqlens = cu_seqlens; a.out = out;
     a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.T = total_tokens;
     a.scale_log2 = scale * kLog2e; a.max_seqlen = max_seqlen;
+    a.out32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
     cudaError_t e = launch_prefill(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "attn_prefill_gqa_causal: kernel launch");
     return ok();

@@ -75,6 +75,7 @@ struct PrefillArgs {
     int B, Hq, Hkv, D, T;
     float scale_log2;
     int max_seqlen;
+    int out32;              // out is 32-byte aligned (the epilogue then stores 32 bytes at a time)
 };
 
 // ------------------------------------------------------------------ launchers (one per TU)

@@ -198,6 +198,14 @@ __device__ __forceinline__ void write_p(uint32_t s_addr, float c, float m, int r
     l += a0 + a1;
 }
 
+// 32-byte store of eight floats (the address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(float *p, float a0, float a1, float a2, float a3, float a4, float a5,
+                                             float a6, float a7) {
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(a0), "f"(a1), "f"(a2),
+                 "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7)
+                 : "memory");
+}
+
 // The k-th item of block `blk` (of `nblk`) in the dealt order: item positions are taken in
 // rounds of nblk, alternating direction, over the list sorted longest first.
 struct Item {
@@ -328,7 +336,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // Issue order for iteration g (KV tile g of this block): S_0(g), P·V_1(g−1), S_1(g),
         // P·V_0(g). Each tile's chain S → softmax → P·V → next S is offset by half a period
         // from the other's, so one tile's softmax runs while the tensor core works for the
-        // other. S_t(g) waits for P·V_t(g−1) to finish, since it overwrites P_t.
+        // other. S_t(g) overwrites P_t, which P·V_t(g−1) reads; it is issued after that P·V
+        // without waiting for it to finish: MMAs issued by one thread execute in issue order,
+        // so the earlier one has read its operands before the later one writes (waiting for
+        // the completion cost an mbarrier round trip, 550-800 cycles, twice per iteration,
+        // with the tensor pipe idle). The commit after S_t(g) still tracks every earlier MMA,
+        // so "S_t(g) full" also means P·V_t(g−1) is done when the softmax rescales O_t.
         const uint64_t q_desc = sdesc_sw128(sb + Q_OFF, 16, 1024);
         const uint64_t k_desc = sdesc_sw128(sb + K_OFF, 16, 1024);
         const uint64_t v_desc = sdesc_sw128(sb + V_OFF, BOX_BYTES, 1024);
@@ -402,7 +415,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 if (n == 0 && !(ok = flush_pv1())) break;
                 if (!(ok = wait_all(kKFull + s, ph, kStatusFullWait))) break;
                 if (n == 0 && !(ok = wait_all(kQFull + q0, u0 & 1, kStatusFullWait))) break;
-                if (g > 0 && !(ok = wait_all(kODone + 0, (g - 1) & 1, kStatusMmaWait))) break;
                 tc_fence_after();
                 issue_s(0, q0, s);
                 if (n == it.qt) commit(kQEmpty + q0);
@@ -410,7 +422,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 if (n_mt == 2) {
                     if (!(ok = flush_pv1())) break;
                     if (n == 0 && !(ok = wait_all(kQFull + q1, u1 & 1, kStatusFullWait))) break;
-                    if (g > 0 && !(ok = wait_all(kODone + 1, (g - 1) & 1, kStatusMmaWait))) break;
                     tc_fence_after();
                     issue_s(1, q1, s);
                     if (n == it.qt) commit(kQEmpty + q1);
@@ -510,18 +521,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             tc_fence_after();
             const int q_row = it.qt * BM + row;
             const float inv = 1.f / l;
-            float4 *dst = reinterpret_cast<float4 *>(a.out + ((size_t)(seq0 + q_row) * a.Hq + it.h0 + t) * HD);
+            float *dst = a.out + ((size_t)(seq0 + q_row) * a.Hq + it.h0 + t) * HD;
 #pragma unroll 1
             for (int c = 0; c < HD / 32; ++c) {
                 uint32_t o[32];
                 tmem_ld32(o_addr + c * 32, o);
                 tmem_ld_wait(o);
-                if (q_row < S) {
+                if (q_row < S && !a.out32) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        dst[c * 8 + i] = make_float4(
+                        reinterpret_cast<float4 *>(dst)[c * 8 + i] = make_float4(
                             __uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
                             __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+                } else if (q_row < S) {
+                    // 32-byte stores: a thread writes its own row, so every store of a warp
+                    // touches 32 rows; the wider store halves their number
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        st_global_v8(dst + c * 32 + 8 * i, __uint_as_float(o[8 * i]) * inv,
+                                     __uint_as_float(o[8 * i + 1]) * inv, __uint_as_float(o[8 * i + 2]) * inv,
+                                     __uint_as_float(o[8 * i + 3]) * inv, __uint_as_float(o[8 * i + 4]) * inv,
+                                     __uint_as_float(o[8 * i + 5]) * inv, __uint_as_float(o[8 * i + 6]) * inv,
+                                     __uint_as_float(o[8 * i + 7]) * inv);
                 }
             }
             // the next item's first P·V overwrites O; it waits for this warpgroup's next

@@ -50,6 +50,21 @@ def test_small_ragged_every_row(hq, hkv):
     assert err <= TOL
 
 
+def test_output_16_byte_aligned_only():
+    # an output that is 16- but not 32-byte aligned takes the 16-byte stores: the same bits
+    w = W.PrefillWorkload("prefill_align", 4, 3, 8, 2, 128, lengths=(130, 1, 257), sub=9)
+    inp = W.prefill_inputs(w, DEV)
+    ref = _run(inp, w.scale)
+    T = ref.shape[0]
+    buf = torch.full((T * 8 * 128 + 4,), float("nan"), dtype=torch.float32, device=DEV)
+    out = buf[4:].view(T, 8, 128)
+    assert out.data_ptr() % 32 == 16
+    mk.prefill_gqa_causal(inp["q"], inp["k"], inp["v"], inp["cu_seqlens"], inp["max_seqlen"], out=out, scale=w.scale)
+    mk.check_status()
+    assert torch.equal(out, ref)
+    assert _err(out, _ref(inp, w.scale)) <= TOL
+
+
 def test_empty_sequences_and_exact_tiles():
     w = W.PrefillWorkload("prefill_edges", 4, 5, 8, 2, 128, lengths=(0, 128, 0, 256, 129), sub=6)
     inp = W.prefill_inputs(w, DEV)
