@@ -970,7 +970,7 @@ struct Plan {
     bool aligned;
 };
 
-Plan plan(long long segs, int n_split, int cps) {
+Plan plan(long long segs, int n_split, int cps, bool whole_blocks = true) {
     Plan p{segs, 1, false};
     const int sms = cps * sm_count();          // resident blocks
     if (n_split == 0 && segs <= sms && 2 * segs >= sms) {
@@ -978,15 +978,17 @@ Plan plan(long long segs, int n_split, int cps) {
         p.n_blocks = (int)segs;
         return p;
     }
-    // A whole number k of blocks per segment when that fills at least 85 % of the resident
-    // slots: with segments of equal length every block then holds one piece of one segment
-    // (no block ends on a second, shared segment), which costs less than the last 15 % of
-    // slots gain (16-head MLA, 64 equal segments on B300: 256 blocks 25.4 us, 296 blocks
-    // 27.8 us, 259 blocks 28.6 us). Ragged lengths stay balanced either way. A merge over
-    // more than kPlist partials lists them on the fly.
+    // MLA (whole_blocks): a whole number k of blocks per segment when that fills at least 85 %
+    // of the resident slots: with segments of equal length every block then holds one piece
+    // of one segment (no block ends on a second, shared segment), which costs less than the
+    // last 15 % of slots gain (16-head MLA, 64 equal segments on B300: 256 blocks 25.4 us,
+    // 296 blocks 27.8 us, 259 blocks 28.6 us). The GQA/MQA kernel, one block per SM, keeps
+    // every SM streaming instead (MQA, 64 segments: 148 blocks 52.8 us, 128 blocks 54.0 us).
+    // Ragged lengths stay balanced either way. A merge over more than kPlist partials lists
+    // them on the fly.
     long long n = sms;
     const long long k = segs > 0 ? sms / segs : 0;
-    if (k >= 1 && 100 * k * segs >= 85LL * sms) n = k * segs;
+    if (whole_blocks && k >= 1 && 100 * k * segs >= 85LL * sms) n = k * segs;
     if (n_split > 0 && (long long)n_split * segs < n) n = (long long)n_split * segs;
     p.n_blocks = (int)(n < 1 ? 1 : n);
     return p;
@@ -1110,7 +1112,7 @@ bool decode_tc_gqa_eligible(int B, int Hq, int Hkv, int D) {
 static Plan gqa_plan_tc(int B, int Hq, int Hkv, int n_split) {
     const int G = Hq / Hkv;
     return plan((long long)B * Hkv * (G / heads_per_block(G)), n_split,
-                heads_per_block(G) == 32 ? Cfg<kGqa, 32>::CPS : Cfg<kGqa, 16>::CPS);
+                heads_per_block(G) == 32 ? Cfg<kGqa, 32>::CPS : Cfg<kGqa, 16>::CPS, false);
 }
 
 int decode_tc_gqa_blocks(int B, int Hq, int Hkv, int n_split) { return gqa_plan_tc(B, Hq, Hkv, n_split).n_blocks; }

@@ -357,9 +357,9 @@ def test_merge_checks(L):
 
 def test_tensor_core_plan(L):
     # MQA / wide groups at D=128 and MLA go to the tensor-core decode: 148 SMs (the plan
-    # without a GPU assumes a 148-SM part), a whole number of blocks per segment when that
-    # fills at least 85% of the resident blocks
-    assert L.attn_decode_gqa_num_splits(64, 32, 1, 128, 8192, 1, 0) == 128       # 2 per sequence
+    # without a GPU assumes a 148-SM part); MQA keeps every SM streaming, MLA takes a whole
+    # number of blocks per segment when that fills at least 85% of the resident blocks
+    assert L.attn_decode_gqa_num_splits(64, 32, 1, 128, 8192, 1, 0) == 148       # every SM
     assert L.attn_decode_mla_num_splits(64, 16, 128, 48, 4096, 0) == 256          # 2 per SM, 4 per seq
     assert L.attn_decode_mla_num_splits(1, 16, 128, 48, 4096, 0) == 296           # one segment
     assert L.attn_decode_gqa_num_splits(64, 32, 8, 128, 8192, 1, 0) == 148        # register-MMA path
@@ -367,7 +367,7 @@ def test_tensor_core_plan(L):
     # slots of N heads x 128 fp32 per block and their lse, each part 256-byte aligned
     up = lambda x: (x + 255) // 256 * 256
     region = 64 << 10
-    n = 128
+    n = 148
     assert L.attn_decode_gqa_workspace_size(64, 32, 1, 128, 8192, 1, 0) == \
         region + up(2 * n * 32 * 128 * 4) + up(2 * n * 32 * 4)
     n = 256
