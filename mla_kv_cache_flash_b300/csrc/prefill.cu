@@ -61,11 +61,13 @@ constexpr int BN = 128;                      // keys per KV tile
 constexpr int NSTAGE = 2;                    // K/V ring depth
 constexpr int TILE_BYTES = BM * HD * 2;      // one 128 × 128 bf16 tile: 32 KB
 constexpr int BOX_BYTES = TILE_BYTES / 2;    // one TMA box: 128 rows × 64 columns (128 B)
-constexpr int Q_SLOTS = 3;                   // Q tiles rotate through three slots
+constexpr int Q_SLOTS = 2;                   // Q tiles rotate through two slots
+constexpr int OST_BYTES = BM * 32 * 4;       // output staging: 128 rows × 32 fp32 columns, per query tile
 constexpr int Q_OFF = 0;
 constexpr int K_OFF = Q_OFF + Q_SLOTS * TILE_BYTES;
 constexpr int V_OFF = K_OFF + NSTAGE * TILE_BYTES;
-constexpr int BAR_OFF = V_OFF + NSTAGE * TILE_BYTES;
+constexpr int OST_OFF = V_OFF + NSTAGE * TILE_BYTES;
+constexpr int BAR_OFF = OST_OFF + 2 * OST_BYTES;
 constexpr int N_BARS = 24;
 constexpr int SLOT_OFF = BAR_OFF + N_BARS * 8;
 constexpr int SMEM = SLOT_OFF + 16 + 1024;   // + alignment slack
@@ -198,6 +200,18 @@ __device__ __forceinline__ void write_p(uint32_t s_addr, float c, float m, int r
     l += a0 + a1;
 }
 
+// Shared → global tensor store of one box (completion tracked by the bulk async-group).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The issuing thread's bulk stores have read their shared-memory source (it may be rewritten).
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... and have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // 32-byte store of eight floats (the address 32-byte aligned).
 __device__ __forceinline__ void st_global_v8(float *p, float a0, float a1, float a2, float a3, float a4, float a5,
                                              float a6, float a7) {
@@ -224,7 +238,8 @@ __device__ __forceinline__ bool item_at(int k, int blk, int nblk, int n_items, i
 
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-               const __grid_constant__ CUtensorMap vmap, const PrefillArgs a, int n_qt, int heads_per_cta) {
+               const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap, const PrefillArgs a,
+               int n_qt, int heads_per_cta) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
@@ -521,6 +536,45 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             tc_fence_after();
             const int q_row = it.qt * BM + row;
             const float inv = 1.f / l;
+            if ((it.qt + 1) * BM <= S) {
+                // a full tile: four 32-column chunks through this tile's shared staging buffer
+                // (128-byte swizzle: chunk j of row r at (j ^ r % 8)·16 in the row's 128 bytes),
+                // each written to global memory by one TMA store, which coalesces what one row
+                // per thread would scatter over 32 rows per store instruction
+                const uint32_t ost = sb + OST_OFF + t * OST_BYTES;
+                const int bar_id = 1 + t;
+                const bool issuer = quarter == 0 && lane == 0;     // one thread of the warpgroup
+#pragma unroll 1
+                for (int c2 = 0; c2 < HD / 64; ++c2) {
+                    // two chunks' columns from TMEM with one wait
+                    uint32_t o[2][32];
+                    tmem_ld32(o_addr + c2 * 64, o[0]);
+                    tmem_ld32(o_addr + c2 * 64 + 32, o[1]);
+                    tmem_ld_wait(o[0]);
+                    tmem_ld_wait(o[1]);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (issuer) bulk_wait_read();              // the previous store has read the buffer
+                        bar_sync_named(bar_id, 128);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const uint32_t dsts = ost + row * 128 + ((j ^ (row & 7)) << 4);
+                            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dsts),
+                                         "f"(__uint_as_float(o[h][4 * j]) * inv),
+                                         "f"(__uint_as_float(o[h][4 * j + 1]) * inv),
+                                         "f"(__uint_as_float(o[h][4 * j + 2]) * inv),
+                                         "f"(__uint_as_float(o[h][4 * j + 3]) * inv)
+                                         : "memory");
+                        }
+                        fence_proxy_async_smem();
+                        bar_sync_named(bar_id, 128);
+                        if (issuer) {
+                            tma_store_3d(&omap, ost, (2 * c2 + h) * 32, it.h0 + t, seq0 + it.qt * BM);
+                            bulk_commit();
+                        }
+                    }
+                }
+            } else {
             float *dst = a.out + ((size_t)(seq0 + q_row) * a.Hq + it.h0 + t) * HD;
 #pragma unroll 1
             for (int c = 0; c < HD / 32; ++c) {
@@ -545,12 +599,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                      __uint_as_float(o[8 * i + 7]) * inv);
                 }
             }
+            }
             // the next item's first P·V overwrites O; it waits for this warpgroup's next
             // "P ready", which comes after these loads
             tc_fence_before();
         }
     }
 
+    if (warp >= 2) bulk_wait_all();            // every output store has landed
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -584,6 +640,15 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t st) {
                                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         if (e != cudaSuccess) return e;
     }
+    CUtensorMap om;
+    {
+        const uint64_t dims[3] = {(uint64_t)HD, (uint64_t)a.Hq, (uint64_t)a.T};
+        const uint64_t strides[2] = {(uint64_t)HD * 4, (uint64_t)a.Hq * HD * 4};
+        const uint32_t obox[3] = {32, 1, BM};
+        cudaError_t e = encode_tensor_map(&om, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.out, dims, strides, obox,
+                                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+        if (e != cudaSuccess) return e;
+    }
     static bool attr_set = false;
     if (!attr_set) {
         const cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
@@ -600,7 +665,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t st) {
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return cudaErrorInvalidDevice;
     const int grid = (int)(n_items < sms ? n_items : sms);
-    const cudaError_t e = launch_pdl(prefill_kernel, dim3(grid), dim3(kThreads), SMEM, st, qm, km, vm, a, n_qt,
+    const cudaError_t e = launch_pdl(prefill_kernel, dim3(grid), dim3(kThreads), SMEM, st, qm, km, vm, om, a, n_qt,
                                      heads_per_cta);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
