@@ -97,3 +97,16 @@ def test_fp8_one_workspace_across_calls():
         assert torch.equal(out, ref)
         assert int(ws[:64 << 10].count_nonzero()) == 0
         assert float(np.abs(to_f64(out) - _ref(inp, w.scale)).max()) <= TOL
+
+
+@pytest.mark.parametrize("hq,hkv,s_max", [(8, 2, 1001), (4, 1, 999), (16, 4, 1000)])
+def test_fp8_more_than_32_sequences(hq, hkv, s_max):
+    """40 sequences (the block start is found over two groups of 32), an odd cache capacity
+    (S_max·Hkv not a multiple of 4: the row scales arrive by 4-byte copies, not one bulk copy
+    per tile) and every split count: the balanced split, a cap of one block per segment, three."""
+    w = W.DecodeWorkload("fp8_b40", 5, 40, hq, hkv, 64, s_max, "bf16", length_range=(0, s_max), sub=hq + s_max)
+    inp = W.fp8_decode_inputs(w, DEV)
+    ref = _ref(inp, w.scale)
+    for n_split in (0, 1, 3):
+        out = _run(inp, w.scale, n_split=n_split)
+        assert float(np.abs(to_f64(out) - ref).max()) <= TOL, n_split
