@@ -190,7 +190,12 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // workspace serves any sequence of calls, whatever their shapes. A call with more counters
 // than the region holds extends it past the region and zeroes its counters itself (one
 // memset on its stream) before its launch, since partials of other shapes may lie there.
-constexpr size_t kCounterRegionBytes = size_t(64) << 10;   // 16384 int32 counters
+constexpr size_t kCounterRegionBytes = size_t(64) << 10;
+// The library's own split choice cuts a segment into at most this many pieces: the block that
+// finishes a shared segment last reads every piece's partial row, a few at a time, so its
+// merge grows with the piece count (B=1, 8192 tokens, 4 KV heads: 148 pieces 58 us, 37 pieces
+// 28 us). An explicit n_split is taken as given.
+constexpr int kMaxPieces = 32;   // 16384 int32 counters
 
 inline size_t counter_region_bytes(size_t n_counters) {
     const size_t c = (n_counters * sizeof(int) + 255) / 256 * 256;

@@ -696,7 +696,8 @@ int fp8_blocks(int B, int Hq, int Hkv, int D, int n_split) {
     const int by_smem = (int)((228 * 1024) / (smem_for(D, B, Hq / Hkv) + 1024));
     const int per_sm = max(1, min(by_regs, by_smem));
     long long n = (long long)per_sm * sm_count();
-    if (n_split > 0 && (long long)n_split * B * Hkv < n) n = (long long)n_split * B * Hkv;
+    const long long per_seg = n_split > 0 ? n_split : kMaxPieces;
+    if (per_seg * B * Hkv < n) n = per_seg * B * Hkv;
     return (int)(n < 1 ? 1 : n);
 }
 

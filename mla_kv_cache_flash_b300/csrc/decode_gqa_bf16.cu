@@ -844,10 +844,9 @@ int decode_gqa_stream_blocks(int B, int Hq, int Hkv, int D, int n_split) {
     const int n_hblk = (G + 16 * MT - 1) / (16 * MT);
     if (decode_gqa_stream_aligned(B, Hq, Hkv, n_split)) return B * Hkv * n_hblk;
     long long n = sm_count();
-    if (n_split > 0) {
-        const long long cap = (long long)n_split * B * (Hkv / hg_for(Hkv, G)) * n_hblk;
-        if (cap < n) n = cap;
-    }
+    const long long segs = (long long)B * (Hkv / hg_for(Hkv, G)) * n_hblk;
+    const long long cap = (long long)(n_split > 0 ? n_split : kMaxPieces) * segs;
+    if (cap < n) n = cap;
     return (int)(n < 1 ? 1 : n);
 }
 

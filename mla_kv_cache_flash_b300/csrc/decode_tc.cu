@@ -989,7 +989,8 @@ Plan plan(long long segs, int n_split, int cps, bool whole_blocks = true) {
     long long n = sms;
     const long long k = segs > 0 ? sms / segs : 0;
     if (whole_blocks && k >= 1 && 100 * k * segs >= 85LL * sms) n = k * segs;
-    if (n_split > 0 && (long long)n_split * segs < n) n = (long long)n_split * segs;
+    const long long per_seg = n_split > 0 ? n_split : kMaxPieces;
+    if (per_seg * segs < n) n = per_seg * segs;
     p.n_blocks = (int)(n < 1 ? 1 : n);
     return p;
 }

@@ -165,10 +165,11 @@ def test_fp8_unsupported(L, kw):
 
 def test_fp8_workspace(L):
     # the tensor-core fp8 plan: persistent blocks, three resident per SM (148 SMs without a
-    # GPU), each with two partial slots of G rows after the counter region; n_split > 0 caps
-    # the blocks at n_split per (sequence, KV head)
+    # GPU), at most 32 per (sequence, KV head), each with two partial slots of G rows after
+    # the counter region; n_split > 0 caps the blocks at n_split per (sequence, KV head)
     n = L.attn_decode_gqa_num_splits(2, 8, 4, 96, 4096, 2, 0)
-    assert n == 3 * 148
+    assert n == 32 * 2 * 4
+    assert L.attn_decode_gqa_num_splits(32, 8, 4, 96, 4096, 2, 0) == 3 * 148
     assert L.attn_decode_gqa_num_splits(2, 8, 4, 96, 4096, 2, 5) == 5 * 2 * 4
     up = lambda x: (x + 255) // 256 * 256
     assert L.attn_decode_gqa_workspace_size(2, 8, 4, 96, 4096, 2, 0) == \
@@ -361,7 +362,8 @@ def test_tensor_core_plan(L):
     # number of blocks per segment when that fills at least 85% of the resident blocks
     assert L.attn_decode_gqa_num_splits(64, 32, 1, 128, 8192, 1, 0) == 148       # every SM
     assert L.attn_decode_mla_num_splits(64, 16, 128, 48, 4096, 0) == 256          # 2 per SM, 4 per seq
-    assert L.attn_decode_mla_num_splits(1, 16, 128, 48, 4096, 0) == 296           # one segment
+    assert L.attn_decode_mla_num_splits(1, 16, 128, 48, 4096, 0) == 32            # one segment: 32 pieces
+    assert L.attn_decode_mla_num_splits(8, 16, 128, 48, 4096, 0) == 256           # 32 per segment
     assert L.attn_decode_gqa_num_splits(64, 32, 8, 128, 8192, 1, 0) == 148        # register-MMA path
     # workspace: the fixed 64 KiB counter region (one counter per segment), then two partial
     # slots of N heads x 128 fp32 per block and their lse, each part 256-byte aligned
