@@ -5,40 +5,45 @@
 //
 // Work split (streamk.cuh): the segments (sequence b, KV head j) are cut into 64-token tiles
 // laid end to end, and each persistent block takes an equal run of tiles, whatever the
-// lengths. A segment a block covers whole is written to `out`; one it shares with its
-// neighbours becomes a partial (normalised output and ln Σ e^s) in one of the block's two
-// slots, and the last block to finish the segment (acquire-release arrival counter, in the
-// workspace's counter region) combines them, inside this launch.
+// lengths (the producer warp finds the run's start once, lane-parallel, and every warp walks
+// its pieces incrementally). A segment a block covers whole is written to `out`; one it
+// shares with its neighbours becomes a partial (normalised output and ln Σ e^s) in one of the
+// block's two slots. The producer warp publishes each such piece once the consumers have
+// stored it (an acquire-release arrival on the segment's counter, in the workspace's counter
+// region); the last block to arrive combines the segment's partials inside this launch: the
+// producer warp for the block's first piece, the consumers (idle by then) for its last.
 //
 // Block = 4 consumer warps + 1 producer warp. The producer brings each tile's K and V codes
 // into a 4-stage shared-memory ring with TMA tensor loads, the tile's K and V row scales on
 // the same barrier (for up to 4 KV heads, when S_max·Hkv is a multiple of 4, those of all
 // heads of the tile's 64 tokens as one contiguous bulk copy each, else the 128 the block needs
 // by 4-byte asynchronous copies), and with a piece's first tile the piece's G bf16 query rows.
-// Each consumer warp takes 16 tokens of a tile and builds its MMA operands straight from the
-// codes in the stage, widening them in registers (every E4M3 value is an fp16 value, so the
-// widening is exact; one instruction per two codes):
-//   S = Q·Kᵀ  mma.sync m16n8k16 (fp16 → fp32), the G ≤ 16 query heads on M, the tokens on N.
-//             A thread's K operand for two k-steps is 8 consecutive codes of one token row,
-//             so the feature order inside each 32-wide block is permuted (the same way for Q:
-//             a dot product does not depend on the order of its terms). Each token's products
-//             times its K scale, in the base-2 domain (scale · log2 e). The bf16 query is
-//             rounded to fp16 once per piece: exact for |q| in [2^-14, 65504], off by at most
-//             2^-25 below;
-//   softmax   running max and sum per head with quad shuffles, as in the bf16 decode kernel;
-//   O += P·V  the weights times each token's V scale and 2^10 (the sum l takes the unscaled
-//             weights; the 2^10 keeps small weights out of fp16's subnormal range and is
-//             divided out at the end), split into an fp16 head and an fp16 residual (about
-//             2^-22 of each weight left), each multiplied with the V codes. A thread's V
-//             operand is a pair of tokens at one feature; it loads D/8 consecutive codes of
-//             each of its four tokens and interleaves them with byte permutes, so output
-//             feature d = (D/8)·n + nd sits at column n of the nd-th 8-column MMA block.
+// Each consumer warp takes 16 tokens of a tile and builds its mma.sync m16n8k16 operands
+// (fp16 in, fp32 accumulate) straight from the codes in the stage, widening them in
+// registers (every E4M3 value is an fp16 value, so the widening is exact; one instruction per
+// two codes). The query heads sit on the MMA's N side in blocks of 8 (one block for G <= 8,
+// two up to 16):
+//   S = K·Qᵀ  the slice's 16 tokens on M. A thread's K operand for two k-steps is 8
+//             consecutive codes of one token row, so the feature order inside each 32-wide
+//             block is permuted (the same way for Q: a dot product does not depend on the
+//             order of its terms). Each token's products times its K scale, in the base-2
+//             domain (scale · log2 e). The bf16 query is rounded to fp16 once per piece:
+//             exact for |q| in [2^-14, 65504], off by at most 2^-25 below;
+//   softmax   running max and sum per head (a column) across the 8 lanes that hold its rows;
+//   Oᵀ += Vᵀ·Pᵀ  the weights times each token's V scale and 2^10 (the sum l takes the
+//             unscaled weights; the 2^10 keeps small weights out of fp16's subnormal range and
+//             is divided out at the end), split into an fp16 head and an fp16 residual (about
+//             2^-22 of each weight left); the score fragment, transposed by movmatrix, is the
+//             B operand, and each part is multiplied with the V codes. A thread's A operand is
+//             a pair of tokens at one feature: it loads D/8 consecutive codes of each of its
+//             four tokens and interleaves them with byte permutes, so output feature
+//             d = (D/8)·g + 2mb (+1) sits at row g (+8) of the mb-th 16-row block.
 // Codes of tokens past the segment are zeroed (the stage may hold anything there).
 // At a piece's end the four warps' states are combined through a small shared buffer.
 //
 // Every mbarrier wait is bounded (MLAKV_WAIT_TIMEOUT_CYCLES); a wait that runs out sets a bit
 // in g_decode_fp8_status and the warp skips its remaining work but still meets its partners
-// at every named barrier, so the block always reaches its end.
+// at every barrier, so the block always reaches its end.
 #include "ptx.cuh"
 #include "streamk.cuh"
 #include "tensor_map.cuh"
