@@ -654,6 +654,7 @@ class MlaChunked(DecodeMla):
 class Prefill:
     kind = "prefill"
     kernel_src = "mla_kv_cache_flash_b300/csrc/prefill.cu"
+    call_name = "attn_prefill_gqa_causal"
 
     def __init__(self, w, device, rank, l2_bytes):
         import mla_kv_cache_flash_b300 as mk
@@ -705,6 +706,83 @@ class Prefill:
                 "lengths": [int(x) for x in self.lens], "causal_flops": self.flops_per_step, "l2": self.l2_note}
 
 
+class ChunkedPrefill(Prefill):
+    """Chunked prefill of long chunks over existing caches: each sequence's last n_new cached
+    rows are its new tokens (start_pos = S - n_new), so new row i sees start_pos + i + 1 rows.
+    Algorithmic flops: 4·D per (new row, visible key) pair and query head (Q·Kᵀ and P·V)."""
+    call_name = "attn_prefill_gqa_chunked (tcgen05 prefill kernel, K and V read from the caches)"
+    n_new = 512
+
+    def _make(self, seed):
+        w, B, n = self.w, self.w.batch, self.n_new
+        s = W.decode_inputs(w, self.device, seed=seed)
+        del s["q"]
+        g = torch.Generator(device=self.device).manual_seed(seed + 700)
+        s["q_chunk"] = torch.randn((B * n, w.n_q_heads, w.head_dim), generator=g, device=self.device).to(torch.bfloat16)
+        s["cu_q"] = torch.arange(0, B * n + 1, n, dtype=torch.int32, device=self.device)
+        s["start_pos"] = (s["seq_lens"] - n).contiguous()
+        return s
+
+    def __init__(self, w, device, rank, l2_bytes):
+        import mla_kv_cache_flash_b300 as mk
+        self.mk, self.w, self.device, self.name = mk, w, device, w.name
+        first = self._make(w.seed + 1000 * rank)
+        B, n, D = w.batch, self.n_new, w.head_dim
+        self.start = [int(x) for x in first["start_pos"].cpu()]
+        self.lens = np.full(B, n)                       # new tokens per sequence
+        self.flops_per_step = sum(self._seq_flops(b) for b in range(B))
+        io = first["q_chunk"].nbytes + first["k_cache"].nbytes + first["v_cache"].nbytes + B * n * w.n_q_heads * D * 4
+        n_sets = max(1, math.ceil(4 * l2_bytes / io))
+        self.sets = [first] + [self._make(w.seed + 1000 * rank) for _ in range(n_sets - 1)]
+        self.out = torch.empty((B * n, w.n_q_heads, D), dtype=torch.float32, device=device)
+        nb = int(mk.lib().attn_prefill_gqa_chunked_workspace_size(B, B * n, w.n_q_heads, w.n_kv_heads, D, w.s_max,
+                                                                  mk.ATTN_BF16, 0))
+        if nb != 0:
+            raise RuntimeError("long chunks are expected on the prefill kernel (no workspace)")
+        self.launches_per_step = 1
+        self.bytes_per_step = io
+        self.l2_note = f"rotating {n_sets} input sets ({n_sets * io / 1e6:.0f} MB, L2 {l2_bytes / 1e6:.0f} MB)"
+
+    def _seq_flops(self, b):
+        n, kv0 = self.n_new, self.start[b]
+        return 4 * self.w.head_dim * self.w.n_q_heads * (n * kv0 + n * (n + 1) // 2)
+
+    def _run(self, s):
+        self.mk.prefill_gqa_chunked(s["q_chunk"], s["k_cache"], s["v_cache"], s["cu_q"], s["start_pos"], self.w.s_max,
+                                    out=self.out, scale=self.w.scale)
+
+    def step(self, i):
+        self._run(self.sets[i % len(self.sets)])
+
+    def host_inputs(self):
+        s = self.sets[0]
+        return {k: s[k].cpu().pin_memory() for k in ("q_chunk", "k_cache", "v_cache", "cu_q", "start_pos")}
+
+    def e2e_step(self, host, dev_bufs, out_host):
+        for k, t in host.items():
+            dev_bufs[k].copy_(t, non_blocking=True)
+        self._run(dev_bufs)
+        out_host.copy_(self.out, non_blocking=True)
+
+    oracle_kind = "chunk"
+
+    def oracle_payload(self):
+        """The first sequence of the batch: its chunk and its caches, one unit."""
+        s, n = self.sets[0], self.n_new
+        arrays = {"q": _f32(s["q_chunk"][:n]), "k": _f32(s["k_cache"][:1]), "v": _f32(s["v_cache"][:1]),
+                  "cu_q": np.array([0, n], dtype=np.int64), "start_pos": _host(s["start_pos"][:1])}
+        return arrays, [(0,)], 1
+
+    def unit_work(self, unit):
+        return self._seq_flops(unit[0])
+
+    def describe(self):
+        w = self.w
+        return {"workload": w.name, "B": w.batch, "Hq": w.n_q_heads, "Hkv": w.n_kv_heads, "D": w.head_dim,
+                "S_max": w.s_max, "start_pos": self.start[0], "new_tokens_per_sequence": self.n_new,
+                "causal_flops": self.flops_per_step, "l2": self.l2_note}
+
+
 WORKLOADS = {
     "minimind_gqa": lambda: (DecodeGqa, W.MINIMIND_GQA),
     "llama_hkv32": lambda: (DecodeGqa, W.LLAMA3_8B[32]),
@@ -718,10 +796,11 @@ WORKLOADS = {
     "mla_step": lambda: (DecodeMlaStep, dataclasses.replace(W.MINIMIND_MLA, name=W.MINIMIND_MLA.name + "_full_step")),
     "prefill": lambda: (Prefill, W.PREFILL_UNIFORM),
     "prefill_ragged": lambda: (Prefill, W.PREFILL_RAGGED),
+    "prefill_chunk512": lambda: (ChunkedPrefill, W.LLAMA3_8B_CHUNK512),
 }
-# the configurations of the benchmark spec's targets come last, so a log's tail keeps them
+# the largest decode and prefill configurations come last, so a log's tail keeps them
 ALSO = ("minimind_gqa", "minimind_gqa_step", "minimind_gqa_fp8", "minimind_gqa_chunk4", "mla_chunk4", "mla_step",
-        "llama_hkv32", "llama_hkv1", "mla", "prefill", "prefill_ragged")
+        "prefill_chunk512", "llama_hkv32", "llama_hkv1", "mla", "prefill", "prefill_ragged")
 
 
 # ============================================================================ timing
@@ -813,7 +892,7 @@ def summarize(wl, t, peaks, peak_src, world):
                 "frac": round(achieved / peaks["bf16_tflops"], 4),
                 "traffic": profiled_traffic(wl.kernel_src, wl.name),
                 "peak_source": f"{peak_src} dense bf16 burst (MEASURED_PEAKS bf16_tflops)",
-                "algorithmic_flops_per_launch": wl.flops_per_step, "kernel": "attn_prefill_gqa_causal"}
+                "algorithmic_flops_per_launch": wl.flops_per_step, "kernel": wl.call_name}
         extra = {"tokens_per_s": round(float(np.sum(wl.lens)) * world / per_step, 1)}
     out = {"value": round(value, 2), "unit": unit, "ms_per_step": round(per_step * 1e3, 5), "roofline": roof,
            "gpu_launches": t["runs"] * t["calls_per_run"] * wl.launches_per_step, "config": wl.describe(),
@@ -968,7 +1047,7 @@ class OraclePool:
                 work = passes * sum(wl.unit_work(u) for u in units)
                 covered = "all" if n_seq == wl.w.batch else f"the first {n_seq} of the {wl.w.batch}"
                 what = (f"{passes} pass(es) over {len(units)} units ({covered} sequences"
-                        f"{', one unit per query head' if wl.kind == 'prefill' else ''}), fp64 oracle, "
+                        f"{', one unit per query head' if wl.oracle_kind == 'prefill' else ''}), fp64 oracle, "
                         f"{workers} worker processes")
                 return work / wall / scale_work, workers, what, None
             per_step_budget = budget_s / max(1, steps + warmup)

@@ -303,12 +303,20 @@ int attn_prefill_gqa_causal(const void *q, const void *k, const void *v,
  *              max_kv = 0 launches nothing.
  *   n_split, workspace: size from attn_prefill_gqa_chunked_workspace_size with the same
  *              dtype; zero-filled before its first use (see "Workspaces").
- * Kernels: a bf16 cache with Hq/Hkv a multiple of 16 at D = 128 runs on the tcgen05 decode
- * kernel, 4 new tokens × 16 query heads per thread block, so each cached row a block reads
- * feeds all of them (n_split > 0 caps the blocks at n_split per segment); other shapes run on
- * the CUDA-core kernel, each new token a decode over its visible cache (n_split as for an
- * fp32 cache), then the K2 merge. With n_b = 1 and start_pos = seq_lens − 1 this is one decode
- * step.
+ * Kernels, chosen from the host arguments alone:
+ *   - bf16 at D = 128 with T >= 128·B (chunks of 128 new tokens or more on average): the
+ *     tcgen05 prefill kernel of attn_prefill_gqa_causal reading K and V from the caches,
+ *     128 new tokens × one query head per MMA tile; no split, no workspace (the size is 0
+ *     and n_split is ignored). Cache rows past start_pos[b] + n_b may hold anything (NaN
+ *     included): they never reach an output.
+ *   - other bf16 caches with Hq/Hkv a multiple of 16 at D = 128: the tcgen05 decode kernel,
+ *     4 new tokens × 16 query heads per thread block, so each cached row a block reads feeds
+ *     all of them (n_split > 0 caps the blocks at n_split per segment);
+ *   - other bf16 caches with at most 16 query heads per KV head: the register-MMA decode
+ *     kernel, 16/G new tokens × G heads per MMA tile (n_split as for the tcgen05 form);
+ *   - the rest (fp32 caches included): the CUDA-core kernel, each new token a decode over its
+ *     visible cache (n_split as for an fp32 cache), then the K2 merge.
+ * With n_b = 1 and start_pos = seq_lens − 1 this is one decode step.
  * ------------------------------------------------------------------------------------- */
 size_t attn_prefill_gqa_chunked_workspace_size(int B, int T, int Hq, int Hkv, int D, int max_kv,
                                                attn_dtype dtype, int n_split);

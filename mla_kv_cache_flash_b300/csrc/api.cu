@@ -347,9 +347,16 @@ SplitPlan chunked_plan(int T, int Hq, int Hkv, int D, int max_kv, int n_split) {
     return gqa_plan(T > 0 ? T : 1, Hq, Hkv, D, max_kv, ATTN_F32, n_split);
 }
 
-// bf16 caches whose query groups are a multiple of 16 heads at D = 128 (and every MLA cache
-// with Hq a multiple of 16) run chunks on the tcgen05 kernel: 4 new tokens × 16 heads per
-// block read each cached row once. Other shapes use the CUDA-core form, one new token per block.
+// bf16 at D = 128 with chunks of at least 128 new tokens on average: the tcgen05 prefill kernel
+// in its cache form, 128 new tokens × one head per MMA tile, so the decode kernels' re-reading
+// of the cache once per few new tokens is gone
+bool chunk_on_prefill(int B, int T, int D, attn_dtype dtype) {
+    return dtype == ATTN_BF16 && D == 128 && B > 0 && (long long)T >= 128LL * B;
+}
+// Shorter chunks: bf16 caches whose query groups are a multiple of 16 heads at D = 128 (and
+// every MLA cache with Hq a multiple of 16) run on the tcgen05 decode kernel, 4 new tokens × 16
+// heads per block reading each cached row once; other bf16 shapes on the register-MMA decode
+// kernel; the rest on the CUDA-core form, one new token per block.
 bool chunk_on_tc_gqa(int B, int Hq, int Hkv, int D, attn_dtype dtype) {
     return dtype == ATTN_BF16 && decode_tc_gqa_chunk_eligible(B, Hq, Hkv, D);
 }
@@ -367,6 +374,7 @@ MLAKV_API size_t attn_prefill_gqa_chunked_workspace_size(int B, int T, int Hq, i
     if (check_chunked(B, T, Hq, Hkv, D, max_kv > 0 ? max_kv : 1, max_kv, dtype, n_split,
                       "attn_prefill_gqa_chunked_workspace_size") != ATTN_OK || T == 0)
         return 0;
+    if (chunk_on_prefill(B, T, D, dtype)) return 0;
     if (chunk_on_tc_gqa(B, Hq, Hkv, D, dtype)) return decode_tc_gqa_chunk_workspace(B, T, Hq, Hkv, n_split);
     if (chunk_on_stream(B, Hq, Hkv, D, dtype)) return decode_gqa_stream_chunk_workspace(B, T, Hq, Hkv, D, n_split);
     return partials_bytes(T, Hq, D, chunked_plan(T, Hq, Hkv, D, max_kv, n_split).n_split);
@@ -387,6 +395,18 @@ MLAKV_API int attn_prefill_gqa_chunked(const void *q, const void *k_cache, const
         return fail(ATTN_ERR_UNSUPPORTED, "%s: every pointer must be 16-byte aligned", who);
     if (T == 0 || max_kv == 0) return ok();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (chunk_on_prefill(B, T, D, dtype)) {
+        PrefillArgs a{};
+        a.q = q; a.k = k_cache; a.v = v_cache; a.cu_seqlens = cu_q; a.out = out;
+        a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.T = T;
+        a.scale_log2 = scale * kLog2e;
+        a.max_seqlen = T < max_kv ? T : max_kv;      // no chunk is longer than either
+        a.out32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
+        a.start_pos = start_pos; a.S_max = S_max;
+        const cudaError_t e = launch_prefill(a, s);
+        if (e != cudaSuccess) return cuda_fail(e, "attn_prefill_gqa_chunked: kernel launch");
+        return ok();
+    }
     if (chunk_on_tc_gqa(B, Hq, Hkv, D, dtype)) {
         const size_t need = decode_tc_gqa_chunk_workspace(B, T, Hq, Hkv, n_split);
         if (!workspace || ws_bytes < need || !aligned16(workspace))

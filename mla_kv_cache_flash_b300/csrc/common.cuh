@@ -76,6 +76,11 @@ struct PrefillArgs {
     float scale_log2;
     int max_seqlen;
     int out32;              // out is 32-byte aligned (the epilogue then stores 32 bytes at a time)
+    // Cache form (chunked prefill): k and v are caches [B, S_max, Hkv, D] already holding the
+    // chunks, and row i of sequence b's chunk sits at position start_pos[b] + i, seeing cache
+    // rows 0 .. start_pos[b] + i. nullptr: k and v are packed like q, positions from 0.
+    const int *start_pos;
+    int S_max;
 };
 
 // ------------------------------------------------------------------ launchers (one per TU)

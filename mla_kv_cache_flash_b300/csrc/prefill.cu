@@ -40,6 +40,16 @@
 // bf16 head and a bf16 residual and both are multiplied with V, which leaves an error near
 // 2^-16 there.
 //
+// Cache form (chunked prefill over an existing cache: "模型架构｜MQA & GQA 调研", section
+// "代码", the new tokens written at start_pos before attending): K and V come from the caches [B, S_max, Hkv, D] through
+// 4D tensor maps, and row i of sequence b's chunk sees cache rows 0 .. start_pos[b] + i. An
+// item then covers KV tiles 0 .. (start_pos + last row) / 128, and the mask starts at the tile
+// holding key start_pos + first row: with an unaligned start_pos two tiles are masked, each
+// row by its own limit. V rows past the chunk's end (the cache may hold anything there, NaN
+// included) are zeroed in shared memory by the MMA warp before P·V reads them; their weights
+// are 0, but 0 · NaN is not. The item list spans the longest chunk, found by every warp at
+// block start from cu_seqlens.
+//
 // Every wait is bounded (MLAKV_WAIT_TIMEOUT_CYCLES): a wait that runs out sets a bit in
 // g_prefill_status and the thread abandons its loop; every thread still reaches the final
 // barrier, so tensor memory is always released.
@@ -236,6 +246,50 @@ __device__ __forceinline__ bool item_at(int k, int blk, int nblk, int n_items, i
     return true;
 }
 
+// One item's extent. kv0: the position of the item's sequence's row 0 among its keys
+// (start_pos in the cache form, else 0); nkv: KV tiles the item reads; mask_from: the first
+// of them holding a key hidden from some row.
+struct Span {
+    int seq0, S, kv0, nkv, mask_from;
+};
+template <bool CACHE>
+__device__ __forceinline__ bool item_span(const PrefillArgs &a, const Item &it, Span &sp) {
+    sp.seq0 = a.cu_seqlens[it.b];
+    sp.S = a.cu_seqlens[it.b + 1] - sp.seq0;
+    if (it.qt * BM >= sp.S) return false;
+    if (CACHE) {
+        sp.kv0 = a.start_pos[it.b];
+        const int last = min((it.qt + 1) * BM, sp.S) - 1;          // the item's last row
+        sp.nkv = (sp.kv0 + last) / BN + 1;
+        sp.mask_from = (sp.kv0 + it.qt * BM) / BN;
+    } else {
+        sp.kv0 = 0;
+        sp.nkv = it.qt + 1;
+        sp.mask_from = it.qt;
+    }
+    return true;
+}
+
+// Query tiles of the longest sequence, at most n_qt (warp-collective).
+__device__ __forceinline__ int longest_tiles(const int *cu, int B, int n_qt, int lane) {
+    int mx = 0;
+    for (int b = lane; b < B; b += 32) mx = max(mx, cu[b + 1] - cu[b]);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    return min(n_qt, (mx + BM - 1) / BM);
+}
+
+// Zero rows z0 .. 127 of a V tile in shared memory (both 64-column boxes; a row's 128 bytes
+// in a box are its own whatever the swizzle), then make the writes visible to the tensor core.
+__device__ __forceinline__ void zero_v_rows(uint8_t *tile, int z0, int lane) {
+    for (int i = lane; i < (BN - z0) * 16; i += 32) {
+        const int r = z0 + (i >> 4), c = i & 15;
+        *reinterpret_cast<uint4 *>(tile + (c >> 3) * BOX_BYTES + r * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+}
+
+template <bool CACHE>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap, const PrefillArgs a,
@@ -250,7 +304,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int lane = threadIdx.x & 31;
     const int n_hgrp = a.Hq / heads_per_cta;
     const int per_qt = a.B * n_hgrp;
-    const int n_items = n_qt * per_qt;
     const int n_mt = heads_per_cta;                 // query tiles per item (heads h0, h0+1)
     const int G = a.Hq / a.Hkv;
     const int blk = blockIdx.x, nblk = gridDim.x;
@@ -282,6 +335,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     griddep_wait();                                 // cu_seqlens and the inputs are read below
+    if (CACHE) n_qt = longest_tiles(a.cu_seqlens, a.B, n_qt, lane);
+    const int n_items = n_qt * per_qt;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -293,10 +348,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             int g_kv = 0, qc = 0;                    // K/V tiles and Q tiles loaded so far
             bool ok = true;
             Item it;
+            Span sp;
             for (int k = 0; ok && item_at(k, blk, nblk, n_items, per_qt, n_hgrp, heads_per_cta, n_qt, it); ++k) {
-                const int seq0 = a.cu_seqlens[it.b];
-                const int S = a.cu_seqlens[it.b + 1] - seq0;
-                if (it.qt * BM >= S) continue;
+                if (!item_span<CACHE>(a, it, sp)) continue;
                 const int j = it.h0 / G;
                 // Q tile t of this item goes to slot qc % 3; the slot's previous tile must be
                 // done with (its last S MMA complete)
@@ -309,28 +363,39 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     mbar_arrive_expect_tx(bar(kQFull + q), TILE_BYTES);
                     for (int bx = 0; bx < 2; ++bx)
                         tma_load_3d(sb + Q_OFF + q * TILE_BYTES + bx * BOX_BYTES, &qmap, bx * 64, it.h0 + t,
-                                    seq0 + it.qt * BM, bar(kQFull + q), pol_q);
+                                    sp.seq0 + it.qt * BM, bar(kQFull + q), pol_q);
                 }
-                for (int n = 0; ok && n <= it.qt; ++n, ++g_kv) {
+                for (int n = 0; ok && n < sp.nkv; ++n, ++g_kv) {
                     const int s = g_kv % NSTAGE;
                     const uint32_t free_ph = ((g_kv / NSTAGE) & 1) ^ 1;
                     if (!mbar_wait_bounded(bar(kKEmpty + s), free_ph, &g_prefill_status, kStatusEmptyWait)) {
                         ok = false;
                         break;
                     }
-                    const int k_tok = seq0 + n * BN;
+                    // the tile's first key: a row of the packed K/V, or a position in the cache
+                    const int k_tok = CACHE ? n * BN : sp.seq0 + n * BN;
                     mbar_arrive_expect_tx(bar(kKFull + s), TILE_BYTES);
-                    for (int bx = 0; bx < 2; ++bx)
-                        tma_load_3d_nohint(sb + K_OFF + s * TILE_BYTES + bx * BOX_BYTES, &kmap, bx * 64, j, k_tok,
-                                           bar(kKFull + s));
+                    for (int bx = 0; bx < 2; ++bx) {
+                        if (CACHE)
+                            tma_load_4d_nohint(sb + K_OFF + s * TILE_BYTES + bx * BOX_BYTES, &kmap, bx * 64, j, k_tok,
+                                               it.b, bar(kKFull + s));
+                        else
+                            tma_load_3d_nohint(sb + K_OFF + s * TILE_BYTES + bx * BOX_BYTES, &kmap, bx * 64, j, k_tok,
+                                               bar(kKFull + s));
+                    }
                     if (!mbar_wait_bounded(bar(kVEmpty + s), free_ph, &g_prefill_status, kStatusEmptyWait)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(bar(kVFull + s), TILE_BYTES);
-                    for (int bx = 0; bx < 2; ++bx)
-                        tma_load_3d_nohint(sb + V_OFF + s * TILE_BYTES + bx * BOX_BYTES, &vmap, bx * 64, j, k_tok,
-                                           bar(kVFull + s));
+                    for (int bx = 0; bx < 2; ++bx) {
+                        if (CACHE)
+                            tma_load_4d_nohint(sb + V_OFF + s * TILE_BYTES + bx * BOX_BYTES, &vmap, bx * 64, j, k_tok,
+                                               it.b, bar(kVFull + s));
+                        else
+                            tma_load_3d_nohint(sb + V_OFF + s * TILE_BYTES + bx * BOX_BYTES, &vmap, bx * 64, j, k_tok,
+                                               bar(kVFull + s));
+                    }
                 }
             }
             // no copy may still be in flight when the block exits
@@ -415,14 +480,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             return true;
         };
         Item it;
+        Span sp;
         for (int k = 0; ok && item_at(k, blk, nblk, n_items, per_qt, n_hgrp, heads_per_cta, n_qt, it); ++k) {
-            const int S = a.cu_seqlens[it.b + 1] - a.cu_seqlens[it.b];
-            if (it.qt * BM >= S) continue;
-            const bool split_p = it.qt < kSplitTiles;
+            if (!item_span<CACHE>(a, it, sp)) continue;
+            const bool split_p = sp.kv0 + it.qt * BM < kSplitTiles * BM;
             const int q0 = qc % Q_SLOTS, u0 = qc / Q_SLOTS;
             const int q1 = (qc + 1) % Q_SLOTS, u1 = (qc + 1) / Q_SLOTS;
             qc += n_mt;
-            for (int n = 0; n <= it.qt; ++n, ++g) {
+            for (int n = 0; n < sp.nkv; ++n, ++g) {
                 const int s = g % NSTAGE;
                 const uint32_t ph = (g / NSTAGE) & 1;
                 // at an item boundary the previous item's last P·V_1 goes first: S_0 may wait
@@ -432,18 +497,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 if (n == 0 && !(ok = wait_all(kQFull + q0, u0 & 1, kStatusFullWait))) break;
                 tc_fence_after();
                 issue_s(0, q0, s);
-                if (n == it.qt) commit(kQEmpty + q0);
+                if (n == sp.nkv - 1) commit(kQEmpty + q0);
                 if (n_mt == 1) commit(kKEmpty + s);
                 if (n_mt == 2) {
                     if (!(ok = flush_pv1())) break;
                     if (n == 0 && !(ok = wait_all(kQFull + q1, u1 & 1, kStatusFullWait))) break;
                     tc_fence_after();
                     issue_s(1, q1, s);
-                    if (n == it.qt) commit(kQEmpty + q1);
+                    if (n == sp.nkv - 1) commit(kQEmpty + q1);
                     commit(kKEmpty + s);                 // both S MMAs of this K tile are issued
                 }
                 if (!(ok = wait_all(kVFull + s, ph, kStatusFullWait) && wait_all(kPReady + 0, g & 1, kStatusMmaWait)))
                     break;
+                if (CACHE && n == sp.nkv - 1) {
+                    // cache rows past the chunk's end (first at z0 >= 1 of this tile) hold
+                    // anything; their weights are 0, so their values must be finite
+                    const int z0 = sp.kv0 + sp.S - n * BN;
+                    if (z0 < BN) zero_v_rows(smem + V_OFF + s * TILE_BYTES, z0, lane);
+                }
                 tc_fence_after();
                 issue_pv(0, s, n == 0, split_p);
                 if (n_mt == 2) {
@@ -475,13 +546,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         int g = 0;
         bool ok = t < n_mt;
         Item it;
+        Span sp;
         for (int k = 0; ok && item_at(k, blk, nblk, n_items, per_qt, n_hgrp, heads_per_cta, n_qt, it); ++k) {
-            const int seq0 = a.cu_seqlens[it.b];
-            const int S = a.cu_seqlens[it.b + 1] - seq0;
-            if (it.qt * BM >= S) continue;
-            const bool split_p = it.qt < kSplitTiles;
+            if (!item_span<CACHE>(a, it, sp)) continue;
+            const int seq0 = sp.seq0, S = sp.S;
+            const bool split_p = sp.kv0 + it.qt * BM < kSplitTiles * BM;
             float m_ref = -INFINITY, l = 0.f;
-            for (int n = 0; n <= it.qt; ++n, ++g) {
+            for (int n = 0; n < sp.nkv; ++n, ++g) {
                 // the warp decides together: the TMEM accesses below are warp-collective
                 const bool got = mbar_wait_bounded(bar(kSFull + t), g & 1, &g_prefill_status, kStatusFullWait);
                 if (!__all_sync(0xffffffffu, got)) {
@@ -489,14 +560,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     break;
                 }
                 tc_fence_after();
-                const bool diag = n == it.qt;
-                const float ext = neg ? (diag ? row_extreme<true, true>(s_addr, row) : row_extreme<false, true>(s_addr, row))
-                                      : (diag ? row_extreme<true, false>(s_addr, row) : row_extreme<false, false>(s_addr, row));
+                // a masked tile: key k of the tile is visible to this row iff k <= lim
+                const bool diag = n >= sp.mask_from;
+                const int lim = row + sp.kv0 + it.qt * BM - n * BN;
+                const float ext = neg ? (diag ? row_extreme<true, true>(s_addr, lim) : row_extreme<false, true>(s_addr, lim))
+                                      : (diag ? row_extreme<true, false>(s_addr, lim) : row_extreme<false, false>(s_addr, lim));
                 const float mt = ext * a.scale_log2;
                 float alpha = 1.f;
                 bool grow = false;
                 if (n == 0) {
-                    m_ref = mt;                      // key 0 of a tile is always visible
+                    m_ref = mt;                      // key 0 of the first tile is always visible
                 } else if (mt > m_ref + kRescaleLog2) {
                     alpha = fast_exp2(m_ref - mt);
                     m_ref = mt;
@@ -516,12 +589,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     }
                 }
                 if (split_p)
-                    diag ? write_p<true, true>(s_addr, a.scale_log2, m_ref, row, l)
-                         : write_p<false, true>(s_addr, a.scale_log2, m_ref, row, l);
+                    diag ? write_p<true, true>(s_addr, a.scale_log2, m_ref, lim, l)
+                         : write_p<false, true>(s_addr, a.scale_log2, m_ref, lim, l);
                 else if (diag)
-                    write_p<true, false>(s_addr, a.scale_log2, m_ref, row, l);
+                    write_p<true, false>(s_addr, a.scale_log2, m_ref, lim, l);
                 else
-                    write_p<false, false>(s_addr, a.scale_log2, m_ref, row, l);
+                    write_p<false, false>(s_addr, a.scale_log2, m_ref, lim, l);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(bar(kPReady + t));
@@ -630,7 +703,19 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t st) {
                                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         if (e != cudaSuccess) return e;
     }
-    {
+    const bool cache = a.start_pos != nullptr;
+    if (cache) {
+        // the caches [B, S_max, Hkv, D]: coordinates (column, KV head, position, sequence)
+        const uint64_t dims[4] = {(uint64_t)HD, (uint64_t)a.Hkv, (uint64_t)a.S_max, (uint64_t)a.B};
+        const uint64_t strides[3] = {(uint64_t)HD * 2, (uint64_t)a.Hkv * HD * 2, (uint64_t)a.S_max * a.Hkv * HD * 2};
+        const uint32_t box4[4] = {64, 1, BN, 1};
+        cudaError_t e = encode_tensor_map(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.k, dims, strides, box4,
+                                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        if (e == cudaSuccess)
+            e = encode_tensor_map(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.v, dims, strides, box4,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        if (e != cudaSuccess) return e;
+    } else {
         const uint64_t dims[3] = {(uint64_t)HD, (uint64_t)a.Hkv, (uint64_t)a.T};
         const uint64_t strides[2] = {(uint64_t)HD * 2, (uint64_t)a.Hkv * HD * 2};
         cudaError_t e = encode_tensor_map(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.k, dims, strides, kvbox,
@@ -649,11 +734,12 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t st) {
                                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
         if (e != cudaSuccess) return e;
     }
-    static bool attr_set = false;
-    if (!attr_set) {
-        const cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    static bool attr_set[2] = {false, false};
+    if (!attr_set[cache]) {
+        const cudaError_t e = cache ? cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM)
+                                    : cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set[cache] = true;
     }
     const int G = a.Hq / a.Hkv;
     const int heads_per_cta = (G % 2 == 0) ? 2 : 1;
@@ -665,8 +751,10 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t st) {
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return cudaErrorInvalidDevice;
     const int grid = (int)(n_items < sms ? n_items : sms);
-    const cudaError_t e = launch_pdl(prefill_kernel, dim3(grid), dim3(kThreads), SMEM, st, qm, km, vm, om, a, n_qt,
-                                     heads_per_cta);
+    const cudaError_t e = cache ? launch_pdl(prefill_kernel<true>, dim3(grid), dim3(kThreads), SMEM, st, qm, km, vm, om,
+                                             a, n_qt, heads_per_cta)
+                                : launch_pdl(prefill_kernel<false>, dim3(grid), dim3(kThreads), SMEM, st, qm, km, vm,
+                                             om, a, n_qt, heads_per_cta);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -149,6 +149,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
 }
 
 // 3-D tiled TMA load without an L2 cache hint (data that other blocks read again).
+__device__ __forceinline__ void tma_load_4d_nohint(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                                   int c3, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
 __device__ __forceinline__ void tma_load_3d_nohint(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
                                                    uint32_t bar) {
     asm volatile(

@@ -218,6 +218,19 @@ def test_chunked_tensor_core_workspace(L):
     assert L.attn_prefill_gqa_chunked_workspace_size(2, 10, 32, 2, 128, 4096, 0, 1) == 0
 
 
+def test_chunked_long_chunks_need_no_workspace(L):
+    # bf16 at D = 128 with chunks of 128 new tokens or more on average: the tcgen05 prefill
+    # kernel over the caches, no split and no workspace, for any n_split
+    for hq, hkv in ((32, 2), (32, 8), (12, 4)):
+        for n_split in (0, 1, 5):
+            assert L.attn_prefill_gqa_chunked_workspace_size(2, 256, hq, hkv, 128, 4096, 1, n_split) == 0
+    # one token short of 128 per sequence: the decode kernels again
+    assert L.attn_prefill_gqa_chunked_workspace_size(2, 255, 32, 2, 128, 4096, 1, 0) > 0
+    # fp32, or D below 128: never the prefill kernel
+    assert L.attn_prefill_gqa_chunked_workspace_size(2, 256, 32, 8, 128, 4096, 0, 4) > 0
+    assert L.attn_prefill_gqa_chunked_workspace_size(2, 256, 32, 8, 96, 4096, 1, 0) > 0
+
+
 def mla_chunked(L, ql=P, qr=P, c=P, kr=P, cu=P, st=P, out=P, B=2, T=10, Hq=16, r=128, dr=48, scale=1 / 12,
                 S_max=64, max_kv=64, n_split=1, ws=N0, ws_bytes=0):
     return L.attn_prefill_mla_chunked(ql, qr, c, kr, cu, st, out, B, T, Hq, r, dr, scale, S_max, max_kv, n_split,

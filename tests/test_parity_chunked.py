@@ -74,6 +74,54 @@ def test_chunked_bf16_long_chunk(hq, hkv):
            n_splits=(0, 3))
 
 
+# bf16 at D = 128 with chunks averaging at least 128 tokens: the tcgen05 prefill kernel reading
+# K and V from the caches. Start positions on and off the 128-key tile grid (0, 1, 127, 128,
+# 700, 2000), chunks of 1, 128, 129, 200, 256, 300 and 512 tokens and an empty one; 32, 4, 3
+# (one head per item) and 1 query heads per KV head.
+_LONG = ((0, 300), (1, 128), (127, 129), (128, 256), (700, 512), (3000, 1), (0, 0), (2000, 200))
+
+
+def _poison_past_chunks(cache, start, cu):
+    """Fill every cache row at or past start_pos + n_b with NaN (the kernel must not let them
+    reach a visible output through a zero weight)."""
+    c = cache.clone()
+    for b in range(c.shape[0]):
+        c[b, int(start[b]) + int(cu[b + 1] - cu[b]):] = float("nan")
+    return c
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (32, 1), (12, 4), (16, 16)])
+def test_chunked_long_chunks_on_the_prefill_kernel(hq, hkv):
+    q, k, v, cu, start, scale = _case(_LONG, hq, hkv, 128, 4096, "bf16", 90 + hq + hkv)
+    k, v = _poison_past_chunks(k, start, cu), _poison_past_chunks(v, start, cu)
+    T, B = int(cu[-1]), len(_LONG)
+    assert T >= 128 * B
+    assert mk.lib().attn_prefill_gqa_chunked_workspace_size(B, T, hq, hkv, 128, 3200, mk.ATTN_BF16, 0) == 0
+    ref = oracle.prefill_gqa_chunked(to_f64(q), to_f64(k), to_f64(v), cu, start, scale)
+    out = mk.prefill_gqa_chunked(q, k, v, torch.from_numpy(cu).to(DEV), torch.from_numpy(start).to(DEV), 3200,
+                                 scale=scale)
+    torch.cuda.synchronize()
+    mk.check_status()
+    assert bool(torch.isfinite(out).all())
+    assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3
+
+
+def test_chunked_long_chunks_negative_scale_and_loose_bound():
+    """A negative scale (the row maximum is then the smallest raw score) and a max_kv far
+    above every chunk end (the item list is cut to the longest chunk inside the kernel)."""
+    chunks = ((5, 640), (0, 129), (4000, 96), (1300, 130))
+    q, k, v, cu, start, _ = _case(chunks, 16, 2, 128, 4096, "bf16", 77)
+    k = _poison_past_chunks(k, start, cu)
+    v = _poison_past_chunks(v, start, cu)
+    scale = -0.07
+    ref = oracle.prefill_gqa_chunked(to_f64(q), to_f64(k), to_f64(v), cu, start, scale)
+    out = mk.prefill_gqa_chunked(q, k, v, torch.from_numpy(cu).to(DEV), torch.from_numpy(start).to(DEV), 4096,
+                                 scale=scale)
+    torch.cuda.synchronize()
+    mk.check_status()
+    assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3
+
+
 def test_chunked_single_tokens_are_decode_steps():
     """Chunks of one token at start_pos = length − 1 give the decode of that length."""
     w = W.MINIMIND_GQA

@@ -117,6 +117,10 @@ PREFILL_UNIFORM = PrefillWorkload("causal_prefill_b8_s2048_hq32_hkv8_d128", 4, 8
                                   lengths=(2048,) * 8)
 PREFILL_RAGGED = PrefillWorkload("causal_prefill_ragged_b8_s256to4096_hq32_hkv8_d128", 4, 8, 32, 8,
                                  128, length_range=(256, 4096), sub=1)
+# chunked prefill of long chunks: the Llama-3-8B layer over 16 caches of 4096 rows whose last
+# 512 rows are the new tokens (start_pos = 3584)
+LLAMA3_8B_CHUNK512 = DecodeWorkload("llama3_8b_chunked_prefill_b16_s4096_chunk512_hq32_hkv8_d128", 7, 16, 32, 8,
+                                    128, 4096, "bf16", lengths=(4096,) * 16)
 
 
 def draw_lengths(n, lengths, length_range, seed):
