@@ -783,6 +783,74 @@ class ChunkedPrefill(Prefill):
                 "causal_flops": self.flops_per_step, "l2": self.l2_note}
 
 
+class MlaChunkedPrefill(ChunkedPrefill):
+    """MLA chunked prefill of long chunks (W_UK absorbed) over existing latent caches: each
+    sequence's last n_new latent rows belong to its new tokens. Algorithmic flops per (new
+    row, visible latent row, head): 2·(r + dr) for the score and 2·r for P·c."""
+    call_name = "attn_prefill_mla_chunked (tcgen05 prefill kernel, MLA form: latent tiles as keys and values)"
+
+    def _make(self, seed):
+        w, B, n = self.w, self.w.batch, self.n_new
+        s = W.mla_inputs(w, self.device, seed=seed)
+        for k in ("q_nope", "q_rope", "w_uk", "w_uv"):
+            del s[k]
+        g = torch.Generator(device=self.device).manual_seed(seed + 800)
+        s["q_lat_chunk"] = torch.randn((B * n, w.n_q_heads, w.kv_lora_rank), generator=g,
+                                       device=self.device).to(torch.bfloat16)
+        s["q_rope_chunk"] = torch.randn((B * n, w.n_q_heads, w.rope_dim), generator=g,
+                                        device=self.device).to(torch.bfloat16)
+        s["cu_q"] = torch.arange(0, B * n + 1, n, dtype=torch.int32, device=self.device)
+        s["start_pos"] = (s["seq_lens"] - n).contiguous()
+        return s
+
+    def __init__(self, w, device, rank, l2_bytes):
+        import mla_kv_cache_flash_b300 as mk
+        self.mk, self.w, self.device, self.name = mk, w, device, w.name
+        first = self._make(w.seed + 1000 * rank)
+        B, n, r = w.batch, self.n_new, w.kv_lora_rank
+        self.start = [int(x) for x in first["start_pos"].cpu()]
+        self.lens = np.full(B, n)
+        self.flops_per_step = sum(self._seq_flops(b) for b in range(B))
+        io = sum(first[k].nbytes for k in ("q_lat_chunk", "q_rope_chunk", "c_cache", "kr_cache")) + B * n * w.n_q_heads * r * 4
+        n_sets = max(1, math.ceil(4 * l2_bytes / io))
+        self.sets = [first] + [self._make(w.seed + 1000 * rank) for _ in range(n_sets - 1)]
+        self.out = torch.empty((B * n, w.n_q_heads, r), dtype=torch.float32, device=device)
+        if int(mk.lib().attn_prefill_mla_chunked_workspace_size(B, B * n, w.n_q_heads, w.s_max, 0)) != 0:
+            raise RuntimeError("long chunks are expected on the prefill kernel (no workspace)")
+        self.launches_per_step = 1
+        self.bytes_per_step = io
+        self.l2_note = f"rotating {n_sets} input sets ({n_sets * io / 1e6:.0f} MB, L2 {l2_bytes / 1e6:.0f} MB)"
+
+    def _seq_flops(self, b):
+        w, n, kv0 = self.w, self.n_new, self.start[b]
+        return (2 * (w.kv_lora_rank + w.rope_dim) + 2 * w.kv_lora_rank) * w.n_q_heads * (n * kv0 + n * (n + 1) // 2)
+
+    def _run(self, s):
+        self.mk.prefill_mla_chunked(s["q_lat_chunk"], s["q_rope_chunk"], s["c_cache"], s["kr_cache"], s["cu_q"],
+                                    s["start_pos"], self.w.s_max, self.w.scale, out_lat=self.out)
+
+    def host_inputs(self):
+        s = self.sets[0]
+        return {k: s[k].cpu().pin_memory() for k in ("q_lat_chunk", "q_rope_chunk", "c_cache", "kr_cache", "cu_q",
+                                                     "start_pos")}
+
+    oracle_kind = "mla_chunk"
+
+    def oracle_payload(self):
+        """The first sequence of the batch: its chunk and its latent caches, one unit."""
+        s, n = self.sets[0], self.n_new
+        arrays = {"q_lat": _f32(s["q_lat_chunk"][:n]), "q_rope": _f32(s["q_rope_chunk"][:n]),
+                  "c": _f32(s["c_cache"][:1]), "kr": _f32(s["kr_cache"][:1]),
+                  "cu_q": np.array([0, n], dtype=np.int64), "start_pos": _host(s["start_pos"][:1])}
+        return arrays, [(0,)], 1
+
+    def describe(self):
+        w = self.w
+        return {"workload": w.name, "B": w.batch, "Hq": w.n_q_heads, "r": w.kv_lora_rank, "dr": w.rope_dim,
+                "S_max": w.s_max, "start_pos": self.start[0], "new_tokens_per_sequence": self.n_new,
+                "causal_flops": self.flops_per_step, "l2": self.l2_note}
+
+
 WORKLOADS = {
     "minimind_gqa": lambda: (DecodeGqa, W.MINIMIND_GQA),
     "llama_hkv32": lambda: (DecodeGqa, W.LLAMA3_8B[32]),
@@ -797,10 +865,11 @@ WORKLOADS = {
     "prefill": lambda: (Prefill, W.PREFILL_UNIFORM),
     "prefill_ragged": lambda: (Prefill, W.PREFILL_RAGGED),
     "prefill_chunk512": lambda: (ChunkedPrefill, W.LLAMA3_8B_CHUNK512),
+    "mla_prefill_chunk512": lambda: (MlaChunkedPrefill, W.MINIMIND_MLA_CHUNK512),
 }
 # the largest decode and prefill configurations come last, so a log's tail keeps them
 ALSO = ("minimind_gqa", "minimind_gqa_step", "minimind_gqa_fp8", "minimind_gqa_chunk4", "mla_chunk4", "mla_step",
-        "prefill_chunk512", "llama_hkv32", "llama_hkv1", "mla", "prefill", "prefill_ragged")
+        "prefill_chunk512", "mla_prefill_chunk512", "llama_hkv32", "llama_hkv1", "mla", "prefill", "prefill_ragged")
 
 
 # ============================================================================ timing

@@ -339,10 +339,15 @@ int attn_prefill_gqa_chunked(const void *q, const void *k_cache, const void *v_c
  *               size from attn_prefill_mla_chunked_workspace_size).
  *   out_lat     [T, Hq, r] fp32, every row written (apply W_UV with attn_mla_apply_uv).
  *   r = 128, dr = 48; 1 <= Hq <= 128; 0 <= T <= 65535.
- * Kernels: Hq a multiple of 16 runs on the tcgen05 MLA decode kernel, 4 new tokens × 16
- * heads per thread block reading each latent row once (n_split > 0 caps the blocks at n_split
- * per segment); other head counts on the CUDA-core kernel (each new token a decode over its
- * visible latent rows), then the K2 merge.
+ * Kernels, chosen from the host arguments alone: T >= 128·B (chunks of 128 new tokens or more
+ * on average, a whole prompt with start_pos = 0 included) runs on the tcgen05 prefill kernel
+ * of attn_prefill_gqa_causal in its MLA form (128 new tokens × one head per MMA tile, each
+ * latent tile both keys, with its rope part, and values; no split, no workspace, n_split
+ * ignored; latent and rope rows past start_pos[b] + n_b may hold anything). Otherwise Hq a
+ * multiple of 16 runs on the tcgen05 MLA decode kernel, 4 new tokens × 16 heads per thread
+ * block reading each latent row once (n_split > 0 caps the blocks at n_split per segment);
+ * other head counts on the CUDA-core kernel (each new token a decode over its visible latent
+ * rows), then the K2 merge.
  * ------------------------------------------------------------------------------------- */
 size_t attn_prefill_mla_chunked_workspace_size(int B, int T, int Hq, int max_kv, int n_split);
 

@@ -454,6 +454,7 @@ MLAKV_API size_t attn_prefill_mla_chunked_workspace_size(int B, int T, int Hq, i
     if (check_chunked(B, T, Hq, 1, 128, max_kv > 0 ? max_kv : 1, max_kv, ATTN_BF16, n_split,
                       "attn_prefill_mla_chunked_workspace_size") != ATTN_OK || T == 0)
         return 0;
+    if (chunk_on_prefill(B, T, kMlaRank, ATTN_BF16)) return 0;
     if (chunk_on_tc_mla(B, Hq)) return decode_tc_mla_chunk_workspace(B, T, Hq, n_split);
     return partials_bytes(T, Hq, kMlaRank, chunked_plan(T, Hq, 1, kMlaRank, max_kv, n_split).n_split);
 }
@@ -475,6 +476,19 @@ MLAKV_API int attn_prefill_mla_chunked(const void *q_lat, const void *q_rope, co
         !aligned16(cu_q) || !aligned16(start_pos) || !aligned16(out_lat))
         return fail(ATTN_ERR_UNSUPPORTED, "%s: every pointer must be 16-byte aligned", who);
     if (T == 0 || max_kv == 0) return ok();
+    if (chunk_on_prefill(B, T, kMlaRank, ATTN_BF16)) {
+        // long chunks: the tcgen05 prefill kernel in its MLA form
+        PrefillArgs a{};
+        a.q = q_lat; a.q_rope = q_rope; a.k = c_cache; a.v = krope_cache; a.cu_seqlens = cu_q; a.out = out_lat;
+        a.B = B; a.Hq = Hq; a.Hkv = 1; a.D = kMlaRank; a.T = T;
+        a.scale_log2 = scale * kLog2e;
+        a.max_seqlen = T < max_kv ? T : max_kv;
+        a.out32 = (reinterpret_cast<uintptr_t>(out_lat) & 31u) == 0;
+        a.start_pos = start_pos; a.S_max = S_max;
+        const cudaError_t e = launch_prefill(a, reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "attn_prefill_mla_chunked: kernel launch");
+        return ok();
+    }
     if (chunk_on_tc_mla(B, Hq)) {
         const size_t need = decode_tc_mla_chunk_workspace(B, T, Hq, n_split);
         if (!workspace || ws_bytes < need || !aligned16(workspace))

@@ -81,6 +81,10 @@ struct PrefillArgs {
     // rows 0 .. start_pos[b] + i. nullptr: k and v are packed like q, positions from 0.
     const int *start_pos;
     int S_max;
+    // MLA form (with start_pos; Hkv = 1, D = r = 128): q is q_lat [T, Hq, 128], q_rope
+    // [T, Hq, 48], k the latent cache c [B, S_max, 128] (keys and values), v the rope keys
+    // kr [B, S_max, 48]; s = q_lat·c + q_rope·kr. nullptr: the GQA forms.
+    const void *q_rope;
 };
 
 // ------------------------------------------------------------------ launchers (one per TU)

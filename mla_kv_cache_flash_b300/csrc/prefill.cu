@@ -73,15 +73,31 @@ constexpr int TILE_BYTES = BM * HD * 2;      // one 128 × 128 bf16 tile: 32 KB
 constexpr int BOX_BYTES = TILE_BYTES / 2;    // one TMA box: 128 rows × 64 columns (128 B)
 constexpr int Q_SLOTS = 2;                   // Q tiles rotate through two slots
 constexpr int OST_BYTES = BM * 32 * 4;       // output staging: 128 rows × 32 fp32 columns, per query tile
-constexpr int Q_OFF = 0;
-constexpr int K_OFF = Q_OFF + Q_SLOTS * TILE_BYTES;
-constexpr int V_OFF = K_OFF + NSTAGE * TILE_BYTES;
-constexpr int OST_OFF = V_OFF + NSTAGE * TILE_BYTES;
-constexpr int BAR_OFF = OST_OFF + 2 * OST_BYTES;
+constexpr int RT_BYTES = 3 * BM * 32;        // MLA rope part of a tile: three 16-column boxes (32-byte swizzle)
+constexpr int RBOX_BYTES = BM * 32;
 constexpr int N_BARS = 24;
-constexpr int SLOT_OFF = BAR_OFF + N_BARS * 8;
-constexpr int SMEM = SLOT_OFF + 16 + 1024;   // + alignment slack
-static_assert(SMEM <= 227 * 1024, "shared memory budget");
+
+// The kernel's three forms: packed K/V (causal prefill), K/V caches (chunked prefill), and
+// the MLA latent caches (chunked MLA prefill, W_UK absorbed).
+enum Form : int { kPacked = 0, kCache = 1, kMla = 2 };
+
+// Shared memory: Q slots, (MLA) q_rope slots, the K stages (MLA: the latent rows c, which
+// are also V), the V stages (MLA: the rope keys kr), two output staging buffers, barriers.
+template <int FORM>
+struct Lay {
+    static constexpr bool MLA = FORM == kMla;
+    static constexpr int Q_OFF = 0;
+    static constexpr int QR_OFF = Q_OFF + Q_SLOTS * TILE_BYTES;
+    static constexpr int K_OFF = QR_OFF + (MLA ? Q_SLOTS * RT_BYTES : 0);
+    static constexpr int V_OFF = K_OFF + NSTAGE * TILE_BYTES;
+    static constexpr int OST_OFF = V_OFF + NSTAGE * (MLA ? RT_BYTES : TILE_BYTES);
+    static constexpr int BAR_OFF = OST_OFF + 2 * OST_BYTES;
+    static constexpr int SLOT_OFF = BAR_OFF + N_BARS * 8;
+    static constexpr int SMEM = SLOT_OFF + 16 + 1024;   // + alignment slack
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static_assert(K_OFF % 1024 == 0 && OST_OFF % 1024 == 0 && QR_OFF % 256 == 0 && V_OFF % 256 == 0,
+                  "128-byte swizzled tiles on 1024 bytes, 32-byte swizzled boxes on 256");
+};
 
 constexpr int kWarps = 10;
 constexpr int kThreads = kWarps * 32;
@@ -289,11 +305,21 @@ __device__ __forceinline__ void zero_v_rows(uint8_t *tile, int z0, int lane) {
     __syncwarp();
 }
 
-template <bool CACHE>
+// qmap: Q (MLA: q_lat); qrmap: MLA q_rope (the other forms do not read it); kmap: K (MLA: the
+// latent cache c); vmap: V (MLA: the rope cache kr); omap: the fp32 output.
+template <int FORM>
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-               const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap, const PrefillArgs a,
-               int n_qt, int heads_per_cta) {
+prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap qrmap,
+               const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+               const __grid_constant__ CUtensorMap omap, const PrefillArgs a, int n_qt, int heads_per_cta) {
+    constexpr bool CACHE = FORM != kPacked;
+    constexpr bool MLA = FORM == kMla;
+    using L = Lay<FORM>;
+    constexpr int Q_OFF = L::Q_OFF, QR_OFF = L::QR_OFF, K_OFF = L::K_OFF, V_OFF = L::V_OFF, OST_OFF = L::OST_OFF;
+    constexpr int BAR_OFF = L::BAR_OFF, SLOT_OFF = L::SLOT_OFF;
+    // bytes one Q slot and one K/V stage receive
+    constexpr uint32_t Q_TX = TILE_BYTES + (MLA ? RT_BYTES : 0);
+    constexpr uint32_t KV_TX = TILE_BYTES + (MLA ? RT_BYTES : 0);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
@@ -360,20 +386,40 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(bar(kQFull + q), TILE_BYTES);
+                    mbar_arrive_expect_tx(bar(kQFull + q), Q_TX);
                     for (int bx = 0; bx < 2; ++bx)
                         tma_load_3d(sb + Q_OFF + q * TILE_BYTES + bx * BOX_BYTES, &qmap, bx * 64, it.h0 + t,
                                     sp.seq0 + it.qt * BM, bar(kQFull + q), pol_q);
+                    if (MLA)
+                        for (int bx = 0; bx < 3; ++bx)
+                            tma_load_3d(sb + QR_OFF + q * RT_BYTES + bx * RBOX_BYTES, &qrmap, bx * 16, it.h0 + t,
+                                        sp.seq0 + it.qt * BM, bar(kQFull + q), pol_q);
                 }
                 for (int n = 0; ok && n < sp.nkv; ++n, ++g_kv) {
                     const int s = g_kv % NSTAGE;
                     const uint32_t free_ph = ((g_kv / NSTAGE) & 1) ^ 1;
+                    // the tile's first key: a row of the packed K/V, or a position in the cache
+                    const int k_tok = CACHE ? n * BN : sp.seq0 + n * BN;
+                    if (MLA) {
+                        // c (K and V) and kr share one barrier; the stage is free once both
+                        // P·V MMAs reading it (issued after its S MMAs) are done
+                        if (!mbar_wait_bounded(bar(kVEmpty + s), free_ph, &g_prefill_status, kStatusEmptyWait)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(bar(kKFull + s), KV_TX);
+                        for (int bx = 0; bx < 2; ++bx)
+                            tma_load_3d_nohint(sb + K_OFF + s * TILE_BYTES + bx * BOX_BYTES, &kmap, bx * 64, k_tok, it.b,
+                                               bar(kKFull + s));
+                        for (int bx = 0; bx < 3; ++bx)
+                            tma_load_3d_nohint(sb + V_OFF + s * RT_BYTES + bx * RBOX_BYTES, &vmap, bx * 16, k_tok, it.b,
+                                               bar(kKFull + s));
+                        continue;
+                    }
                     if (!mbar_wait_bounded(bar(kKEmpty + s), free_ph, &g_prefill_status, kStatusEmptyWait)) {
                         ok = false;
                         break;
                     }
-                    // the tile's first key: a row of the packed K/V, or a position in the cache
-                    const int k_tok = CACHE ? n * BN : sp.seq0 + n * BN;
                     mbar_arrive_expect_tx(bar(kKFull + s), TILE_BYTES);
                     for (int bx = 0; bx < 2; ++bx) {
                         if (CACHE)
@@ -403,7 +449,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 mbar_wait_bounded(bar(kQFull + i % Q_SLOTS), (i / Q_SLOTS) & 1, &g_prefill_status, kStatusDrainWait);
             for (int g = g_kv > NSTAGE ? g_kv - NSTAGE : 0; g < g_kv; ++g) {
                 mbar_wait_bounded(bar(kKFull + g % NSTAGE), (g / NSTAGE) & 1, &g_prefill_status, kStatusDrainWait);
-                mbar_wait_bounded(bar(kVFull + g % NSTAGE), (g / NSTAGE) & 1, &g_prefill_status, kStatusDrainWait);
+                if (!MLA)
+                    mbar_wait_bounded(bar(kVFull + g % NSTAGE), (g / NSTAGE) & 1, &g_prefill_status, kStatusDrainWait);
             }
         }
     } else if (warp == 1) {
@@ -422,9 +469,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // the completion cost an mbarrier round trip, 550-800 cycles, twice per iteration,
         // with the tensor pipe idle). The commit after S_t(g) still tracks every earlier MMA,
         // so "S_t(g) full" also means P·V_t(g−1) is done when the softmax rescales O_t.
+        //
+        // MLA: S adds q_rope · krᵀ (three K = 16 steps over the 32-byte swizzled boxes) to
+        // q_lat · cᵀ, and P·V reads its B operand from the c stage.
         const uint64_t q_desc = sdesc_sw128(sb + Q_OFF, 16, 1024);
         const uint64_t k_desc = sdesc_sw128(sb + K_OFF, 16, 1024);
-        const uint64_t v_desc = sdesc_sw128(sb + V_OFF, BOX_BYTES, 1024);
+        const uint64_t v_desc = sdesc_sw128(sb + (MLA ? K_OFF : V_OFF), BOX_BYTES, 1024);
+        const uint64_t qr_desc = sdesc(sb + QR_OFF, 16, 256, kSw32);
+        const uint64_t kr_desc = sdesc(sb + V_OFF, 16, 256, kSw32);
         auto wait_all = [&](int idx, uint32_t parity, unsigned code) {
             const bool got = mbar_wait_bounded(bar(idx), parity, &g_prefill_status, code);
             return __all_sync(0xffffffffu, got);
@@ -437,6 +489,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t off = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
                     umma_ss(tmem + 256 * t, qd + off, kd + off, kIdescS, kk > 0);
+                }
+                if (MLA) {
+                    const uint64_t qrd = qr_desc + (uint64_t)((qslot * RT_BYTES) >> 4);
+                    const uint64_t krd = kr_desc + (uint64_t)((s * RT_BYTES) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < 3; ++kk)
+                        umma_ss(tmem + 256 * t, qrd + ((kk * RBOX_BYTES) >> 4), krd + ((kk * RBOX_BYTES) >> 4), kIdescS,
+                                1u);
                 }
                 umma_commit(bar(kSFull + t));
             }
@@ -495,21 +555,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 if (n == 0 && !(ok = flush_pv1())) break;
                 if (!(ok = wait_all(kKFull + s, ph, kStatusFullWait))) break;
                 if (n == 0 && !(ok = wait_all(kQFull + q0, u0 & 1, kStatusFullWait))) break;
+                if (MLA && n == sp.nkv - 1) {
+                    // latent rows past the chunk's end (first at z0 >= 1 of this tile) hold
+                    // anything; as values their weights are 0, so they must be finite
+                    const int z0 = sp.kv0 + sp.S - n * BN;
+                    if (z0 < BN) zero_v_rows(smem + K_OFF + s * TILE_BYTES, z0, lane);
+                }
                 tc_fence_after();
                 issue_s(0, q0, s);
                 if (n == sp.nkv - 1) commit(kQEmpty + q0);
-                if (n_mt == 1) commit(kKEmpty + s);
+                if (n_mt == 1 && !MLA) commit(kKEmpty + s);
                 if (n_mt == 2) {
                     if (!(ok = flush_pv1())) break;
                     if (n == 0 && !(ok = wait_all(kQFull + q1, u1 & 1, kStatusFullWait))) break;
                     tc_fence_after();
                     issue_s(1, q1, s);
                     if (n == sp.nkv - 1) commit(kQEmpty + q1);
-                    commit(kKEmpty + s);                 // both S MMAs of this K tile are issued
+                    if (!MLA) commit(kKEmpty + s);       // both S MMAs of this K tile are issued
                 }
-                if (!(ok = wait_all(kVFull + s, ph, kStatusFullWait) && wait_all(kPReady + 0, g & 1, kStatusMmaWait)))
+                if (!(ok = (MLA || wait_all(kVFull + s, ph, kStatusFullWait)) &&
+                           wait_all(kPReady + 0, g & 1, kStatusMmaWait)))
                     break;
-                if (CACHE && n == sp.nkv - 1) {
+                if (CACHE && !MLA && n == sp.nkv - 1) {
                     // cache rows past the chunk's end (first at z0 >= 1 of this tile) hold
                     // anything; their weights are 0, so their values must be finite
                     const int z0 = sp.kv0 + sp.S - n * BN;
@@ -530,7 +597,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (ok) ok = flush_pv1();                   // the last iteration's P·V_1 (iteration g-1)
         // the last commits must have arrived before the block exits
         for (int i = g > NSTAGE ? g - NSTAGE : 0; i < g; ++i) {
-            mbar_wait_bounded(bar(kKEmpty + i % NSTAGE), (i / NSTAGE) & 1, &g_prefill_status, kStatusDrainWait);
+            if (!MLA)
+                mbar_wait_bounded(bar(kKEmpty + i % NSTAGE), (i / NSTAGE) & 1, &g_prefill_status, kStatusDrainWait);
             mbar_wait_bounded(bar(kVEmpty + i % NSTAGE), (i / NSTAGE) & 1, &g_prefill_status, kStatusDrainWait);
         }
         for (int i = qc > Q_SLOTS ? qc - Q_SLOTS : 0; i < qc; ++i)
@@ -691,55 +759,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t st) {
-    if (a.D != HD) return cudaErrorInvalidValue;
-    CUtensorMap qm, km, vm;
-    const uint32_t qbox[3] = {64, 1, BM};
-    const uint32_t kvbox[3] = {64, 1, BN};
-    {
-        const uint64_t dims[3] = {(uint64_t)HD, (uint64_t)a.Hq, (uint64_t)a.T};
-        const uint64_t strides[2] = {(uint64_t)HD * 2, (uint64_t)a.Hq * HD * 2};
-        cudaError_t e = encode_tensor_map(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, dims, strides, qbox,
-                                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+template <int FORM>
+cudaError_t launch_form(const PrefillArgs &a, cudaStream_t st, const CUtensorMap &qm, const CUtensorMap &qrm,
+                        const CUtensorMap &km, const CUtensorMap &vm, const CUtensorMap &om) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(prefill_kernel<FORM>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<FORM>::SMEM);
         if (e != cudaSuccess) return e;
-    }
-    const bool cache = a.start_pos != nullptr;
-    if (cache) {
-        // the caches [B, S_max, Hkv, D]: coordinates (column, KV head, position, sequence)
-        const uint64_t dims[4] = {(uint64_t)HD, (uint64_t)a.Hkv, (uint64_t)a.S_max, (uint64_t)a.B};
-        const uint64_t strides[3] = {(uint64_t)HD * 2, (uint64_t)a.Hkv * HD * 2, (uint64_t)a.S_max * a.Hkv * HD * 2};
-        const uint32_t box4[4] = {64, 1, BN, 1};
-        cudaError_t e = encode_tensor_map(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.k, dims, strides, box4,
-                                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-        if (e == cudaSuccess)
-            e = encode_tensor_map(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.v, dims, strides, box4,
-                                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-        if (e != cudaSuccess) return e;
-    } else {
-        const uint64_t dims[3] = {(uint64_t)HD, (uint64_t)a.Hkv, (uint64_t)a.T};
-        const uint64_t strides[2] = {(uint64_t)HD * 2, (uint64_t)a.Hkv * HD * 2};
-        cudaError_t e = encode_tensor_map(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.k, dims, strides, kvbox,
-                                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-        if (e == cudaSuccess)
-            e = encode_tensor_map(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.v, dims, strides, kvbox,
-                                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-        if (e != cudaSuccess) return e;
-    }
-    CUtensorMap om;
-    {
-        const uint64_t dims[3] = {(uint64_t)HD, (uint64_t)a.Hq, (uint64_t)a.T};
-        const uint64_t strides[2] = {(uint64_t)HD * 4, (uint64_t)a.Hq * HD * 4};
-        const uint32_t obox[3] = {32, 1, BM};
-        cudaError_t e = encode_tensor_map(&om, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.out, dims, strides, obox,
-                                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
-        if (e != cudaSuccess) return e;
-    }
-    static bool attr_set[2] = {false, false};
-    if (!attr_set[cache]) {
-        const cudaError_t e = cache ? cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM)
-                                    : cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-        if (e != cudaSuccess) return e;
-        attr_set[cache] = true;
+        attr_set = true;
     }
     const int G = a.Hq / a.Hkv;
     const int heads_per_cta = (G % 2 == 0) ? 2 : 1;
@@ -751,11 +779,71 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t st) {
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return cudaErrorInvalidDevice;
     const int grid = (int)(n_items < sms ? n_items : sms);
-    const cudaError_t e = cache ? launch_pdl(prefill_kernel<true>, dim3(grid), dim3(kThreads), SMEM, st, qm, km, vm, om,
-                                             a, n_qt, heads_per_cta)
-                                : launch_pdl(prefill_kernel<false>, dim3(grid), dim3(kThreads), SMEM, st, qm, km, vm,
-                                             om, a, n_qt, heads_per_cta);
+    const cudaError_t e = launch_pdl(prefill_kernel<FORM>, dim3(grid), dim3(kThreads), Lay<FORM>::SMEM, st, qm, qrm, km,
+                                     vm, om, a, n_qt, heads_per_cta);
     return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t st) {
+    if (a.D != HD) return cudaErrorInvalidValue;
+    const bool mla = a.q_rope != nullptr, cache = a.start_pos != nullptr;
+    if (mla && (!cache || a.Hkv != 1)) return cudaErrorInvalidValue;
+    constexpr auto SW128 = CU_TENSOR_MAP_SWIZZLE_128B, SW32 = CU_TENSOR_MAP_SWIZZLE_32B;
+    constexpr auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    constexpr auto L2_256 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+    CUtensorMap qm, qrm, km, vm, om;
+    const uint32_t box128[3] = {64, 1, BM};              // 64 columns of one head, 128 rows
+    cudaError_t e;
+    {
+        const uint64_t dims[3] = {(uint64_t)HD, (uint64_t)a.Hq, (uint64_t)a.T};
+        const uint64_t strides[2] = {(uint64_t)HD * 2, (uint64_t)a.Hq * HD * 2};
+        e = encode_tensor_map(&qm, BF16, 3, a.q, dims, strides, box128, SW128, L2_256);
+        if (e != cudaSuccess) return e;
+    }
+    if (mla) {
+        // q_rope [T, Hq, 48] and kr [B, S_max, 48] in 16-column boxes (32-byte swizzle); the
+        // latent cache c [B, S_max, 128] in 64-column boxes: coordinates (column, position, sequence)
+        const uint64_t qr_dims[3] = {48, (uint64_t)a.Hq, (uint64_t)a.T};
+        const uint64_t qr_strides[2] = {96, (uint64_t)a.Hq * 96};
+        const uint32_t qr_box[3] = {16, 1, BM};
+        e = encode_tensor_map(&qrm, BF16, 3, a.q_rope, qr_dims, qr_strides, qr_box, SW32, L2_256);
+        if (e != cudaSuccess) return e;
+        const uint64_t c_dims[3] = {(uint64_t)HD, (uint64_t)a.S_max, (uint64_t)a.B};
+        const uint64_t c_strides[2] = {(uint64_t)HD * 2, (uint64_t)a.S_max * HD * 2};
+        const uint32_t c_box[3] = {64, BN, 1};
+        e = encode_tensor_map(&km, BF16, 3, a.k, c_dims, c_strides, c_box, SW128, L2_256);
+        if (e != cudaSuccess) return e;
+        const uint64_t r_dims[3] = {48, (uint64_t)a.S_max, (uint64_t)a.B};
+        const uint64_t r_strides[2] = {96, (uint64_t)a.S_max * 96};
+        const uint32_t r_box[3] = {16, BN, 1};
+        e = encode_tensor_map(&vm, BF16, 3, a.v, r_dims, r_strides, r_box, SW32, L2_256);
+        if (e != cudaSuccess) return e;
+    } else if (cache) {
+        // the caches [B, S_max, Hkv, D]: coordinates (column, KV head, position, sequence)
+        const uint64_t dims[4] = {(uint64_t)HD, (uint64_t)a.Hkv, (uint64_t)a.S_max, (uint64_t)a.B};
+        const uint64_t strides[3] = {(uint64_t)HD * 2, (uint64_t)a.Hkv * HD * 2, (uint64_t)a.S_max * a.Hkv * HD * 2};
+        const uint32_t box4[4] = {64, 1, BN, 1};
+        e = encode_tensor_map(&km, BF16, 4, a.k, dims, strides, box4, SW128, L2_256);
+        if (e == cudaSuccess) e = encode_tensor_map(&vm, BF16, 4, a.v, dims, strides, box4, SW128, L2_256);
+        if (e != cudaSuccess) return e;
+    } else {
+        const uint64_t dims[3] = {(uint64_t)HD, (uint64_t)a.Hkv, (uint64_t)a.T};
+        const uint64_t strides[2] = {(uint64_t)HD * 2, (uint64_t)a.Hkv * HD * 2};
+        e = encode_tensor_map(&km, BF16, 3, a.k, dims, strides, box128, SW128, L2_256);
+        if (e == cudaSuccess) e = encode_tensor_map(&vm, BF16, 3, a.v, dims, strides, box128, SW128, L2_256);
+        if (e != cudaSuccess) return e;
+    }
+    {
+        const uint64_t dims[3] = {(uint64_t)HD, (uint64_t)a.Hq, (uint64_t)a.T};
+        const uint64_t strides[2] = {(uint64_t)HD * 4, (uint64_t)a.Hq * HD * 4};
+        const uint32_t obox[3] = {32, 1, BM};
+        e = encode_tensor_map(&om, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.out, dims, strides, obox, SW128,
+                              CU_TENSOR_MAP_L2_PROMOTION_NONE);
+        if (e != cudaSuccess) return e;
+    }
+    if (mla) return launch_form<kMla>(a, st, qm, qrm, km, vm, om);
+    if (cache) return launch_form<kCache>(a, st, qm, qm, km, vm, om);
+    return launch_form<kPacked>(a, st, qm, qm, km, vm, om);
 }
 
 int prefill_read_and_clear_status(cudaStream_t s, unsigned *flag) {

@@ -231,6 +231,14 @@ def test_chunked_long_chunks_need_no_workspace(L):
     assert L.attn_prefill_gqa_chunked_workspace_size(2, 256, 32, 8, 96, 4096, 1, 0) > 0
 
 
+def test_mla_chunked_long_chunks_need_no_workspace(L):
+    # chunks of 128 new tokens or more on average: the prefill kernel's MLA form, no workspace
+    for hq in (16, 8, 3):
+        for n_split in (0, 2):
+            assert L.attn_prefill_mla_chunked_workspace_size(4, 512, hq, 4096, n_split) == 0
+    assert L.attn_prefill_mla_chunked_workspace_size(4, 511, 16, 4096, 0) > 0
+
+
 def mla_chunked(L, ql=P, qr=P, c=P, kr=P, cu=P, st=P, out=P, B=2, T=10, Hq=16, r=128, dr=48, scale=1 / 12,
                 S_max=64, max_kv=64, n_split=1, ws=N0, ws_bytes=0):
     return L.attn_prefill_mla_chunked(ql, qr, c, kr, cu, st, out, B, T, Hq, r, dr, scale, S_max, max_kv, n_split,

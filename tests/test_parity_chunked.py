@@ -216,9 +216,10 @@ def test_mla_chunked_single_tokens_are_decode_steps():
 
 
 def test_mla_chunked_ragged_and_long():
-    # the tcgen05 form's edge cases: chunks of 1 .. 9 tokens (not multiples of 4), an empty
-    # chunk, a 512-token chunk and one ending at S_max, with the split plan forced several ways
-    chunks = ((0, 1), (3, 2), (10, 3), (0, 0), (77, 5), (1200, 9), (0, 512), (1528, 512))
+    # the tcgen05 decode form's edge cases: chunks of 1 .. 9 tokens (not multiples of 4), empty
+    # chunks, a 512-token chunk and one ending at S_max, with the split plan forced several
+    # ways (nine sequences keep the average chunk under 128 tokens, off the prefill kernel)
+    chunks = ((0, 1), (3, 2), (10, 3), (0, 0), (77, 5), (1200, 9), (0, 512), (1528, 512), (0, 0))
     q_lat, q_rope, c, kr, cu, start, scale = _mla_case(chunks, 16, 2040, 41)
     ref = oracle.mla_prefill_absorbed(to_f64(q_lat), to_f64(q_rope), to_f64(c), to_f64(kr), cu, start, scale)
     max_kv = int((start + np.diff(cu)).max())
@@ -227,6 +228,36 @@ def test_mla_chunked_ragged_and_long():
                                      torch.from_numpy(start).to(DEV), max_kv, scale, n_split=n_split)
         torch.cuda.synchronize()
         assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3, n_split
+
+
+@pytest.mark.parametrize("hq", [16, 8, 3, 32])
+def test_mla_chunked_long_chunks_on_the_prefill_kernel(hq):
+    # chunks averaging 128 tokens or more: the tcgen05 prefill kernel's MLA form, each latent
+    # tile serving as keys (with its rope part) and as values; every latent and rope row past
+    # a chunk is NaN. 3 heads: one head per item.
+    q_lat, q_rope, c, kr, cu, start, scale = _mla_case(_LONG, hq, 4096, 120 + hq)
+    c, kr = _poison_past_chunks(c, start, cu), _poison_past_chunks(kr, start, cu)
+    T, B = int(cu[-1]), len(_LONG)
+    assert mk.lib().attn_prefill_mla_chunked_workspace_size(B, T, hq, 3200, 0) == 0
+    ref = oracle.mla_prefill_absorbed(to_f64(q_lat), to_f64(q_rope), to_f64(c), to_f64(kr), cu, start, scale)
+    out = mk.prefill_mla_chunked(q_lat, q_rope, c, kr, torch.from_numpy(cu).to(DEV), torch.from_numpy(start).to(DEV),
+                                 3200, scale)
+    torch.cuda.synchronize()
+    mk.check_status()
+    assert bool(torch.isfinite(out).all())
+    assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3
+
+
+def test_mla_prefill_from_an_empty_cache():
+    """MLA prefill of whole prompts (start_pos = 0): row i sees latent rows 0 .. i."""
+    chunks = ((0, 1000), (0, 129), (0, 384), (0, 1))
+    q_lat, q_rope, c, kr, cu, start, scale = _mla_case(chunks, 16, 1024, 55)
+    ref = oracle.mla_prefill_absorbed(to_f64(q_lat), to_f64(q_rope), to_f64(c), to_f64(kr), cu, start, scale)
+    out = mk.prefill_mla_chunked(q_lat, q_rope, c, kr, torch.from_numpy(cu).to(DEV), torch.from_numpy(start).to(DEV),
+                                 1000, scale)
+    torch.cuda.synchronize()
+    mk.check_status()
+    assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3
 
 
 def test_mla_chunked_four_new_tokens_bench_size():

@@ -121,6 +121,9 @@ PREFILL_RAGGED = PrefillWorkload("causal_prefill_ragged_b8_s256to4096_hq32_hkv8_
 # 512 rows are the new tokens (start_pos = 3584)
 LLAMA3_8B_CHUNK512 = DecodeWorkload("llama3_8b_chunked_prefill_b16_s4096_chunk512_hq32_hkv8_d128", 7, 16, 32, 8,
                                     128, 4096, "bf16", lengths=(4096,) * 16)
+# and the MiniMind MLA layer (W_UK absorbed) over 32 latent caches of 4096 rows, the last 512 new
+MINIMIND_MLA_CHUNK512 = MlaWorkload("minimind_mla_chunked_prefill_b32_s4096_chunk512_hq16_r128_dr48", 8, 32, 16,
+                                    96, 128, 48, 96, 4096, lengths=(4096,) * 32)
 
 
 def draw_lengths(n, lengths, length_range, seed):
