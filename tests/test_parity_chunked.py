@@ -277,3 +277,63 @@ def test_mla_chunked_four_new_tokens_bench_size():
     ref = oracle.mla_prefill_absorbed(to_f64(q_lat), to_f64(q_rope), to_f64(inp["c_cache"]),
                                       to_f64(inp["kr_cache"]), cu.cpu().numpy(), start.cpu().numpy(), w.scale)
     assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3
+
+
+# ------------------------------------------------------------- the 512-token chunk lines
+
+def _sampled_chunk_check(out, q_rows, refs):
+    """refs: {b: (lo, hi, oracle rows)}; compares every row and head of the sampled sequences."""
+    for b, (lo, hi, ref) in refs.items():
+        err = float(np.abs(to_f64(out[lo:hi]) - ref).max())
+        assert err <= 3e-3, (b, err)
+
+
+def test_chunked_prefill_512_at_the_bench_size():
+    """The bench's GQA long-chunk line (Llama-3-8B layer, 16 caches of 4096 rows, the last 512
+    of each the new tokens) in the one launch bench.py times; sequences 0, 7 and 15 against the
+    oracle, every row and head."""
+    w = W.LLAMA3_8B_CHUNK512
+    inp = W.decode_inputs(w, DEV)
+    B, n = w.batch, 512
+    g = torch.Generator(device=DEV).manual_seed(w.seed + 700)
+    q = torch.randn((B * n, w.n_q_heads, w.head_dim), generator=g, device=DEV).to(torch.bfloat16)
+    cu = torch.arange(0, B * n + 1, n, dtype=torch.int32, device=DEV)
+    start = (inp["seq_lens"] - n).contiguous()
+    assert mk.lib().attn_prefill_gqa_chunked_workspace_size(B, B * n, w.n_q_heads, w.n_kv_heads, w.head_dim,
+                                                            w.s_max, mk.ATTN_BF16, 0) == 0
+    out = mk.prefill_gqa_chunked(q, inp["k_cache"], inp["v_cache"], cu, start, w.s_max, scale=w.scale)
+    torch.cuda.synchronize()
+    mk.check_status()
+    refs = {}
+    st = start.cpu().numpy()
+    for b in (0, 7, 15):
+        lo, hi = b * n, (b + 1) * n
+        refs[b] = (lo, hi, oracle.prefill_gqa_chunked(to_f64(q[lo:hi]), to_f64(inp["k_cache"][b:b + 1]),
+                                                      to_f64(inp["v_cache"][b:b + 1]), np.array([0, n]),
+                                                      st[b:b + 1], w.scale))
+    _sampled_chunk_check(out, q, refs)
+
+
+def test_mla_chunked_prefill_512_at_the_bench_size():
+    """The bench's MLA long-chunk line (MiniMind MLA, 32 latent caches of 4096 rows, the last 512
+    of each the new tokens) in the one launch bench.py times; sequences 0, 13 and 31 against the
+    oracle, every row and head."""
+    w = W.MINIMIND_MLA_CHUNK512
+    inp = W.mla_inputs(w, DEV)
+    B, n = w.batch, 512
+    g = torch.Generator(device=DEV).manual_seed(w.seed + 800)
+    q_lat = torch.randn((B * n, w.n_q_heads, w.kv_lora_rank), generator=g, device=DEV).to(torch.bfloat16)
+    q_rope = torch.randn((B * n, w.n_q_heads, w.rope_dim), generator=g, device=DEV).to(torch.bfloat16)
+    cu = torch.arange(0, B * n + 1, n, dtype=torch.int32, device=DEV)
+    start = (inp["seq_lens"] - n).contiguous()
+    out = mk.prefill_mla_chunked(q_lat, q_rope, inp["c_cache"], inp["kr_cache"], cu, start, w.s_max, w.scale)
+    torch.cuda.synchronize()
+    mk.check_status()
+    refs = {}
+    st = start.cpu().numpy()
+    for b in (0, 13, 31):
+        lo, hi = b * n, (b + 1) * n
+        refs[b] = (lo, hi, oracle.mla_prefill_absorbed(to_f64(q_lat[lo:hi]), to_f64(q_rope[lo:hi]),
+                                                       to_f64(inp["c_cache"][b:b + 1]), to_f64(inp["kr_cache"][b:b + 1]),
+                                                       np.array([0, n]), st[b:b + 1], w.scale))
+    _sampled_chunk_check(out, q_lat, refs)
