@@ -155,71 +155,78 @@ __device__ __forceinline__ float fmin3(float a, float b, float c) {
 }
 
 // The largest (NEG: smallest) visible raw score of one row of the S tile in TMEM, so that the
-// row max of x = s·c is c times it (c = scale·log2 e; NEG when c < 0). DIAG: the diagonal tile,
-// where key i is visible only to rows `row` >= i (key 0 always is, so the result is finite).
-// The row is read in two 64-column halves to keep register use low; eight independent partial
-// extrema keep the dependency chains short.
+// row max of x = s·c is c times it (c = scale·log2 e; NEG when c < 0). DIAG: a masked tile,
+// where key i is visible only if i <= row (key 0 of an item's first tile always is, so the
+// result there is finite). The row is read in 32-column quarters, the next quarter's load in
+// flight while the current one is reduced; eight independent partial extrema keep the
+// dependency chains short.
 template <bool DIAG, bool NEG>
 __device__ __forceinline__ float row_extreme(uint32_t s_addr, int row) {
     constexpr float kNone = NEG ? INFINITY : -INFINITY;
     float e[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) e[i] = kNone;
+    uint32_t ra[32], rb[32];
+    tmem_ld32(s_addr, ra);
+    tmem_ld_wait(ra);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint32_t r[64];
-        tmem_ld64_sync(s_addr + 64 * h, r);
+    for (int q = 0; q < 4; ++q) {
+        uint32_t(&cur)[32] = (q & 1) ? rb : ra;
+        uint32_t(&nxt)[32] = (q & 1) ? ra : rb;
+        if (q < 3) tmem_ld32(s_addr + 32 * (q + 1), nxt);
 #pragma unroll
-        for (int i = 0; i < 64; i += 2) {
-            float v0 = __uint_as_float(r[i]), v1 = __uint_as_float(r[i + 1]);
+        for (int i = 0; i < 32; i += 2) {
+            float v0 = __uint_as_float(cur[i]), v1 = __uint_as_float(cur[i + 1]);
             if (DIAG) {
-                v0 = 64 * h + i <= row ? v0 : kNone;
-                v1 = 64 * h + i + 1 <= row ? v1 : kNone;
+                v0 = 32 * q + i <= row ? v0 : kNone;
+                v1 = 32 * q + i + 1 <= row ? v1 : kNone;
             }
             const int k = (i >> 1) & 7;
             e[k] = NEG ? fmin3(e[k], v0, v1) : fmax3(e[k], v0, v1);
         }
+        if (q < 3) tmem_ld_wait(nxt);
     }
     return NEG ? fminf(fmin3(e[0], e[1], e[2]), fmin3(fmin3(e[3], e[4], e[5]), e[6], e[7]))
                : fmaxf(fmax3(e[0], e[1], e[2]), fmax3(fmax3(e[3], e[4], e[5]), e[6], e[7]));
 }
 
 // P = 2^(s·c − m) for the same row (0 for hidden keys), as bf16 pairs. Keys 32q .. 32q+31
-// (chunk q) own TMEM columns [32q, 32q+32) of the row's S region: P goes to the first 16 of
-// them and, with SPLIT, the bf16 residual p − bf16(p) to the last 16. A chunk's columns are
-// written only after that chunk of S has been read. Adds the unrounded weights to l.
+// (quarter q) own TMEM columns [32q, 32q+32) of the row's S region: P goes to the first 16 of
+// them and, with SPLIT, the bf16 residual p − bf16(p) to the last 16. A quarter's columns are
+// written only after that quarter of S has been read, while the next quarter's load is in
+// flight (it reads other columns). Adds the unrounded weights to l.
 template <bool DIAG, bool SPLIT>
 __device__ __forceinline__ void write_p(uint32_t s_addr, float c, float m, int row, float &l) {
     const uint64_t c2 = f2pack(c, c), nm2 = f2pack(-m, -m);
     uint64_t acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = 0;
+    uint32_t ra[32], rb[32];
+    tmem_ld32(s_addr, ra);
+    tmem_ld_wait(ra);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint32_t r[64];
-        tmem_ld64_sync(s_addr + 64 * h, r);
+    for (int q = 0; q < 4; ++q) {
+        uint32_t(&cur)[32] = (q & 1) ? rb : ra;
+        uint32_t(&nxt)[32] = (q & 1) ? ra : rb;
+        if (q < 3) tmem_ld32(s_addr + 32 * (q + 1), nxt);
+        uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-            const int q = 2 * h + ch;
-            uint32_t hi[16], lo[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int kr = ch * 32 + 2 * i;      // index within the half
-                const int k0 = 64 * h + kr;          // key index within the tile
-                float x0, x1;
-                f2unpack(ffma2(f2pack(__uint_as_float(r[kr]), __uint_as_float(r[kr + 1])), c2, nm2), x0, x1);
-                float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-                if (DIAG) {
-                    p0 = k0 <= row ? p0 : 0.f;
-                    p1 = k0 + 1 <= row ? p1 : 0.f;
-                }
-                acc[i & 3] = fadd2(acc[i & 3], f2pack(p0, p1));
-                hi[i] = pack_bf16x2(p0, p1);
-                if constexpr (SPLIT) lo[i] = pack_bf16x2(p0 - bf16_lo(hi[i]), p1 - bf16_hi(hi[i]));
+        for (int i = 0; i < 16; ++i) {
+            const int k0 = 32 * q + 2 * i;           // key index within the tile
+            float x0, x1;
+            f2unpack(ffma2(f2pack(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), c2, nm2), x0, x1);
+            float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            if (DIAG) {
+                p0 = k0 <= row ? p0 : 0.f;
+                p1 = k0 + 1 <= row ? p1 : 0.f;
             }
-            tmem_st16(s_addr + 32 * q, hi);
-            if constexpr (SPLIT) tmem_st16(s_addr + 32 * q + 16, lo);
+            acc[i & 3] = fadd2(acc[i & 3], f2pack(p0, p1));
+            hi[i] = pack_bf16x2(p0, p1);
+            if constexpr (SPLIT) lo[i] = pack_bf16x2(p0 - bf16_lo(hi[i]), p1 - bf16_hi(hi[i]));
         }
+        tmem_st16(s_addr + 32 * q, hi);
+        if constexpr (SPLIT) tmem_st16(s_addr + 32 * q + 16, lo);
+        if (q < 3) tmem_ld_wait(nxt);
     }
     float a0, a1;
     f2unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), a0, a1);
