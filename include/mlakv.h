@@ -60,7 +60,10 @@ enum {
     ATTN_ERR_UNSUPPORTED = -3, /* head width / rank / dtype / alignment not built in */
     ATTN_ERR_WORKSPACE = -4,   /* workspace NULL or smaller than the *_workspace_size query */
     ATTN_ERR_CUDA = -5,        /* a CUDA call or kernel launch failed (see attn_last_error) */
-    ATTN_ERR_TIMEOUT = -6      /* a kernel's bounded wait gave up (from attn_check_status) */
+    ATTN_ERR_TIMEOUT = -6,     /* a kernel's bounded wait gave up (from attn_check_status) */
+    ATTN_ERR_INPUT = -7        /* a device-side length, offset or start position out of its
+                                  stated bounds (only with the device checks on, see
+                                  attn_set_device_checks) */
 };
 
 /* Element type of q and of the cache for attn_decode_gqa (ATTN_F32, ATTN_BF16) and of the
@@ -378,6 +381,26 @@ const char *attn_last_error(void);
  * the current device. Returns ATTN_OK, ATTN_ERR_TIMEOUT if a kernel gave up a bounded
  * wait since the last check, or ATTN_ERR_CUDA if the stream reported an error. */
 int attn_check_status(mlakv_stream_t stream);
+
+/* Device-side checks of the length arrays (a debugging aid; off by default). The host checks
+ * only the sizes it is given; seq_lens, cu_seqlens, cu_q and start_pos live on the device and
+ * are trusted within their stated bounds (a length above the cache capacity would make a
+ * kernel read past the cache). With the checks on, every entry point that takes such an array
+ * first checks it on its stream with a small kernel, synchronises the stream, and returns
+ * ATTN_ERR_INPUT (attn_last_error names the rule and the first offending index) before
+ * launching anything else:
+ *   attn_decode_gqa, attn_decode_gqa_fp8, attn_decode_mla_absorbed, attn_decode_gqa_noalloc:
+ *       0 <= seq_lens[b] <= max_S;
+ *   attn_prefill_gqa_causal: cu_seqlens[0] = 0, non-decreasing, cu_seqlens[B] <= total_tokens,
+ *       each length <= max_seqlen;
+ *   attn_prefill_gqa_chunked, attn_prefill_mla_chunked: cu_q as cu_seqlens with T, and
+ *       0 <= start_pos[b], start_pos[b] + n_b <= max_kv.
+ * The checks cost a launch and a synchronisation per call and cannot run under stream
+ * capture. Turned on by MLAKV_DEVICE_CHECKS=1 in the environment when first consulted, or by
+ * this call; process-wide, not thread-safe against concurrent calls. Returns the previous
+ * setting (0 or 1). */
+int attn_set_device_checks(int on);
+int attn_device_checks(void);
 
 /* Failure-path self-test (no source page has a counterpart; it exists to test the library).
  * Launches one thread that waits, bounded by `timeout_cycles` SM clock cycles (1e3 .. 1e9),

@@ -25,16 +25,16 @@ __all__ = [
     "decode_gqa_num_splits", "decode_gqa_noalloc", "decode_mla_absorbed", "decode_mla_workspace_size", "decode_mla_num_splits",
     "prefill_gqa_causal", "merge_partials", "check_status", "last_error", "version",
     "selftest_bounded_wait", "mla_absorb_query", "mla_apply_uv", "decode_mla", "kv_append_rope",
-    "mla_append_rope", "prefill_gqa_chunked", "prefill_mla_chunked",
+    "mla_append_rope", "prefill_gqa_chunked", "prefill_mla_chunked", "set_device_checks", "device_checks",
 ]
 
 ATTN_F32 = 0
 ATTN_BF16 = 1
 ATTN_FP8_E4M3 = 2
 ATTN_OK, ATTN_ERR_NULL, ATTN_ERR_SHAPE, ATTN_ERR_UNSUPPORTED = 0, -1, -2, -3
-ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = -4, -5, -6
+ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT, ATTN_ERR_INPUT = -4, -5, -6, -7
 _STATUS = {0: "ATTN_OK", -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_SHAPE", -3: "ATTN_ERR_UNSUPPORTED",
-           -4: "ATTN_ERR_WORKSPACE", -5: "ATTN_ERR_CUDA", -6: "ATTN_ERR_TIMEOUT"}
+           -4: "ATTN_ERR_WORKSPACE", -5: "ATTN_ERR_CUDA", -6: "ATTN_ERR_TIMEOUT", -7: "ATTN_ERR_INPUT"}
 
 lib_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmlakv.so")
 _lib = None
@@ -72,6 +72,8 @@ _SIGNATURES = {
     "attn_check_status": (_c_int, [_vp]),
     "attn_version": (ctypes.c_char_p, []),
     "attn_selftest_bounded_wait": (_c_int, [ctypes.c_longlong, _vp]),
+    "attn_set_device_checks": (_c_int, [_c_int]),
+    "attn_device_checks": (_c_int, []),
 }
 
 
@@ -98,6 +100,16 @@ def last_error():
 
 def version():
     return lib().attn_version().decode()
+
+
+def set_device_checks(on):
+    """Turn the device-side checks of seq_lens / cu_seqlens / cu_q / start_pos on or off (see
+    attn_set_device_checks: a synchronising debugging aid); returns the previous setting."""
+    return bool(lib().attn_set_device_checks(1 if on else 0))
+
+
+def device_checks():
+    return bool(lib().attn_device_checks())
 
 
 def _check(rc):

@@ -187,6 +187,9 @@ MLAKV_API const char *attn_last_error(void) { return g_err; }
 
 MLAKV_API const char *attn_version(void) { return "mlakv 0.1.0 (sm_103a)"; }
 
+MLAKV_API int attn_set_device_checks(int on) { return set_device_checks(on); }
+MLAKV_API int attn_device_checks(void) { return device_checks_on() ? 1 : 0; }
+
 // ======================================================================== GQA decode
 
 namespace {
@@ -255,6 +258,7 @@ MLAKV_API int attn_decode_gqa(const void *q, const void *k_cache, const void *v_
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(seq_lens))
         return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_gqa: every pointer must be 16-byte aligned");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (device_checks_on() && (rc = check_lengths(seq_lens, B, max_S, s, "attn_decode_gqa")) != ATTN_OK) return rc;
     if (!gqa_use_fma(dtype)) {
         // bf16: persistent blocks over an even share of all cached tokens, merged in-kernel
         const bool tc = decode_tc_gqa_eligible(B, Hq, Hkv, D);
@@ -308,6 +312,10 @@ MLAKV_API int attn_decode_gqa_fp8(const void *q, const void *k_cache, const void
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_scale) ||
         !aligned16(v_scale) || !aligned16(out) || !aligned16(seq_lens))
         return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_gqa_fp8: every pointer must be 16-byte aligned");
+    if (device_checks_on() &&
+        (rc = check_lengths(seq_lens, B, max_S, reinterpret_cast<cudaStream_t>(stream), "attn_decode_gqa_fp8")) !=
+            ATTN_OK)
+        return rc;
     if (fp8_on_mma(B, Hq, Hkv, D, ATTN_FP8_E4M3)) {
         const size_t need = decode_fp8_workspace(B, Hq, Hkv, D, n_split);
         if (!workspace || ws_bytes < need || !aligned16(workspace))
@@ -395,6 +403,10 @@ MLAKV_API int attn_prefill_gqa_chunked(const void *q, const void *k_cache, const
         return fail(ATTN_ERR_UNSUPPORTED, "%s: every pointer must be 16-byte aligned", who);
     if (T == 0 || max_kv == 0) return ok();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (device_checks_on()) {
+        const int crc = check_chunks(cu_q, start_pos, B, T, max_kv, s, who);
+        if (crc != ATTN_OK) return crc;
+    }
     if (chunk_on_prefill(B, T, D, dtype)) {
         PrefillArgs a{};
         a.q = q; a.k = k_cache; a.v = v_cache; a.cu_seqlens = cu_q; a.out = out;
@@ -476,6 +488,10 @@ MLAKV_API int attn_prefill_mla_chunked(const void *q_lat, const void *q_rope, co
         !aligned16(cu_q) || !aligned16(start_pos) || !aligned16(out_lat))
         return fail(ATTN_ERR_UNSUPPORTED, "%s: every pointer must be 16-byte aligned", who);
     if (T == 0 || max_kv == 0) return ok();
+    if (device_checks_on()) {
+        const int crc = check_chunks(cu_q, start_pos, B, T, max_kv, reinterpret_cast<cudaStream_t>(stream), who);
+        if (crc != ATTN_OK) return crc;
+    }
     if (chunk_on_prefill(B, T, kMlaRank, ATTN_BF16)) {
         // long chunks: the tcgen05 prefill kernel in its MLA form
         PrefillArgs a{};
@@ -549,6 +565,9 @@ MLAKV_API int attn_decode_mla_absorbed(const void *q_lat, const void *q_rope, co
     if (!aligned16(q_lat) || !aligned16(q_rope) || !aligned16(c_cache) || !aligned16(krope_cache) ||
         !aligned16(out_lat) || !aligned16(seq_lens))
         return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_mla_absorbed: every pointer must be 16-byte aligned");
+    if (device_checks_on() && (rc = check_lengths(seq_lens, B, max_S, reinterpret_cast<cudaStream_t>(stream),
+                                                  "attn_decode_mla_absorbed")) != ATTN_OK)
+        return rc;
     const size_t need = decode_tc_mla_workspace(B, Hq, n_split);
     if (!workspace || ws_bytes < need || !aligned16(workspace))
         return fail(ATTN_ERR_WORKSPACE, "attn_decode_mla_absorbed: workspace of %zu bytes (16-byte aligned) "
@@ -576,6 +595,11 @@ MLAKV_API int attn_prefill_gqa_causal(const void *q, const void *k, const void *
     if (total_tokens == 0 || max_seqlen == 0) return ok();
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(cu_seqlens))
         return fail(ATTN_ERR_UNSUPPORTED, "attn_prefill_gqa_causal: every pointer must be 16-byte aligned");
+    if (device_checks_on()) {
+        const int crc = check_offsets(cu_seqlens, B, total_tokens, max_seqlen, reinterpret_cast<cudaStream_t>(stream),
+                                      "attn_prefill_gqa_causal");
+        if (crc != ATTN_OK) return crc;
+    }
     PrefillArgs a{};
     a.q = q; a.k = k; a.v = v; a.cu_seqlens = cu_seqlens; a.out = out;
     a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.T = total_tokens;

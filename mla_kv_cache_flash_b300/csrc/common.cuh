@@ -222,6 +222,19 @@ MLAKV_HIDDEN int report_error(int code, const char *message);
 // Sets the message to "<what>: <CUDA error name> (<description>)" and returns ATTN_ERR_CUDA.
 MLAKV_HIDDEN int report_cuda_error(cudaError_t e, const char *what);
 
+// Device-side checks of the length arrays (input_checks.cu): off unless MLAKV_DEVICE_CHECKS=1 or
+// attn_set_device_checks(1). Each runs on the stream, synchronises it and returns ATTN_OK or
+// ATTN_ERR_INPUT (with attn_last_error set) before the caller launches anything.
+MLAKV_HIDDEN bool device_checks_on();
+MLAKV_HIDDEN int set_device_checks(int on);
+// lens[i] in [0, bound], i < n
+MLAKV_HIDDEN int check_lengths(const int *lens, int n, int bound, cudaStream_t s, const char *who);
+// offsets[0] == 0, non-decreasing, offsets[n] <= T, every difference <= max_len
+MLAKV_HIDDEN int check_offsets(const int *offsets, int n, int T, int max_len, cudaStream_t s, const char *who);
+// the offsets rule without max_len, and 0 <= start[i], start[i] + cu[i+1] - cu[i] <= max_kv
+MLAKV_HIDDEN int check_chunks(const int *cu, const int *start, int n, int T, int max_kv, cudaStream_t s,
+                              const char *who);
+
 // Every pointer the C ABI takes must sit on a 16-byte boundary.
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
