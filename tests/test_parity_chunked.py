@@ -337,3 +337,42 @@ def test_mla_chunked_prefill_512_at_the_bench_size():
                                                        to_f64(inp["c_cache"][b:b + 1]), to_f64(inp["kr_cache"][b:b + 1]),
                                                        np.array([0, n]), st[b:b + 1], w.scale))
     _sampled_chunk_check(out, q_lat, refs)
+
+
+@pytest.mark.parametrize("case", range(6))
+def test_long_chunks_random_shapes(case):
+    """Seeded random batches on the prefill kernel's cache and MLA forms: chunk lengths 1-700,
+    start positions anywhere that fits, 2-6 sequences (the average kept at 128 or more so the
+    prefill kernel runs), group sizes 1-16, every cache row past a chunk NaN."""
+    rng = np.random.default_rng(5000 + case)
+    B = int(rng.integers(2, 7))
+    s_max = int(rng.choice([768, 1024, 1536]))
+    n = rng.integers(1, 701, size=B)
+    n[0] = max(int(n[0]), 128 * B - int(n[1:].sum()), 1)          # average >= 128 tokens
+    n = np.minimum(n, s_max)
+    while int(n.sum()) < 128 * B:
+        n[int(np.argmin(n))] = min(s_max, int(n.min()) + 128)
+    start = np.array([int(rng.integers(0, s_max - int(x) + 1)) for x in n])
+    chunks = tuple((int(s), int(x)) for s, x in zip(start, n))
+    hq, hkv = [(8, 8), (16, 4), (12, 4), (32, 2), (6, 3), (16, 1)][case]
+    q, k, v, cu, st, scale = _case(chunks, hq, hkv, 128, s_max, "bf16", 300 + case)
+    k, v = _poison_past_chunks(k, st, cu), _poison_past_chunks(v, st, cu)
+    T = int(cu[-1])
+    assert mk.lib().attn_prefill_gqa_chunked_workspace_size(B, T, hq, hkv, 128, s_max, mk.ATTN_BF16, 0) == 0
+    max_kv = int((st + np.diff(cu)).max())
+    ref = oracle.prefill_gqa_chunked(to_f64(q), to_f64(k), to_f64(v), cu, st, scale)
+    out = mk.prefill_gqa_chunked(q, k, v, torch.from_numpy(cu).to(DEV), torch.from_numpy(st).to(DEV), max_kv,
+                                 scale=scale)
+    torch.cuda.synchronize()
+    mk.check_status()
+    assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3, chunks
+    # the same chunks through the MLA form (16 heads, or 8 on odd cases)
+    mq = 16 if case % 2 == 0 else 8
+    ql, qr, c, kr, cu2, st2, mscale = _mla_case(chunks, mq, s_max, 400 + case)
+    c, kr = _poison_past_chunks(c, st2, cu2), _poison_past_chunks(kr, st2, cu2)
+    mref = oracle.mla_prefill_absorbed(to_f64(ql), to_f64(qr), to_f64(c), to_f64(kr), cu2, st2, mscale)
+    mout = mk.prefill_mla_chunked(ql, qr, c, kr, torch.from_numpy(cu2).to(DEV), torch.from_numpy(st2).to(DEV),
+                                  max_kv, mscale)
+    torch.cuda.synchronize()
+    mk.check_status()
+    assert float(np.abs(to_f64(mout) - mref).max()) <= 3e-3, chunks
