@@ -20,19 +20,23 @@
 //                O_t += P_t · V_n   (A = P from TMEM, B = V MN-major in shared memory)
 //              and commits each group to an mbarrier.
 //   warps 2-9  softmax, one warpgroup per query tile; thread = one query row (one TMEM
-//              lane). It reads its 128 scores from TMEM, masks the diagonal tile, keeps a
-//              running max m and sum l in the base-2 domain and writes
+//              lane). It reads its 128 scores from TMEM in 32-column quarters (the next
+//              quarter's load in flight while one is processed), masks the diagonal tile,
+//              keeps a running max m and sum l in the base-2 domain and writes
 //              P = 2^(s·scale·log2 e − m) as bf16 over its scores. The output is rescaled
 //              only when the row max grows by more than 2^8 (the result is exact for any
 //              reference value; this only bounds the range of P and l). At the end of an
-//              item it reads its O row from TMEM and writes O / l (fp32).
+//              item it reads its O row from TMEM and writes O / l (fp32): a full tile through
+//              a shared staging buffer and TMA stores, a sequence's partial last tile from
+//              registers.
 // The softmax uses Blackwell's paired fp32 FMA/add (two lanes of work per instruction) and
 // the three-input max, which halve its instruction count.
 //
 // TMEM: per query tile t, columns [256t, 256t+128) hold S and [256t+128, 256t+256) hold O.
 // P (two bf16 per column) overwrites S in place: keys 32q .. 32q+31 use the first 16 of
-// columns [32q, 32q+32), and the residual of the first kSplitTiles tiles the other 16. An S tile is written only after the
-// previous P·V of the same tile has completed, so P is never overwritten while in use.
+// columns [32q, 32q+32), and the residual of the first kSplitTiles tiles the other 16. The
+// next S of a tile is issued after that tile's P·V, and one thread's MMAs run in issue order,
+// so P is read before it is overwritten.
 //
 // Precision: P is rounded to bf16 for the tensor cores, a relative error of up to 2^-8 per
 // weight. Rows with many keys average it away, but rows near the start of a sequence see
@@ -41,14 +45,22 @@
 // 2^-16 there.
 //
 // Cache form (chunked prefill over an existing cache: "模型架构｜MQA & GQA 调研", section
-// "代码", the new tokens written at start_pos before attending): K and V come from the caches [B, S_max, Hkv, D] through
-// 4D tensor maps, and row i of sequence b's chunk sees cache rows 0 .. start_pos[b] + i. An
+// "代码", the new tokens written at start_pos before attending): K and V come from the caches
+// [B, S_max, Hkv, D] through 4D tensor maps, and row i of sequence b's chunk sees cache rows
+// 0 .. start_pos[b] + i. An
 // item then covers KV tiles 0 .. (start_pos + last row) / 128, and the mask starts at the tile
 // holding key start_pos + first row: with an unaligned start_pos two tiles are masked, each
 // row by its own limit. V rows past the chunk's end (the cache may hold anything there, NaN
 // included) are zeroed in shared memory by the MMA warp before P·V reads them; their weights
 // are 0, but 0 · NaN is not. The item list spans the longest chunk, found by every warp at
 // block start from cu_seqlens.
+//
+// MLA form (the qqstock DeepSeek MLA article, sections 2 and 6: with W_UK absorbed, MLA is
+// MQA whose key is the latent row c with its decoupled RoPE part kr, and whose value is c):
+// the cache form over c [B, S_max, 128] and kr [B, S_max, 48]. Each latent tile in shared
+// memory is both the K operand of the score (with the rope part: three more K = 16 steps over
+// 32-byte swizzled boxes of q_rope and kr) and the V operand of P·V; c and kr arrive on one
+// barrier, and a stage is free once both P·V MMAs reading it are done.
 //
 // Every wait is bounded (MLAKV_WAIT_TIMEOUT_CYCLES): a wait that runs out sets a bit in
 // g_prefill_status and the thread abandons its loop; every thread still reaches the final
