@@ -82,3 +82,34 @@ def test_oracle_leg_runs_every_kind_and_counts_the_line_work(name, tmp_path):
     else:
         assert n_seq == w.batch
         assert work == wl.bytes_per_step
+
+
+def test_long_chunk_lines_count_each_visible_pair():
+    # new row i of a 512-token chunk after 3584 cached rows sees 3585 + i keys: Σ = 512·3584 +
+    # 512·513/2 pairs a sequence, 4·D flops a pair and query head (GQA), 2·(r + dr) + 2·r (MLA)
+    pairs = 512 * 3584 + 512 * 513 // 2
+    wl, w = _make("prefill_chunk512")
+    assert wl.start == [3584] * w.batch
+    assert wl.flops_per_step == w.batch * 4 * w.head_dim * w.n_q_heads * pairs
+    assert wl.sets[0]["q_chunk"].shape == (w.batch * 512, w.n_q_heads, w.head_dim)
+    assert wl.sets[0]["cu_q"].tolist() == list(range(0, w.batch * 512 + 1, 512))
+    wm, m = _make("mla_prefill_chunk512")
+    assert wm.flops_per_step == m.batch * (2 * (m.kv_lora_rank + m.rope_dim) + 2 * m.kv_lora_rank) * m.n_q_heads * pairs
+    assert wm.sets[0]["q_rope_chunk"].shape == (m.batch * 512, m.n_q_heads, m.rope_dim)
+
+
+@pytest.mark.parametrize("name", ["prefill_chunk512", "mla_prefill_chunk512"])
+def test_long_chunk_oracle_leg(name, tmp_path):
+    # the CPU baseline's unit (the first sequence's whole chunk) runs from the mapped files and
+    # counts that sequence's flops
+    import json
+    import numpy as np
+    wl, w = _make(name)
+    arrays, units, n_seq = wl.oracle_payload()
+    assert units == [(0,)] and n_seq == 1
+    for k, v in arrays.items():
+        np.save(tmp_path / (k + ".npy"), np.ascontiguousarray(v))
+    (tmp_path / "meta.json").write_text(json.dumps({"kind": wl.oracle_kind, "scale": w.scale,
+                                                    "arrays": sorted(arrays)}))
+    assert bench._oracle_task((str(tmp_path), units)) == 1
+    assert wl.unit_work((0,)) * w.batch == wl.flops_per_step
