@@ -376,3 +376,26 @@ def test_long_chunks_random_shapes(case):
     torch.cuda.synchronize()
     mk.check_status()
     assert float(np.abs(to_f64(mout) - mref).max()) <= 3e-3, chunks
+
+
+def test_long_chunks_cache_capacity_off_the_tile_grid():
+    """S_max = 1000 (not a multiple of 128): the last K/V tile of a chunk ending at S_max reaches
+    past the cache (zeros from the tensor map), one ending 3 rows short has NaN rows to zero
+    inside it; both forms."""
+    chunks = ((700, 300), (0, 997), (500, 130))
+    q, k, v, cu, st, scale = _case(chunks, 16, 4, 128, 1000, "bf16", 333)
+    k, v = _poison_past_chunks(k, st, cu), _poison_past_chunks(v, st, cu)
+    ref = oracle.prefill_gqa_chunked(to_f64(q), to_f64(k), to_f64(v), cu, st, scale)
+    out = mk.prefill_gqa_chunked(q, k, v, torch.from_numpy(cu).to(DEV), torch.from_numpy(st).to(DEV), 1000,
+                                 scale=scale)
+    torch.cuda.synchronize()
+    mk.check_status()
+    assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3
+    ql, qr, c, kr, cu2, st2, mscale = _mla_case(chunks, 16, 1000, 334)
+    c, kr = _poison_past_chunks(c, st2, cu2), _poison_past_chunks(kr, st2, cu2)
+    mref = oracle.mla_prefill_absorbed(to_f64(ql), to_f64(qr), to_f64(c), to_f64(kr), cu2, st2, mscale)
+    mout = mk.prefill_mla_chunked(ql, qr, c, kr, torch.from_numpy(cu2).to(DEV), torch.from_numpy(st2).to(DEV), 1000,
+                                  mscale)
+    torch.cuda.synchronize()
+    mk.check_status()
+    assert float(np.abs(to_f64(mout) - mref).max()) <= 3e-3
