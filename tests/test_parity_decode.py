@@ -153,3 +153,29 @@ def test_merge_partials_against_oracle():
         ref = oracle.lse_merge(on[r][:, None, :], ln[r][:, None])[0]
         assert np.abs(out[r].cpu().double().numpy() - ref).max() <= 1e-5
     assert torch.all(out[3] == 0)
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (32, 1)])
+def test_sharp_weights_within_the_bf16_weight_bound(hq, hkv):
+    """A large scale (0.5) concentrates the weights on a few keys, so their bf16 rounding no
+    longer averages out. Per output element the register-MMA decode (bf16 weights) stays within
+    2^-8 · max |v| over the sequence's keys (each weight rounded to nearest, relative error at
+    most 2^-8, over l of the unrounded weights) plus a margin for fp32 arithmetic; the tcgen05
+    form (MQA here), which adds each weight's bf16 residual, stays within a sixteenth of it."""
+    w = W.DecodeWorkload("decode_sharp", 1, 4, hq, hkv, 128, 700, "bf16", lengths=(700, 300, 129, 1), sub=60)
+    inp = W.decode_inputs(w, DEV)
+    scale = 0.5
+    out = mk.decode_gqa(inp["q"], inp["k_cache"], inp["v_cache"], inp["seq_lens"], scale=scale)
+    torch.cuda.synchronize()
+    got = to_f64(out)
+    ref = _oracle_decode(inp, scale)
+    lens = inp["seq_lens"].cpu().numpy()
+    v = np.abs(to_f64(inp["v_cache"]))                             # [B, S_max, Hkv, D]
+    g = hq // hkv
+    for b in range(w.batch):
+        vmax = v[b, :int(lens[b])].max(axis=0)                     # [Hkv, D]
+        bound = 2.0 ** -8 * np.repeat(vmax, g, axis=0) + 1e-5
+        if hkv == 1:
+            bound = bound / 16
+        err = np.abs(got[b] - ref[b])
+        assert bool((err <= bound).all()), (b, float((err - bound).max()))
