@@ -1158,12 +1158,22 @@ def split_plan(cfg):
     return cfg, plan
 
 
+# The fields of one secondary line, in the order compact() lists them.
+ALSO_FIELDS = ["workload", "value", "unit", "ms_per_step", "roofline_frac", "traffic_MB", "cpu", "sm_mhz",
+               "reasons"]
+# throttle reasons, abbreviated in the secondary lines
+_REASON_ABBREV = {"sw_power_cap": "pc", "hw_slowdown": "hw", "hw_thermal_slowdown": "hwt", "sw_thermal_slowdown": "swt"}
+
+
 def compact(name, s, cpu):
-    """One secondary line, kept short so the whole list survives in a log's last lines."""
+    """One secondary line as a list in ALSO_FIELDS order, kept short so that the whole list
+    survives in the last 1500 characters of a log (the line ends with it)."""
     c = s["clocks"]
-    return {"workload": name, "value": s["value"], "unit": s["unit"], "ms_per_step": s["ms_per_step"],
-            "frac": s["roofline"]["frac"], "traffic": s["roofline"]["traffic"], "cpu": cpu,
-            "sm_mhz": c.get("sm_mhz"), "reasons": c.get("reasons")}
+    traffic = s["roofline"]["traffic"]
+    return [name, s["value"], s["unit"], s["ms_per_step"], s["roofline"]["frac"],
+            round(traffic / 1e6, 2) if traffic is not None else None, cpu,
+            round(c["sm_mhz"]) if c.get("sm_mhz") is not None else None,
+            [_REASON_ABBREV.get(r, r) for r in (c.get("reasons") or [])]]
 
 
 def main():
@@ -1268,7 +1278,7 @@ def run_gpu(args, world, rank, local, steps, peaks, peak_src, cls, w, pool):
                 also.append(compact(name, s2, cpu2))
                 del wl2
             except Exception as e:   # a secondary line must not cost the headline line
-                also.append({"workload": name, "error": f"{type(e).__name__}: {e}"[:200]})
+                also.append([name, "error", f"{type(e).__name__}: {e}"[:200]])
             torch.cuda.empty_cache()
 
     if rank == 0:
@@ -1281,9 +1291,11 @@ def run_gpu(args, world, rank, local, steps, peaks, peak_src, cls, w, pool):
                 "timing": head["timing"], "tokens_per_s": head.get("tokens_per_s"),
                 "pct_of_8tbs": head.get("pct_of_8tbs"), "roofline": head["roofline"], "cpu_baseline": cpu,
                 "e2e": head.get("e2e"), "gpu_launches": launches, "clocks": head["clocks"],
-                "also_note": "also: workload, value, unit, ms_per_step, roofline frac and traffic (DRAM bytes per "
-                             "launch from profiles/, null if none), cpu = the fp64 oracle on this host in the same "
-                             "unit, SM clock median and throttle reasons; timed like the headline",
+                "also_note": "also: one list per secondary line, fields as also_fields; traffic_MB = DRAM bytes "
+                             "per launch from profiles/ (null if none), cpu = the fp64 oracle on this host in the "
+                             "line's unit, sm_mhz and throttle reasons (pc = sw_power_cap) while timed; each line "
+                             "is timed like the headline",
+                "also_fields": ALSO_FIELDS,
                 "also": also}
         print(json.dumps(line, separators=(",", ":")), flush=True)
     if world > 1:
