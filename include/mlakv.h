@@ -96,6 +96,10 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1, ATTN_FP8_E4M3 = 2 } attn_dtype;
  *            16: those shapes run on the tcgen05 tensor cores), for one KV head and a block
  *            of 16 or 32 of its query heads.
  *   D        64, 96 or 128. Any Hq/Hkv with Hq % Hkv == 0 and Hq/Hkv <= 128.
+ *   B        bf16 cache: the kernels keep 8 bytes of per-sequence tables in shared memory
+ *            beside their K/V ring and take a shallower ring for a batch that would not fit
+ *            beside the deepest one; at least 4800 sequences fit for every shape (at the
+ *            Llama-3-8B shape, over 9000). A larger batch returns ATTN_ERR_CUDA.
  *   workspace, ws_bytes: scratch for the split partials, at least
  *            attn_decode_gqa_workspace_size(...) bytes with the same arguments; may be
  *            NULL when that size is 0. For a bf16 cache the workspace also holds one arrival

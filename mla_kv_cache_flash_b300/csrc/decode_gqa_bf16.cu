@@ -761,17 +761,29 @@ int sm_count() {
     return n;
 }
 
-template <int D, int MT, int HG, int NC, bool CH>
-cudaError_t launch_cfg(const DecodeStreamArgs &a, cudaStream_t st) {
-    constexpr int NS = ring_depth<D, MT, HG, NC, CH>();
+// query rows: the group's HG·G rows (one head block when n_hblk > 1), plus the padding
+// the last head's 16·MT-row MMA tile reaches past them; chunked prefill, nt tokens × HG·G
+// heads, plus one zero row that stands for the rows past the block's tokens
+template <int HG, int MT, bool CH>
+void query_rows(const DecodeStreamArgs &a, int &q_loaded, int &q_rows) {
+    const int G = a.Hq / a.Hkv;
+    q_loaded = CH ? a.nt * HG * G : a.n_hblk == 1 ? HG * G : a.heads;
+    q_rows = CH ? (q_loaded + 1 + 7) / 8 * 8 : ((a.n_hblk == 1 ? (HG - 1) * G : 0) + 16 * MT + 7) / 8 * 8;
+}
+
+template <int D, int MT, int HG, int NS, int NC, bool CH>
+int layout_total(const DecodeStreamArgs &a) {
+    int q_loaded, q_rows;
+    query_rows<HG, MT, CH>(a, q_loaded, q_rows);
+    return layout<D, MT, HG, NS, NC>(q_rows, a.heads, a.B, a.n_blocks, CH).total;
+}
+
+template <int D, int MT, int HG, int NS, int NC, bool CH>
+cudaError_t launch_ns(const DecodeStreamArgs &a, cudaStream_t st) {
     using C = Cfg<D, MT, HG, NS, NC>;
     const int G = a.Hq / a.Hkv;
-    // query rows: the group's HG·G rows (one head block when n_hblk > 1), plus the padding
-    // the last head's 16·MT-row MMA tile reaches past them; chunked prefill, nt tokens × HG·G
-    // heads, plus one zero row that stands for the rows past the block's tokens
-    const int q_loaded = CH ? a.nt * HG * G : a.n_hblk == 1 ? HG * G : a.heads;
-    const int q_rows = CH ? (q_loaded + 1 + 7) / 8 * 8
-                          : ((a.n_hblk == 1 ? (HG - 1) * G : 0) + 16 * MT + 7) / 8 * 8;
+    int q_loaded, q_rows;
+    query_rows<HG, MT, CH>(a, q_loaded, q_rows);
     const Layout L = layout<D, MT, HG, NS, NC>(q_rows, a.heads, a.B, a.n_blocks, CH);
     if (L.total > 227 * 1024) return cudaErrorInvalidValue;
     CUtensorMap km, vm, qm;
@@ -798,6 +810,15 @@ cudaError_t launch_cfg(const DecodeStreamArgs &a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     e = launch_pdl(kern, dim3(a.n_blocks), dim3(C::kThreads), L.total, st, km, vm, qm, a, L, q_loaded);
     return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// The ring as deep as ring_depth gives, or two stages where the per-sequence tables of a large
+// batch (8 bytes a sequence, beside the ring) would not fit in shared memory beside it.
+template <int D, int MT, int HG, int NC, bool CH>
+cudaError_t launch_cfg(const DecodeStreamArgs &a, cudaStream_t st) {
+    constexpr int NS = ring_depth<D, MT, HG, NC, CH>();
+    if (NS == 2 || layout_total<D, MT, HG, NS, NC, CH>(a) <= 227 * 1024) return launch_ns<D, MT, HG, NS, NC, CH>(a, st);
+    return launch_ns<D, MT, HG, 2, NC, CH>(a, st);
 }
 
 // One KV head per tile with a single MMA row tile per head: 7 consumer warps over 112-token
