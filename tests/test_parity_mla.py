@@ -78,3 +78,16 @@ def test_decompressed_output_close_to_naive():
                                   to_f64(inp["kr_cache"]), to_f64(inp["w_uk"]), to_f64(inp["w_uv"]),
                                   inp["seq_lens"].cpu().numpy(), w.scale)
     assert np.all(np.abs(o - ref) <= mb.full_step_tolerance(inp, w.scale, oracle))
+
+
+@pytest.mark.parametrize("B", [1200, 3000])
+def test_large_batches(B):
+    """Past about 1000 sequences the per-sequence tables (8 bytes each in shared memory) leave
+    room for one block per SM instead of two, so the persistent blocks of the split run in two
+    waves; short ragged lengths, every output compared."""
+    w = W.MlaWorkload("mla_large_b", 3, B, 16, 96, 128, 48, 96, 48, length_range=(0, 48), sub=7)
+    inp = W.mla_inputs(w, DEV)
+    q_lat, out = _run(inp, w.scale)
+    mk.check_status()
+    err = np.abs(out.cpu().double().numpy() - _ref(inp, q_lat, w.scale)).max()
+    assert err <= TOL, err
