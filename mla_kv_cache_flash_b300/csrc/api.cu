@@ -369,9 +369,10 @@ bool chunk_on_tc_gqa(int B, int Hq, int Hkv, int D, attn_dtype dtype) {
     return dtype == ATTN_BF16 && decode_tc_gqa_chunk_eligible(B, Hq, Hkv, D);
 }
 // other bf16 caches with up to 16 query heads per KV head: the register-MMA decode kernel,
-// 16 / G new tokens × G heads per MMA tile
-bool chunk_on_stream(int B, int Hq, int Hkv, int D, attn_dtype dtype) {
-    return dtype == ATTN_BF16 && !chunk_on_tc_gqa(B, Hq, Hkv, D, dtype) && decode_gqa_stream_chunk_eligible(Hq, Hkv);
+// 16 / G new tokens × G heads per MMA tile, when the batch's tables fit beside its ring
+bool chunk_on_stream(int B, int T, int Hq, int Hkv, int D, attn_dtype dtype, int n_split) {
+    return dtype == ATTN_BF16 && !chunk_on_tc_gqa(B, Hq, Hkv, D, dtype) && decode_gqa_stream_chunk_eligible(Hq, Hkv) &&
+           decode_gqa_stream_chunk_fits(B, T, Hq, Hkv, D, n_split);
 }
 bool chunk_on_tc_mla(int B, int Hq) { return Hq % 16 == 0 && Hq <= 128 && decode_tc_mla_chunk_fits(B); }
 
@@ -384,7 +385,8 @@ MLAKV_API size_t attn_prefill_gqa_chunked_workspace_size(int B, int T, int Hq, i
         return 0;
     if (chunk_on_prefill(B, T, D, dtype)) return 0;
     if (chunk_on_tc_gqa(B, Hq, Hkv, D, dtype)) return decode_tc_gqa_chunk_workspace(B, T, Hq, Hkv, n_split);
-    if (chunk_on_stream(B, Hq, Hkv, D, dtype)) return decode_gqa_stream_chunk_workspace(B, T, Hq, Hkv, D, n_split);
+    if (chunk_on_stream(B, T, Hq, Hkv, D, dtype, n_split))
+        return decode_gqa_stream_chunk_workspace(B, T, Hq, Hkv, D, n_split);
     return partials_bytes(T, Hq, D, chunked_plan(T, Hq, Hkv, D, max_kv, n_split).n_split);
 }
 
@@ -429,7 +431,7 @@ MLAKV_API int attn_prefill_gqa_chunked(const void *q, const void *k_cache, const
         if (e != cudaSuccess) return cuda_fail(e, "attn_prefill_gqa_chunked: kernel launch");
         return ok();
     }
-    if (chunk_on_stream(B, Hq, Hkv, D, dtype)) {
+    if (chunk_on_stream(B, T, Hq, Hkv, D, dtype, n_split)) {
         const size_t need = decode_gqa_stream_chunk_workspace(B, T, Hq, Hkv, D, n_split);
         if (!workspace || ws_bytes < need || !aligned16(workspace))
             return fail(ATTN_ERR_WORKSPACE, "%s: workspace of %zu bytes (16-byte aligned) needed, got %zu at %p",

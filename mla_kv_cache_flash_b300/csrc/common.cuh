@@ -110,6 +110,8 @@ MLAKV_HIDDEN cudaError_t launch_decode_gqa_stream(const DecodeStreamArgs &a, cud
 // Chunked prefill on the same kernel for query groups of up to 16 heads: 16 / G new tokens ×
 // G heads per MMA tile, each token with its own key limit.
 MLAKV_HIDDEN bool decode_gqa_stream_chunk_eligible(int Hq, int Hkv);
+// Whether a batch's per-sequence tables fit beside the chunk mode's ring (else the CUDA-core form).
+MLAKV_HIDDEN bool decode_gqa_stream_chunk_fits(int B, int T, int Hq, int Hkv, int D, int n_split);
 MLAKV_HIDDEN int decode_gqa_stream_chunk_blocks(int B, int T, int Hq, int Hkv, int n_split);
 MLAKV_HIDDEN size_t decode_gqa_stream_chunk_workspace(int B, int T, int Hq, int Hkv, int D, int n_split);
 MLAKV_HIDDEN cudaError_t launch_decode_gqa_stream_chunk(const void *q, const void *k, const void *v,

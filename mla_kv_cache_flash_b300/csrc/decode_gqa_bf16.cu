@@ -959,15 +959,11 @@ size_t decode_gqa_stream_chunk_workspace(int B, int T, int Hq, int Hkv, int D, i
            (rows * sizeof(float) + 255) / 256 * 256;
 }
 
-cudaError_t launch_decode_gqa_stream_chunk(const void *q, const void *k, const void *v, const int *cu_q,
-                                           const int *start_pos, float *out, int B, int T, int Hq, int Hkv, int D,
-                                           float scale_log2, int S_max, int n_split, void *ws, cudaStream_t st) {
+// The chunk mode's plan (everything but the pointers), shared by the launch and the fit check.
+static DecodeStreamArgs chunk_plan_args(int B, int T, int Hq, int Hkv, int D, int n_split) {
     DecodeStreamArgs a{};
     const int G = Hq / Hkv;
-    a.q = q; a.k = k; a.v = v; a.out = out; a.cu_q = cu_q; a.start_pos = start_pos;
     a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.T = T;
-    a.scale_log2 = scale_log2;
-    a.S_max = S_max;
     a.nt = chunk_tokens(G);
     a.heads = a.nt * G;
     a.n_hblk = 1;
@@ -975,6 +971,33 @@ cudaError_t launch_decode_gqa_stream_chunk(const void *q, const void *k, const v
     a.hg = a.aligned ? 1 : hg_for(Hkv, G);
     a.tile_tokens = a.hg == 4 ? 32 : a.hg == 1 ? 112 : 64;
     a.n_blocks = decode_gqa_stream_chunk_blocks(B, T, Hq, Hkv, n_split);
+    return a;
+}
+
+// Does the chunk mode's shared memory (its per-sequence tables beside a ring of at least two
+// stages) fit for this batch? The launch takes the configuration launch_mt<D, 1, true> picks.
+template <int D>
+static bool chunk_fits_d(const DecodeStreamArgs &a) {
+    constexpr int kMax = 227 * 1024;
+    switch (a.hg) {
+        case 4: return layout_total<D, 1, 4, 2, 4, true>(a) <= kMax;
+        case 2: return layout_total<D, 1, 2, 2, 4, true>(a) <= kMax;
+        default: return layout_total<D, 1, 1, 2, 7, true>(a) <= kMax;
+    }
+}
+
+bool decode_gqa_stream_chunk_fits(int B, int T, int Hq, int Hkv, int D, int n_split) {
+    const DecodeStreamArgs a = chunk_plan_args(B, T, Hq, Hkv, D, n_split);
+    return D == 64 ? chunk_fits_d<64>(a) : D == 96 ? chunk_fits_d<96>(a) : D == 128 ? chunk_fits_d<128>(a) : false;
+}
+
+cudaError_t launch_decode_gqa_stream_chunk(const void *q, const void *k, const void *v, const int *cu_q,
+                                           const int *start_pos, float *out, int B, int T, int Hq, int Hkv, int D,
+                                           float scale_log2, int S_max, int n_split, void *ws, cudaStream_t st) {
+    DecodeStreamArgs a = chunk_plan_args(B, T, Hq, Hkv, D, n_split);
+    a.q = q; a.k = k; a.v = v; a.out = out; a.cu_q = cu_q; a.start_pos = start_pos;
+    a.scale_log2 = scale_log2;
+    a.S_max = S_max;
     const size_t rows = 2 * (size_t)a.n_blocks * a.hg * a.heads;
     const size_t n_cnt = (size_t)stream_chunk_segs(B, T, Hq, Hkv) * a.hg;
     char *w = static_cast<char *>(ws);

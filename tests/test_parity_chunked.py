@@ -399,3 +399,24 @@ def test_long_chunks_cache_capacity_off_the_tile_grid():
     torch.cuda.synchronize()
     mk.check_status()
     assert float(np.abs(to_f64(mout) - mref).max()) <= 3e-3
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(8, 4, 96), (32, 2, 128), (12, 4, 64)])
+def test_short_chunks_large_batches(hq, hkv, d):
+    """2500 sequences with chunks of 0-3 new tokens (far below 128 on average: the decode
+    kernels' chunk modes) over caches of at most 64 rows: the per-sequence tables then take a
+    shallower ring, or the next kernel form. Every output within the derived bf16-weight bound
+    of the chunk modes, which carry each weight's bf16 residual (about 2^-16 relative)."""
+    rng = np.random.default_rng(2500 + hq)
+    B = 2500
+    n = rng.integers(0, 4, size=B)
+    start = np.array([int(rng.integers(0, 64 - int(x) + 1)) for x in n])
+    chunks = tuple((int(s), int(x)) for s, x in zip(start, n))
+    q, k, v, cu, st, scale = _case(chunks, hq, hkv, d, 64, "bf16", 500 + hq)
+    max_kv = int((st + np.diff(cu)).max())
+    ref = oracle.prefill_gqa_chunked(to_f64(q), to_f64(k), to_f64(v), cu, st, scale)
+    out = mk.prefill_gqa_chunked(q, k, v, torch.from_numpy(cu).to(DEV), torch.from_numpy(st).to(DEV), max_kv,
+                                 scale=scale)
+    torch.cuda.synchronize()
+    mk.check_status()
+    assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3

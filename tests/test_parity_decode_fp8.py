@@ -110,3 +110,15 @@ def test_fp8_more_than_32_sequences(hq, hkv, s_max):
     for n_split in (0, 1, 3):
         out = _run(inp, w.scale, n_split=n_split)
         assert float(np.abs(to_f64(out) - ref).max()) <= TOL, n_split
+
+
+@pytest.mark.parametrize("hq,hkv,d,B", [(8, 4, 96, 3000), (16, 2, 128, 2500)])
+def test_fp8_large_batches(hq, hkv, d, B):
+    """Thousands of short ragged sequences: past what the tensor-core kernel's per-sequence
+    tables leave room for, the call runs on the CUDA-core E4M3 kernel (and its merge); every
+    output at the fp8 bound."""
+    w = W.DecodeWorkload("fp8_large_b", 5, B, hq, hkv, d, 48, "bf16", length_range=(0, 48), sub=B)
+    inp = W.fp8_decode_inputs(w, DEV)
+    out = _run(inp, w.scale)
+    mk.check_status()
+    assert float(np.abs(to_f64(out) - _ref(inp, w.scale)).max()) <= TOL
