@@ -205,3 +205,15 @@ def test_large_batches(hq, hkv, d, B):
     err = np.abs(to_f64(out) - _oracle_decode(inp, w.scale))
     bound = _bf16_weight_bound(inp, hq, hkv)
     assert bool((err <= bound).all()), float((err - bound).max())
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (32, 1)])
+def test_long_context(hq, hkv):
+    """131072 cached tokens (and a ragged 70001): the split plan's tile counts run to thousands
+    per segment; every output compared (register-MMA GQA, and MQA on the tensor cores)."""
+    w = W.DecodeWorkload("decode_128k", 1, 2, hq, hkv, 128, 131072, "bf16", lengths=(131072, 70001), sub=62)
+    inp = W.decode_inputs(w, DEV)
+    out = mk.decode_gqa(inp["q"], inp["k_cache"], inp["v_cache"], inp["seq_lens"], scale=w.scale)
+    torch.cuda.synchronize()
+    mk.check_status()
+    assert _max_err(out, _oracle_decode(inp, w.scale)) <= TOL_BF16

@@ -91,3 +91,13 @@ def test_large_batches(B):
     mk.check_status()
     err = np.abs(out.cpu().double().numpy() - _ref(inp, q_lat, w.scale)).max()
     assert err <= TOL, err
+
+
+def test_long_context():
+    """MLA over 131072 and 70001 latent rows, every output compared."""
+    w = W.MlaWorkload("mla_128k", 3, 2, 16, 96, 128, 48, 96, 131072, lengths=(131072, 70001), sub=8)
+    inp = W.mla_inputs(w, DEV)
+    q_lat, out = _run(inp, w.scale)
+    mk.check_status()
+    err = np.abs(out.cpu().double().numpy() - _ref(inp, q_lat, w.scale)).max()
+    assert err <= TOL, err
