@@ -420,3 +420,25 @@ def test_short_chunks_large_batches(hq, hkv, d):
     torch.cuda.synchronize()
     mk.check_status()
     assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3
+
+
+def test_long_chunks_after_a_long_context():
+    """512- and 300-token chunks after 130000 and 99000 cached rows (items of about a thousand
+    KV tiles) on the prefill kernel's cache and MLA forms, NaN past every chunk."""
+    chunks = ((130000, 512), (99000, 300))
+    q, k, v, cu, st, scale = _case(chunks, 16, 2, 128, 131072, "bf16", 777)
+    k, v = _poison_past_chunks(k, st, cu), _poison_past_chunks(v, st, cu)
+    ref = oracle.prefill_gqa_chunked(to_f64(q), to_f64(k), to_f64(v), cu, st, scale)
+    out = mk.prefill_gqa_chunked(q, k, v, torch.from_numpy(cu).to(DEV), torch.from_numpy(st).to(DEV), 130512,
+                                 scale=scale)
+    torch.cuda.synchronize()
+    mk.check_status()
+    assert float(np.abs(to_f64(out) - ref).max()) <= 3e-3
+    ql, qr, c, kr, cu2, st2, mscale = _mla_case(chunks, 16, 131072, 778)
+    c, kr = _poison_past_chunks(c, st2, cu2), _poison_past_chunks(kr, st2, cu2)
+    mref = oracle.mla_prefill_absorbed(to_f64(ql), to_f64(qr), to_f64(c), to_f64(kr), cu2, st2, mscale)
+    mout = mk.prefill_mla_chunked(ql, qr, c, kr, torch.from_numpy(cu2).to(DEV), torch.from_numpy(st2).to(DEV),
+                                  130512, mscale)
+    torch.cuda.synchronize()
+    mk.check_status()
+    assert float(np.abs(to_f64(mout) - mref).max()) <= 3e-3

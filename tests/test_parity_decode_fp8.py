@@ -122,3 +122,12 @@ def test_fp8_large_batches(hq, hkv, d, B):
     out = _run(inp, w.scale)
     mk.check_status()
     assert float(np.abs(to_f64(out) - _ref(inp, w.scale)).max()) <= TOL
+
+
+def test_fp8_long_context():
+    """131072 and 70001 cached tokens over the E4M3 cache (tensor-core form), every output."""
+    w = W.DecodeWorkload("fp8_128k", 5, 2, 8, 4, 96, 131072, "bf16", lengths=(131072, 70001), sub=99)
+    inp = W.fp8_decode_inputs(w, DEV)
+    out = _run(inp, w.scale)
+    mk.check_status()
+    assert float(np.abs(to_f64(out) - _ref(inp, w.scale)).max()) <= TOL
